@@ -1,0 +1,404 @@
+"""Benchmark: paged GQA decode (B=32, Q_N=32, KV_N=8, D=128, kv len ~
+U[512,4096], block 128, permuted pages) through libfia on one GB300 per rank.
+
+A step is one fia_run (tile scheduler + split-KV decode with its in-kernel
+combine) over the whole batch, inputs resident in HBM.  `value` is KV GB/s:
+the algorithmic bytes (every visible K and V row once) over the step time.
+Between timed steps L2 is flushed by writing a buffer of twice its size.
+
+Extra lines of evidence in the same JSON object: the decode kernel's own
+roofline (CUDA events around fia_execute on the launching stream), the
+end-to-end number through the C ABI with host buffers, the CPU oracle baseline,
+SM clocks sampled during the timed region, and the other workloads
+(varlen causal prefill, long FP8 decode, sparse shared-KV decode) when built.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fia|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "paged-decode KV GB/s and prefill TFLOP/s on 1 GB300, % of roofline"
+WORKLOAD = ("paged GQA decode: B=32, S_q=1, Q_N=32, KV_N=8, D=128, bf16, kv len ~ U[512,4096], "
+            "block 128, permuted block table")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def _src_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "decode_tile_scheduler_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(kernel_key, src_files, units_now):
+    """DRAM bytes per launch from the committed ncu summary, scaled by the
+    units processed; None when absent or when the kernel source changed."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f).get(kernel_key)
+    if not d or d.get("src_hash") != _src_hash(*src_files):
+        return None
+    return d["dram_bytes_per_launch"] * units_now / d["units"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons (every 200 ms)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [r.strip().split(", ") for r in self.tmp.read().splitlines() if r.strip()]
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for nm, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(nm)
+            except Exception:
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _flush_buf():
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    return torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+
+
+def _time_steps(fn_plan, fn_exec, steps, flush):
+    """Per-step CUDA events on the current stream: (step ms list, exec ms list)."""
+    s = torch.cuda.current_stream()
+    step_ms, exec_ms = [], []
+    for _ in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        fn_plan()
+        e1.record(s)
+        fn_exec()
+        e2.record(s)
+        e2.synchronize()
+        step_ms.append(e0.elapsed_time(e2))
+        exec_ms.append(e1.elapsed_time(e2))
+    return step_ms, exec_ms
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(prob_cpu, bytes_per_run, min_seconds=10.0):
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    oracle.fia(prob_cpu, cores)  # build + warm
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.fia(prob_cpu, cores)
+        n += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": bytes_per_run * n / dt / 1e9, "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"the whole paged GQA decode batch, repeated {n}x ({dt:.1f} s, fp64, "
+                      f"OpenMP over output rows)"}
+
+
+# ---------------------------------------------------------------------------
+# extra workloads (evidence only)
+# ---------------------------------------------------------------------------
+
+def _bench_call(call, steps, warmup, flush):
+    for _ in range(warmup):
+        call.run()
+    torch.cuda.synchronize()
+    st, ex = _time_steps(call.plan, call.execute, steps, flush)
+    return statistics.mean(st), statistics.mean(ex)
+
+
+def extra_workloads(steps, warmup, flush, peaks):
+    import decode_tile_scheduler_gb300 as fia
+    import fia_inputs as fi
+    res = {}
+    # long-context FP8 decode
+    try:
+        p = fi.workload_fp8_long_decode(device="cuda")
+        call = fia.FiaCall(p, with_lse=True)
+        ms, ex = _bench_call(call, steps, warmup, flush)
+        by = p.kv_bytes_visible()
+        res["fp8_long_decode"] = {
+            "workload": "B=4, Q_N=64, KV_N=8, D=128, E4M3 KV + fp32/64 scales, kv len ~ "
+                        "U[32768,131072], block 128",
+            "ms_per_step": ms, "kernel_ms": ex, "GB/s": by / ms / 1e6,
+            "kernel_GB/s": by / ex / 1e6, "frac_of_hbm": by / ex / 1e6 / peaks["hbm_gbs"],
+            "algorithmic_bytes": by}
+        del call, p
+    except Exception as e:  # not built yet
+        res["fp8_long_decode"] = {"unavailable": str(e)[:200]}
+    torch.cuda.empty_cache()
+    try:
+        p = fi.workload_varlen_prefill(device="cuda")
+        call = fia.FiaCall(p, with_lse=True)
+        ms, ex = _bench_call(call, steps, warmup, flush)
+        fl = 4 * p.D * p.QN * sum(L * (L + 1) // 2 for L in p.q_lens)
+        res["varlen_causal_prefill"] = {
+            "workload": "TND B=8, L ~ U[256,4096], Q_N=32, KV_N=8, D=128, paged block 128, "
+                        "right-down causal, sinks",
+            "ms_per_step": ms, "kernel_ms": ex, "TFLOP/s": fl / ms / 1e9,
+            "kernel_TFLOP/s": fl / ex / 1e9,
+            "frac_of_bf16": fl / ex / 1e9 / peaks["bf16_tflops"], "flops": fl}
+        del call, p
+    except Exception as e:
+        res["varlen_causal_prefill"] = {"unavailable": str(e)[:200]}
+    torch.cuda.empty_cache()
+    try:
+        sp = fi.workload_sparse_csa(device="cuda")
+        call = fia.SparseCall(sp, with_lse=True)
+        call.plan()
+        for _ in range(warmup):
+            call.run()
+        torch.cuda.synchronize()
+        st, ex = _time_steps(call.plan, call.run, steps, flush)
+        by = sp.B * (sp.win_left + 1 + sp.K2) * sp.D * 2
+        res["sparse_csa_decode"] = {
+            "workload": "B=16, N1=64, D=512, ori 8192 band 127/0, cmp 2048 (ratio 4), top-512",
+            "ms_per_step": statistics.mean(st), "kernel_ms": statistics.mean(ex),
+            "GB/s": by / statistics.mean(st) / 1e6, "kernel_GB/s": by / statistics.mean(ex) / 1e6,
+            "algorithmic_bytes": by}
+    except Exception as e:
+        res["sparse_csa_decode"] = {"unavailable": str(e)[:200]}
+    return res
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import fia_inputs as fi
+    import oracle
+    p = fi.workload_paged_decode(device="cpu")
+    by = p.kv_bytes_visible()
+    cores = len(os.sched_getaffinity(0))
+    for _ in range(args.warmup):
+        oracle.fia(p, cores)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.fia(p, cores)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    val = by / (ms / 1e3) / 1e9
+    sample = "the whole paged GQA decode batch per step (fp64 oracle, OpenMP)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "oracle on host cores"},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_fia(args):
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import decode_tile_scheduler_gb300 as fia
+    import fia_inputs as fi
+    fia.lib()
+    peaks = _peaks()
+
+    # ---- device-resident workload (each rank: one replica of the batch) ----
+    p = fi.workload_paged_decode(device="cuda")
+    by = p.kv_bytes_visible()
+    call = fia.FiaCall(p, with_lse=True)
+    flush = _flush_buf()
+    for _ in range(max(args.warmup, 3)):
+        call.run()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    clocks = ClockSampler(local)
+    clocks.start()
+    torch.cuda.synchronize()
+    step_ms, exec_ms = _time_steps(call.plan, call.execute, args.steps, flush)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    _barrier(ws)
+    ms = _max_over_ranks(statistics.mean(step_ms), ws)
+    kern_ms = _max_over_ranks(statistics.mean(exec_ms), ws)
+    value = ws * by / (ms / 1e3) / 1e9
+    achieved = by / (kern_ms / 1e3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers ----
+    host_q = p.q.cpu().pin_memory()
+    host_len = p.seqused_kv.cpu().pin_memory()
+    host_bt = p.block_table.cpu().pin_memory()
+    host_out = torch.empty(call.out.shape, dtype=call.out.dtype).pin_memory()
+    host_lse = torch.empty(call.lse.shape, dtype=call.lse.dtype).pin_memory()
+    s = torch.cuda.current_stream()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        p.q.copy_(host_q, non_blocking=True)
+        p.seqused_kv.copy_(host_len, non_blocking=True)
+        p.block_table.copy_(host_bt, non_blocking=True)
+        call.run()
+        host_out.copy_(call.out, non_blocking=True)
+        host_lse.copy_(call.lse, non_blocking=True)
+        e1.record(s)
+        e1.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    h2d = sum(t.numel() * t.element_size() for t in (host_q, host_len, host_bt))
+    d2h = sum(t.numel() * t.element_size() for t in (host_out, host_lse))
+    e2e = ws * by / (_max_over_ranks(statistics.mean(e2e_ms), ws) / 1e3) / 1e9
+
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        extras = extra_workloads(max(3, min(args.steps, 10)), 3, flush, peaks)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(p.to("cpu"), by, min_seconds=args.cpu_seconds)
+
+    traffic = _ncu_traffic("decode_kernel_bf16_d128", ["decode.cu", "common.cuh", "internal.h"], by)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "l2": "flushed between timed steps (2x L2 write)",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                       "algorithmic_bytes_per_step": by},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": traffic, "kernel": "decode_kernel<128,bf16> (fia_execute)",
+                         "peak_source": peaks["source"] + " (burst copy)"},
+            "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "extra": extras,
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="fia", choices=["fia", "reference"])
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_fia(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,352 @@
+// fia_api.cu -- host side of libfia: the C ABI declared in include/fia.h.
+// Validation and workspace sizing follow the two-phase convention of the FIA
+// pages ("aclnnFusedInferAttentionScoreV5": GetWorkspaceSize checks the
+// inputs and computes the workspace; the execute call runs); launches go to
+// the caller's stream only, and nothing here allocates or synchronises.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fia.h"
+#include "internal.h"
+
+using namespace fia;
+
+namespace {
+
+constexpr int64_t kAlign = 256;
+int64_t align_up(int64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int gcd_i(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------
+// device properties and the tensor-map encoder (driver entry point)
+// ---------------------------------------------------------------------------
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+fia_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !f)
+      return FIA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  *fn = g_encode;
+  return FIA_OK;
+}
+
+fia_status sm_count(int requested, int* n) {
+  if (requested > 0) {
+    *n = requested;
+    return FIA_OK;
+  }
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FIA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FIA_ERR_CUDA;
+  *n = v;
+  return FIA_OK;
+}
+
+// 2-D tiled map over a row-major [rows, cols] matrix with 128-byte swizzling.
+fia_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
+                    uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+                    uint64_t row_stride_elems) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  fia_status st = get_encoder(&enc);
+  if (st != FIA_OK) return st;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_stride_elems * (uint64_t)esize};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FIA_OK : FIA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// FIA validation ("...V5" constraint catalogue, the parts this library builds)
+// ---------------------------------------------------------------------------
+bool is_decode(const fia_params* p) { return p->max_seqlen_q == 1; }
+
+fia_status validate(const fia_params* p) {
+  if (!p) return FIA_ERR_NULL_ARG;
+  for (int i = 0; i < 7; ++i)
+    if (p->reserved[i] != 0) return FIA_ERR_BAD_SHAPE;
+  if (p->batch < 1 || p->batch > 65536) return FIA_ERR_BAD_SHAPE;
+  if (p->num_q_heads < 1 || p->num_q_heads > 256) return FIA_ERR_BAD_SHAPE;
+  if (p->num_kv_heads < 1 || p->num_kv_heads > 256) return FIA_ERR_BAD_SHAPE;
+  if (p->num_q_heads % p->num_kv_heads) return FIA_ERR_BAD_SHAPE;
+  if (p->num_q_heads / p->num_kv_heads > 64) return FIA_ERR_BAD_SHAPE;
+  if (p->head_dim < 1 || p->head_dim > 512) return FIA_ERR_BAD_SHAPE;
+  if (p->layout != FIA_LAYOUT_BSND && p->layout != FIA_LAYOUT_TND) return FIA_ERR_BAD_SHAPE;
+  if (p->max_seqlen_q < 0 || p->max_seqlen_q > 20971520) return FIA_ERR_BAD_SHAPE;
+  if (p->layout == FIA_LAYOUT_TND) {
+    if (p->total_q < 0) return FIA_ERR_BAD_SHAPE;
+    if (!p->cu_seqlens_q) return FIA_ERR_NULL_ARG;
+  }
+  if (p->kv_dtype != FIA_KV_BF16 && p->kv_dtype != FIA_KV_FP8_E4M3) return FIA_ERR_BAD_DTYPE;
+  if (p->mask_mode != FIA_MASK_NONE && p->mask_mode != FIA_MASK_RIGHT_DOWN_CAUSAL &&
+      p->mask_mode != FIA_MASK_BAND)
+    return FIA_ERR_BAD_SHAPE;
+  if (p->mask_mode == FIA_MASK_BAND && (int64_t)p->pre_tokens + p->next_tokens < 0)
+    return FIA_ERR_BAD_SHAPE;
+  if (!std::isfinite(p->scale)) return FIA_ERR_BAD_SHAPE;
+  if (p->num_sms < 0 || p->num_sms > 4096) return FIA_ERR_BAD_SHAPE;
+  if (p->q_token_stride < 0 || p->out_token_stride < 0) return FIA_ERR_BAD_SHAPE;
+  const int64_t ND = (int64_t)p->num_q_heads * p->head_dim;
+  if (p->q_token_stride && (p->q_token_stride < ND || p->q_token_stride % 8)) return FIA_ERR_BAD_SHAPE;
+  if (p->out_token_stride && (p->out_token_stride < ND || p->out_token_stride % 8))
+    return FIA_ERR_BAD_SHAPE;
+  if (!p->q || !p->out || !p->k_cache || !p->v_cache) return FIA_ERR_NULL_ARG;
+  if (!aligned16(p->q) || !aligned16(p->out) || !aligned16(p->k_cache) || !aligned16(p->v_cache))
+    return FIA_ERR_BAD_SHAPE;
+  if (p->lse && (reinterpret_cast<uintptr_t>(p->lse) & 3u)) return FIA_ERR_BAD_SHAPE;
+  if (p->kv_dtype == FIA_KV_FP8_E4M3) {
+    if (!p->k_scale || !p->v_scale) return FIA_ERR_NULL_ARG;
+    if (p->quant_tile != 64) return FIA_ERR_BAD_SHAPE;
+    if (p->head_dim % 64) return FIA_ERR_BAD_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(p->k_scale) & 7u) ||
+        (reinterpret_cast<uintptr_t>(p->v_scale) & 7u))
+      return FIA_ERR_BAD_SHAPE;
+  }
+  if (p->block_table) {
+    if (!p->seqused_kv) return FIA_ERR_NULL_ARG;
+    if (p->block_size <= 0 || p->block_size % 16 || p->block_size > 1024) return FIA_ERR_BAD_SHAPE;
+    if (p->kv_dtype == FIA_KV_FP8_E4M3 && (p->block_size % 32 || p->block_size > 512))
+      return FIA_ERR_BAD_SHAPE;
+    if (p->num_blocks <= 0 || p->max_blocks_per_seq <= 0) return FIA_ERR_BAD_SHAPE;
+    if ((int64_t)p->num_blocks * p->block_size > INT32_MAX) return FIA_ERR_BAD_SHAPE;
+    if ((int64_t)p->max_blocks_per_seq * p->block_size > 20971520) return FIA_ERR_BAD_SHAPE;
+  } else {
+    if (p->max_seqlen_kv < 0 || p->max_seqlen_kv > 20971520) return FIA_ERR_BAD_SHAPE;
+    if ((int64_t)p->batch * p->max_seqlen_kv > INT32_MAX) return FIA_ERR_BAD_SHAPE;
+  }
+  // what is built
+  if (p->head_dim != 64 && p->head_dim != 128) return FIA_ERR_UNSUPPORTED;
+  if (p->kv_dtype == FIA_KV_FP8_E4M3 && (p->head_dim != 128 || !is_decode(p)))
+    return FIA_ERR_UNSUPPORTED;
+  if (!is_decode(p) && p->max_seqlen_q > 1) return FIA_ERR_UNSUPPORTED;  // prefill: see below
+  return FIA_OK;
+}
+
+int64_t kv_capacity(const fia_params* p) {
+  return p->block_table ? (int64_t)p->max_blocks_per_seq * p->block_size : p->max_seqlen_kv;
+}
+
+struct DecodePlan {
+  int n;
+  int64_t U;
+  int64_t off_prefix, off_beg, off_cnt, off_part, total;
+};
+
+fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
+  int n;
+  fia_status st = sm_count(p->num_sms, &n);
+  if (st != FIA_OK) return st;
+  const int G = p->num_q_heads / p->num_kv_heads;
+  const int HG = (int)ceil_div(G, kHeadGroup);
+  pl->n = n;
+  pl->U = (int64_t)p->batch * p->num_kv_heads * HG;
+  int64_t off = kAlign;  // [0, 256): error word
+  pl->off_prefix = off;
+  off = align_up(off + 8 * (pl->U + 1));
+  pl->off_beg = off;
+  off = align_up(off + 8 * ((int64_t)n + 1));
+  pl->off_cnt = off;
+  off = align_up(off + 4 * pl->U);
+  pl->off_part = off;
+  off = align_up(off + 4 * (int64_t)2 * n * kHeadGroup * (p->head_dim + 2));
+  pl->total = off;
+  return FIA_OK;
+}
+
+DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
+  DecodeArgs a;
+  memset(&a, 0, sizeof a);
+  const int G = p->num_q_heads / p->num_kv_heads;
+  a.B = p->batch;
+  a.QN = p->num_q_heads;
+  a.KVN = p->num_kv_heads;
+  a.D = p->head_dim;
+  a.G = G;
+  a.HG = (int)ceil_div(G, kHeadGroup);
+  a.layout = p->layout;
+  a.S_q = p->layout == FIA_LAYOUT_BSND ? p->max_seqlen_q : 1;
+  a.q = static_cast<const uint16_t*>(p->q);
+  a.q_stride = p->q_token_stride ? p->q_token_stride : (int64_t)p->num_q_heads * p->head_dim;
+  a.out = static_cast<uint16_t*>(p->out);
+  a.out_stride = p->out_token_stride ? p->out_token_stride : (int64_t)p->num_q_heads * p->head_dim;
+  a.lse = p->lse;
+  a.cu_seqlens_q = p->cu_seqlens_q;
+  a.seqused_kv = p->seqused_kv;
+  a.S_kv = p->block_table ? (int)kv_capacity(p) : p->max_seqlen_kv;
+  a.block_table = p->block_table;
+  a.max_blocks = p->max_blocks_per_seq;
+  a.block_size = p->block_table ? p->block_size : 1;
+  a.box_rows = p->block_table ? gcd_i(p->block_size, kKvTile) : kKvTile;
+  a.k_scale = p->k_scale;
+  a.v_scale = p->v_scale;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.mask_mode = p->mask_mode;
+  a.pre_tokens = p->pre_tokens;
+  a.next_tokens = p->next_tokens;
+  a.sinks = p->sinks;
+  a.num_ctas = pl.n;
+  a.num_units = pl.U;
+  char* w = static_cast<char*>(ws);
+  a.unit_prefix = reinterpret_cast<const int64_t*>(w + pl.off_prefix);
+  a.cta_begin = reinterpret_cast<const int64_t*>(w + pl.off_beg);
+  a.counters = reinterpret_cast<int*>(w + pl.off_cnt);
+  a.partials = reinterpret_cast<float*>(w + pl.off_part);
+  a.err = reinterpret_cast<int*>(w);
+  return a;
+}
+
+fia_status kv_maps(const fia_params* p, int box_rows, CUtensorMap* tk, CUtensorMap* tv) {
+  const bool fp8 = p->kv_dtype == FIA_KV_FP8_E4M3;
+  const uint64_t cols = (uint64_t)p->num_kv_heads * p->head_dim;
+  const uint64_t rows = p->block_table ? (uint64_t)p->num_blocks * p->block_size
+                                       : (uint64_t)p->batch * p->max_seqlen_kv;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int es = fp8 ? 1 : 2;
+  const uint32_t bc = fp8 ? 128 : 64;
+  fia_status st = make_map(tk, p->k_cache, dt, es, cols, rows ? rows : 1, bc, (uint32_t)box_rows, cols);
+  if (st != FIA_OK) return st;
+  return make_map(tv, p->v_cache, dt, es, cols, rows ? rows : 1, bc, (uint32_t)box_rows, cols);
+}
+
+bool q_empty(const fia_params* p) {
+  return p->layout == FIA_LAYOUT_TND ? p->total_q == 0 : p->max_seqlen_q == 0;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+const char* fia_status_string(fia_status s) {
+  switch (s) {
+    case FIA_OK: return "FIA_OK";
+    case FIA_ERR_NULL_ARG: return "FIA_ERR_NULL_ARG";
+    case FIA_ERR_BAD_SHAPE: return "FIA_ERR_BAD_SHAPE";
+    case FIA_ERR_BAD_DTYPE: return "FIA_ERR_BAD_DTYPE";
+    case FIA_ERR_UNSUPPORTED: return "FIA_ERR_UNSUPPORTED";
+    case FIA_ERR_WORKSPACE_TOO_SMALL: return "FIA_ERR_WORKSPACE_TOO_SMALL";
+    case FIA_ERR_CUDA: return "FIA_ERR_CUDA";
+    default: return "FIA_ERR_UNKNOWN";
+  }
+}
+
+int32_t fia_abi_version(void) { return FIA_ABI_VERSION; }
+
+size_t fia_sizeof_params(void) { return sizeof(fia_params); }
+size_t fia_sizeof_sparse_params(void) { return sizeof(sparse_attn_params); }
+
+fia_status fia_get_plan_layout(const fia_params* p, fia_plan_layout* out) {
+  if (!out) return FIA_ERR_NULL_ARG;
+  fia_status st = validate(p);
+  if (st != FIA_OK) return st;
+  memset(out, 0, sizeof *out);
+  if (q_empty(p)) {
+    out->total_bytes = kAlign;
+    return FIA_OK;
+  }
+  if (is_decode(p)) {
+    DecodePlan pl;
+    st = decode_plan(p, &pl);
+    if (st != FIA_OK) return st;
+    out->branch = 1;
+    out->num_ctas = pl.n;
+    out->num_units = pl.U;
+    out->unit_prefix_off = pl.off_prefix;
+    out->cta_begin_off = pl.off_beg;
+    out->total_bytes = pl.total;
+    return FIA_OK;
+  }
+  return FIA_ERR_UNSUPPORTED;
+}
+
+fia_status fia_get_workspace_size(const fia_params* p, size_t* bytes) {
+  if (!bytes) return FIA_ERR_NULL_ARG;
+  fia_plan_layout l;
+  fia_status st = fia_get_plan_layout(p, &l);
+  if (st != FIA_OK) return st;
+  *bytes = (size_t)l.total_bytes;
+  return FIA_OK;
+}
+
+fia_status fia_plan(const fia_params* p, void* ws, size_t ws_bytes, void* stream) {
+  fia_plan_layout l;
+  fia_status st = fia_get_plan_layout(p, &l);
+  if (st != FIA_OK) return st;
+  if (!ws || ws_bytes < (size_t)l.total_bytes) return FIA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (q_empty(p)) return FIA_OK;
+  DecodePlan pl;
+  st = decode_plan(p, &pl);
+  if (st != FIA_OK) return st;
+  DecodeArgs a = decode_args(p, pl, ws);
+  if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return FIA_ERR_CUDA;
+  return launch_decode_schedule(a, s) == cudaSuccess ? FIA_OK : FIA_ERR_CUDA;
+}
+
+fia_status fia_execute(const fia_params* p, void* ws, size_t ws_bytes, void* stream) {
+  fia_plan_layout l;
+  fia_status st = fia_get_plan_layout(p, &l);
+  if (st != FIA_OK) return st;
+  if (!ws || ws_bytes < (size_t)l.total_bytes) return FIA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (q_empty(p)) return FIA_OK;
+  DecodePlan pl;
+  st = decode_plan(p, &pl);
+  if (st != FIA_OK) return st;
+  DecodeArgs a = decode_args(p, pl, ws);
+  CUtensorMap tk, tv;
+  st = kv_maps(p, a.box_rows, &tk, &tv);
+  if (st != FIA_OK) return st;
+  return launch_decode(a, tk, tv, p->kv_dtype == FIA_KV_FP8_E4M3, s) == cudaSuccess ? FIA_OK
+                                                                                     : FIA_ERR_CUDA;
+}
+
+fia_status fia_run(const fia_params* p, void* ws, size_t ws_bytes, void* stream) {
+  fia_status st = fia_plan(p, ws, ws_bytes, stream);
+  if (st != FIA_OK) return st;
+  return fia_execute(p, ws, ws_bytes, stream);
+}
+
+fia_status sparse_attn_metadata(const sparse_attn_params* p, int32_t* metadata,
+                                size_t* workspace_bytes, void* stream) {
+  (void)stream;
+  if (!p || !metadata || !workspace_bytes) return FIA_ERR_NULL_ARG;
+  return FIA_ERR_UNSUPPORTED;
+}
+
+fia_status sparse_attn_run(const sparse_attn_params* p, const int32_t* metadata, void* ws,
+                           size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  (void)stream;
+  if (!p || !metadata) return FIA_ERR_NULL_ARG;
+  return FIA_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

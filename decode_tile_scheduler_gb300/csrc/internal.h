@@ -1,0 +1,114 @@
+// internal.h -- argument blocks shared between the host side of libfia
+// (fia_api.cu) and its kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fia {
+
+constexpr int kKvTile = 128;   // KV positions per tile (one split granule)
+constexpr int kQTile = 128;    // query rows per prefill tile
+constexpr int kHeadGroup = 16; // query heads packed per decode unit (mma M)
+
+// Everything the decode schedule and the decode kernel read.
+struct DecodeArgs {
+  int B, QN, KVN, D, G, HG;
+  int layout;            // 0 BSND, 1 TND
+  int S_q;               // BSND query length (1)
+  const uint16_t* q;     // bf16
+  int64_t q_stride;      // elements between tokens
+  uint16_t* out;
+  int64_t out_stride;
+  float* lse;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqused_kv;  // may be null (contiguous: S_kv for every batch)
+  int S_kv;
+  const int32_t* block_table;  // null: contiguous
+  int max_blocks, block_size, box_rows;
+  const float* k_scale;
+  const float* v_scale;
+  float scale_log2;      // scale * log2(e)
+  int mask_mode, pre_tokens, next_tokens;
+  const float* sinks;
+  // plan (workspace)
+  int num_ctas;
+  int64_t num_units;
+  const int64_t* unit_prefix;  // [U+1]
+  const int64_t* cta_begin;    // [n+1]
+  int* counters;               // [U]
+  float* partials;             // [2n][16][D + 2]
+  int* err;
+};
+
+struct PrefillArgs {
+  int B, QN, KVN, D, G, npairs, per_pair;
+  int layout;
+  int S_q;
+  const uint16_t* q;
+  int64_t q_stride;
+  uint16_t* out;
+  int64_t out_stride;
+  float* lse;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqused_kv;
+  int S_kv;
+  const int32_t* block_table;
+  int max_blocks, block_size, box_rows;
+  float scale_log2;
+  int mask_mode, pre_tokens, next_tokens;
+  const float* sinks;
+  int64_t q_rows_total;  // rows of the q tensor view (for the tensor map bound)
+  // plan
+  int num_ctas;
+  int64_t max_units;
+  int64_t* num_units;     // device: units written by the scheduler
+  const int2* unit_list;  // [U] (b, packed(q_tile, hk, pair))
+  int* claim;             // dynamic claim counter
+  int* hist;              // cost histogram scratch
+  int max_cost;
+  int* err;
+};
+
+struct SparseArgs {
+  int B, N1, D, layout, S1;
+  const uint16_t* q;
+  uint16_t* out;
+  float* lse;
+  const uint16_t* ori_kv;
+  const int32_t* ori_block_table;
+  int ori_max_blocks, ori_block_size;
+  const uint16_t* cmp_kv;
+  const int32_t* cmp_block_table;
+  int cmp_max_blocks, cmp_block_size;
+  const int32_t* cmp_sparse_indices;
+  int K2;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqused_kv;
+  const float* sinks;
+  float scale_log2;
+  int cmp_ratio, win_left, win_right;
+  int mode;              // 0 SWA, 1 CSA, 2 HCA
+  int64_t rows;
+  int chunk;
+  int max_chunks;        // partial slots per row
+  float* partials;       // [rows][max_chunks][N1][D + 2]
+  int* err;
+  int num_ctas;
+};
+
+// host launchers (return cudaSuccess or the launch error)
+cudaError_t launch_decode_schedule(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                          int fp8, cudaStream_t s);
+size_t decode_smem_bytes(int D, int fp8);
+
+cudaError_t launch_prefill_schedule(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, cudaStream_t s);
+
+cudaError_t launch_sparse_metadata(const SparseArgs& a, int32_t* md, cudaStream_t s);
+cudaError_t launch_sparse(const SparseArgs& a, const int32_t* md, cudaStream_t s);
+
+}  // namespace fia

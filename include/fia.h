@@ -1,0 +1,268 @@
+/*
+ * fia.h -- C ABI of libfia: fused inference attention over a paged KV cache
+ * for NVIDIA GB300 (sm_103a), and the shared-KV sparse attention variant.
+ *
+ * Operations
+ *   FIA     O = softmax(Q K^T * scale + mask) V, per query head h against KV
+ *           head floor(h / G), G = Q_N / KV_N ("aclnnFusedInferAttentionScoreV5",
+ *           formula section; "...V2": the IncreFlashAttention branch runs when
+ *           the query S is 1, the PromptFlashAttention branch otherwise; GQA
+ *           needs Q_N divisible by KV_N with ratio <= 64).
+ *   SPARSE  O = softmax(Q K~^T * softmax_scale) V~ with K~ = V~ gathered from a
+ *           band window of the original KV and from compressed KV rows
+ *           ("kv_quant_sparse_attn_sharedkv", formula and parameter table;
+ *           "sparse_flash_mla", SWA / CSA / HCA modes).
+ *
+ * Calling convention (two phases, as on the pages: a first call checks the
+ * inputs and sizes the workspace, a second call executes):
+ *   fia_get_workspace_size -> fia_run        (fia_run = fia_plan + fia_execute)
+ *   sparse_attn_metadata   -> sparse_attn_run
+ * Every pointer in a params struct is a DEVICE pointer unless stated
+ * otherwise.  The caller owns every buffer; the library never allocates,
+ * never synchronises the host and launches only on the given stream, so the
+ * execute calls can be captured in a CUDA graph.  All functions return a
+ * status code; no C++ exception crosses this boundary.  `stream` is a
+ * cudaStream_t passed as void* (NULL = the legacy default stream).
+ *
+ * Readings where the pages are silent (they are restated in the design notes):
+ *  - query rows are aligned to the bottom-right corner of the score matrix:
+ *    row i of a sequence sits at KV position p = kv_len - q_len + i;
+ *  - mask modes: 0 none; 3 right-down causal (j <= p); 4 band
+ *    (p - pre_tokens <= j <= p + next_tokens);
+ *  - a sink is one extra logit per query head that enters the softmax
+ *    denominator only (not multiplied by scale, carries no value); lse
+ *    includes it;
+ *  - a row that sees no key (empty KV, or fully masked) gets O = 0 and
+ *    lse = +inf, with or without a sink ("...V4" empty-tensor rule; "...V2"
+ *    invalid-row correction);
+ *  - FP8 KV: E4M3 codes with one fp32 scale per 64 consecutive elements of D,
+ *    value = code * scale.
+ */
+#ifndef FIA_H_
+#define FIA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FIA_ABI_VERSION 1
+
+/* Status codes ("...V5" two-phase API: the first phase validates the inputs
+ * and reports errors before anything is launched). */
+typedef int fia_status;
+#define FIA_OK 0
+#define FIA_ERR_NULL_ARG 1            /* a required pointer is NULL                  */
+#define FIA_ERR_BAD_SHAPE 2           /* a size, stride, alignment or attribute is   */
+                                      /* out of range or inconsistent                */
+#define FIA_ERR_BAD_DTYPE 3           /* unknown kv_dtype                            */
+#define FIA_ERR_UNSUPPORTED 4         /* valid on the pages, not built here          */
+#define FIA_ERR_WORKSPACE_TOO_SMALL 5 /* workspace NULL or smaller than required     */
+#define FIA_ERR_CUDA 6                /* a CUDA runtime/driver call failed           */
+
+#define FIA_LAYOUT_BSND 0 /* q/out [B, S, N, D]                                   */
+#define FIA_LAYOUT_TND 1  /* q/out [T, N, D] with cu_seqlens_q [B+1]               */
+
+#define FIA_KV_BF16 0
+#define FIA_KV_FP8_E4M3 1
+
+#define FIA_MASK_NONE 0
+#define FIA_MASK_RIGHT_DOWN_CAUSAL 3
+#define FIA_MASK_BAND 4
+
+/* Fused inference attention parameters.
+ *
+ * Shapes and limits ("...V2", restrictions when Q_S > 1: B <= 65536, N <= 256,
+ * D <= 512, S <= 20M; GQA ratio <= 64).  Built here: D in {64, 128}.
+ *
+ * KV cache ("...V2" page-attention scenario; "...V5" Paged Attention group):
+ *  - paged (block_table != NULL): k_cache/v_cache are pools
+ *    [num_blocks, block_size, KV_N, D] (BnBsH); logical row j of batch b is
+ *    pool row block_table[b*max_blocks_per_seq + j/block_size]*block_size
+ *    + j%block_size.  Block ids are not validated; table entries past a
+ *    sequence's last block are never read.  seqused_kv is required.
+ *    block_size: multiple of 16, <= 1024 (FP8: multiple of 32, <= 512).
+ *  - contiguous (block_table == NULL): k_cache/v_cache are [B, max_seqlen_kv,
+ *    KV_N, D]; seqused_kv optional (default max_seqlen_kv for every batch).
+ *  - FP8: k_scale/v_scale fp32 with the same leading shape and D/64 in place
+ *    of D ([num_blocks, block_size, KV_N, D/64] or [B, S_kv, KV_N, D/64]).
+ * Alignment: q, out, k_cache, v_cache 16-byte aligned; token strides multiples
+ * of 8 elements. */
+typedef struct fia_params {
+    int32_t batch;            /* B                                             */
+    int32_t num_q_heads;      /* Q_N                                           */
+    int32_t num_kv_heads;     /* KV_N                                          */
+    int32_t head_dim;         /* D                                             */
+    int32_t layout;           /* FIA_LAYOUT_*                                  */
+    int32_t max_seqlen_q;     /* BSND: S_q.  TND: upper bound of the query     */
+                              /* lengths (1 selects the decode branch)         */
+    int32_t total_q;          /* TND: T (rows of q and out); BSND: ignored     */
+    int32_t pad0_;
+    const void *q;            /* bf16                                          */
+    void *out;                /* bf16, same layout and strides as q            */
+    float *lse;               /* fp32, nullable: BSND [B,Q_N,S_q,1],           */
+                              /* TND [T,Q_N,1]                                 */
+    int64_t q_token_stride;   /* elements between tokens of q (0: Q_N*D)       */
+    int64_t out_token_stride; /* elements between tokens of out (0: Q_N*D)     */
+    const void *k_cache;
+    const void *v_cache;
+    const float *k_scale;     /* FP8 only                                      */
+    const float *v_scale;     /* FP8 only                                      */
+    int32_t kv_dtype;         /* FIA_KV_*                                      */
+    int32_t quant_tile;       /* FP8: 64                                       */
+    const int32_t *block_table;   /* int32 [B, max_blocks_per_seq] or NULL     */
+    int32_t max_blocks_per_seq;
+    int32_t block_size;
+    int32_t num_blocks;
+    int32_t max_seqlen_kv;    /* contiguous KV: S_kv; paged: ignored           */
+    const int32_t *cu_seqlens_q;  /* TND: int32 [B+1], non-decreasing, last=T */
+    const int32_t *seqused_kv;    /* int32 [B]: KV length of each batch        */
+    float scale;              /* multiplies Q K^T (typically 1/sqrt(D))         */
+    int32_t mask_mode;        /* FIA_MASK_*                                    */
+    int32_t pre_tokens;       /* band: keys before p (may be negative)         */
+    int32_t next_tokens;      /* band: keys after p;  pre + next >= 0          */
+    const float *sinks;       /* fp32 [Q_N] or NULL                            */
+    int32_t num_sms;          /* persistent CTAs; 0 = the device's SM count    */
+    int32_t reserved[7];      /* must be 0                                     */
+} fia_params;
+
+/* Returns a static string naming a status code. */
+const char *fia_status_string(fia_status s);
+
+/* Version of this ABI (FIA_ABI_VERSION). */
+int32_t fia_abi_version(void);
+
+/* sizeof(fia_params) and sizeof(sparse_attn_params) as compiled into the
+ * library, so that a binding can check its mirror of the structs. */
+size_t fia_sizeof_params(void);
+size_t fia_sizeof_sparse_params(void);
+
+/* Phase 1 ("...V5": the GetWorkspaceSize call validates the inputs and
+ * computes the workspace).  Host-only, pure, idempotent: reads only the
+ * struct's scalar fields and checks pointers for NULL and alignment (it never
+ * dereferences a device pointer).  *bytes receives the workspace size that
+ * fia_plan / fia_execute / fia_run need; the size depends only on scalar
+ * fields, never on device-side lengths. */
+fia_status fia_get_workspace_size(const fia_params *p, size_t *bytes);
+
+/* Phase 2a: launch the tile scheduler on `stream`.  It reads the device-side
+ * lengths (seqused_kv, cu_seqlens_q) and writes into `workspace` the balanced
+ * split of (batch, kv-head, q-tile, kv-split) work items across persistent
+ * CTAs, and resets the counters fia_execute uses.  The plan stays valid for
+ * later fia_execute calls with the same shapes and lengths (e.g. every layer
+ * of a model step). */
+fia_status fia_plan(const fia_params *p, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/* Phase 2b: launch the attention kernels on `stream` using the plan in
+ * `workspace`.  Writes every element of out (and lse when non-NULL).
+ * Deterministic: the same inputs give bitwise the same outputs. */
+fia_status fia_execute(const fia_params *p, void *workspace, size_t workspace_bytes,
+                       void *stream);
+
+/* Phase 2: fia_plan followed by fia_execute. */
+fia_status fia_run(const fia_params *p, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace layout of the plan, for inspection (host-only). */
+typedef struct fia_plan_layout {
+    int32_t branch;           /* 1 decode (split-KV), 2 prefill                */
+    int32_t num_ctas;         /* persistent CTAs                               */
+    int64_t num_units;        /* work units                                    */
+    int64_t unit_prefix_off;  /* decode: int64 [num_units+1] cost prefix       */
+    int64_t cta_begin_off;    /* decode: int64 [num_ctas+1] cost interval      */
+    int64_t unit_list_off;    /* prefill: int32 [num_units][2] ordered units   */
+    int64_t total_bytes;
+} fia_plan_layout;
+fia_status fia_get_plan_layout(const fia_params *p, fia_plan_layout *layout);
+
+/* ------------------------------------------------------------------------ */
+/* shared-KV sparse attention                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Parameters ("kv_quant_sparse_attn_sharedkv" parameter table and
+ * constraints; "sparse_flash_mla" modes):
+ *  - q bf16 BSND [B, S1, N1, D] or TND [T1, N1, D]; out the same; KV_N = 1.
+ *  - ori_kv bf16 [ori_num_blocks, ori_block_size, 1, D] with ori_block_table
+ *    int32 [B, >= ceil(S2_max/ori_block_size)] (required).
+ *  - cmp_kv bf16 [cmp_num_blocks, cmp_block_size, 1, D] with cmp_block_table
+ *    int32 [B, >= ceil(floor(S2_max/cmp_ratio)/cmp_block_size)]; NULL for SWA.
+ *  - cmp_sparse_indices int32 [rows, 1, topk]: logical compressed rows, valid
+ *    entries first, -1 after; NULL with cmp_kv given selects HCA (every
+ *    causally visible compressed row).
+ *  - seqused_kv int32 [B]: S2 of each batch (required).
+ *  - query row i of batch b sits at p = S2 - q_len + i; window rows
+ *    p - ori_win_left .. p + ori_win_right of ori_kv; compressed row c is
+ *    visible iff (c+1)*cmp_ratio <= p+1.
+ *  - sinks fp32 [N1] or NULL; lse fp32 [B, 1, S1, N1] / [1, T1, N1] or NULL.
+ * Built here: D = 512 (the pages' only value) and D in {128, 256}; N1 a power
+ * of two <= 128; block sizes multiples of 16, <= 1024; topk <= 2048. */
+typedef struct sparse_attn_params {
+    int32_t batch;            /* B                                             */
+    int32_t num_q_heads;      /* N1                                            */
+    int32_t head_dim;         /* D                                             */
+    int32_t layout;           /* FIA_LAYOUT_BSND | FIA_LAYOUT_TND              */
+    int32_t max_seqlen_q;     /* BSND: S1; TND: upper bound of query lengths   */
+    int32_t total_q;          /* TND: T1                                       */
+    const void *q;
+    void *out;
+    float *lse;
+    const void *ori_kv;
+    const int32_t *ori_block_table;
+    int32_t ori_max_blocks;
+    int32_t ori_block_size;
+    int32_t ori_num_blocks;
+    int32_t pad0_;
+    const void *cmp_kv;
+    const int32_t *cmp_block_table;
+    int32_t cmp_max_blocks;
+    int32_t cmp_block_size;
+    int32_t cmp_num_blocks;
+    int32_t topk;             /* K2 (CSA)                                      */
+    const int32_t *cmp_sparse_indices;
+    const int32_t *cu_seqlens_q;  /* TND [B+1]                                 */
+    const int32_t *seqused_kv;    /* [B]                                       */
+    const float *sinks;
+    float softmax_scale;
+    int32_t cmp_ratio;        /* 1 for SWA; 4 (CSA) or 128 (HCA) on the pages  */
+    int32_t ori_win_left;     /* 127 on the pages                              */
+    int32_t ori_win_right;    /* 0 on the pages                                */
+    int32_t num_sms;          /* CTAs of the split; 0 = the device's SM count  */
+    int32_t reserved[7];      /* must be 0                                     */
+} sparse_attn_params;
+
+/* Metadata step ("sparse_flash_mla_metadata": generates, before the main call,
+ * the task list of every core: where in (batch/query row, KV chunk) its work
+ * starts and ends; "kv_quant_sparse_attn_sharedkv": metadata int32 [1024]).
+ * Validates p, launches the scheduler kernel on `stream`, which writes
+ * `metadata` (device int32 [1024]), and stores the workspace size that
+ * sparse_attn_run needs in *workspace_bytes (host).  Layout of metadata:
+ *   [0] 0x46534D31  [1] n = CTAs  [2] units (query rows)  [3] chunk rows
+ *   [4] total chunks  [5] B  [6] N1  [7] topk  [8] cmp_ratio  [9] win_left
+ *   [10] win_right  [11] mode (0 SWA, 1 CSA, 2 HCA)  [12..15] 0
+ *   [16+2c], [17+2c]: (query row, chunk) where CTA c begins, c = 0..n
+ *   remaining entries 0.
+ * The concatenated K~ of a query row is cut into fixed chunks of `chunk`
+ * logical positions: ceil(W/chunk) window chunks (W = win_left + win_right
+ * + 1) then ceil(kc/chunk) compressed chunks (kc = visible compressed rows,
+ * capped at topk for CSA; 0 for SWA).  CTA c takes the chunk interval
+ * [floor(c*total/n), floor((c+1)*total/n)).  Chunk boundaries do not depend
+ * on the other rows of the batch, so results are batch invariant
+ * ("sparse_flash_mla": deterministic and batch invariant by default).  n is
+ * capped at 503 so that the list fits. */
+fia_status sparse_attn_metadata(const sparse_attn_params *p, int32_t *metadata,
+                                size_t *workspace_bytes, void *stream);
+
+/* Main call: launches the gather-attention kernel and the chunk combine on
+ * `stream`.  `metadata` must come from sparse_attn_metadata with the same
+ * shapes; a header mismatch (B, N1, topk, units) is detected on the device and
+ * leaves out/lse untouched... it is reported by sparse_attn_check_metadata. */
+fia_status sparse_attn_run(const sparse_attn_params *p, const int32_t *metadata,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FIA_H_ */

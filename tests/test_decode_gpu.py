@@ -1,0 +1,139 @@
+"""GPU parity of the decode branch (query length 1) against the fp64 oracle,
+through the C ABI: bf16 and FP8 KV, GQA groups, block sizes, mask modes,
+sinks, empty and ragged KV, forced split-KV (few CTAs / many CTAs), the paged
+GQA decode workload at full size, bit-exact schedule metadata, determinism."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import fia_inputs as fi
+import oracle
+from helpers import check_close
+
+pytestmark = pytest.mark.gpu
+
+dev = "cuda"
+
+
+def _run(p, num_sms=0):
+    import decode_tile_scheduler_gb300 as fia
+    c = fia.FiaCall(p, with_lse=True, num_sms=num_sms)
+    out, lse = c.run()
+    torch.cuda.synchronize()
+    assert c.error_word() == 0
+    return c, out, lse
+
+
+def _ref(p):
+    return oracle.fia(p.to("cpu"))
+
+
+CASES = {
+    "gqa4_bs128": dict(B=3, QN=8, KVN=2, D=128, kv_lens=[700, 1, 300], block_size=128),
+    "gqa1_d64_bs16": dict(B=2, QN=4, KVN=4, D=64, kv_lens=[33, 200], block_size=16),
+    "gqa8_bs48": dict(B=2, QN=16, KVN=2, D=128, kv_lens=[257, 129], block_size=48),
+    "gqa32_two_groups": dict(B=2, QN=32, KVN=1, D=128, kv_lens=[300, 77], block_size=64),
+    "gqa20_ragged_group": dict(B=1, QN=20, KVN=1, D=64, kv_lens=[150], block_size=32),
+    "empty_kv": dict(B=3, QN=4, KVN=2, D=128, kv_lens=[0, 5, 0], block_size=16),
+    "sinks": dict(B=2, QN=8, KVN=2, D=128, kv_lens=[513, 64], block_size=128, with_sinks=True),
+    "band": dict(B=2, QN=8, KVN=2, D=128, kv_lens=[1000, 90], block_size=32, mask_mode=4,
+                 pre_tokens=300, next_tokens=0),
+    "band_neg_pre": dict(B=2, QN=4, KVN=2, D=64, kv_lens=[500, 3], block_size=16, mask_mode=4,
+                         pre_tokens=-1, next_tokens=5),
+    "causal": dict(B=2, QN=4, KVN=1, D=128, kv_lens=[129, 128], block_size=128, mask_mode=3),
+    "contiguous": dict(B=2, QN=8, KVN=2, D=128, kv_lens=[200, 17], paged=False),
+    "fp8": dict(B=3, QN=16, KVN=2, D=128, kv_lens=[1000, 31, 257], block_size=64,
+                kv_dtype=fi.KV_FP8_E4M3),
+    "fp8_sinks_band": dict(B=2, QN=8, KVN=1, D=128, kv_lens=[3000, 200], block_size=32,
+                           kv_dtype=fi.KV_FP8_E4M3, with_sinks=True, mask_mode=4,
+                           pre_tokens=1000, next_tokens=0),
+    "fp8_contiguous": dict(B=2, QN=8, KVN=2, D=128, kv_lens=[100, 300], paged=False,
+                           kv_dtype=fi.KV_FP8_E4M3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("num_sms", [0, 3])
+def test_decode_matches_oracle(name, num_sms):
+    kw = dict(q_lens=None, seed=zlib.crc32(name.encode()) % 1000, device=dev)
+    kw.update(CASES[name])
+    kw["q_lens"] = [1] * kw["B"]
+    p = fi.make_fia(**kw)
+    _, out, lse = _run(p, num_sms)
+    ro, rl = _ref(p)
+    check_close(out, lse, ro, rl, name)
+
+
+def test_decode_tnd_layout_with_empty_query_rows():
+    p = fi.make_fia(B=3, QN=8, KVN=2, D=128, q_lens=[1, 0, 1], kv_lens=[300, 50, 7],
+                    layout=fi.LAYOUT_TND, block_size=32, seed=5, device=dev)
+    _, out, lse = _run(p)
+    ro, rl = _ref(p)
+    check_close(out, lse, ro, rl, "tnd")
+
+
+@pytest.mark.parametrize("num_sms", [1, 2, 7, 64, 152, 500])
+def test_split_kv_combine_any_cta_count(num_sms):
+    p = fi.make_fia(B=4, QN=16, KVN=4, D=128, q_lens=[1] * 4, kv_lens=[2000, 130, 1, 900],
+                    block_size=64, with_sinks=True, seed=11, device=dev)
+    _, out, lse = _run(p, num_sms)
+    ro, rl = _ref(p)
+    check_close(out, lse, ro, rl, f"ctas={num_sms}")
+
+
+def test_schedule_metadata_bit_exact():
+    import decode_tile_scheduler_gb300 as fia
+    p = fi.make_fia(B=6, QN=32, KVN=2, D=128, q_lens=[1] * 6, kv_lens=[0, 5000, 1, 128, 129, 3001],
+                    block_size=16, seed=3, device=dev)
+    for n in (1, 5, 152, 333):
+        c, _, _ = _run(p, n)
+        lay = c.plan_layout()
+        ws = c.ws.cpu()
+        U = lay.num_units
+        pre = ws[lay.unit_prefix_off: lay.unit_prefix_off + 8 * (U + 1)].view(torch.int64).numpy()
+        beg = ws[lay.cta_begin_off: lay.cta_begin_off + 8 * (n + 1)].view(torch.int64).numpy()
+        rpre, rbeg, total = oracle.decode_schedule(p.to("cpu"), n)
+        assert np.array_equal(pre, rpre)
+        assert np.array_equal(beg, rbeg)
+
+
+def test_deterministic_bitwise():
+    p = fi.make_fia(B=5, QN=32, KVN=8, D=128, q_lens=[1] * 5, kv_lens=[4000, 700, 1, 129, 2500],
+                    block_size=128, seed=9, device=dev)
+    _, o1, l1 = _run(p)
+    o1, l1 = o1.clone(), l1.clone()
+    _, o2, l2 = _run(p)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_poisoned_unused_pages_never_reach_the_output():
+    # every row past kv_len in the pool is NaN (generator poison); also the
+    # table slots past each sequence's last block point at a NaN block
+    p = fi.make_fia(B=4, QN=8, KVN=2, D=128, q_lens=[1] * 4, kv_lens=[17, 129, 255, 1],
+                    block_size=16, seed=13, device=dev)
+    _, out, lse = _run(p)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+def test_paged_gqa_decode_workload_full_size():
+    p = fi.workload_paged_decode(device=dev)
+    _, out, lse = _run(p)
+    ro, rl = _ref(p)
+    check_close(out, lse, ro, rl, "paged GQA decode")
+
+
+def test_fp8_long_decode_workload_sampled():
+    p = fi.workload_fp8_long_decode(device=dev)
+    _, out, lse = _run(p)
+    pc = p.to("cpu")
+    g = np.random.default_rng(0)
+    rows = g.integers(0, p.B, 24)
+    heads = g.integers(0, p.QN, 24)
+    ro, rl = oracle.fia_sample(pc, rows, heads)
+    o = out.float().cpu().numpy().reshape(p.B, p.QN, p.D)
+    l = lse.cpu().numpy().reshape(p.B, p.QN)
+    err = np.abs(o[rows, heads] - ro)
+    assert err.max() <= 2e-2 and err.mean() <= 2e-3
+    assert np.abs(l[rows, heads] - rl).max() <= 1e-3

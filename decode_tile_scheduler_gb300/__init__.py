@@ -10,7 +10,7 @@ from ._abi import (  # noqa: F401
     EXPORTS, FIA_ERR_BAD_DTYPE, FIA_ERR_BAD_SHAPE, FIA_ERR_CUDA, FIA_ERR_NULL_ARG, FIA_ERR_UNSUPPORTED,
     FIA_ERR_WORKSPACE_TOO_SMALL, FIA_OK, KV_BF16, KV_FP8_E4M3, LAYOUT_BSND, LAYOUT_TND, MASK_BAND,
     MASK_NONE, MASK_RIGHT_DOWN_CAUSAL, FiaError, FiaParams, FiaPlanLayout, SparseParams,
-    fia_execute, fia_get_plan_layout, fia_get_workspace_size, fia_plan, fia_run, lib, lib_path,
+    fia_decode_run_noalloc, fia_execute, fia_get_plan_layout, fia_get_workspace_size, fia_plan, fia_run, lib, lib_path,
     sparse_attn_metadata, sparse_attn_run, status_string)
 from ._build import build  # noqa: F401
 from .api import (  # noqa: F401

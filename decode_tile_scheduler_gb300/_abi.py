@@ -77,8 +77,9 @@ class FiaPlanLayout(ctypes.Structure):
 EXPORTS = (
     "fia_status_string", "fia_abi_version", "fia_sizeof_params", "fia_sizeof_sparse_params",
     "fia_get_workspace_size", "fia_plan", "fia_execute", "fia_run", "fia_get_plan_layout",
-    "sparse_attn_metadata", "sparse_attn_run",
+    "sparse_attn_metadata", "sparse_attn_run", "fia_decode_run_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class FiaError(RuntimeError):
@@ -124,6 +125,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
                                                ctypes.POINTER(ctypes.c_size_t), _P]
             L.sparse_attn_run.argtypes = [ctypes.POINTER(SparseParams), _P, _P, ctypes.c_size_t,
                                           _P]
+            L.fia_decode_run_noalloc.argtypes = [ctypes.POINTER(FiaParams), _P]
             for f in EXPORTS:
                 if f not in ("fia_status_string", "fia_abi_version", "fia_sizeof_params",
                              "fia_sizeof_sparse_params"):
@@ -168,6 +170,10 @@ def fia_execute(p: FiaParams, ws: int, nbytes: int, stream: int = 0):
 
 def fia_run(p: FiaParams, ws: int, nbytes: int, stream: int = 0):
     _check(lib().fia_run(ctypes.byref(p), ws, nbytes, stream), "fia_run")
+
+
+def fia_decode_run_noalloc(p: FiaParams, stream: int = 0):
+    _check(lib().fia_decode_run_noalloc(ctypes.byref(p), stream), "fia_decode_run_noalloc")
 
 
 def sparse_attn_metadata(p: SparseParams, metadata: int, stream: int = 0) -> int:

@@ -165,6 +165,27 @@ fia_status fia_execute(const fia_params *p, void *workspace, size_t workspace_by
 /* Phase 2: fia_plan followed by fia_execute. */
 fia_status fia_run(const fia_params *p, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Decode without a workspace.  The pages have no counterpart to this call; it
+ * exists for callers that cannot allocate device memory when they run
+ * attention (a device fully owned by another component's memory pool, a host
+ * process that forbids allocations after start-up, a latency-critical path
+ * that must not touch the allocator).  It behaves like fia_run on the decode
+ * branch (max_seqlen_q == 1) but keeps the scheduler's scratch -- the plan,
+ * the split-KV counters and the partial slots -- in a device array of
+ * FIA_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
+ * loads libfia holds until the process exits.  It allocates nothing.
+ *  - Returns FIA_ERR_WORKSPACE_TOO_SMALL, before launching anything, when the
+ *    decode plan needs more than FIA_NOALLOC_SCRATCH_BYTES (what fia_get_
+ *    workspace_size reports for the same params), FIA_ERR_UNSUPPORTED for the
+ *    prefill branch, and any status fia_run returns.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents; every value that must start at zero is reset by the call.
+ *    Calls that overlap on the GPU (unordered streams) race on the array. */
+#define FIA_NOALLOC_SCRATCH_BYTES (8u << 20)
+fia_status fia_decode_run_noalloc(const fia_params *p, void *stream);
+
 /* Workspace layout of the plan, for inspection (host-only). */
 typedef struct fia_plan_layout {
     int32_t branch;           /* 1 decode (split-KV), 2 prefill                */

@@ -4,7 +4,8 @@ U[512,4096], block 128, permuted pages) through libfia on one GB300 per rank.
 A step is one fia_run (tile scheduler + split-KV decode with its in-kernel
 combine) over the whole batch, inputs resident in HBM.  `value` is KV GB/s:
 the algorithmic bytes (every visible K and V row once) over the step time.
-Between timed steps L2 is flushed by writing a buffer of twice its size.
+Between timed steps L2 is flushed: a buffer of twice its size is written, then
+another of the same size is read, so no dirty line is written back in a step.
 
 Extra lines of evidence in the same JSON object: the decode kernel's own
 roofline (CUDA events around fia_execute on the launching stream), the
@@ -142,9 +143,25 @@ def _max_over_ranks(x, ws):
     return float(t.item())
 
 
+class L2Flush:
+    """Evicts L2 between timed steps: writes a buffer of twice the L2 size, then
+    reads a second one of the same size, so that L2 ends up holding only clean
+    lines and no write-back of the flush itself lands inside a timed step."""
+
+    def __init__(self):
+        l2 = torch.cuda.get_device_properties(0).L2_cache_size
+        n = max(2 * l2, 256 << 20) // 4
+        self.w = torch.empty(n, dtype=torch.float32, device="cuda")
+        self.r = torch.ones(n, dtype=torch.float32, device="cuda")
+        self.sink = torch.empty(1, dtype=torch.float32, device="cuda")
+
+    def zero_(self):
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink[0])
+
+
 def _flush_buf():
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    return torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+    return L2Flush()
 
 
 def _time_steps(fn_plan, fn_exec, steps, flush):
@@ -362,7 +379,7 @@ def run_fia(args):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "l2": "flushed between timed steps (2x L2 write)",
+            "config": {"workload": WORKLOAD, "l2": "flushed between timed steps (write 2x L2, then read another 2x L2 buffer)",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "algorithmic_bytes_per_step": by},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],

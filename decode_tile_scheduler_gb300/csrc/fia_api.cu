@@ -161,7 +161,7 @@ fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
   fia_status st = sm_count(p->num_sms, &n);
   if (st != FIA_OK) return st;
   const int G = p->num_q_heads / p->num_kv_heads;
-  const int HG = (int)ceil_div(G, kHeadGroup);
+  const int HG = (int)ceil_div(G, decode_group_heads(G));
   pl->n = n;
   pl->U = (int64_t)p->batch * p->num_kv_heads * HG;
   int64_t off = kAlign;  // [0, 256): error word
@@ -172,7 +172,7 @@ fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
   pl->off_cnt = off;
   off = align_up(off + 4 * pl->U);
   pl->off_part = off;
-  off = align_up(off + 4 * (int64_t)2 * n * kHeadGroup * (p->head_dim + 2));
+  off = align_up(off + 4 * (int64_t)2 * n * kMaxHeadGroup * (p->head_dim + 2));
   pl->total = off;
   return FIA_OK;
 }
@@ -186,7 +186,8 @@ DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
   a.KVN = p->num_kv_heads;
   a.D = p->head_dim;
   a.G = G;
-  a.HG = (int)ceil_div(G, kHeadGroup);
+  a.GH = decode_group_heads(G);
+  a.HG = (int)ceil_div(G, a.GH);
   a.layout = p->layout;
   a.S_q = p->layout == FIA_LAYOUT_BSND ? p->max_seqlen_q : 1;
   a.q = static_cast<const uint16_t*>(p->q);
@@ -305,7 +306,6 @@ fia_status fia_plan(const fia_params* p, void* ws, size_t ws_bytes, void* stream
   st = decode_plan(p, &pl);
   if (st != FIA_OK) return st;
   DecodeArgs a = decode_args(p, pl, ws);
-  if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return FIA_ERR_CUDA;
   return launch_decode_schedule(a, s) == cudaSuccess ? FIA_OK : FIA_ERR_CUDA;
 }
 

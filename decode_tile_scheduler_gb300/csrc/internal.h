@@ -10,11 +10,14 @@ namespace fia {
 
 constexpr int kKvTile = 128;   // KV positions per tile (one split granule)
 constexpr int kQTile = 128;    // query rows per prefill tile
-constexpr int kHeadGroup = 16; // query heads packed per decode unit (mma M)
+constexpr int kMaxHeadGroup = 16;  // query heads packed per decode unit, at most
+
+// Query heads per decode unit: the GQA group in mma N columns of 8.
+inline int decode_group_heads(int G) { return G <= 8 ? 8 : 16; }
 
 // Everything the decode schedule and the decode kernel read.
 struct DecodeArgs {
-  int B, QN, KVN, D, G, HG;
+  int B, QN, KVN, D, G, GH, HG;  // GH heads per unit, HG units per GQA group
   int layout;            // 0 BSND, 1 TND
   int S_q;               // BSND query length (1)
   const uint16_t* q;     // bf16
@@ -38,7 +41,7 @@ struct DecodeArgs {
   const int64_t* unit_prefix;  // [U+1]
   const int64_t* cta_begin;    // [n+1]
   int* counters;               // [U]
-  float* partials;             // [2n][16][D + 2]
+  float* partials;             // [2n][16][D + 2]: acc, then m and l
   int* err;
 };
 

@@ -14,8 +14,8 @@
 //
 // The array is shared by all calls on a device and keeps the previous call's
 // contents.  Everything that must start at zero is cleared by the call itself
-// (the error word by fia_plan, the split-KV counters by the scheduler kernel),
-// so a stale plan never leaks into a new call; but two calls whose work
+// (the scheduler kernel resets the error word and the split-KV counters), so
+// a stale plan never leaks into a new call; but two calls whose work
 // overlaps on the GPU (different streams without ordering) race on the array.
 #include <mutex>
 

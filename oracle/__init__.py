@@ -280,7 +280,7 @@ def decode_schedule(p, num_ctas: int):
     """(unit_prefix int64 [U+1], cta_begin int64 [n+1], total)."""
     s, keep = _fia_struct(p)
     G = p.QN // p.KVN
-    HG = -(-G // 16)
+    HG = -(-G // (8 if G <= 8 else 16))
     U = p.B * p.KVN * HG
     pre = np.zeros(U + 1, dtype=np.int64)
     beg = np.zeros(num_ctas + 1, dtype=np.int64)

@@ -477,7 +477,6 @@ int64_t oracle_sparse_rows(const oracle_sparse_args *a, int b, int64_t i, int64_
 
 #define OR_KV_TILE 128
 #define OR_Q_TILE 128
-#define OR_DEC_HGROUP 16
 
 static int64_t or_ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -488,7 +487,8 @@ static int64_t or_tiles(int64_t lo, int64_t hi)
     return hi / OR_KV_TILE - lo / OR_KV_TILE + 1;
 }
 
-/* Decode schedule.  Units u = ((b*KVN + hk)*HG + hg), HG = ceil(G/16).  A
+/* Decode schedule.  Units u = ((b*KVN + hk)*HG + hg): the G query heads of a
+ * KV head are taken in groups of GH = 8 (G <= 8) or 16, HG = ceil(G/GH).  A
  * unit whose batch has no query row costs 0; otherwise it costs the number of
  * KV tiles its single query row can see, at least 1.  unit_prefix[u] is the
  * exclusive prefix sum of the costs (U+1 entries), and CTA c of n owns the
@@ -498,7 +498,7 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int64
                                int64_t *cta_begin)
 {
     int G = a->QN / a->KVN;
-    int HG = (int)or_ceil_div(G, OR_DEC_HGROUP);
+    int HG = (int)or_ceil_div(G, G <= 8 ? 8 : 16);
     int64_t U = (int64_t)a->B * a->KVN * HG, u, acc = 0;
     int c;
     for (u = 0; u < U; ++u) {

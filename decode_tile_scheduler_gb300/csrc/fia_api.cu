@@ -142,7 +142,6 @@ fia_status validate(const fia_params* p) {
   if (p->head_dim != 64 && p->head_dim != 128) return FIA_ERR_UNSUPPORTED;
   if (p->kv_dtype == FIA_KV_FP8_E4M3 && (p->head_dim != 128 || !is_decode(p)))
     return FIA_ERR_UNSUPPORTED;
-  if (!is_decode(p) && p->max_seqlen_q > 1) return FIA_ERR_UNSUPPORTED;  // prefill: see below
   return FIA_OK;
 }
 
@@ -233,6 +232,82 @@ fia_status kv_maps(const fia_params* p, int box_rows, CUtensorMap* tk, CUtensorM
   return make_map(tv, p->v_cache, dt, es, cols, rows ? rows : 1, bc, (uint32_t)box_rows, cols);
 }
 
+struct PrefillPlan {
+  int n, per_pair, npairs, max_cost;
+  int64_t U_max;
+  int64_t off_seq, off_hist, off_list, total;
+};
+
+fia_status prefill_plan(const fia_params* p, PrefillPlan* pl) {
+  fia_status st = sm_count(p->num_sms, &pl->n);
+  if (st != FIA_OK) return st;
+  const int G = p->num_q_heads / p->num_kv_heads;
+  pl->per_pair = (G % 2 == 0) ? 2 : 1;
+  pl->npairs = G / pl->per_pair;
+  const int64_t H = (int64_t)p->num_kv_heads * pl->npairs;
+  const int64_t qtiles = p->layout == FIA_LAYOUT_TND
+                             ? ceil_div(p->total_q, kQTile) + p->batch
+                             : (int64_t)p->batch * ceil_div(p->max_seqlen_q, kQTile);
+  pl->U_max = qtiles * H;
+  pl->max_cost = (int)(1 + ceil_div(kv_capacity(p), kKvTile));
+  int64_t off = kAlign;  // [0,4) error word, [4,8) claim counter, [8,16) units
+  pl->off_seq = off;
+  off = align_up(off + 8 * ((int64_t)p->batch + 1));
+  pl->off_hist = off;
+  off = align_up(off + 4 * ((int64_t)pl->max_cost + 2));
+  pl->off_list = off;
+  off = align_up(off + 8 * pl->U_max);
+  pl->total = off;
+  return FIA_OK;
+}
+
+PrefillArgs prefill_args(const fia_params* p, const PrefillPlan& pl, void* ws) {
+  PrefillArgs a;
+  memset(&a, 0, sizeof a);
+  a.B = p->batch;
+  a.QN = p->num_q_heads;
+  a.KVN = p->num_kv_heads;
+  a.D = p->head_dim;
+  a.G = p->num_q_heads / p->num_kv_heads;
+  a.npairs = pl.npairs;
+  a.per_pair = pl.per_pair;
+  a.layout = p->layout;
+  a.S_q = p->max_seqlen_q;
+  a.out = static_cast<uint16_t*>(p->out);
+  a.out_stride = p->out_token_stride ? p->out_token_stride : (int64_t)p->num_q_heads * p->head_dim;
+  a.lse = p->lse;
+  a.cu_seqlens_q = p->cu_seqlens_q;
+  a.seqused_kv = p->seqused_kv;
+  a.S_kv = p->block_table ? (int)kv_capacity(p) : p->max_seqlen_kv;
+  a.block_table = p->block_table;
+  a.max_blocks = p->max_blocks_per_seq;
+  a.block_size = p->block_table ? p->block_size : 1;
+  a.box_rows = p->block_table ? gcd_i(p->block_size, kKvTile) : kKvTile;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.mask_mode = p->mask_mode;
+  a.pre_tokens = p->pre_tokens;
+  a.next_tokens = p->next_tokens;
+  a.sinks = p->sinks;
+  a.num_ctas = pl.n;
+  a.max_cost = pl.max_cost;
+  char* w = static_cast<char*>(ws);
+  a.err = reinterpret_cast<int*>(w);
+  a.claim = reinterpret_cast<int*>(w + 4);
+  a.num_units = reinterpret_cast<int64_t*>(w + 8);
+  a.seq_prefix = reinterpret_cast<int64_t*>(w + pl.off_seq);
+  a.hist = reinterpret_cast<int*>(w + pl.off_hist);
+  a.unit_list = reinterpret_cast<int2*>(w + pl.off_list);
+  return a;
+}
+
+fia_status q_map(const fia_params* p, CUtensorMap* tq) {
+  const uint64_t cols = (uint64_t)p->num_q_heads * p->head_dim;
+  const uint64_t rows = p->layout == FIA_LAYOUT_TND ? (uint64_t)p->total_q
+                                                    : (uint64_t)p->batch * p->max_seqlen_q;
+  const uint64_t stride = p->q_token_stride ? (uint64_t)p->q_token_stride : cols;
+  return make_map(tq, p->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, 64, 128, stride);
+}
+
 bool q_empty(const fia_params* p) {
   return p->layout == FIA_LAYOUT_TND ? p->total_q == 0 : p->max_seqlen_q == 0;
 }
@@ -283,7 +358,15 @@ fia_status fia_get_plan_layout(const fia_params* p, fia_plan_layout* out) {
     out->total_bytes = pl.total;
     return FIA_OK;
   }
-  return FIA_ERR_UNSUPPORTED;
+  PrefillPlan pp;
+  st = prefill_plan(p, &pp);
+  if (st != FIA_OK) return st;
+  out->branch = 2;
+  out->num_ctas = pp.n;
+  out->num_units = pp.U_max;
+  out->unit_list_off = pp.off_list;
+  out->total_bytes = pp.total;
+  return FIA_OK;
 }
 
 fia_status fia_get_workspace_size(const fia_params* p, size_t* bytes) {
@@ -302,6 +385,13 @@ fia_status fia_plan(const fia_params* p, void* ws, size_t ws_bytes, void* stream
   if (!ws || ws_bytes < (size_t)l.total_bytes) return FIA_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (q_empty(p)) return FIA_OK;
+  if (l.branch == 2) {
+    PrefillPlan pp;
+    st = prefill_plan(p, &pp);
+    if (st != FIA_OK) return st;
+    PrefillArgs a = prefill_args(p, pp, ws);
+    return launch_prefill_schedule(a, s) == cudaSuccess ? FIA_OK : FIA_ERR_CUDA;
+  }
   DecodePlan pl;
   st = decode_plan(p, &pl);
   if (st != FIA_OK) return st;
@@ -316,6 +406,18 @@ fia_status fia_execute(const fia_params* p, void* ws, size_t ws_bytes, void* str
   if (!ws || ws_bytes < (size_t)l.total_bytes) return FIA_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (q_empty(p)) return FIA_OK;
+  if (l.branch == 2) {
+    PrefillPlan pp;
+    st = prefill_plan(p, &pp);
+    if (st != FIA_OK) return st;
+    PrefillArgs a = prefill_args(p, pp, ws);
+    CUtensorMap tq, tk, tv;
+    st = q_map(p, &tq);
+    if (st != FIA_OK) return st;
+    st = kv_maps(p, a.box_rows, &tk, &tv);
+    if (st != FIA_OK) return st;
+    return launch_prefill(a, tq, tk, tv, s) == cudaSuccess ? FIA_OK : FIA_ERR_CUDA;
+  }
   DecodePlan pl;
   st = decode_plan(p, &pl);
   if (st != FIA_OK) return st;

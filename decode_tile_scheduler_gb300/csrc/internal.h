@@ -46,13 +46,11 @@ struct DecodeArgs {
 };
 
 struct PrefillArgs {
-  int B, QN, KVN, D, G, npairs, per_pair;
+  int B, QN, KVN, D, G, npairs, per_pair;  // per_pair query heads per unit (2, or 1 if G odd)
   int layout;
   int S_q;
-  const uint16_t* q;
-  int64_t q_stride;
-  uint16_t* out;
   int64_t out_stride;
+  uint16_t* out;
   float* lse;
   const int32_t* cu_seqlens_q;
   const int32_t* seqused_kv;
@@ -62,15 +60,14 @@ struct PrefillArgs {
   float scale_log2;
   int mask_mode, pre_tokens, next_tokens;
   const float* sinks;
-  int64_t q_rows_total;  // rows of the q tensor view (for the tensor map bound)
-  // plan
+  // plan (workspace)
   int num_ctas;
-  int64_t max_units;
-  int64_t* num_units;     // device: units written by the scheduler
-  const int2* unit_list;  // [U] (b, packed(q_tile, hk, pair))
+  int max_cost;           // costs above are clamped (ordering only)
+  int64_t* num_units;     // written by the scheduler
+  int64_t* seq_prefix;    // [B+1] units before each sequence
+  int* hist;              // [max_cost + 2] cost histogram, then offsets
+  int2* unit_list;        // [units] (b, q_tile | hk << 18 | pair << 26), cost-descending
   int* claim;             // dynamic claim counter
-  int* hist;              // cost histogram scratch
-  int max_cost;
   int* err;
 };
 

@@ -1,0 +1,673 @@
+// prefill.cu -- the full-inference branch of fused inference attention (query
+// length > 1; "aclnnFusedInferAttentionScoreV2": the PromptFlashAttention branch)
+// over a paged or contiguous KV cache, on the 5th-generation tensor cores.
+//
+// Work unit: (batch b, 128-row query tile t, KV head hk, head pair).  Two query
+// heads of the same GQA group share every K/V tile, so one unit runs two
+// 128 x D query tiles ("slots") against one stream of 128-row K/V tiles.
+//
+// Scheduler (prefill_schedule_kernel): every unit gets cost 1 + (KV tiles its
+// query tile can see); units are ordered by non-increasing cost (a counting
+// sort) and persistent CTAs claim them one by one with an atomic counter, so
+// the longest units start first (longest-processing-time order).  A unit runs
+// entirely in one CTA, so results do not depend on which CTA took it.
+//
+// Kernel roles (12 warps, one CTA per SM, all 512 TMEM columns):
+//   warp 0      producer: TMA loads of the Q tiles and of K/V tiles whose rows
+//               come from block_table (128-byte swizzled boxes)
+//   warp 1      MMA issuer (one thread): S = Q K^T (both operands in shared
+//               memory) and O += P V (P in TMEM, V in shared memory), fp32
+//               accumulators in TMEM, ordered so that the two slots ping-pong
+//   warp 2      V guard: zeroes V rows past kv_len in a tail tile, so that a
+//               zero probability never meets a NaN in unused cache rows
+//   warps 4-7   softmax of slot 0; warps 8-11 softmax of slot 1: one TMEM lane
+//               (query row) per thread, online softmax in the exp2 domain with
+//               a lazily moved maximum (O is rescaled only when the running
+//               maximum grows by more than 2^8), P written back to TMEM as bf16,
+//               and the epilogue (sink, 1/l, lse, bf16 store).
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace fia {
+
+namespace {
+
+constexpr int kPWarps = 12;
+constexpr int kPThreads = 32 * kPWarps;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct PrefillCfg {
+  static constexpr int kNsub = D / 64;                    // 128-byte slices per row
+  static constexpr int kTileBytes = kNsub * 128 * 128;    // a 128-row tile of Q, K or V
+  static constexpr int kKStages = D == 128 ? 2 : 4;
+  static constexpr int kVStages = D == 128 ? 2 : 4;
+  static constexpr int kOffQ = 0;                         // 2 slots
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+  // barriers: mfull[2] mempty[2] qfull qempty kfull[KS] kempty[KS] vfull[VS]
+  // vready[VS] vempty[VS] sfull[2] pfull[2] ofull[2] ofree[2] drain
+  static constexpr int kNumBars = 4 + 2 + 2 * kKStages + 3 * kVStages + 8 + 1;
+  static constexpr int kOffMsg = kOffBar + 8 * kNumBars;
+  static constexpr int kOffMisc = kOffMsg + 2 * 64;
+  static constexpr int kSmem = kOffMisc + 64 + 1024;
+  static_assert(kSmem <= 232448, "shared memory");
+};
+
+struct PMsg {
+  int b, t, hk, nslots, h0, h1;
+  int q_len, kv_len, tile0, ntiles, done, pad;
+  int64_t q_row0;  // token row of the tile's first query row
+};
+static_assert(sizeof(PMsg) <= 64, "message slot");
+
+__device__ __forceinline__ void pwait(uint64_t* bar, uint32_t parity, int* err, int* abort_flag) {
+  if (*reinterpret_cast<volatile int*>(abort_flag)) return;
+  if (!mbar_wait(bar, parity, err)) *reinterpret_cast<volatile int*>(abort_flag) = 1;
+}
+
+__device__ __forceinline__ void seq_lengths(const PrefillArgs& a, int b, int64_t* q_start,
+                                            int64_t* q_len, int64_t* kv_len) {
+  if (a.layout == 1) {
+    *q_start = a.cu_seqlens_q[b];
+    *q_len = (int64_t)a.cu_seqlens_q[b + 1] - *q_start;
+  } else {
+    *q_start = (int64_t)b * a.S_q;
+    *q_len = a.S_q;
+  }
+  *kv_len = a.seqused_kv ? a.seqused_kv[b] : a.S_kv;
+}
+
+// KV interval [lo, hi] (clipped) seen by query rows i0..i1 of a sequence, as a
+// tile range; returns the number of 128-wide KV tiles (0 if none).
+__device__ __forceinline__ int tile_span(const PrefillArgs& a, int64_t q_len, int64_t kv_len,
+                                         int64_t i0, int64_t i1, int* tile0) {
+  const int64_t p0 = kv_len - q_len + i0, p1 = kv_len - q_len + i1;
+  int64_t lo = a.mask_mode == 4 ? p0 - a.pre_tokens : 0;
+  int64_t hi = a.mask_mode == 3 ? p1 : (a.mask_mode == 4 ? p1 + a.next_tokens : kv_len - 1);
+  lo = max(lo, (int64_t)0);
+  hi = min(hi, kv_len - 1);
+  *tile0 = 0;
+  if (kv_len <= 0 || hi < lo) return 0;
+  *tile0 = (int)(lo / kKvTile);
+  return (int)(hi / kKvTile - lo / kKvTile + 1);
+}
+
+__device__ __forceinline__ int64_t kv_phys_row(const PrefillArgs& a, int b, int64_t j) {
+  if (a.block_table) {
+    const int64_t blk = a.block_table[(int64_t)b * a.max_blocks + j / a.block_size];
+    return blk * a.block_size + j % a.block_size;
+  }
+  return (int64_t)b * a.S_kv + j;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// scheduler: enumerate units, cost them, counting-sort by non-increasing cost
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) prefill_schedule_kernel(const PrefillArgs a) {
+  __shared__ int64_t warp_sums[32];
+  __shared__ int64_t carry;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int nthr = blockDim.x;
+  const int H = a.KVN * a.npairs;
+  int64_t* seq_prefix = a.seq_prefix;
+
+  auto block_scan = [&](int64_t v, int64_t* excl_out) {  // returns block total via carry
+    int64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+      int64_t w = lane < (nthr >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    *excl_out = carry + (wid ? warp_sums[wid - 1] : 0) + x - v;
+    __syncthreads();
+    if (tid == nthr - 1) carry = *excl_out + v;
+    __syncthreads();
+  };
+
+  // 1. units per sequence -> prefix
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < a.B; base += nthr) {
+    const int b = base + tid;
+    int64_t nu = 0;
+    if (b < a.B) {
+      int64_t qs, ql, kl;
+      seq_lengths(a, b, &qs, &ql, &kl);
+      nu = (ql + kQTile - 1) / kQTile * H;
+    }
+    int64_t ex;
+    block_scan(nu, &ex);
+    if (b < a.B) seq_prefix[b] = ex;
+  }
+  const int64_t U = carry;
+  if (tid == 0) seq_prefix[a.B] = U;
+  // 2. histogram of costs
+  const int nb = a.max_cost + 2;
+  for (int c = tid; c < nb; c += nthr) a.hist[c] = 0;
+  __syncthreads();
+  auto unit_of = [&](int64_t k, int* b_out, int* t_out, int* hk_out, int* pr_out, int* cost) {
+    int lo = 0, hi = a.B;  // largest b with seq_prefix[b] <= k
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (seq_prefix[mid] <= k) lo = mid; else hi = mid;
+    }
+    const int b = lo;
+    const int64_t r = k - seq_prefix[b];
+    const int t = (int)(r / H);
+    const int hh = (int)(r % H);
+    *b_out = b;
+    *t_out = t;
+    *hk_out = hh / a.npairs;
+    *pr_out = hh % a.npairs;
+    int64_t qs, ql, kl;
+    seq_lengths(a, b, &qs, &ql, &kl);
+    const int64_t i0 = (int64_t)t * kQTile, i1 = min(i0 + kQTile, ql) - 1;
+    int tile0;
+    const int n = tile_span(a, ql, kl, i0, i1, &tile0);
+    *cost = min(1 + n, a.max_cost + 1);
+  };
+  for (int64_t k = tid; k < U; k += nthr) {
+    int b, t, hk, pr, cost;
+    unit_of(k, &b, &t, &hk, &pr, &cost);
+    atomicAdd(&a.hist[cost], 1);
+  }
+  __syncthreads();
+  // 3. offsets in non-increasing cost order: off[c] = sum of hist[c'] for c' > c
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < nb; base += nthr) {
+    const int c = nb - 1 - (base + tid);  // high costs first
+    const int64_t v = c >= 0 ? a.hist[c] : 0;
+    int64_t ex;
+    block_scan(v, &ex);
+    if (c >= 0) a.hist[c] = (int)ex;
+  }
+  __syncthreads();
+  // 4. scatter
+  for (int64_t k = tid; k < U; k += nthr) {
+    int b, t, hk, pr, cost;
+    unit_of(k, &b, &t, &hk, &pr, &cost);
+    const int pos = atomicAdd(&a.hist[cost], 1);
+    a.unit_list[pos] = make_int2(b, t | (hk << 18) | (pr << 26));
+  }
+  if (tid == 0) {
+    *a.num_units = U;
+    *a.claim = 0;
+    *a.err = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// attention kernel
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kPThreads, 1)
+    prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tq,
+                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+  using Cfg = PrefillCfg<D>;
+  constexpr int KS = Cfg::kKStages, VS = Cfg::kVStages, NSUB = Cfg::kNsub;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
+  uint64_t* mfull = bars;
+  uint64_t* mempty = mfull + 2;
+  uint64_t* qfull = mempty + 2;
+  uint64_t* qempty = qfull + 1;
+  uint64_t* kfull = qempty + 1;
+  uint64_t* kempty = kfull + KS;
+  uint64_t* vfull = kempty + KS;
+  uint64_t* vready = vfull + VS;
+  uint64_t* vempty = vready + VS;
+  uint64_t* sfull = vempty + VS;
+  uint64_t* pfull = sfull + 2;
+  uint64_t* ofull = pfull + 2;
+  uint64_t* ofree = ofull + 2;
+  uint64_t* drain = ofree + 2;
+  PMsg* msg = reinterpret_cast<PMsg*>(smem + Cfg::kOffMsg);
+  int* misc = reinterpret_cast<int*>(smem + Cfg::kOffMisc);  // [0] abort, [1] tmem base
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&mfull[s], 1);
+      mbar_init(&mempty[s], 4);
+      mbar_init(&sfull[s], 1);
+      mbar_init(&pfull[s], 128);
+      mbar_init(&ofull[s], 1);
+      mbar_init(&ofree[s], 128);
+    }
+    mbar_init(qfull, 1);
+    mbar_init(qempty, 1);
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vready[s], 1);
+      mbar_init(&vempty[s], 1);
+    }
+    mbar_init(drain, 1);
+    misc[0] = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(reinterpret_cast<uint32_t*>(&misc[1]), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = static_cast<uint32_t>(misc[1]);
+  const int64_t num_units = *a.num_units;
+
+  if (warp == 0) {
+    // ============================ producer ============================
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+    }
+    int ucnt = 0, kv_it = 0, q_cnt = 0;
+    while (true) {
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(a.claim, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      const int ms = ucnt & 1;
+      pwait(&mempty[ms], ((ucnt >> 1) & 1) ^ 1, a.err, misc);
+      ++ucnt;
+      if (idx >= num_units || *reinterpret_cast<volatile int*>(misc)) {
+        if (lane == 0) {
+          msg[ms].done = 1;
+          mbar_arrive(&mfull[ms]);
+        }
+        break;
+      }
+      const int2 pk = a.unit_list[idx];
+      PMsg m;
+      m.b = pk.x;
+      m.t = pk.y & 0x3FFFF;
+      m.hk = (pk.y >> 18) & 0xFF;
+      const int pr = (pk.y >> 26) & 0x3F;
+      m.nslots = a.per_pair;
+      m.h0 = m.hk * a.G + pr * a.per_pair;
+      m.h1 = m.h0 + 1;
+      int64_t qs, ql, kl;
+      seq_lengths(a, m.b, &qs, &ql, &kl);
+      m.q_len = (int)ql;
+      m.kv_len = (int)kl;
+      const int64_t i0 = (int64_t)m.t * kQTile, i1 = min(i0 + kQTile, ql) - 1;
+      m.ntiles = tile_span(a, ql, kl, i0, i1, &m.tile0);
+      m.q_row0 = qs + i0;
+      m.done = 0;
+      m.pad = 0;
+      if (lane == 0) {
+        msg[ms] = m;
+        mbar_arrive(&mfull[ms]);
+      }
+      if (m.ntiles == 0) continue;
+      // query tiles of the slots
+      pwait(qempty, (q_cnt & 1) ^ 1, a.err, misc);
+      ++q_cnt;
+      if (lane == 0) mbar_arrive_expect_tx(qfull, (uint32_t)(m.nslots * Cfg::kTileBytes));
+      __syncwarp();
+      if (lane < m.nslots * NSUB) {
+        const int s = lane / NSUB, sub = lane % NSUB;
+        const int h = s ? m.h1 : m.h0;
+        tma_load_2d(smem + Cfg::kOffQ + s * Cfg::kTileBytes + sub * 16384, &tq, qfull,
+                    h * D + sub * 64, (int)m.q_row0);
+      }
+      // K and V tiles
+      const int nrb = kKvTile / a.box_rows;
+      for (int j = 0; j < m.ntiles; ++j, ++kv_it) {
+        const int64_t j0 = (int64_t)(m.tile0 + j) * kKvTile;
+        const int rb = lane / NSUB, sub = lane % NSUB;
+        const int64_t jb = j0 + (int64_t)rb * a.box_rows;
+        const bool mine = lane < nrb * NSUB && jb < kl;
+        const int64_t prow = mine ? kv_phys_row(a, m.b, jb) : 0;
+        int nvalid = 0;
+        for (int q = 0; q < nrb; ++q)
+          if (j0 + (int64_t)q * a.box_rows < kl) ++nvalid;
+        const uint32_t bytes = (uint32_t)(nvalid * NSUB * a.box_rows * 128);
+        const int ks = kv_it % KS, vs = kv_it % VS;
+        pwait(&kempty[ks], ((kv_it / KS) & 1) ^ 1, a.err, misc);
+        if (lane == 0) mbar_arrive_expect_tx(&kfull[ks], bytes);
+        __syncwarp();
+        if (mine)
+          tma_load_2d(smem + Cfg::kOffK + ks * Cfg::kTileBytes + sub * 16384 + rb * a.box_rows * 128,
+                      &tk, &kfull[ks], m.hk * D + sub * 64, (int)prow);
+        pwait(&vempty[vs], ((kv_it / VS) & 1) ^ 1, a.err, misc);
+        if (lane == 0) mbar_arrive_expect_tx(&vfull[vs], bytes);
+        __syncwarp();
+        if (mine)
+          tma_load_2d(smem + Cfg::kOffV + vs * Cfg::kTileBytes + sub * 16384 + rb * a.box_rows * 128,
+                      &tv, &vfull[vs], m.hk * D + sub * 64, (int)prow);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer ============================
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false);
+      constexpr uint32_t kIdO = idesc_bf16(128, 64, true);
+      const uint32_t sq = smem_u32(smem + Cfg::kOffQ);
+      const uint32_t sk = smem_u32(smem + Cfg::kOffK);
+      const uint32_t sv = smem_u32(smem + Cfg::kOffV);
+      int ucnt = 0, kv_it = 0, q_cnt = 0;
+      int s_it[2] = {0, 0}, u_cnt[2] = {0, 0};
+      auto issue_qk = [&](int s, int ks) {
+        const uint32_t d = tmem + 256 * s;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint64_t ad = smem_desc_sw128(sq + s * Cfg::kTileBytes + off, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(sk + ks * Cfg::kTileBytes + off, 16, 1024);
+          mma_ss(d, ad, bd, kIdS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int s, int vs, bool first_tile) {
+        const uint32_t p = tmem + 256 * s;
+        const uint32_t o = tmem + 256 * s + 128;
+#pragma unroll
+        for (int kk = 0; kk < kKvTile / 16; ++kk) {
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub) {
+            const uint64_t bd =
+                smem_desc_sw128(sv + vs * Cfg::kTileBytes + sub * 16384 + kk * 2048, 1024, 1024);
+            mma_ts(o + sub * 64, p + kk * 8, bd, kIdO, (!first_tile || kk > 0) ? 1u : 0u);
+          }
+        }
+      };
+      while (true) {
+        const int ms = ucnt & 1;
+        pwait(&mfull[ms], (ucnt >> 1) & 1, a.err, misc);
+        ++ucnt;
+        const PMsg m = msg[ms];
+        mbar_arrive(&mempty[ms]);
+        if (m.done || *reinterpret_cast<volatile int*>(misc)) break;
+        const int n = m.ntiles, ns = m.nslots;
+        for (int s = 0; s < ns; ++s) {
+          pwait(&ofree[s], (u_cnt[s] & 1) ^ 1, a.err, misc);
+          ++u_cnt[s];
+        }
+        if (n == 0) continue;
+        pwait(qfull, q_cnt & 1, a.err, misc);
+        ++q_cnt;
+        {
+          const int ks0 = kv_it % KS;
+          pwait(&kfull[ks0], (kv_it / KS) & 1, a.err, misc);
+          tc_fence_after();
+          for (int s = 0; s < ns; ++s) {
+            issue_qk(s, ks0);
+            tc_commit(&sfull[s]);
+          }
+          tc_commit(&kempty[ks0]);
+          if (n == 1) tc_commit(qempty);
+        }
+        for (int j = 0; j < n; ++j) {
+          const int it = kv_it + j;
+          const int vs = it % VS;
+          pwait(&vready[vs], (it / VS) & 1, a.err, misc);
+          tc_fence_after();
+          for (int s = 0; s < ns; ++s) {
+            pwait(&pfull[s], s_it[s] & 1, a.err, misc);
+            ++s_it[s];
+            tc_fence_after();
+            issue_pv(s, vs, j == 0);
+            if (j == n - 1) tc_commit(&ofull[s]);
+            if (j + 1 < n) {
+              const int itn = it + 1, ksn = itn % KS;
+              if (s == 0) {
+                pwait(&kfull[ksn], (itn / KS) & 1, a.err, misc);
+                tc_fence_after();
+              }
+              issue_qk(s, ksn);
+              tc_commit(&sfull[s]);
+              if (s == ns - 1) {
+                tc_commit(&kempty[ksn]);
+                if (j + 1 == n - 1) tc_commit(qempty);
+              }
+            }
+          }
+          tc_commit(&vempty[vs]);
+        }
+        kv_it += n;
+      }
+      // everything issued has finished before the TMEM is released
+      tc_commit(drain);
+      mbar_wait(drain, 0, a.err);
+    }
+  } else if (warp == 2) {
+    // ============================ V guard ============================
+    int ucnt = 0, kv_it = 0;
+    while (true) {
+      const int ms = ucnt & 1;
+      pwait(&mfull[ms], (ucnt >> 1) & 1, a.err, misc);
+      ++ucnt;
+      const PMsg m = msg[ms];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mempty[ms]);
+      if (m.done || *reinterpret_cast<volatile int*>(misc)) break;
+      for (int j = 0; j < m.ntiles; ++j, ++kv_it) {
+        const int vs = kv_it % VS;
+        pwait(&vfull[vs], (kv_it / VS) & 1, a.err, misc);
+        const int64_t j0 = (int64_t)(m.tile0 + j) * kKvTile;
+        const int nv = (int)min((int64_t)kKvTile, (int64_t)m.kv_len - j0);
+        if (nv < kKvTile) {
+          uint8_t* vt = smem + Cfg::kOffV + vs * Cfg::kTileBytes;
+          for (int x = nv * 8 + lane; x < kKvTile * 8; x += 32) {  // 16-byte pieces
+            const int row = x >> 3, piece = x & 7;
+#pragma unroll
+            for (int sub = 0; sub < NSUB; ++sub)
+              *reinterpret_cast<uint4*>(vt + sub * 16384 + row * 128 + piece * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&vready[vs]);
+      }
+    }
+  } else if (warp >= 4) {
+    // ============================ softmax + epilogue ============================
+    const int s = (warp - 4) >> 2;      // slot
+    const int row = tid - 128 - 128 * s;  // query row of the tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t tS = tmem + lane_base + 256 * s;
+    const uint32_t tO = tS + 128;
+    int ucnt = 0, s_it = 0, o_cnt = 0;
+    while (true) {
+      const int ms = ucnt & 1;
+      pwait(&mfull[ms], (ucnt >> 1) & 1, a.err, misc);
+      ++ucnt;
+      const PMsg m = msg[ms];
+      named_bar_sync(2 + s, 128);
+      if (row == 0) mbar_arrive(&mempty[ms]);
+      if (m.done || *reinterpret_cast<volatile int*>(misc)) break;
+      if (s >= m.nslots) continue;
+      const int h = s ? m.h1 : m.h0;
+      const int64_t i = (int64_t)m.t * kQTile + row;
+      const bool valid = i < m.q_len;
+      const int64_t p = (int64_t)m.kv_len - m.q_len + i;
+      int64_t lo = a.mask_mode == 4 ? p - a.pre_tokens : 0;
+      int64_t hi = a.mask_mode == 3 ? p : (a.mask_mode == 4 ? p + a.next_tokens : m.kv_len - 1);
+      lo = max(lo, (int64_t)0);
+      hi = min(hi, (int64_t)m.kv_len - 1);
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < m.ntiles; ++j) {
+        pwait(&sfull[s], s_it & 1, a.err, misc);
+        ++s_it;
+        tc_fence_after();
+        // pass 1: row maximum of the (masked) scores, exp2 domain
+        const int64_t j0 = (int64_t)(m.tile0 + j) * kKvTile;
+        const bool full_row = lo <= j0 && j0 + kKvTile - 1 <= hi;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tS + 32 * c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int64_t jj = j0 + 32 * c + e;
+            const float xv = (full_row || (jj >= lo && jj <= hi))
+                                 ? __uint_as_float(v[e]) * a.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, xv);
+          }
+        }
+        if (mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx != -INFINITY)) {
+          if (m_used != -INFINITY) {
+            // move the reference maximum: rescale l and the O accumulator
+            const float corr = fast_exp2(m_used - mx);
+            l *= corr;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tO + 32 * c, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * corr);
+              tmem_st32(tO + 32 * c, v);
+            }
+            tmem_wait_st();
+          }
+          m_used = mx;
+        }
+        const float base = m_used == -INFINITY ? 0.f : m_used;
+        // pass 2: probabilities, packed to bf16 pairs over the first 64 columns
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tS + 64 * c, v0);
+          tmem_ld32(tS + 64 * c + 32, v1);
+          tmem_wait_ld();
+          uint32_t pv[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = 2 * e;  // columns 64c + col, +1
+            const uint32_t ra = col < 32 ? v0[col] : v1[col - 32];
+            const uint32_t rb = col + 1 < 32 ? v0[col + 1] : v1[col + 1 - 32];
+            const int64_t jj = j0 + 64 * c + col;
+            const float xa = (full_row || (jj >= lo && jj <= hi))
+                                 ? __uint_as_float(ra) * a.scale_log2 : -INFINITY;
+            const float xb = (full_row || (jj + 1 >= lo && jj + 1 <= hi))
+                                 ? __uint_as_float(rb) * a.scale_log2 : -INFINITY;
+            const float p0 = fast_exp2(xa - base), p1 = fast_exp2(xb - base);
+            sum += p0 + p1;
+            pv[e] = pack_bf16(p0, p1);
+          }
+          tmem_st32(tS + 32 * c, pv);
+        }
+        tmem_wait_st();
+        l += sum;
+        tc_fence_before();
+        mbar_arrive(&pfull[s]);
+      }
+      // ---- epilogue ----
+      float scl = 0.f, lse = INFINITY;
+      if (m_used != -INFINITY) {
+        float Mp = m_used, L = l;
+        if (a.sinks) {
+          const float sk = a.sinks[h] * 1.4426950408889634f;
+          Mp = fmaxf(m_used, sk);
+          L = l * exp2f(m_used - Mp) + exp2f(sk - Mp);
+        }
+        scl = exp2f(m_used - Mp) / L;
+        lse = (Mp + log2f(L)) * 0.6931471805599453f;
+      }
+      uint16_t* orow = a.out + (m.q_row0 + row) * a.out_stride + (int64_t)h * D;
+      if (m.ntiles > 0) {
+        pwait(&ofull[s], o_cnt & 1, a.err, misc);
+        ++o_cnt;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + 32 * c, v);
+          tmem_wait_ld();
+          if (valid) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16(__uint_as_float(v[2 * e]) * scl, __uint_as_float(v[2 * e + 1]) * scl);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<uint4*>(orow + 32 * c + 8 * e) =
+                  make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
+        }
+      } else if (valid) {
+#pragma unroll
+        for (int e = 0; e < D / 8; ++e)
+          *reinterpret_cast<uint4*>(orow + 8 * e) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (valid && a.lse) {
+        const int64_t li = a.layout == 1 ? (m.q_row0 + row) * a.QN + h
+                                         : ((int64_t)m.b * a.QN + h) * a.S_q + i;
+        a.lse[li] = lse;
+      }
+      tc_fence_before();
+      mbar_arrive(&ofree[s]);
+    }
+  }
+  // warp 3 has no role
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// host launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_prefill_schedule(const PrefillArgs& a, cudaStream_t s) {
+  prefill_schedule_kernel<<<1, 1024, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& tq,
+                                    const CUtensorMap& tk, const CUtensorMap& tv,
+                                    cudaStream_t s) {
+  using Cfg = PrefillCfg<D>;
+  auto kern = prefill_kernel<D>;
+  static std::atomic<uint64_t> done_mask[4];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(done_mask[(dev >> 6) & 3].load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    done_mask[(dev >> 6) & 3].fetch_or(bit);
+  }
+  kern<<<a.num_ctas, kPThreads, Cfg::kSmem, s>>>(a, tq, tk, tv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, cudaStream_t s) {
+  return a.D == 64 ? launch_prefill_t<64>(a, tq, tk, tv, s) : launch_prefill_t<128>(a, tq, tk, tv, s);
+}
+
+}  // namespace fia

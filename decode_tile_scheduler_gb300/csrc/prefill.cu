@@ -65,6 +65,13 @@ struct PMsg {
 };
 static_assert(sizeof(PMsg) <= 64, "message slot");
 
+// ex2.approx without `volatile`, so the compiler may schedule it freely.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void pwait(uint64_t* bar, uint32_t parity, int* err, int* abort_flag) {
   if (*reinterpret_cast<volatile int*>(abort_flag)) return;
   if (!mbar_wait(bar, parity, err)) *reinterpret_cast<volatile int*>(abort_flag) = 1;
@@ -405,11 +412,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_arrive(&mempty[ms]);
         if (m.done || *reinterpret_cast<volatile int*>(misc)) break;
         const int n = m.ntiles, ns = m.nslots;
+        if (n == 0) continue;  // no MMA work: the softmax warps write the zeros
+        // O of each slot is free once the previous unit's epilogue read it.
+        // Only units with tiles take part in this handshake, so the softmax
+        // side can never run two phases ahead of these waits.
         for (int s = 0; s < ns; ++s) {
           pwait(&ofree[s], (u_cnt[s] & 1) ^ 1, a.err, misc);
           ++u_cnt[s];
         }
-        if (n == 0) continue;
         pwait(qfull, q_cnt & 1, a.err, misc);
         ++q_cnt;
         {
@@ -456,6 +466,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tc_commit(drain);
       mbar_wait(drain, 0, a.err);
     }
+    __syncwarp();
   } else if (warp == 2) {
     // ============================ V guard ============================
     int ucnt = 0, kv_it = 0;
@@ -517,67 +528,98 @@ __global__ void __launch_bounds__(kPThreads, 1)
         pwait(&sfull[s], s_it & 1, a.err, misc);
         ++s_it;
         tc_fence_after();
-        // pass 1: row maximum of the (masked) scores, exp2 domain
+        // visible columns of this row in the tile: [c0, c1) (tile-local)
         const int64_t j0 = (int64_t)(m.tile0 + j) * kKvTile;
-        const bool full_row = lo <= j0 && j0 + kKvTile - 1 <= hi;
-        float mx = -INFINITY;
+        const int c0 = (int)min(max(lo - j0, (int64_t)0), (int64_t)kKvTile);
+        const int c1 = (int)min(max(hi - j0 + 1, (int64_t)0), (int64_t)kKvTile);
+        const bool all_full = __all_sync(0xffffffffu, c0 == 0 && c1 == kKvTile);
+        const float sl = a.scale_log2;
+        const float hole = sl >= 0.f ? -INFINITY : INFINITY;  // masked score
+        // pass 1: row maximum of the raw scores (minimum when the scale is
+        // negative), 64 columns per TMEM round trip, eight partial chains
+        float pm[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tS + 32 * c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int64_t jj = j0 + 32 * c + e;
-            const float xv = (full_row || (jj >= lo && jj <= hi))
-                                 ? __uint_as_float(v[e]) * a.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, xv);
-          }
-        }
-        if (mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx != -INFINITY)) {
-          if (m_used != -INFINITY) {
-            // move the reference maximum: rescale l and the O accumulator
-            const float corr = fast_exp2(m_used - mx);
-            l *= corr;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t v[32];
-              tmem_ld32(tO + 32 * c, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * corr);
-              tmem_st32(tO + 32 * c, v);
-            }
-            tmem_wait_st();
-          }
-          m_used = mx;
-        }
-        const float base = m_used == -INFINITY ? 0.f : m_used;
-        // pass 2: probabilities, packed to bf16 pairs over the first 64 columns
-        float sum = 0.f;
+        for (int k = 0; k < 8; ++k) pm[k] = hole;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t v0[32], v1[32];
-          tmem_ld32(tS + 64 * c, v0);
-          tmem_ld32(tS + 64 * c + 32, v1);
+          uint32_t v[64];
+          tmem_ld32(tS + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tS + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          if (!all_full) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (64 * c + e < c0 || 64 * c + e >= c1) v[e] = __float_as_uint(hole);
+          }
+          if (sl >= 0.f) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) pm[e & 7] = fminf(pm[e & 7], __uint_as_float(v[e]));
+          }
+        }
+        float best;
+        if (sl >= 0.f)
+          best = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+        else
+          best = fminf(fminf(fminf(pm[0], pm[1]), fminf(pm[2], pm[3])),
+                       fminf(fminf(pm[4], pm[5]), fminf(pm[6], pm[7])));
+        const float mx = isinf(best) ? -INFINITY : best * sl;  // all masked -> -inf
+        // lazily moved reference maximum: a row moves it when the new maximum
+        // exceeds it by more than 2^8 (or on its first visible key); rows
+        // that move it rescale l and their O row.  TMEM loads and stores are
+        // warp-collective, so the rescale runs for the whole warp with a
+        // factor of 1 on the rows that keep their reference.
+        const bool move = mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx != -INFINITY);
+        const bool rescale = move && m_used != -INFINITY;
+        float corr = 1.f;
+        if (rescale) {
+          corr = ex2_approx(m_used - mx);
+          l *= corr;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t w[32];
+            tmem_ld32(tO + 32 * c, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * corr);
+            tmem_st32(tO + 32 * c, w);
+          }
+          tmem_wait_st();
+        }
+        if (move) m_used = mx;
+        const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+        // pass 2: p = 2^(s * scale * log2e - m) (masked columns give 0), packed
+        // to bf16 pairs over the first 64 columns
+        float ps[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[64];
+          tmem_ld32(tS + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tS + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           tmem_wait_ld();
           uint32_t pv[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const int col = 2 * e;  // columns 64c + col, +1
-            const uint32_t ra = col < 32 ? v0[col] : v1[col - 32];
-            const uint32_t rb = col + 1 < 32 ? v0[col + 1] : v1[col + 1 - 32];
-            const int64_t jj = j0 + 64 * c + col;
-            const float xa = (full_row || (jj >= lo && jj <= hi))
-                                 ? __uint_as_float(ra) * a.scale_log2 : -INFINITY;
-            const float xb = (full_row || (jj + 1 >= lo && jj + 1 <= hi))
-                                 ? __uint_as_float(rb) * a.scale_log2 : -INFINITY;
-            const float p0 = fast_exp2(xa - base), p1 = fast_exp2(xb - base);
-            sum += p0 + p1;
+            float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * e]), sl, nbase));
+            float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * e + 1]), sl, nbase));
+            if (!all_full) {
+              const int ca = 64 * c + 2 * e;
+              p0 = (ca >= c0 && ca < c1) ? p0 : 0.f;
+              p1 = (ca + 1 >= c0 && ca + 1 < c1) ? p1 : 0.f;
+            }
+            ps[e & 7] += p0 + p1;
             pv[e] = pack_bf16(p0, p1);
           }
           tmem_st32(tS + 32 * c, pv);
         }
+        const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         tmem_wait_st();
         l += sum;
         tc_fence_before();
@@ -626,8 +668,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                          : ((int64_t)m.b * a.QN + h) * a.S_q + i;
         a.lse[li] = lse;
       }
-      tc_fence_before();
-      mbar_arrive(&ofree[s]);
+      if (m.ntiles > 0) {
+        tc_fence_before();
+        mbar_arrive(&ofree[s]);
+      }
     }
   }
   // warp 3 has no role

@@ -43,7 +43,7 @@ template <int D>
 struct PrefillCfg {
   static constexpr int kNsub = D / 64;                    // 128-byte slices per row
   static constexpr int kTileBytes = kNsub * 128 * 128;    // a 128-row tile of Q, K or V
-  static constexpr int kKStages = D == 128 ? 2 : 4;
+  static constexpr int kKStages = D == 128 ? 3 : 4;
   static constexpr int kVStages = D == 128 ? 2 : 4;
   static constexpr int kOffQ = 0;                         // 2 slots
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
@@ -70,6 +70,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed fp32 pair arithmetic (one instruction for two lanes of work).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ void pwait(uint64_t* bar, uint32_t parity, int* err, int* abort_flag) {
@@ -259,9 +287,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&mfull[s], 1);
       mbar_init(&mempty[s], 4);
       mbar_init(&sfull[s], 1);
-      mbar_init(&pfull[s], 128);
+      mbar_init(&pfull[s], 4);  // one arrival per softmax warp
       mbar_init(&ofull[s], 1);
-      mbar_init(&ofree[s], 128);
+      mbar_init(&ofree[s], 4);
     }
     mbar_init(qfull, 1);
     mbar_init(qempty, 1);
@@ -375,33 +403,38 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // ============================ MMA issuer ============================
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false);
-      constexpr uint32_t kIdO = idesc_bf16(128, 64, true);
+      constexpr uint32_t kIdO = idesc_bf16(128, D, true);
       const uint32_t sq = smem_u32(smem + Cfg::kOffQ);
       const uint32_t sk = smem_u32(smem + Cfg::kOffK);
       const uint32_t sv = smem_u32(smem + Cfg::kOffV);
       int ucnt = 0, kv_it = 0, q_cnt = 0;
       int s_it[2] = {0, 0}, u_cnt[2] = {0, 0};
+      // descriptors of every operand buffer, built once; a k-step only adds
+      // its byte offset (>> 4) to the start-address field
+      const uint64_t qd0 = smem_desc_sw128(sq, 16, 1024);
+      const uint64_t kd0 = smem_desc_sw128(sk, 16, 1024);
+      // V is the MN-major B operand of P V: 64-column swizzle atoms 16 KB apart
+      // (leading byte offset), 8-row groups along K 1 KB apart (stride offset)
+      const uint64_t vd0 = smem_desc_sw128(sv, 16384, 1024);
+      constexpr uint64_t kTileUnits = Cfg::kTileBytes >> 4;
       auto issue_qk = [&](int s, int ks) {
         const uint32_t d = tmem + 256 * s;
+        const uint64_t qd = qd0 + (uint64_t)s * kTileUnits;
+        const uint64_t kd = kd0 + (uint64_t)ks * kTileUnits;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(sq + s * Cfg::kTileBytes + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(sk + ks * Cfg::kTileBytes + off, 16, 1024);
-          mma_ss(d, ad, bd, kIdS, kk > 0);
+          const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          mma_ss(d, qd + off, kd + off, kIdS, kk > 0);
         }
       };
       auto issue_pv = [&](int s, int vs, bool first_tile) {
         const uint32_t p = tmem + 256 * s;
         const uint32_t o = tmem + 256 * s + 128;
+        const uint64_t vd = vd0 + (uint64_t)vs * kTileUnits;
 #pragma unroll
         for (int kk = 0; kk < kKvTile / 16; ++kk) {
-#pragma unroll
-          for (int sub = 0; sub < NSUB; ++sub) {
-            const uint64_t bd =
-                smem_desc_sw128(sv + vs * Cfg::kTileBytes + sub * 16384 + kk * 2048, 1024, 1024);
-            mma_ts(o + sub * 64, p + kk * 8, bd, kIdO, (!first_tile || kk > 0) ? 1u : 0u);
-          }
+          const uint64_t off = (uint64_t)((kk * 2048) >> 4);
+          mma_ts(o, p + kk * 8, vd + off, kIdO, (!first_tile || kk > 0) ? 1u : 0u);
         }
       };
       while (true) {
@@ -535,11 +568,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const bool all_full = __all_sync(0xffffffffu, c0 == 0 && c1 == kKvTile);
         const float sl = a.scale_log2;
         const float hole = sl >= 0.f ? -INFINITY : INFINITY;  // masked score
-        // pass 1: row maximum of the raw scores (minimum when the scale is
-        // negative), 64 columns per TMEM round trip, eight partial chains
-        float pm[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) pm[k] = hole;
+        // pass 1: row maximum of the raw scores (minimum for a negative scale),
+        // 64 columns per TMEM round trip, four three-input chains
+        float pm[4] = {hole, hole, hole, hole};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t v[64];
@@ -553,19 +584,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
           if (sl >= 0.f) {
 #pragma unroll
-            for (int e = 0; e < 64; ++e) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v[e]));
+            for (int e = 0; e < 64; e += 8)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                pm[k] = fmax3(pm[k], __uint_as_float(v[e + k]), __uint_as_float(v[e + 4 + k]));
           } else {
 #pragma unroll
-            for (int e = 0; e < 64; ++e) pm[e & 7] = fminf(pm[e & 7], __uint_as_float(v[e]));
+            for (int e = 0; e < 64; e += 8)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                pm[k] = fmin3(pm[k], __uint_as_float(v[e + k]), __uint_as_float(v[e + 4 + k]));
           }
         }
-        float best;
-        if (sl >= 0.f)
-          best = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-        else
-          best = fminf(fminf(fminf(pm[0], pm[1]), fminf(pm[2], pm[3])),
-                       fminf(fminf(pm[4], pm[5]), fminf(pm[6], pm[7])));
+        const float best = sl >= 0.f ? fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]))
+                                     : fminf(fminf(pm[0], pm[1]), fminf(pm[2], pm[3]));
         const float mx = isinf(best) ? -INFINITY : best * sl;  // all masked -> -inf
         // lazily moved reference maximum: a row moves it when the new maximum
         // exceeds it by more than 2^8 (or on its first visible key); rows
@@ -593,11 +625,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         if (move) m_used = mx;
         const float nbase = m_used == -INFINITY ? 0.f : -m_used;
-        // pass 2: p = 2^(s * scale * log2e - m) (masked columns give 0), packed
-        // to bf16 pairs over the first 64 columns
-        float ps[8];
+        // pass 2: p = 2^(s * scale * log2e - m), two columns per packed FMA,
+        // masked columns give 0, packed to bf16 pairs over the first 64 columns
+        float2 ps[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+        for (int k = 0; k < 4; ++k) ps[k] = make_float2(0.f, 0.f);
+        const float2 sl2 = make_float2(sl, sl), nb2 = make_float2(nbase, nbase);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t v[64];
@@ -607,27 +640,30 @@ __global__ void __launch_bounds__(kPThreads, 1)
           uint32_t pv[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * e]), sl, nbase));
-            float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * e + 1]), sl, nbase));
+            const float2 x = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                   sl2, nb2);
+            float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             if (!all_full) {
               const int ca = 64 * c + 2 * e;
-              p0 = (ca >= c0 && ca < c1) ? p0 : 0.f;
-              p1 = (ca + 1 >= c0 && ca + 1 < c1) ? p1 : 0.f;
+              pp.x = (ca >= c0 && ca < c1) ? pp.x : 0.f;
+              pp.y = (ca + 1 >= c0 && ca + 1 < c1) ? pp.y : 0.f;
             }
-            ps[e & 7] += p0 + p1;
-            pv[e] = pack_bf16(p0, p1);
+            ps[e & 3] = fadd2(ps[e & 3], pp);
+            pv[e] = pack_bf16(pp.x, pp.y);
           }
           tmem_st32(tS + 32 * c, pv);
         }
-        const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        const float2 s2 = fadd2(fadd2(ps[0], ps[1]), fadd2(ps[2], ps[3]));
+        const float sum = s2.x + s2.y;
         tmem_wait_st();
         l += sum;
         tc_fence_before();
-        mbar_arrive(&pfull[s]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfull[s]);
       }
       // ---- epilogue ----
       float scl = 0.f, lse = INFINITY;
-      if (m_used != -INFINITY) {
+      if (m_used != -INFINITY && l > 0.f) {  // l == 0: the row saw no key
         float Mp = m_used, L = l;
         if (a.sinks) {
           const float sk = a.sinks[h] * 1.4426950408889634f;
@@ -670,11 +706,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       if (m.ntiles > 0) {
         tc_fence_before();
-        mbar_arrive(&ofree[s]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ofree[s]);
       }
     }
   }
-  // warp 3 has no role
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -68,12 +68,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity.  Returns false (and sets
 // the error flag) if the barrier did not complete within the time limit, so
 // that no kernel of this library can spin forever.
+// The global timer is read only every 256 polls: reading it is slow, and a
+// thread busy reading it would notice a completed phase late.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (true) {
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > FIA_WAIT_TIMEOUT_NS) {
+    if ((n & 255u) == 0 && globaltimer_ns() - t0 > FIA_WAIT_TIMEOUT_NS) {
       if (err) atomicExch(err, 1);
       return false;
     }

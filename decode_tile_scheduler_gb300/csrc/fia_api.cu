@@ -308,6 +308,115 @@ fia_status q_map(const fia_params* p, CUtensorMap* tq) {
   return make_map(tq, p->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, 64, 128, stride);
 }
 
+// ---------------------------------------------------------------------------
+// shared-KV sparse attention ("kv_quant_sparse_attn_sharedkv" constraints)
+// ---------------------------------------------------------------------------
+constexpr int kSparseChunk = 64;
+constexpr int kSparseMaxCtas = 503;  // (1024 - 16) / 2 - 1 begins fit the metadata
+
+struct SparsePlan {
+  int n, mode, max_chunks;
+  int64_t rows, total;
+};
+
+fia_status sparse_validate(const sparse_attn_params* p) {
+  if (!p) return FIA_ERR_NULL_ARG;
+  for (int i = 0; i < 7; ++i)
+    if (p->reserved[i] != 0) return FIA_ERR_BAD_SHAPE;
+  if (p->batch < 1 || p->batch > 65536) return FIA_ERR_BAD_SHAPE;
+  if (p->num_q_heads < 1 || p->num_q_heads > 128 || (p->num_q_heads & (p->num_q_heads - 1)))
+    return FIA_ERR_BAD_SHAPE;
+  if (p->head_dim < 1 || p->head_dim > 512) return FIA_ERR_BAD_SHAPE;
+  if (p->layout != FIA_LAYOUT_BSND && p->layout != FIA_LAYOUT_TND) return FIA_ERR_BAD_SHAPE;
+  if (p->max_seqlen_q < 0 || p->total_q < 0) return FIA_ERR_BAD_SHAPE;
+  if (p->layout == FIA_LAYOUT_TND && !p->cu_seqlens_q) return FIA_ERR_NULL_ARG;
+  if (!p->q || !p->out || !p->ori_kv || !p->ori_block_table || !p->seqused_kv)
+    return FIA_ERR_NULL_ARG;
+  if (!aligned16(p->q) || !aligned16(p->out) || !aligned16(p->ori_kv)) return FIA_ERR_BAD_SHAPE;
+  if (p->ori_block_size <= 0 || p->ori_block_size % 16 || p->ori_block_size > 1024)
+    return FIA_ERR_BAD_SHAPE;
+  if (p->ori_max_blocks <= 0 || p->ori_num_blocks <= 0) return FIA_ERR_BAD_SHAPE;
+  if (p->ori_win_left < 0 || p->ori_win_right < 0 ||
+      (int64_t)p->ori_win_left + p->ori_win_right + 1 > 65536)
+    return FIA_ERR_BAD_SHAPE;
+  if (!std::isfinite(p->softmax_scale)) return FIA_ERR_BAD_SHAPE;
+  if (p->num_sms < 0 || p->num_sms > 4096) return FIA_ERR_BAD_SHAPE;
+  if (p->cmp_kv) {
+    if (!p->cmp_block_table) return FIA_ERR_NULL_ARG;
+    if (!aligned16(p->cmp_kv)) return FIA_ERR_BAD_SHAPE;
+    if (p->cmp_block_size <= 0 || p->cmp_block_size % 16 || p->cmp_block_size > 1024)
+      return FIA_ERR_BAD_SHAPE;
+    if (p->cmp_max_blocks <= 0 || p->cmp_num_blocks <= 0) return FIA_ERR_BAD_SHAPE;
+    if (p->cmp_ratio < 1) return FIA_ERR_BAD_SHAPE;
+    if (p->cmp_sparse_indices && (p->topk < 1 || p->topk > 2048)) return FIA_ERR_BAD_SHAPE;
+  } else if (p->cmp_sparse_indices) {
+    return FIA_ERR_BAD_SHAPE;  // indices without a compressed cache
+  }
+  if (p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512) return FIA_ERR_UNSUPPORTED;
+  return FIA_OK;
+}
+
+fia_status sparse_plan(const sparse_attn_params* p, SparsePlan* pl) {
+  fia_status st = sparse_validate(p);
+  if (st != FIA_OK) return st;
+  int n;
+  st = sm_count(p->num_sms, &n);
+  if (st != FIA_OK) return st;
+  pl->n = n < kSparseMaxCtas ? n : kSparseMaxCtas;
+  pl->mode = !p->cmp_kv ? 0 : (p->cmp_sparse_indices ? 1 : 2);
+  pl->rows = p->layout == FIA_LAYOUT_TND ? (int64_t)p->total_q
+                                         : (int64_t)p->batch * p->max_seqlen_q;
+  const int64_t W = (int64_t)p->ori_win_left + p->ori_win_right + 1;
+  int64_t kc = 0;
+  if (pl->mode == 1) kc = p->topk;
+  else if (pl->mode == 2) kc = (int64_t)p->cmp_max_blocks * p->cmp_block_size;
+  pl->max_chunks = (int)(ceil_div(W, kSparseChunk) + ceil_div(kc, kSparseChunk));
+  pl->total = align_up(kAlign + 4 * pl->rows * pl->max_chunks * (int64_t)p->num_q_heads *
+                                    (p->head_dim + 2));
+  return FIA_OK;
+}
+
+SparseArgs sparse_args(const sparse_attn_params* p, const SparsePlan& pl, void* ws) {
+  SparseArgs a;
+  memset(&a, 0, sizeof a);
+  a.B = p->batch;
+  a.N1 = p->num_q_heads;
+  a.D = p->head_dim;
+  a.layout = p->layout;
+  a.S1 = p->max_seqlen_q;
+  a.q = static_cast<const uint16_t*>(p->q);
+  a.out = static_cast<uint16_t*>(p->out);
+  a.lse = p->lse;
+  a.ori_kv = static_cast<const uint16_t*>(p->ori_kv);
+  a.ori_block_table = p->ori_block_table;
+  a.ori_max_blocks = p->ori_max_blocks;
+  a.ori_block_size = p->ori_block_size;
+  a.cmp_kv = static_cast<const uint16_t*>(p->cmp_kv);
+  a.cmp_block_table = p->cmp_block_table;
+  a.cmp_max_blocks = p->cmp_max_blocks;
+  a.cmp_block_size = p->cmp_kv ? p->cmp_block_size : 1;
+  a.cmp_sparse_indices = p->cmp_sparse_indices;
+  a.K2 = pl.mode == 1 ? p->topk : 0;
+  a.cu_seqlens_q = p->cu_seqlens_q;
+  a.seqused_kv = p->seqused_kv;
+  a.sinks = p->sinks;
+  a.scale_log2 = p->softmax_scale * 1.4426950408889634f;
+  a.cmp_ratio = p->cmp_kv ? p->cmp_ratio : 1;
+  a.win_left = p->ori_win_left;
+  a.win_right = p->ori_win_right;
+  a.mode = pl.mode;
+  a.rows = pl.rows;
+  a.chunk = kSparseChunk;
+  a.max_chunks = pl.max_chunks;
+  a.num_ctas = pl.n;
+  if (ws) {
+    char* w = static_cast<char*>(ws);
+    a.err = reinterpret_cast<int*>(w);
+    a.partials = reinterpret_cast<float*>(w + kAlign);
+  }
+  return a;
+}
+
 bool q_empty(const fia_params* p) {
   return p->layout == FIA_LAYOUT_TND ? p->total_q == 0 : p->max_seqlen_q == 0;
 }
@@ -437,18 +546,30 @@ fia_status fia_run(const fia_params* p, void* ws, size_t ws_bytes, void* stream)
 
 fia_status sparse_attn_metadata(const sparse_attn_params* p, int32_t* metadata,
                                 size_t* workspace_bytes, void* stream) {
-  (void)stream;
   if (!p || !metadata || !workspace_bytes) return FIA_ERR_NULL_ARG;
-  return FIA_ERR_UNSUPPORTED;
+  SparsePlan pl;
+  fia_status st = sparse_plan(p, &pl);
+  if (st != FIA_OK) return st;
+  *workspace_bytes = (size_t)pl.total;
+  SparseArgs a = sparse_args(p, pl, nullptr);
+  if (a.rows == 0) return FIA_OK;
+  return launch_sparse_metadata(a, metadata, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FIA_OK
+             : FIA_ERR_CUDA;
 }
 
 fia_status sparse_attn_run(const sparse_attn_params* p, const int32_t* metadata, void* ws,
                            size_t ws_bytes, void* stream) {
-  (void)ws;
-  (void)ws_bytes;
-  (void)stream;
   if (!p || !metadata) return FIA_ERR_NULL_ARG;
-  return FIA_ERR_UNSUPPORTED;
+  SparsePlan pl;
+  fia_status st = sparse_plan(p, &pl);
+  if (st != FIA_OK) return st;
+  if (!ws || ws_bytes < (size_t)pl.total) return FIA_ERR_WORKSPACE_TOO_SMALL;
+  SparseArgs a = sparse_args(p, pl, ws);
+  if (a.rows == 0) return FIA_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return FIA_ERR_CUDA;
+  return launch_sparse(a, metadata, s) == cudaSuccess ? FIA_OK : FIA_ERR_CUDA;
 }
 
 }  // extern "C"

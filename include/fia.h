@@ -276,9 +276,12 @@ fia_status sparse_attn_metadata(const sparse_attn_params *p, int32_t *metadata,
                                 size_t *workspace_bytes, void *stream);
 
 /* Main call: launches the gather-attention kernel and the chunk combine on
- * `stream`.  `metadata` must come from sparse_attn_metadata with the same
- * shapes; a header mismatch (B, N1, topk, units) is detected on the device and
- * leaves out/lse untouched... it is reported by sparse_attn_check_metadata. */
+ * `stream`; `workspace` needs the size sparse_attn_metadata reported.
+ * `metadata` must come from sparse_attn_metadata with the same shapes.  The
+ * kernels check its header (magic, CTA count, rows, B, N1, topk) on the
+ * device; on a mismatch they write nothing to out/lse and set the int32
+ * status word at workspace offset 0 to FIA_ERR_BAD_SHAPE (0 otherwise; read
+ * it with any device-to-host copy after the call). */
 fia_status sparse_attn_run(const sparse_attn_params *p, const int32_t *metadata,
                            void *workspace, size_t workspace_bytes, void *stream);
 

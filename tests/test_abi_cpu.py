@@ -142,3 +142,62 @@ def test_plan_layout_describes_decode_schedule():
     lay = fia.fia_get_plan_layout(_decode_params())
     assert lay.branch == 1 and lay.num_ctas == 152 and lay.num_units == 4 * 2 * 1
     assert lay.unit_prefix_off >= 256 and lay.cta_begin_off > lay.unit_prefix_off
+
+
+# --------------------------------------------------------------------------
+# shared-KV sparse attention: first-phase validation (no GPU: a metadata
+# pointer is needed only after validation passes, so invalid calls return
+# before anything is launched)
+# --------------------------------------------------------------------------
+
+def _sparse_params(**kw):
+    p = _abi.SparseParams()
+    p.batch, p.num_q_heads, p.head_dim, p.layout = 4, 64, 512, fia.LAYOUT_BSND
+    p.max_seqlen_q = 1
+    p.q = p.out = p.ori_kv = p.ori_block_table = p.seqused_kv = FAKE
+    p.ori_max_blocks, p.ori_block_size, p.ori_num_blocks = 64, 128, 300
+    p.cmp_kv = p.cmp_block_table = p.cmp_sparse_indices = FAKE
+    p.cmp_max_blocks, p.cmp_block_size, p.cmp_num_blocks, p.topk = 16, 128, 80, 512
+    p.softmax_scale = 0.044
+    p.cmp_ratio, p.ori_win_left, p.ori_win_right = 4, 127, 0
+    p.num_sms = 152
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def _sparse_status(p):
+    n = ctypes.c_size_t(0)
+    # a fake metadata pointer: validation fails before anything is launched
+    return fia.lib().sparse_attn_metadata(ctypes.byref(p), ctypes.c_void_p(FAKE),
+                                          ctypes.byref(n), None)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("q", 0, fia.FIA_ERR_NULL_ARG),
+    ("ori_block_table", 0, fia.FIA_ERR_NULL_ARG),
+    ("seqused_kv", 0, fia.FIA_ERR_NULL_ARG),
+    ("num_q_heads", 48, fia.FIA_ERR_BAD_SHAPE),      # a power of two
+    ("num_q_heads", 256, fia.FIA_ERR_BAD_SHAPE),     # <= 128
+    ("head_dim", 640, fia.FIA_ERR_BAD_SHAPE),        # <= 512
+    ("head_dim", 192, fia.FIA_ERR_UNSUPPORTED),      # valid, not built
+    ("ori_block_size", 40, fia.FIA_ERR_BAD_SHAPE),   # multiple of 16
+    ("cmp_block_size", 2048, fia.FIA_ERR_BAD_SHAPE),  # <= 1024
+    ("topk", 4096, fia.FIA_ERR_BAD_SHAPE),
+    ("cmp_ratio", 0, fia.FIA_ERR_BAD_SHAPE),
+    ("ori_win_left", -1, fia.FIA_ERR_BAD_SHAPE),
+    ("layout", 1, fia.FIA_ERR_NULL_ARG),             # TND needs cu_seqlens_q
+])
+def test_sparse_invalid_params_are_rejected(field, value, status):
+    assert _sparse_status(_sparse_params(**{field: value})) == status
+
+
+def test_sparse_indices_need_a_compressed_cache():
+    assert _sparse_status(_sparse_params(cmp_kv=0, cmp_block_table=0)) == fia.FIA_ERR_BAD_SHAPE
+
+
+def test_sparse_metadata_pointer_required():
+    p = _sparse_params()
+    n = ctypes.c_size_t(0)
+    assert fia.lib().sparse_attn_metadata(ctypes.byref(p), None, ctypes.byref(n), None) == \
+        fia.FIA_ERR_NULL_ARG

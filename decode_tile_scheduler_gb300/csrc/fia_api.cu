@@ -66,7 +66,8 @@ fia_status sm_count(int requested, int* n) {
 // 2-D tiled map over a row-major [rows, cols] matrix with 128-byte swizzling.
 fia_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
                     uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
-                    uint64_t row_stride_elems) {
+                    uint64_t row_stride_elems,
+                    CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   fia_status st = get_encoder(&enc);
   if (st != FIA_OK) return st;
@@ -75,8 +76,8 @@ fia_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, in
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FIA_OK : FIA_ERR_CUDA;
 }
 
@@ -227,9 +228,17 @@ fia_status kv_maps(const fia_params* p, int box_rows, CUtensorMap* tk, CUtensorM
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int es = fp8 ? 1 : 2;
   const uint32_t bc = fp8 ? 128 : 64;
-  fia_status st = make_map(tk, p->k_cache, dt, es, cols, rows ? rows : 1, bc, (uint32_t)box_rows, cols);
+  // One head's slice of a token is D * esize bytes: 256 for bf16 D=128 (two
+  // 128-byte boxes, so a 256-byte L2 fill is used in full) but 128 for FP8,
+  // where a 256-byte fill would also drag in the next head's slice.
+  const CUtensorMapL2promotion promo = (uint64_t)p->head_dim * es >= 256
+                                           ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                           : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+  fia_status st = make_map(tk, p->k_cache, dt, es, cols, rows ? rows : 1, bc, (uint32_t)box_rows,
+                           cols, promo);
   if (st != FIA_OK) return st;
-  return make_map(tv, p->v_cache, dt, es, cols, rows ? rows : 1, bc, (uint32_t)box_rows, cols);
+  return make_map(tv, p->v_cache, dt, es, cols, rows ? rows : 1, bc, (uint32_t)box_rows, cols,
+                  promo);
 }
 
 struct PrefillPlan {

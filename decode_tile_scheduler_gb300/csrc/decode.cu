@@ -155,6 +155,18 @@ __device__ __forceinline__ int64_t phys_row(const DecodeArgs& a, int b, int64_t 
   return (int64_t)b * a.S_kv + j;
 }
 
+// Row of the FP8 scale arrays for logical KV row j of batch b, KV head hk:
+// scales are stored head-major inside each page, [pages, KV_N, page rows,
+// D/64] (the paged per-token, per-head scale shape (blockNum, N, blockSize) of
+// the FIA dequantisation parameters, with the 64-element tiles last).
+__device__ __forceinline__ int64_t scale_row(const DecodeArgs& a, int b, int hk, int64_t j) {
+  if (a.block_table) {
+    const int64_t blk = a.block_table[(int64_t)b * a.max_blocks + j / a.block_size];
+    return (blk * a.KVN + hk) * a.block_size + j % a.block_size;
+  }
+  return ((int64_t)b * a.KVN + hk) * a.S_kv + j;
+}
+
 // Bounded barrier wait; after the first time-out in the CTA every later wait
 // returns at once, so a broken pipeline ends the kernel instead of hanging it.
 __device__ __forceinline__ void wait_or_abort(uint64_t* bar, uint32_t parity, int* err,
@@ -274,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], FP8 ? 33 : 1);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumers);
     }
     for (int s = 0; s < 2; ++s) {
@@ -347,43 +359,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool mine = lane < nbox && jb < r.kv_len;
         const int64_t prow = mine ? phys_row(a, r.b, jb) : 0;
         constexpr int NT = D / 64;
-        constexpr int kRowsPerLane = kKvTile / 32;
-        int64_t soff[kRowsPerLane];
+        // FP8: the scales of one head inside a page are contiguous rows of NT
+        // floats, so each (K or V, page piece) is one bulk copy next to its
+        // TMA box.  Pieces are even-length at even rows (block sizes are
+        // multiples of 32; contiguous caches have an even length), hence
+        // 16-byte aligned.
+        int64_t srow = 0;
+        int srows = a.box_rows;
         if constexpr (FP8) {
-#pragma unroll
-          for (int k = 0; k < kRowsPerLane; ++k) {
-            const int64_t j = j0 + lane + 32 * k;
-            soff[k] = j < r.kv_len ? (phys_row(a, r.b, j) * a.KVN + r.hk) * NT : -1;
+          if (mine) srow = scale_row(a, r.b, r.hk, jb);
+          if (!a.block_table) srows = (int)min((int64_t)a.box_rows, (int64_t)a.S_kv - jb);
+        }
+        int nvalid = 0, scale_rows = 0;
+        for (int q = 0; q < nrb; ++q) {
+          const int64_t jq = j0 + (int64_t)q * a.box_rows;
+          if (jq < r.kv_len) {
+            ++nvalid;
+            scale_rows += a.block_table ? a.box_rows : (int)min((int64_t)a.box_rows, (int64_t)a.S_kv - jq);
           }
         }
-        int nvalid = 0;
-        for (int q = 0; q < nrb; ++q)
-          if (j0 + (int64_t)q * a.box_rows < r.kv_len) ++nvalid;
         wait_or_abort(&empty[s], par, a.err, misc);
         uint8_t* st = smem + s * Cfg::kStageBytes;
-        if (lane == 0)
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * nvalid * Cfg::kNsub * a.box_rows * 128));
+        if (lane == 0) {
+          uint32_t bytes = (uint32_t)(2 * nvalid * Cfg::kNsub * a.box_rows * 128);
+          if constexpr (FP8) bytes += (uint32_t)(2 * scale_rows * NT * 4);
+          mbar_arrive_expect_tx(&full[s], bytes);
+        }
         __syncwarp();
         if (mine) {
           uint8_t* dst = st + isv * Cfg::kTileBytes + sub * (kKvTile * 128) + rb * a.box_rows * 128;
           const int col = FP8 ? r.hk * D : r.hk * D + sub * 64;
           tma_load_2d(dst, isv ? &tv : &tk, &full[s], col, (int)prow);
-        }
-        if constexpr (FP8) {
-          float* ks = reinterpret_cast<float*>(st + 2 * Cfg::kTileBytes);
-          float* vs = ks + kKvTile * NT;
-#pragma unroll
-          for (int k = 0; k < kRowsPerLane; ++k) {
-            const int rr = lane + 32 * k;
-            if (soff[k] >= 0) {
-#pragma unroll
-              for (int t2 = 0; t2 < NT; t2 += 2) {
-                cp_async_8(ks + rr * NT + t2, a.k_scale + soff[k] + t2);
-                cp_async_8(vs + rr * NT + t2, a.v_scale + soff[k] + t2);
-              }
-            }
+          if constexpr (FP8) {
+            float* sdst = reinterpret_cast<float*>(st + 2 * Cfg::kTileBytes) +
+                          isv * (kKvTile * NT) + rb * a.box_rows * NT;
+            bulk_load(sdst, (isv ? a.v_scale : a.k_scale) + srow * NT,
+                      (uint32_t)(srows * NT * 4), &full[s]);
           }
-          cp_async_arrive_noinc(&full[s]);
         }
       }
       if (!has_next) break;

@@ -123,9 +123,9 @@ fia_status validate(const fia_params* p) {
     if (!p->k_scale || !p->v_scale) return FIA_ERR_NULL_ARG;
     if (p->quant_tile != 64) return FIA_ERR_BAD_SHAPE;
     if (p->head_dim % 64) return FIA_ERR_BAD_SHAPE;
-    if ((reinterpret_cast<uintptr_t>(p->k_scale) & 7u) ||
-        (reinterpret_cast<uintptr_t>(p->v_scale) & 7u))
-      return FIA_ERR_BAD_SHAPE;
+    if (!aligned16(p->k_scale) || !aligned16(p->v_scale)) return FIA_ERR_BAD_SHAPE;
+    // scale pieces of a contiguous cache are copied in 16-byte units
+    if (!p->block_table && (p->max_seqlen_kv & 1)) return FIA_ERR_BAD_SHAPE;
   }
   if (p->block_table) {
     if (!p->seqused_kv) return FIA_ERR_NULL_ARG;

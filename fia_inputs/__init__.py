@@ -54,7 +54,7 @@ class FiaProblem:
     kv_dtype: int
     k_cache: torch.Tensor         # bf16 or uint8 (E4M3 codes)
     v_cache: torch.Tensor
-    k_scale: Optional[torch.Tensor]        # fp32 [nb,bs,KVN,D/64] (FP8)
+    k_scale: Optional[torch.Tensor]        # fp32 [nb,KVN,bs,D/64] / [B,KVN,S_kv,D/64] (FP8)
     v_scale: Optional[torch.Tensor]
     block_table: Optional[torch.Tensor]    # int32 [B,max_blocks] or None
     block_size: int
@@ -179,6 +179,15 @@ def quantize_e4m3_per_tile(x: torch.Tensor, tile: int = FP8_TILE):
     return codes.contiguous(), scale.contiguous()
 
 
+def scales_head_major(scales: torch.Tensor) -> torch.Tensor:
+    """Reorder per-row scales [pages, rows, KVN, D/64] (the shape the quantiser
+    returns for a pool [pages, rows, KVN, D]) to the stored layout
+    [pages, KVN, rows, D/64]: inside a page the scales of one KV head are
+    contiguous, as the page-managed per-token, per-head scale shape
+    (blockNum, N, blockSize) of the FIA dequantisation parameter group."""
+    return scales.permute(0, 2, 1, 3).contiguous()
+
+
 def _paged_layout(kv_lens, block_size, gen_cpu, max_blocks=None):
     """Block table for the given KV lengths over a randomly permuted pool
     with N_SPARE_BLOCKS poisoned spare blocks.  Returns (table int32
@@ -267,7 +276,8 @@ def make_fia(*, B, QN, KVN, D, q_lens, kv_lens, layout=LAYOUT_BSND, paged=True,
             vc.view(rows, -1)[inv] = 0x7F
             ks.view(rows, -1)[inv] = float("nan")
             vs.view(rows, -1)[inv] = float("nan")
-        k_cache, v_cache, k_scale, v_scale = kc, vc, ks, vs
+        k_cache, v_cache = kc, vc
+        k_scale, v_scale = scales_head_major(ks), scales_head_major(vs)
     else:
         if poison:
             inv = ~valid

@@ -86,10 +86,14 @@ typedef int fia_status;
  *    block_size: multiple of 16, <= 1024 (FP8: multiple of 32, <= 512).
  *  - contiguous (block_table == NULL): k_cache/v_cache are [B, max_seqlen_kv,
  *    KV_N, D]; seqused_kv optional (default max_seqlen_kv for every batch).
- *  - FP8: k_scale/v_scale fp32 with the same leading shape and D/64 in place
- *    of D ([num_blocks, block_size, KV_N, D/64] or [B, S_kv, KV_N, D/64]).
- * Alignment: q, out, k_cache, v_cache 16-byte aligned; token strides multiples
- * of 8 elements. */
+ *  - FP8: k_scale/v_scale fp32, head-major inside each page:
+ *    [num_blocks, KV_N, block_size, D/64] (paged) or [B, KV_N, max_seqlen_kv,
+ *    D/64] (contiguous; max_seqlen_kv even).  This is the page-managed
+ *    per-token, per-head scale shape (blockNum, N, blockSize) of the "V5"
+ *    dequantisation parameter group (DequantChecker), and its non-paged form
+ *    (B, N, KV_S), with the D/64 tiles of a row as the last axis.
+ * Alignment: q, out, k_cache, v_cache, k_scale, v_scale 16-byte aligned;
+ * token strides multiples of 8 elements. */
 typedef struct fia_params {
     int32_t batch;            /* B                                             */
     int32_t num_q_heads;      /* Q_N                                           */

@@ -42,7 +42,9 @@ def _dense_kv(p, b, which):
     if p.kv_dtype == 0:
         vals = _bf16_bits_to_f64(pool)
     else:
+        # stored [pages, KVN, rows, D/64]; back to [pages, rows, KVN, D/64]
         sc = _as_np(p.k_scale if which == "k" else p.v_scale).astype(np.float64)
+        sc = sc.transpose(0, 2, 1, 3)
         vals = _e4m3_to_f64(pool) * np.repeat(sc, 64, axis=-1)
     if p.block_table is not None:
         bt = _as_np(p.block_table)

@@ -83,7 +83,7 @@ typedef struct {
     const int32_t *cu_seqlens_q; /* TND: [B+1] cumulative query lengths          */
     int32_t kv_dtype;            /* 0 bf16, 1 FP8 E4M3 with fp32 tile scales     */
     const void *k, *v;           /* paged pool [nb,bs,KVN,D] or contiguous       */
-    const float *k_scale, *v_scale; /* [nb,bs,KVN,D/tile] (or contiguous)        */
+    const float *k_scale, *v_scale; /* [nb,KVN,bs,D/tile] or [B,KVN,S_kv,D/tile] */
     int32_t quant_tile;
     const int32_t *block_table;  /* [B,max_blocks] or NULL (contiguous)          */
     int32_t max_blocks, block_size;
@@ -109,6 +109,21 @@ static int64_t kv_row_base(const oracle_fia_args *a, int b, int64_t j, int g)
     return phys_row * a->KVN + g; /* row-head index; multiply by D (or D/tile) */
 }
 
+/* Index of the scale row of logical KV row j of batch b, head g.  The scales
+ * are laid out head-major inside each page, as [FIA-V5]'s DequantChecker group
+ * gives the page-managed per-token, per-head scale: (blockNum, N, blockSize),
+ * here with the D/tile tiles of a row as a last axis; without a block table
+ * the page is the whole sequence, (B, N, S_kv), as the non-paged per-token,
+ * per-head shape (B, N, KV_S) in the same group. */
+static int64_t scale_row(const oracle_fia_args *a, int b, int64_t j, int g)
+{
+    if (a->block_table) {
+        int64_t blk = a->block_table[(int64_t)b * a->max_blocks + j / a->block_size];
+        return (blk * a->KVN + g) * a->block_size + j % a->block_size;
+    }
+    return ((int64_t)b * a->KVN + g) * a->S_kv + j;
+}
+
 static double kv_value(const oracle_fia_args *a, const void *pool, const float *scales,
                        int b, int64_t j, int g, int d)
 {
@@ -119,7 +134,7 @@ static double kv_value(const oracle_fia_args *a, const void *pool, const float *
     {
         double c = oracle_e4m3_to_double(((const uint8_t *)pool)[rh * a->D + d]);
         int ntile = a->D / a->quant_tile;
-        double s = (double)scales[rh * ntile + d / a->quant_tile];
+        double s = (double)scales[scale_row(a, b, j, g) * ntile + d / a->quant_tile];
         return c * s;
     }
 }

@@ -118,6 +118,19 @@ def test_fp8_needs_scales_and_tile_64():
                                   block_size=48))[0] == fia.FIA_ERR_BAD_SHAPE
 
 
+def test_fp8_scale_alignment_and_contiguous_length():
+    fp8 = dict(kv_dtype=1, quant_tile=64, k_scale=FAKE, v_scale=FAKE)
+    # scale arrays are copied in 16-byte pieces
+    assert _status(_decode_params(**{**fp8, "k_scale": FAKE + 8}))[0] == fia.FIA_ERR_BAD_SHAPE
+    assert _status(_decode_params(**{**fp8, "v_scale": FAKE + 8}))[0] == fia.FIA_ERR_BAD_SHAPE
+    # a contiguous FP8 cache needs an even max_seqlen_kv
+    contig = dict(block_table=None, seqused_kv=None, max_blocks_per_seq=0, num_blocks=0,
+                  block_size=0)
+    assert _status(_decode_params(**fp8, **contig, max_seqlen_kv=301))[0] == \
+        fia.FIA_ERR_BAD_SHAPE
+    assert _status(_decode_params(**fp8, **contig, max_seqlen_kv=300))[0] == fia.FIA_OK
+
+
 def test_tnd_needs_cu_seqlens():
     assert _status(_decode_params(layout=fia.LAYOUT_TND, total_q=4))[0] == fia.FIA_ERR_NULL_ARG
     assert _status(_decode_params(layout=fia.LAYOUT_TND, total_q=4, cu_seqlens_q=FAKE))[0] == \

@@ -194,13 +194,14 @@ def _to_contiguous(p):
             v[b, j] = p.v_cache[blk, j % bs]
     q.k_cache, q.v_cache = k, v
     if p.k_scale is not None:
-        ks = torch.zeros((p.B, S, p.KVN, p.D // 64), dtype=torch.float32)
+        # head-major inside a page: [pages, KVN, rows, D/64]
+        ks = torch.zeros((p.B, p.KVN, S, p.D // 64), dtype=torch.float32)
         vs = torch.zeros_like(ks)
         for b in range(p.B):
             for j in range(p.kv_lens[b]):
                 blk = int(p.block_table[b, j // bs])
-                ks[b, j] = p.k_scale[blk, j % bs]
-                vs[b, j] = p.v_scale[blk, j % bs]
+                ks[b, :, j] = p.k_scale[blk, :, j % bs]
+                vs[b, :, j] = p.v_scale[blk, :, j % bs]
         q.k_scale, q.v_scale = ks, vs
     q.block_table = None
     q.S_kv = S
@@ -270,8 +271,9 @@ def test_fp8_on_grid_equals_bf16():
     p.k_scale, p.v_scale = ks, vs
     b = copy.copy(p)
     b.kv_dtype = fi.KV_BF16
-    dk = p.k_cache.view(torch.float8_e4m3fn).float() * ks.repeat_interleave(64, -1)
-    dv = p.v_cache.view(torch.float8_e4m3fn).float() * vs.repeat_interleave(64, -1)
+    # scales are stored [pages, KVN, rows, D/64]; the pool is [pages, rows, KVN, D]
+    dk = p.k_cache.view(torch.float8_e4m3fn).float() * ks.transpose(1, 2).repeat_interleave(64, -1)
+    dv = p.v_cache.view(torch.float8_e4m3fn).float() * vs.transpose(1, 2).repeat_interleave(64, -1)
     b.k_cache, b.v_cache = dk.to(torch.bfloat16), dv.to(torch.bfloat16)
     assert torch.equal(b.k_cache.float(), dk) and torch.equal(b.v_cache.float(), dv)
     b.k_scale = b.v_scale = None

@@ -158,6 +158,10 @@ class L2Flush:
     def zero_(self):
         self.w.zero_()
         torch.sum(self.r, dim=0, out=self.sink[0])
+        # Hold the stream for ~50 us after the flush so that the host has
+        # queued the whole step before its first event runs: the events then
+        # time device work only, never the host's launch latency.
+        torch.cuda._sleep(100_000)
 
 
 def _flush_buf():

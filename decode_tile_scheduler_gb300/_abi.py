@@ -68,8 +68,8 @@ class SparseParams(ctypes.Structure):
 
 class FiaPlanLayout(ctypes.Structure):
     _fields_ = [
-        ("branch", _I), ("num_ctas", _I), ("num_units", _L), ("unit_prefix_off", _L),
-        ("cta_begin_off", _L), ("unit_list_off", _L), ("total_bytes", _L),
+        ("branch", _I), ("num_ctas", _I), ("num_units", _L), ("max_chunks", _L),
+        ("sched_off", _L), ("queue_off", _L), ("unit_list_off", _L), ("total_bytes", _L),
     ]
 
 

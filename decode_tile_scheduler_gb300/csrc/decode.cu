@@ -9,11 +9,18 @@
 // unit owns the KV tiles (128 positions) its query row can see.
 //
 // Scheduler (decode_schedule_kernel): cost(u) = visible tiles (>= 1; 0 when
-// the batch has no query row); CTA c of n persistent CTAs owns the global tile
-// interval [floor(c*total/n), floor((c+1)*total/n)) of the units laid end to
-// end, so all CTAs get the same number of tiles within one.  A unit cut by a
-// CTA boundary is split-KV: each piece writes its (m, l, acc) partial and the
-// last piece to finish folds all pieces in CTA order (deterministic).
+// the batch has no query row).  With T the total cost and n persistent CTAs,
+// the chunk size is C = ceil(T / (n * W)) tiles (W chunks per CTA, at least
+// one tile), and a unit of cost c is cut into n1 = max(0, floor(c/C) - 1) big
+// chunks of C tiles followed by the remaining r = c - n1*C tiles (C <= r < 2C
+// unless c < C) in small chunks of c2 = ceil(C/2) tiles.  The claim queue
+// lists every big chunk (batch-major, then chunk, then unit of the batch)
+// before every small chunk (same order), so the work left at the end is
+// always small pieces.  CTAs claim chunks from the queue with one atomic each:
+// an SM that streams faster simply takes more chunks.  A unit cut into several
+// chunks is split-KV: each chunk writes its (m, l, acc) partial to the slot
+// of its (unit, chunk index), and a combine kernel, launched next on the
+// stream, folds them in chunk order (deterministic, whichever CTAs ran them).
 //
 // Decode kernel: one producer warp streams K and V pages with TMA (page rows
 // from block_table) into a ring of shared-memory stages; eight consumer warps
@@ -24,6 +31,7 @@
 // head (column).  FP8 E4M3 pages are widened to fp16 in registers (exact);
 // K tile scales multiply the per-64-column partial scores and V tile scales
 // are folded into P^T, so the dequantised cache is never materialised.
+#include <algorithm>
 #include <atomic>
 
 #include "common.cuh"
@@ -74,24 +82,18 @@ struct UnitInfo {
   int tile0, ntiles;
 };
 
-__device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int64_t u) {
+// Unit u of batch b (unit w of the batch) with the batch's query row, query
+// length and KV length already known.
+__device__ __forceinline__ UnitInfo unit_from(const DecodeArgs& a, int b, int w, int64_t qrow,
+                                              int64_t ql, int64_t kv_len) {
   UnitInfo r;
-  const int per_b = a.KVN * a.HG;
-  r.b = (int)(u / per_b);
-  const int rem = (int)(u % per_b);
-  r.hk = rem / a.HG;
-  r.hg = rem % a.HG;
+  r.b = b;
+  r.hk = w / a.HG;
+  r.hg = w % a.HG;
   r.h0 = r.hk * a.G + r.hg * a.GH;
   r.nrows = min(a.GH, a.G - r.hg * a.GH);
-  int64_t ql;
-  if (a.layout == 1) {
-    r.qrow = a.cu_seqlens_q[r.b];
-    ql = (int64_t)a.cu_seqlens_q[r.b + 1] - r.qrow;
-  } else {
-    r.qrow = (int64_t)r.b * a.S_q;
-    ql = a.S_q;
-  }
-  r.kv_len = a.seqused_kv ? a.seqused_kv[r.b] : a.S_kv;
+  r.qrow = qrow;
+  r.kv_len = kv_len;
   const int64_t p = r.kv_len - 1;  // the single query row sits at the last key
   int64_t lo = 0, hi = r.kv_len - 1;
   if (a.mask_mode == 3) {
@@ -112,37 +114,66 @@ __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int64_t u) {
   return r;
 }
 
-// What the producer hands the consumers with each unit's query rows (one per
-// query buffer), so that consumers never wait on global loads between units.
+// Query row, query length and KV length of batch b.
+__device__ __forceinline__ void batch_lengths(const DecodeArgs& a, int b, int64_t* qrow,
+                                              int64_t* ql, int64_t* kv_len) {
+  if (a.layout == 1) {
+    *qrow = a.cu_seqlens_q[b];
+    *ql = (int64_t)a.cu_seqlens_q[b + 1] - *qrow;
+  } else {
+    *qrow = (int64_t)b * a.S_q;
+    *ql = a.S_q;
+  }
+  *kv_len = a.seqused_kv ? a.seqused_kv[b] : a.S_kv;
+}
+
+__device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int64_t u) {
+  const int per_b = a.KVN * a.HG;
+  const int b = (int)(u / per_b);
+  int64_t qrow, ql, kv_len;
+  batch_lengths(a, b, &qrow, &ql, &kv_len);
+  return unit_from(a, b, (int)(u % per_b), qrow, ql, kv_len);
+}
+
+// What the producer hands the consumers with each chunk's query rows (one per
+// query buffer), so that consumers never wait on global loads between chunks.
 struct UnitMsg {
   UnitInfo r;
-  int64_t u, pu, pu1;
-  int t_begin, t_end, split, first, done;
+  int64_t u;      // unit; its chunk i owns partial slot Q[b] + i * UPB + (u - b * UPB)
+  int ci, nch;    // chunk index within the unit, chunks of the unit
+  int t_begin, t_end, done;
 };
 static_assert(sizeof(UnitMsg) <= 128, "message slot");
 
-// largest u with prefix[u] <= g (prefix[U] > g)
-__device__ __forceinline__ int64_t find_unit(const int64_t* prefix, int64_t U, int64_t g) {
-  int64_t lo = 0, hi = U;  // invariant prefix[lo] <= g < prefix[hi]
-  while (hi - lo > 1) {
-    const int64_t mid = (lo + hi) >> 1;
-    if (prefix[mid] <= g) lo = mid; else hi = mid;
-  }
-  return lo;
+// Chunking of a unit of `cost` tiles: n1 big chunks of C tiles, then small
+// chunks of c2 tiles over the rest.
+struct ChunkGeom {
+  int n1, nch;
+};
+__device__ __forceinline__ ChunkGeom chunk_geom(int64_t cost, int64_t C, int64_t c2) {
+  ChunkGeom g;
+  const int64_t n1 = max((int64_t)0, cost / C - 1);
+  const int64_t rest = cost - n1 * C;
+  g.n1 = (int)n1;
+  g.nch = (int)(n1 + (rest + c2 - 1) / c2);
+  return g;
 }
 
-__device__ __forceinline__ int64_t next_unit(const int64_t* prefix, int64_t U, int64_t u) {
-  ++u;
-  while (u < U && prefix[u + 1] == prefix[u]) ++u;
-  return u;
+// Cost of every unit of batch b (all units of a batch see the same tiles).
+__device__ __forceinline__ int64_t batch_cost(const DecodeArgs& a, int b) {
+  const UnitInfo r = unit_info(a, (int64_t)b * a.KVN * a.HG);
+  int64_t ql;
+  if (a.layout == 1) ql = (int64_t)a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b];
+  else ql = a.S_q;
+  return ql > 0 ? max(1, r.ntiles) : 0;
 }
 
-// largest c with cta_begin[c] <= g
-__device__ __forceinline__ int find_cta(const int64_t* beg, int n, int64_t g) {
-  int lo = 0, hi = n;
+// largest b with prefix[b] <= g (prefix[0] = 0 <= g < prefix[B])
+__device__ __forceinline__ int find_batch(const int64_t* prefix, int B, int64_t g) {
+  int lo = 0, hi = B;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (beg[mid] <= g) lo = mid; else hi = mid;
+    if (prefix[mid] <= g) lo = mid; else hi = mid;
   }
   return lo;
 }
@@ -204,58 +235,145 @@ __device__ __forceinline__ void finish_head(const DecodeArgs& a, int h, float M,
 // ---------------------------------------------------------------------------
 // scheduler
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs a) {
-  __shared__ int64_t warp_sums[32];
-  __shared__ int64_t carry;
-  const int64_t U = a.num_units;
-  int64_t* prefix = const_cast<int64_t*>(a.unit_prefix);
-  int64_t* beg = const_cast<int64_t*>(a.cta_begin);
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (tid == 0) carry = 0;
-  __syncthreads();
-  for (int64_t base = 0; base < U; base += blockDim.x) {
-    const int64_t u = base + tid;
-    int64_t cost = 0;
-    if (u < U) {
-      UnitInfo r = unit_info(a, u);
-      int64_t ql;
-      if (a.layout == 1) ql = (int64_t)a.cu_seqlens_q[r.b + 1] - a.cu_seqlens_q[r.b];
-      else ql = a.S_q;
-      cost = ql > 0 ? max(1, r.ntiles) : 0;
-      a.counters[u] = 0;
-    }
-    // block-wide inclusive scan of cost
-    int64_t x = cost;
+// Block-wide exclusive scan of three counters over the 1024 threads; returns
+// the block totals in tot[] (every thread).
+__device__ __forceinline__ void scan3(int64_t (&x)[3], int64_t (&tot)[3], int64_t (*ws)[3]) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int64_t incl[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    int64_t v = x[k];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+      const int64_t y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
     }
-    if (lane == 31) warp_sums[wid] = x;
-    __syncthreads();
-    if (wid == 0) {
-      int64_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+    incl[k] = v;
+    if (lane == 31) ws[wid][k] = v;
+  }
+  __syncthreads();
+  if (wid == 0) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      int64_t v = lane < (int)(blockDim.x >> 5) ? ws[lane][k] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += y;
+        const int64_t y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
       }
-      warp_sums[lane] = w;
+      ws[lane][k] = v;
     }
-    __syncthreads();
-    const int64_t excl = carry + (wid ? warp_sums[wid - 1] : 0) + x - cost;
-    if (u < U) prefix[u] = excl;
-    __syncthreads();
-    if (tid == blockDim.x - 1) carry = excl + cost;
-    __syncthreads();
   }
-  const int64_t total = carry;
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const int64_t before = wid ? ws[wid - 1][k] : 0;
+    tot[k] = ws[31][k];
+    x[k] = before + incl[k] - x[k];
+  }
+  __syncthreads();
+}
+
+constexpr int kSchedSmemBatches = 2048;  // queue prefixes kept in shared memory up to this B
+
+__global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs a) {
+  __shared__ int64_t ws[32][3];
+  __shared__ int64_t s_total;
+  __shared__ int64_t sR[2][kSchedSmemBatches + 1];
+  const int tid = threadIdx.x, lane = tid & 31;
+  pdl_trigger();  // the decode kernel may set up while the plan is built
+  const int B = a.B;
+  const int UPB = a.KVN * a.HG;
+  int64_t* sched = a.sched;
+  int64_t* Q = sched + 4;            // [B+1] partial slots before batch b
+  int64_t* R1 = Q + (B + 1);         // [B+1] big-chunk queue positions
+  int64_t* R2 = R1 + (B + 1);        // [B+1] small-chunk queue positions
+
+  // total cost
+  int64_t part = 0;
+  for (int b = tid; b < B; b += blockDim.x) part += batch_cost(a, b);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if (tid == 0) s_total = 0;
+  __syncthreads();
+  if (lane == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&s_total),
+                           (unsigned long long)part);
+  __syncthreads();
+  const int64_t T = s_total * UPB;
+  const int64_t per = (int64_t)a.num_ctas * a.chunks_per_cta;
+  const int64_t C = max((int64_t)1, (T + per - 1) / per);
+  const int64_t c2 = (C + 1) / 2;
+
+  // per batch: chunks of each unit (all, big, small) -> three exclusive scans
+  int64_t carry[3] = {0, 0, 0};
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + tid;
+    int64_t x[3] = {0, 0, 0};
+    if (b < B) {
+      const int64_t cost = batch_cost(a, b);
+      if (cost > 0) {
+        const ChunkGeom gm = chunk_geom(cost, C, c2);
+        x[0] = (int64_t)gm.nch * UPB;
+        x[1] = (int64_t)gm.n1 * UPB;
+        x[2] = (int64_t)(gm.nch - gm.n1) * UPB;
+      }
+    }
+    int64_t tot[3];
+    scan3(x, tot, ws);
+    if (b < B) {
+      Q[b] = carry[0] + x[0];
+      R1[b] = carry[1] + x[1];
+      R2[b] = carry[2] + x[2];
+      if (B <= kSchedSmemBatches) {
+        sR[0][b] = R1[b];
+        sR[1][b] = R2[b];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k) carry[k] += tot[k];
+  }
+  // N <= n*W + 4*U always holds (the workspace bound); a plan that broke it
+  // would run nothing and say so in the error word
+  const bool fits = carry[0] <= a.max_chunks;
+  const int64_t F = fits ? carry[1] : 0, N = fits ? carry[0] : 0;
   if (tid == 0) {
-    prefix[U] = total;
-    *a.err = 0;  // error word of this plan's execution
+    Q[B] = carry[0];
+    R1[B] = carry[1];
+    R2[B] = carry[2];
+    if (B <= kSchedSmemBatches) {
+      sR[0][B] = carry[1];
+      sR[1][B] = carry[2];
+    }
+    sched[0] = C;
+    sched[1] = c2;
+    sched[2] = N;
+    sched[3] = F;
+    a.claim[0] = 0;
+    a.claim[1] = 0;
+    *a.err = fits ? 0 : 2;  // error word of this plan's execution
   }
-  for (int c = tid; c <= a.num_ctas; c += blockDim.x)
-    beg[c] = (int64_t)c * total / a.num_ctas;
+  __syncthreads();
+  // the claim queue: big chunks, then small chunks
+  const int64_t* P1 = B <= kSchedSmemBatches ? sR[0] : R1;
+  const int64_t* P2 = B <= kSchedSmemBatches ? sR[1] : R2;
+  for (int64_t g = tid; g < N; g += blockDim.x) {
+    int b, ci, w;
+    if (g < F) {
+      b = find_batch(P1, B, g);
+      const int64_t local = g - P1[b];
+      ci = (int)(local / UPB);
+      w = (int)(local % UPB);
+    } else {
+      b = find_batch(P2, B, g - F);
+      const int64_t local = g - F - P2[b];
+      const int n1 = (int)((P1[b + 1] - P1[b]) / UPB);
+      ci = n1 + (int)(local / UPB);
+      w = (int)(local % UPB);
+    }
+    int64_t qrow, ql, kv_len;
+    batch_lengths(a, b, &qrow, &ql, &kv_len);
+    a.queue[g] = make_int4(b, (ci << 10) | w, (int)kv_len, (int)qrow);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -280,9 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* red_ml = reinterpret_cast<float*>(smem + Cfg::kOffRedMl);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x;
-  const int64_t U = a.num_units;
-  const int64_t g0 = a.cta_begin[c], g1 = a.cta_begin[c + 1];
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -296,47 +411,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[0] = 0;  // abort flag
     fence_barrier_init();
   }
+  if (tid == 0) {
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+  }
   __syncthreads();
-  if (g0 >= g1) return;
-
-  const int64_t u0 = find_unit(a.unit_prefix, U, g0);
+  pdl_wait();  // the plan (and anything else before us on the stream) is complete
 
   if (warp == 0) {
     // ======================= producer =======================
-    if (lane == 0) {
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-    }
+    const int64_t C = a.sched[0], c2 = a.sched[1], N = a.sched[2];
+    const int UPB = a.KVN * a.HG;
     int it = 0, ucount = 0;
-    int64_t u = u0;
-    UnitInfo r = unit_info(a, u);
-    int64_t pu = a.unit_prefix[u], pu1 = a.unit_prefix[u + 1];
-    while (true) {
-      // the next unit's description is loaded one unit ahead
-      const int64_t un = next_unit(a.unit_prefix, U, u);
-      const int64_t pun = un < U ? a.unit_prefix[un] : g1;
-      const bool has_next = un < U && pun < g1;
-      UnitInfo rn = r;
-      int64_t pun1 = pu1;
-      if (has_next) {
-        rn = unit_info(a, un);
-        pun1 = a.unit_prefix[un + 1];
+    // claim the first chunk; every later claim is issued one chunk ahead and
+    // only read after the chunk's tiles are queued, so its latency hides
+    int64_t g = 0;
+    if (lane == 0) g = atomicAdd(a.claim, 1);
+    g = __shfl_sync(0xffffffffu, g, 0);
+    int4 ent = g < N ? a.queue[g] : make_int4(0, 0, 0, 0);
+    bool aborted = false;
+    while (g < N) {
+      // claim the next chunk now; its result and queue entry are read once
+      // the first tile of this chunk is queued, so neither latency is exposed
+      int gn_l = 0;
+      if (lane == 0) gn_l = atomicAdd(a.claim, 1);
+      int64_t gn = N;
+      int4 ent_n = make_int4(0, 0, 0, 0);
+      bool fetched = false;
+      const int b = ent.x, ci = ent.y >> 10, w = ent.y & 1023;
+      const int64_t u = (int64_t)b * UPB + w;
+      const UnitInfo r = unit_from(a, b, w, ent.w, 1, ent.z);
+      const int64_t cost = max(1, r.ntiles);
+      const ChunkGeom gm = chunk_geom(cost, C, c2);
+      int t_begin, t_end;
+      if (ci < gm.n1) {
+        t_begin = (int)(ci * C);
+        t_end = (int)(t_begin + C);
+      } else {
+        t_begin = (int)(gm.n1 * C + (ci - gm.n1) * c2);
+        t_end = (int)min(cost, t_begin + c2);
       }
-      const int t_begin = (int)(max(g0, pu) - pu);
-      const int t_end = (int)(min(g1, pu1) - pu);
-      {  // unit description + query rows of the group (one bulk copy)
+      {  // chunk description + query rows of the group (one bulk copy)
         const int qs = ucount & 1;
         wait_or_abort(&qempty[qs], ((ucount >> 1) & 1) ^ 1, a.err, misc);
         if (lane == 0) {
           UnitMsg& m = msg[qs];
           m.r = r;
           m.u = u;
-          m.pu = pu;
-          m.pu1 = pu1;
+          m.ci = ci;
+          m.nch = gm.nch;
           m.t_begin = t_begin;
           m.t_end = t_end;
-          m.split = (pu < g0) || (pu1 > g1);
-          m.first = (u == u0);
           m.done = 0;
           const uint32_t bytes = (uint32_t)(r.nrows * D * 2);
           mbar_arrive_expect_tx(&qfull[qs], bytes);
@@ -379,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         wait_or_abort(&empty[s], par, a.err, misc);
+        if (*reinterpret_cast<volatile int*>(misc)) break;  // issue nothing after a time-out
         uint8_t* st = smem + s * Cfg::kStageBytes;
         if (lane == 0) {
           uint32_t bytes = (uint32_t)(2 * nvalid * Cfg::kNsub * a.box_rows * 128);
@@ -397,12 +523,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (uint32_t)(srows * NT * 4), &full[s]);
           }
         }
+        if (!fetched) {
+          gn = __shfl_sync(0xffffffffu, (int64_t)gn_l, 0);
+          if (gn < N) ent_n = a.queue[gn];
+          fetched = true;
+        }
       }
-      if (!has_next) break;
-      u = un;
-      r = rn;
-      pu = pun;
-      pu1 = pun1;
+      if (*reinterpret_cast<volatile int*>(misc)) {
+        aborted = true;
+        break;
+      }
+      if (!fetched) {
+        gn = __shfl_sync(0xffffffffu, (int64_t)gn_l, 0);
+        if (gn < N) ent_n = a.queue[gn];
+      }
+      g = gn;
+      ent = ent_n;
+    }
+    if (aborted) {
+      // a wait timed out: issue nothing more, give the copies already in
+      // flight a bounded time to land, and leave (the error word is set)
+      for (int k = max(0, it - S); k < it; ++k) mbar_wait(&full[k % S], (k / S) & 1, a.err);
+      return;
+    }
+    pdl_trigger();  // this CTA loads nothing more: the combine kernel may launch
+    // this CTA claims no more: the last CTA out resets the queue for the
+    // next fia_execute with the same plan
+    if (lane == 0) {
+      __threadfence();  // this CTA's last claim is performed before it counts out
+      if (atomicAdd(a.claim + 1, 1) == a.num_ctas - 1) {
+        a.claim[0] = 0;
+        a.claim[1] = 0;
+      }
     }
     {  // end of the CTA's work: an empty message
       const int qs = ucount & 1;
@@ -432,9 +584,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait_or_abort(&qfull[qs], (ucount >> 1) & 1, a.err, misc);
     if (msg[qs].done || *reinterpret_cast<volatile int*>(misc)) break;
     const UnitInfo r = msg[qs].r;
-    const int64_t u = msg[qs].u, pu = msg[qs].pu, pu1 = msg[qs].pu1;
+    const int64_t slot0 = a.sched[4 + r.b] + (msg[qs].u - (int64_t)r.b * a.KVN * a.HG);
     const int t_begin = msg[qs].t_begin, t_end = msg[qs].t_end;
-    const bool split = msg[qs].split, first = msg[qs].first;
+    const int ci = msg[qs].ci, nch = msg[qs].nch;
+    const bool split = nch > 1;
+    const int64_t UPB = (int64_t)a.KVN * a.HG;
+    const int64_t pstride = (int64_t)a.GH * (D + 2);  // floats per partial slot
 
     // ---- Q^T fragments (mma B operand: k = d, n = head) ----
     uint32_t qb[NG][KS][2];
@@ -840,64 +995,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        const int slot = 2 * c + (first ? 0 : 1);
-        float* pp = a.partials + (size_t)slot * kMaxGH * (D + 2);
+        float* pp = a.partials + (slot0 + ci * UPB) * pstride;
         for (int idx = ctid; idx < nh * (D + 2); idx += nthr) {
           const int hh = idx / (D + 2), d = idx % (D + 2);
           const float v = d < D ? red[d * 8 + hh] : red_ml[hh * 2 + (d - D)];
           pp[(ng * 8 + hh) * (D + 2) + d] = v;
-        }
-        __threadfence();
-      }
-      named_bar_sync(1, nthr);
-    }
-    if (split) {
-      // the last piece of a split unit folds all pieces in CTA order; pieces:
-      // CTA cf (the one holding tile pu) and every later CTA up to cl whose
-      // interval is non-empty (CTAs with empty intervals hold nothing)
-      const int cf = find_cta(a.cta_begin, a.num_ctas, pu);
-      const int cl = find_cta(a.cta_begin, a.num_ctas, pu1 - 1);
-      int nseg = 1;
-      for (int cc = cf + 1; cc <= cl; ++cc) nseg += a.cta_begin[cc] < a.cta_begin[cc + 1];
-      if (ctid == 0) {
-        const int prev = atomicAdd(&a.counters[u], 1);
-        misc[1] = (prev == nseg - 1);
-      }
-      named_bar_sync(1, nthr);
-      if (misc[1]) {
-        __threadfence();
-        for (int idx = ctid; idx < r.nrows * (D / 2); idx += nthr) {
-          const int head = idx / (D / 2);
-          const int d = (idx % (D / 2)) * 2;
-          float M = -INFINITY;
-          for (int cc = cf; cc <= cl; ++cc) {
-            if (cc > cf && a.cta_begin[cc] == a.cta_begin[cc + 1]) continue;
-            const int slot = 2 * cc + ((cc == cf && a.cta_begin[cc] < pu) ? 1 : 0);
-            const float* pp = a.partials + (size_t)slot * kMaxGH * (D + 2) + head * (D + 2);
-            M = fmaxf(M, __ldcg(pp + D));
-          }
-          const float Mu = M == -INFINITY ? 0.f : M;
-          float L = 0.f, o0 = 0.f, o1 = 0.f;
-          for (int cc = cf; cc <= cl; ++cc) {
-            if (cc > cf && a.cta_begin[cc] == a.cta_begin[cc + 1]) continue;
-            const int slot = 2 * cc + ((cc == cf && a.cta_begin[cc] < pu) ? 1 : 0);
-            const float* pp = a.partials + (size_t)slot * kMaxGH * (D + 2) + head * (D + 2);
-            const float mw = __ldcg(pp + D);
-            if (mw == -INFINITY) continue;
-            const float f = exp2f(mw - Mu);
-            L += __ldcg(pp + D + 1) * f;
-            o0 += __ldcg(pp + d) * f;
-            o1 += __ldcg(pp + d + 1) * f;
-          }
-          const int h = r.h0 + head;
-          float scl, lse;
-          finish_head(a, h, M, L, &scl, &lse);
-          uint16_t* o = a.out + r.qrow * a.out_stride + (int64_t)h * D + d;
-          *reinterpret_cast<uint32_t*>(o) = pack_bf16(o0 * scl, o1 * scl);
-          if (a.lse && d == 0) {
-            const int64_t li = a.layout == 1 ? r.qrow * a.QN + h : ((int64_t)r.b * a.QN + h) * a.S_q;
-            a.lse[li] = lse;
-          }
         }
       }
       named_bar_sync(1, nthr);
@@ -906,8 +1008,154 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// split-KV combine: one CTA per unit cut into several chunks; the partials of
+// its chunks are folded in chunk order (deterministic), then the sink and the
+// final normalisation are applied.
+// ---------------------------------------------------------------------------
+// Fold chunk partials k = k0, k0 + step, ... (< nch) of one (unit, head) into
+// (M, L, o0, o1) for the d-pair at d, eight loads in flight at a time.
+template <int D>
+__device__ __forceinline__ void fold_chunks(const float* base, int64_t kstride, int d, int k0,
+                                            int step, int nch, float& M, float& L, float& o0,
+                                            float& o1) {
+  constexpr int NB = 4;  // partials in flight per thread
+  for (int kb = k0; kb < nch; kb += NB * step) {
+    float2 ml[NB], ov[NB];
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      const int kk = kb + k * step;
+      ml[k] = make_float2(-INFINITY, 0.f);
+      ov[k] = make_float2(0.f, 0.f);
+      if (kk < nch) {
+        const float* pp = base + kk * kstride;
+        ml[k] = __ldcg(reinterpret_cast<const float2*>(pp + D));  // (m, l)
+        ov[k] = __ldcg(reinterpret_cast<const float2*>(pp + d));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      if (ml[k].x == -INFINITY) continue;
+      const float Mn = fmaxf(M, ml[k].x);
+      const float fo = M == -INFINITY ? 0.f : exp2f(M - Mn);
+      const float fn = exp2f(ml[k].x - Mn);
+      L = L * fo + ml[k].y * fn;
+      o0 = o0 * fo + ov[k].x * fn;
+      o1 = o1 * fo + ov[k].y * fn;
+      M = Mn;
+    }
+  }
+}
+
+// Unit and head of combine item pr, and whether it needs combining: returns
+// the number of chunks (0 when the item is skipped) and the partial base.
+__device__ __forceinline__ int combine_item(const DecodeArgs& a, int64_t pr, int D, UnitInfo* r,
+                                            int* head, const float** base) {
+  const int64_t UPB = (int64_t)a.KVN * a.HG;
+  const int64_t u = pr / a.GH;
+  *head = (int)(pr % a.GH);
+  const int b = (int)(u / UPB), w = (int)(u % UPB);
+  if (*head >= min(a.GH, a.G - (w % a.HG) * a.GH)) return 0;  // past the group's heads
+  int64_t qrow, ql, kv_len;
+  batch_lengths(a, b, &qrow, &ql, &kv_len);
+  if (ql <= 0) return 0;
+  *r = unit_from(a, b, w, qrow, ql, kv_len);
+  const ChunkGeom gm = chunk_geom(max(1, r->ntiles), a.sched[0], a.sched[1]);
+  if (gm.nch <= 1) return 0;  // written by the decode kernel itself
+  *base = a.partials + (a.sched[4 + b] + w) * (int64_t)a.GH * (D + 2) + *head * (D + 2);
+  return gm.nch;
+}
+
+__device__ __forceinline__ void combine_store(const DecodeArgs& a, const UnitInfo& r, int head,
+                                              int D, int d, float M, float L, float o0,
+                                              float o1) {
+  const int h = r.h0 + head;
+  float scl, lse;
+  finish_head(a, h, M, L, &scl, &lse);
+  uint16_t* o = a.out + r.qrow * a.out_stride + (int64_t)h * D + d;
+  *reinterpret_cast<uint32_t*>(o) = pack_bf16(o0 * scl, o1 * scl);
+  if (a.lse && d == 0) {
+    const int64_t li = a.layout == 1 ? r.qrow * a.QN + h : ((int64_t)r.b * a.QN + h) * a.S_q;
+    a.lse[li] = lse;
+  }
+}
+
+// Few chunks per unit: one thread per (unit, head, d-pair), chunks folded in
+// order.
+template <int D>
+__global__ void __launch_bounds__(256, 4) decode_combine_flat(const DecodeArgs a) {
+  constexpr int TPP = D / 2, PPB = 256 / TPP;
+  pdl_wait();  // every partial of the decode kernel is written
+  const int64_t pr = (int64_t)blockIdx.x * PPB + threadIdx.x / TPP;
+  if (pr >= a.num_units * a.GH) return;
+  const int d = 2 * (threadIdx.x % TPP);
+  UnitInfo r;
+  int head;
+  const float* base;
+  const int nch = combine_item(a, pr, D, &r, &head, &base);
+  if (nch == 0) return;
+  const int64_t kstride = (int64_t)a.KVN * a.HG * a.GH * (D + 2);
+  float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f;
+  fold_chunks<D>(base, kstride, d, 0, 1, nch, M, L, o0, o1);
+  combine_store(a, r, head, D, d, M, L, o0, o1);
+}
+
+// Many chunks per unit: one CTA per (unit, head); NGRP thread groups fold
+// every NGRP-th chunk, then group 0 folds the groups in order.
+template <int D>
+__global__ void __launch_bounds__(256, 4) decode_combine_grouped(const DecodeArgs a) {
+  constexpr int TPP = D / 2, NGRP = 256 / TPP;
+  __shared__ float4 st[NGRP][TPP];
+  pdl_wait();  // every partial of the decode kernel is written
+  const int grp = threadIdx.x / TPP, d = 2 * (threadIdx.x % TPP);
+  const int64_t kstride = (int64_t)a.KVN * a.HG * a.GH * (D + 2);
+  for (int64_t pr = blockIdx.x; pr < a.num_units * a.GH; pr += gridDim.x) {
+    UnitInfo r;
+    int head;
+    const float* base;
+    const int nch = combine_item(a, pr, D, &r, &head, &base);  // uniform over the CTA
+    if (nch == 0) continue;
+    float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f;
+    fold_chunks<D>(base, kstride, d, grp, NGRP, nch, M, L, o0, o1);
+    st[grp][threadIdx.x % TPP] = make_float4(M, L, o0, o1);
+    __syncthreads();
+    if (grp == 0) {
+      for (int g2 = 1; g2 < NGRP; ++g2) {
+        const float4 x = st[g2][threadIdx.x % TPP];
+        if (x.x == -INFINITY) continue;
+        const float Mn = fmaxf(M, x.x);
+        const float fo = M == -INFINITY ? 0.f : exp2f(M - Mn);
+        const float fn = exp2f(x.x - Mn);
+        L = L * fo + x.y * fn;
+        o0 = o0 * fo + x.z * fn;
+        o1 = o1 * fo + x.w * fn;
+        M = Mn;
+      }
+      combine_store(a, r, head, D, d, M, L, o0, o1);
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous kernel on the stream finishes, and waits in pdl_wait().
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 size_t decode_smem_bytes(int D, int fp8) {
   if (fp8) return DecodeCfg<128, true>::kSmem;
   return D == 64 ? DecodeCfg<64, false>::kSmem : DecodeCfg<128, false>::kSmem;
@@ -934,12 +1182,11 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& tk,
     if (e != cudaSuccess) return e;
     done_mask[(dev >> 6) & 3].fetch_or(bit);
   }
-  kern<<<a.num_ctas, kThreads, Cfg::kSmem, s>>>(a, tk, tv);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.num_ctas), dim3(kThreads), Cfg::kSmem, s, a, tk, tv);
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                          int fp8, cudaStream_t s) {
+static cudaError_t launch_decode_main(const DecodeArgs& a, const CUtensorMap& tk,
+                                      const CUtensorMap& tv, int fp8, cudaStream_t s) {
   const bool two = a.GH > 8;
   if (fp8) return two ? launch_decode_t<128, true, 2>(a, tk, tv, s)
                       : launch_decode_t<128, true, 1>(a, tk, tv, s);
@@ -947,6 +1194,27 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUte
                             : launch_decode_t<64, false, 1>(a, tk, tv, s);
   return two ? launch_decode_t<128, false, 2>(a, tk, tv, s)
              : launch_decode_t<128, false, 1>(a, tk, tv, s);
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                          int fp8, cudaStream_t s) {
+  cudaError_t e = launch_decode_main(a, tk, tv, fp8, s);
+  if (e != cudaSuccess) return e;
+  // The plan bounds the chunks by n*W + 4*U, so a unit has about n*W/U + 4;
+  // with more than 16 a (unit, head) gets a whole CTA.  The choice depends on
+  // shapes only, so results stay deterministic.
+  const int64_t pairs = a.num_units * a.GH;
+  if (pairs <= 0) return cudaSuccess;
+  const int64_t est = (int64_t)a.num_ctas * a.chunks_per_cta / a.num_units + 4;
+  if (est > 16) {
+    const int grid = (int)std::min<int64_t>(pairs, (int64_t)a.num_ctas * 16);
+    if (a.D == 64) return launch_pdl(decode_combine_grouped<64>, dim3(grid), dim3(256), 0, s, a);
+    return launch_pdl(decode_combine_grouped<128>, dim3(grid), dim3(256), 0, s, a);
+  }
+  const int ppb = 256 / (a.D / 2);
+  const int grid = (int)((pairs + ppb - 1) / ppb);
+  if (a.D == 64) return launch_pdl(decode_combine_flat<64>, dim3(grid), dim3(256), 0, s, a);
+  return launch_pdl(decode_combine_flat<128>, dim3(grid), dim3(256), 0, s, a);
 }
 
 }  // namespace fia

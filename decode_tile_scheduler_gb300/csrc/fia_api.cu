@@ -152,27 +152,32 @@ int64_t kv_capacity(const fia_params* p) {
 
 struct DecodePlan {
   int n;
-  int64_t U;
-  int64_t off_prefix, off_beg, off_cnt, off_part, total;
+  int64_t U, max_chunks;
+  int64_t off_sched, off_queue, off_part, total;
 };
 
+// Decode workspace: [0, 256) error word (offset 0) and the claim counters
+// (offset 16); the schedule header and prefixes; the claim queue; the partial
+// slots.  A unit of cost c gets at most c/C big chunks
+// (so at most n*W over all units) and at most 4 small ones, hence
+// max_chunks = n*W + 4*U bounds the chunks of any lengths.
 fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
   int n;
   fia_status st = sm_count(p->num_sms, &n);
   if (st != FIA_OK) return st;
   const int G = p->num_q_heads / p->num_kv_heads;
-  const int HG = (int)ceil_div(G, decode_group_heads(G));
+  const int GH = decode_group_heads(G);
+  const int HG = (int)ceil_div(G, GH);
   pl->n = n;
   pl->U = (int64_t)p->batch * p->num_kv_heads * HG;
-  int64_t off = kAlign;  // [0, 256): error word
-  pl->off_prefix = off;
-  off = align_up(off + 8 * (pl->U + 1));
-  pl->off_beg = off;
-  off = align_up(off + 8 * ((int64_t)n + 1));
-  pl->off_cnt = off;
-  off = align_up(off + 4 * pl->U);
+  pl->max_chunks = (int64_t)n * kDecodeChunksPerCta + 4 * pl->U;
+  int64_t off = kAlign;
+  pl->off_sched = off;
+  off = align_up(off + 8 * (4 + 3 * ((int64_t)p->batch + 1)));
+  pl->off_queue = off;
+  off = align_up(off + 16 * pl->max_chunks);
   pl->off_part = off;
-  off = align_up(off + 4 * (int64_t)2 * n * kMaxHeadGroup * (p->head_dim + 2));
+  off = align_up(off + 4 * pl->max_chunks * GH * (p->head_dim + 2));
   pl->total = off;
   return FIA_OK;
 }
@@ -211,10 +216,12 @@ DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
   a.sinks = p->sinks;
   a.num_ctas = pl.n;
   a.num_units = pl.U;
+  a.chunks_per_cta = kDecodeChunksPerCta;
+  a.max_chunks = pl.max_chunks;
   char* w = static_cast<char*>(ws);
-  a.unit_prefix = reinterpret_cast<const int64_t*>(w + pl.off_prefix);
-  a.cta_begin = reinterpret_cast<const int64_t*>(w + pl.off_beg);
-  a.counters = reinterpret_cast<int*>(w + pl.off_cnt);
+  a.sched = reinterpret_cast<int64_t*>(w + pl.off_sched);
+  a.queue = reinterpret_cast<int4*>(w + pl.off_queue);
+  a.claim = reinterpret_cast<int*>(w + 16);
   a.partials = reinterpret_cast<float*>(w + pl.off_part);
   a.err = reinterpret_cast<int*>(w);
   return a;
@@ -259,7 +266,7 @@ fia_status prefill_plan(const fia_params* p, PrefillPlan* pl) {
                              : (int64_t)p->batch * ceil_div(p->max_seqlen_q, kQTile);
   pl->U_max = qtiles * H;
   pl->max_cost = (int)(1 + ceil_div(kv_capacity(p), kKvTile));
-  int64_t off = kAlign;  // [0,4) error word, [4,8) claim counter, [8,16) units
+  int64_t off = kAlign;  // [0,4) error word, [8,16) units, [16,24) claim counters
   pl->off_seq = off;
   off = align_up(off + 8 * ((int64_t)p->batch + 1));
   pl->off_hist = off;
@@ -301,7 +308,7 @@ PrefillArgs prefill_args(const fia_params* p, const PrefillPlan& pl, void* ws) {
   a.max_cost = pl.max_cost;
   char* w = static_cast<char*>(ws);
   a.err = reinterpret_cast<int*>(w);
-  a.claim = reinterpret_cast<int*>(w + 4);
+  a.claim = reinterpret_cast<int*>(w + 16);
   a.num_units = reinterpret_cast<int64_t*>(w + 8);
   a.seq_prefix = reinterpret_cast<int64_t*>(w + pl.off_seq);
   a.hist = reinterpret_cast<int*>(w + pl.off_hist);
@@ -471,8 +478,9 @@ fia_status fia_get_plan_layout(const fia_params* p, fia_plan_layout* out) {
     out->branch = 1;
     out->num_ctas = pl.n;
     out->num_units = pl.U;
-    out->unit_prefix_off = pl.off_prefix;
-    out->cta_begin_off = pl.off_beg;
+    out->max_chunks = pl.max_chunks;
+    out->sched_off = pl.off_sched;
+    out->queue_off = pl.off_queue;
     out->total_bytes = pl.total;
     return FIA_OK;
   }

@@ -37,13 +37,19 @@ struct DecodeArgs {
   const float* sinks;
   // plan (workspace)
   int num_ctas;
-  int64_t num_units;
-  const int64_t* unit_prefix;  // [U+1]
-  const int64_t* cta_begin;    // [n+1]
-  int* counters;               // [U]
-  float* partials;             // [2n][16][D + 2]: acc, then m and l
+  int chunks_per_cta;          // W: the chunk size aims at W chunks per CTA
+  int64_t num_units;           // B * KVN * HG
+  int64_t max_chunks;          // partial slots: a bound on the number of chunks
+  int64_t* sched;              // [4 + 3(B+1)]: C, c2, chunks, big chunks, then the
+                               // partial-slot prefix Q and the queue prefixes R1, R2
+  int4* queue;                 // [max_chunks] (b, chunk << 10 | unit of b, kv_len, qrow)
+  int* claim;                  // [2]: next queue entry, CTAs done claiming
+  float* partials;             // [max_chunks][GH][D + 2]: acc, then m and l
   int* err;
 };
+
+// Target number of big chunks per persistent CTA in the decode schedule.
+constexpr int kDecodeChunksPerCta = 8;
 
 struct PrefillArgs {
   int B, QN, KVN, D, G, npairs, per_pair;  // per_pair query heads per unit (2, or 1 if G odd)
@@ -67,7 +73,7 @@ struct PrefillArgs {
   int64_t* seq_prefix;    // [B+1] units before each sequence
   int* hist;              // [max_cost + 2] cost histogram, then offsets
   int2* unit_list;        // [units] (b, q_tile | hk << 18 | pair << 26), cost-descending
-  int* claim;             // dynamic claim counter
+  int* claim;             // [2]: next unit to claim, CTAs done claiming
   int* err;
 };
 

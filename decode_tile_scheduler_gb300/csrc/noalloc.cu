@@ -7,14 +7,14 @@
 // allocations after start-up, or real-time paths that must not take the
 // allocator's locks or latency.  They still own q, the KV cache and the
 // outputs, but have no way to obtain the scheduler's scratch (the work plan,
-// the split-KV counters and the partial (m, l, acc) slots).  This entry point
+// the chunk claim queue and the partial (m, l, acc) slots).  This entry point
 // uses a fixed scratch array compiled into the library instead: a file-scope
 // __device__ array of FIA_NOALLOC_SCRATCH_BYTES, which every GPU that loads
 // libfia holds from module load until the process exits.
 //
 // The array is shared by all calls on a device and keeps the previous call's
 // contents.  Everything that must start at zero is cleared by the call itself
-// (the scheduler kernel resets the error word and the split-KV counters), so
+// (the scheduler kernel resets the error word and the claim counters), so
 // a stale plan never leaks into a new call; but two calls whose work
 // overlaps on the GPU (different streams without ordering) race on the array.
 #include <mutex>

@@ -246,7 +246,8 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(const PrefillArg
   }
   if (tid == 0) {
     *a.num_units = U;
-    *a.claim = 0;
+    a.claim[0] = 0;
+    a.claim[1] = 0;
     *a.err = 0;
   }
 }
@@ -333,6 +334,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
       ++ucnt;
       if (idx >= num_units || *reinterpret_cast<volatile int*>(misc)) {
         if (lane == 0) {
+          if (idx >= num_units) {
+            // this CTA claims no more: the last CTA out re-arms the counter
+            // for the next fia_execute with the same plan
+            __threadfence();
+            if (atomicAdd(a.claim + 1, 1) == a.num_ctas - 1) {
+              a.claim[0] = 0;
+              a.claim[1] = 0;
+            }
+          }
           msg[ms].done = 1;
           mbar_arrive(&mfull[ms]);
         }

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define FIA_ABI_VERSION 1
+#define FIA_ABI_VERSION 2
 
 /* Status codes ("...V5" two-phase API: the first phase validates the inputs
  * and reports errors before anything is launched). */
@@ -162,7 +162,13 @@ fia_status fia_plan(const fia_params *p, void *workspace, size_t workspace_bytes
 
 /* Phase 2b: launch the attention kernels on `stream` using the plan in
  * `workspace`.  Writes every element of out (and lse when non-NULL).
- * Deterministic: the same inputs give bitwise the same outputs. */
+ * Deterministic: the same inputs give bitwise the same outputs.
+ * Device error word: the first int32 of the workspace is 0 after a clean
+ * execute; 1 when a bounded wait inside a kernel gave up (about 2 s; the
+ * kernel returned early and the outputs are undefined); 2 when a decode plan
+ * held more chunks than the workspace bound (not reachable for validated
+ * inputs; nothing ran).  Reading it needs a device-to-host copy after the
+ * stream has reached the call. */
 fia_status fia_execute(const fia_params *p, void *workspace, size_t workspace_bytes,
                        void *stream);
 
@@ -190,13 +196,27 @@ fia_status fia_run(const fia_params *p, void *workspace, size_t workspace_bytes,
 #define FIA_NOALLOC_SCRATCH_BYTES (8u << 20)
 fia_status fia_decode_run_noalloc(const fia_params *p, void *stream);
 
-/* Workspace layout of the plan, for inspection (host-only). */
+/* Workspace layout of the plan, for inspection (host-only).
+ *
+ * Decode schedule (written by fia_plan): work unit u = (b, kv head, head
+ * group); cost = KV tiles (128 positions) its query row sees, at least 1 (0
+ * when the batch has no query row).  With T the total cost, n CTAs and W
+ * chunks per CTA, C = max(1, ceil(T / (n W))) and c2 = ceil(C / 2).  A unit
+ * of cost c gets n1 = max(0, floor(c/C) - 1) chunks of C tiles, then chunks
+ * of c2 tiles over the rest.  sched holds int64 {C, c2, chunks N, big chunks
+ * F}, then Q[B+1] (partial slots before batch b: chunk i of unit w of batch b
+ * owns slot Q[b] + i*UPB + w, UPB = units per batch), then R1[B+1] and
+ * R2[B+1] (big and small chunks before batch b).  The claim queue lists the
+ * big chunks, batch-major then chunk then unit, followed by the small chunks
+ * in the same order; entry = four int32 (b, i << 10 | w, KV length of b,
+ * first query row of b). */
 typedef struct fia_plan_layout {
     int32_t branch;           /* 1 decode (split-KV), 2 prefill                */
     int32_t num_ctas;         /* persistent CTAs                               */
-    int64_t num_units;        /* work units                                    */
-    int64_t unit_prefix_off;  /* decode: int64 [num_units+1] cost prefix       */
-    int64_t cta_begin_off;    /* decode: int64 [num_ctas+1] cost interval      */
+    int64_t num_units;        /* decode: units; prefill: bound on units        */
+    int64_t max_chunks;       /* decode: partial slots, bound on chunks        */
+    int64_t sched_off;        /* decode: int64 [4 + 3(B+1)] schedule           */
+    int64_t queue_off;        /* decode: int32 [max_chunks][4] claim queue     */
     int64_t unit_list_off;    /* prefill: int32 [num_units][2] ordered units   */
     int64_t total_bytes;
 } fia_plan_layout;

@@ -110,7 +110,8 @@ def lib():
                                                ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
             L.oracle_fia_row_probs.restype = ctypes.c_int64
             L.oracle_decode_schedule.argtypes = [ctypes.POINTER(_FiaArgs), ctypes.c_int32,
-                                                 ctypes.c_void_p, ctypes.c_void_p]
+                                                 ctypes.c_int32, ctypes.c_void_p,
+                                                 ctypes.c_void_p, ctypes.c_int64]
             L.oracle_decode_schedule.restype = ctypes.c_int64
             L.oracle_prefill_units.argtypes = [ctypes.POINTER(_FiaArgs), ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_int64]
@@ -276,17 +277,20 @@ def bf16_to_double(bits: int) -> float:
     return lib().oracle_bf16_to_double(bits)
 
 
-def decode_schedule(p, num_ctas: int):
-    """(unit_prefix int64 [U+1], cta_begin int64 [n+1], total)."""
+def decode_schedule(p, num_ctas: int, per_cta: int):
+    """(sched int64 [4 + 3(B+1)], queue int32 [N, 4]) of the decode chunk
+    schedule for n CTAs and W = per_cta chunks per CTA."""
     s, keep = _fia_struct(p)
     G = p.QN // p.KVN
     HG = -(-G // (8 if G <= 8 else 16))
     U = p.B * p.KVN * HG
-    pre = np.zeros(U + 1, dtype=np.int64)
-    beg = np.zeros(num_ctas + 1, dtype=np.int64)
-    total = lib().oracle_decode_schedule(ctypes.byref(s), num_ctas, pre.ctypes.data,
-                                         beg.ctypes.data)
-    return pre, beg, int(total)
+    cap = num_ctas * per_cta + 4 * U
+    sched = np.zeros(4 + 3 * (p.B + 1), dtype=np.int64)
+    queue = np.zeros((max(cap, 1), 4), dtype=np.int32)
+    n = lib().oracle_decode_schedule(ctypes.byref(s), num_ctas, per_cta, sched.ctypes.data,
+                                     queue.ctypes.data, cap)
+    assert n >= 0, "more chunks than the bound"
+    return sched, queue[:n].copy()
 
 
 def prefill_units(p):

@@ -503,34 +503,96 @@ static int64_t or_tiles(int64_t lo, int64_t hi)
 }
 
 /* Decode schedule.  Units u = ((b*KVN + hk)*HG + hg): the G query heads of a
- * KV head are taken in groups of GH = 8 (G <= 8) or 16, HG = ceil(G/GH).  A
- * unit whose batch has no query row costs 0; otherwise it costs the number of
- * KV tiles its single query row can see, at least 1.  unit_prefix[u] is the
- * exclusive prefix sum of the costs (U+1 entries), and CTA c of n owns the
- * cost interval [floor(c*total/n), floor((c+1)*total/n)) (n+1 entries in
- * cta_begin).  Returns the total cost. */
-int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int64_t *unit_prefix,
-                               int64_t *cta_begin)
+ * KV head are taken in groups of GH = 8 (G <= 8) or 16, HG = ceil(G/GH), so
+ * a batch has UPB = KVN*HG units, all with the same cost: 0 when the batch has
+ * no query row, else the number of KV tiles its single query row can see, at
+ * least 1.  With T the sum of all unit costs, n CTAs and W chunks per CTA:
+ *   C  = max(1, ceil(T / (n*W))),  c2 = ceil(C/2);
+ *   a unit of cost c has n1 = max(0, floor(c/C) - 1) big chunks of C tiles,
+ *   then its remaining c - n1*C tiles in small chunks of c2 tiles (the last
+ *   one shorter), n2 of them.
+ * Outputs (int64 sched[4 + 3(B+1)]): C, c2, N (all chunks), F (big chunks),
+ * Q[b] = sum over b' < b of (n1+n2)(b')*UPB, then R1[b] (big) and R2[b]
+ * (small) the same sums of n1*UPB and n2*UPB; each array has B+1 entries.
+ * The queue (N entries of four int32) lists for b = 0..B-1, chunk i =
+ * 0..n1-1, unit w = 0..UPB-1 the entry (b, i << 10 | w, kv_len(b), first
+ * query row of b), then the small chunks in the same nesting with i =
+ * n1..n1+n2-1.  Returns N, or -1 if N > cap. */
+int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32_t per_cta,
+                               int64_t *sched, int32_t *queue, int64_t cap)
 {
     int G = a->QN / a->KVN;
     int HG = (int)or_ceil_div(G, G <= 8 ? 8 : 16);
-    int64_t U = (int64_t)a->B * a->KVN * HG, u, acc = 0;
-    int c;
-    for (u = 0; u < U; ++u) {
-        int b = (int)(u / ((int64_t)a->KVN * HG));
-        int64_t ql, qs, kl, lo, hi, cost = 0;
+    int64_t UPB = (int64_t)a->KVN * HG;
+    int B = a->B, b;
+    int64_t *Q = sched + 4, *R1 = Q + (B + 1), *R2 = R1 + (B + 1);
+    int64_t *cost = (int64_t *)malloc(sizeof(int64_t) * (B > 0 ? B : 1));
+    int64_t T = 0, C, c2, q = 0, r1 = 0, r2 = 0, n = 0;
+    for (b = 0; b < B; ++b) {
+        int64_t ql, qs, kl, lo, hi, c = 0;
         fia_lengths(a, b, &ql, &qs, &kl);
         if (ql > 0) {
-            cost = 0;
-            if (kl > 0 && fia_visible(a, ql, kl, ql - 1, &lo, &hi)) cost = or_tiles(lo, hi);
-            if (cost < 1) cost = 1;
+            if (kl > 0 && fia_visible(a, ql, kl, ql - 1, &lo, &hi)) c = or_tiles(lo, hi);
+            if (c < 1) c = 1;
         }
-        unit_prefix[u] = acc;
-        acc += cost;
+        cost[b] = c;
+        T += c * UPB;
     }
-    unit_prefix[U] = acc;
-    for (c = 0; c <= num_ctas; ++c) cta_begin[c] = (int64_t)c * acc / num_ctas;
-    return acc;
+    C = or_ceil_div(T, (int64_t)num_ctas * per_cta);
+    if (C < 1) C = 1;
+    c2 = (C + 1) / 2;
+    for (b = 0; b < B; ++b) {
+        int64_t n1 = 0, n2 = 0;
+        if (cost[b] > 0) {
+            n1 = cost[b] / C - 1;
+            if (n1 < 0) n1 = 0;
+            n2 = or_ceil_div(cost[b] - n1 * C, c2);
+        }
+        Q[b] = q;
+        R1[b] = r1;
+        R2[b] = r2;
+        q += (n1 + n2) * UPB;
+        r1 += n1 * UPB;
+        r2 += n2 * UPB;
+    }
+    Q[B] = q;
+    R1[B] = r1;
+    R2[B] = r2;
+    sched[0] = C;
+    sched[1] = c2;
+    sched[2] = q;
+    sched[3] = r1;
+    if (q > cap) {
+        free(cost);
+        return -1;
+    }
+    /* big chunks, then small chunks */
+    for (b = 0; b < B; ++b) {
+        int64_t n1 = (R1[b + 1] - R1[b]) / UPB, i, w, ql, qs, kl;
+        fia_lengths(a, b, &ql, &qs, &kl);
+        for (i = 0; i < n1; ++i)
+            for (w = 0; w < UPB; ++w) {
+                queue[4 * n] = b;
+                queue[4 * n + 1] = (int32_t)((i << 10) | w);
+                queue[4 * n + 2] = (int32_t)kl;
+                queue[4 * n + 3] = (int32_t)qs;
+                ++n;
+            }
+    }
+    for (b = 0; b < B; ++b) {
+        int64_t n1 = (R1[b + 1] - R1[b]) / UPB, n2 = (R2[b + 1] - R2[b]) / UPB, i, w, ql, qs, kl;
+        fia_lengths(a, b, &ql, &qs, &kl);
+        for (i = n1; i < n1 + n2; ++i)
+            for (w = 0; w < UPB; ++w) {
+                queue[4 * n] = b;
+                queue[4 * n + 1] = (int32_t)((i << 10) | w);
+                queue[4 * n + 2] = (int32_t)kl;
+                queue[4 * n + 3] = (int32_t)qs;
+                ++n;
+            }
+    }
+    free(cost);
+    return n;
 }
 
 /* Prefill work units in canonical order (b, q_tile, hk, pair) and their

@@ -35,7 +35,7 @@ def test_struct_layouts_agree():
     L = fia.lib()
     assert L.fia_sizeof_params() == ctypes.sizeof(_abi.FiaParams)
     assert L.fia_sizeof_sparse_params() == ctypes.sizeof(_abi.SparseParams)
-    assert L.fia_abi_version() == 1
+    assert L.fia_abi_version() == 2
 
 
 def test_status_strings():
@@ -154,7 +154,11 @@ def test_workspace_too_small_is_reported_before_launch():
 def test_plan_layout_describes_decode_schedule():
     lay = fia.fia_get_plan_layout(_decode_params())
     assert lay.branch == 1 and lay.num_ctas == 152 and lay.num_units == 4 * 2 * 1
-    assert lay.unit_prefix_off >= 256 and lay.cta_begin_off > lay.unit_prefix_off
+    per_cta = (lay.max_chunks - 4 * lay.num_units) // lay.num_ctas
+    assert per_cta >= 1 and lay.max_chunks == 152 * per_cta + 4 * lay.num_units
+    assert lay.sched_off >= 256 and lay.queue_off >= lay.sched_off + 8 * (4 + 3 * 5)
+    # partial slots: max_chunks x 8 heads x (D + 2) floats fit in the workspace
+    assert lay.total_bytes >= lay.queue_off + 16 * lay.max_chunks + 4 * lay.max_chunks * 8 * 130
 
 
 # --------------------------------------------------------------------------

@@ -92,11 +92,35 @@ def test_schedule_metadata_bit_exact():
         lay = c.plan_layout()
         ws = c.ws.cpu()
         U = lay.num_units
-        pre = ws[lay.unit_prefix_off: lay.unit_prefix_off + 8 * (U + 1)].view(torch.int64).numpy()
-        beg = ws[lay.cta_begin_off: lay.cta_begin_off + 8 * (n + 1)].view(torch.int64).numpy()
-        rpre, rbeg, total = oracle.decode_schedule(p.to("cpu"), n)
-        assert np.array_equal(pre, rpre)
-        assert np.array_equal(beg, rbeg)
+        per_cta = (lay.max_chunks - 4 * U) // n
+        nsched = 4 + 3 * (p.B + 1)
+        sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
+        rs, rq = oracle.decode_schedule(p.to("cpu"), n, per_cta)
+        assert np.array_equal(sched, rs)
+        N = int(sched[2])
+        queue = ws[lay.queue_off: lay.queue_off + 16 * N].view(torch.int32).numpy().reshape(N, 4)
+        assert np.array_equal(queue, rq)
+
+
+def test_execute_reuses_one_plan():
+    # fia_plan once, fia_execute three times: the claim queue and the split
+    # counters re-arm themselves, so every execute gives the same result
+    import decode_tile_scheduler_gb300 as fia
+    p = fi.make_fia(B=5, QN=32, KVN=8, D=128, q_lens=[1] * 5, kv_lens=[4000, 700, 1, 129, 2500],
+                    block_size=128, with_sinks=True, seed=19, device=dev)
+    c = fia.FiaCall(p, with_lse=True)
+    c.plan()
+    outs = []
+    for _ in range(3):
+        c.out.fill_(float("nan"))
+        c.execute()
+        torch.cuda.synchronize()
+        assert c.error_word() == 0
+        outs.append((c.out.clone(), c.lse.clone()))
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    ro, rl = _ref(p)
+    check_close(outs[0][0], outs[0][1], ro, rl, "plan reuse")
 
 
 def test_deterministic_bitwise():

@@ -445,29 +445,63 @@ def test_sparse_csa_equals_dense_over_gathered_rows():
 # schedules
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("ctas", [1, 7, 152, 500])
-def test_decode_schedule_covers_each_tile_once_balanced(ctas):
-    p = fi.make_fia(B=5, QN=8, KVN=2, D=16, q_lens=[1] * 5, kv_lens=[0, 1, 300, 129, 1000],
+def _unit_chunks(sched, queue, B, UPB):
+    """{unit: [(queue position, chunk index)]} from the queue entries."""
+    out = {}
+    for pos, (b, y, _, _) in enumerate(queue.tolist()):
+        w, i = y & 1023, y >> 10
+        assert 0 <= b < B and w < UPB
+        out.setdefault(b * UPB + w, []).append((pos, i))
+    return out
+
+
+@pytest.mark.parametrize("ctas,per_cta", [(1, 8), (7, 8), (152, 8), (500, 8), (152, 1), (3, 50)])
+def test_decode_schedule_chunks_cover_each_unit_once(ctas, per_cta):
+    kv = [0, 1, 300, 129, 1000, 5000, 128]
+    p = fi.make_fia(B=len(kv), QN=8, KVN=2, D=16, q_lens=[1] * len(kv), kv_lens=kv,
                     block_size=16, seed=2)
-    pre, beg, total = oracle.decode_schedule(p, ctas)
-    G = 4
-    costs = []
-    for b in range(p.B):
-        for hk in range(p.KVN):
-            kl = p.kv_lens[b]
-            costs.append(max(1, -(-kl // 128)))
-    assert np.array_equal(np.diff(pre), np.array(costs))
-    assert total == sum(costs) and beg[0] == 0 and beg[-1] == total
-    sizes = np.diff(beg)
-    assert np.all(sizes >= 0) and sizes.max() - sizes.min() <= 1
+    sched, queue = oracle.decode_schedule(p, ctas, per_cta)
+    B, UPB = p.B, 2
+    costs = [max(1, -(-k // 128)) for k in kv]          # no mask: every tile, at least 1
+    T = UPB * sum(costs)
+    C = max(1, -(-T // (ctas * per_cta)))
+    c2 = -(-C // 2)
+    assert list(sched[:2]) == [C, c2]
+    N, F = int(sched[2]), int(sched[3])
+    assert N == queue.shape[0] and 0 <= F <= N
+    assert N <= ctas * per_cta + 4 * B * UPB             # the workspace bound
+    Q = sched[4:4 + B + 1]
+    chunks = _unit_chunks(sched, queue, B, UPB)
+    for b in range(B):
+        for w in range(UPB):
+            lst = chunks[b * UPB + w]
+            idx = sorted(i for _, i in lst)
+            assert idx == list(range(len(idx)))          # chunks 0..k-1, once each
+            assert Q[b + 1] - Q[b] == len(idx) * UPB
+            n1 = sum(pos < F for pos, _ in lst)
+            # big chunks come first in the unit; the small ones cover the rest
+            assert all(i < n1 for pos, i in lst if pos < F)
+            rest = costs[b] - n1 * C
+            n2 = len(idx) - n1
+            assert n2 >= 1 and (n2 - 1) * c2 < rest <= n2 * c2
+            if n1 > 0:
+                assert C <= rest < 2 * C                 # one big chunk left for the small ones
+    # claim order: big chunks, then small, each batch-major, chunk, then unit
+    keys = [(b, y >> 10, y & 1023) for b, y, _, _ in queue.tolist()]
+    assert keys[:F] == sorted(keys[:F]) and keys[F:] == sorted(keys[F:])
+    # every entry carries its batch's KV length and query row (BSND: b * S_q)
+    assert [(kl, qr) for b, _, kl, qr in queue.tolist()] == [(kv[b], b) for b, _, _, _ in queue.tolist()]
 
 
 def test_decode_schedule_band_counts_window_tiles_only():
     p = fi.make_fia(B=2, QN=2, KVN=1, D=16, q_lens=[1, 1], kv_lens=[1000, 100], block_size=16,
                     mask_mode=4, pre_tokens=200, next_tokens=0, seed=2)
-    pre, beg, total = oracle.decode_schedule(p, 3)
+    sched, queue = oracle.decode_schedule(p, 3, 8)
     # row position 999 sees [799, 999] -> tiles 6..7; position 99 sees [0, 99] -> tile 0
-    assert list(np.diff(pre)) == [2, 1]
+    # T = 3 tiles over 24 chunk slots: C = 1, so each tile is one chunk
+    assert sched[0] == 1
+    Q = sched[4:7]
+    assert list(np.diff(Q)) == [2, 1]
 
 
 def test_prefill_units_enumerate_every_tile_and_head_pair():

@@ -125,3 +125,23 @@ def test_varlen_causal_prefill_workload_sampled():
     err = np.abs(o[rows, heads] - ro)
     assert err.max() <= 2e-2 and err.mean() <= 2e-3, (err.max(), err.mean())
     assert np.abs(l[rows, heads] - rl).max() <= 1e-3
+
+
+def test_execute_reuses_one_plan():
+    # fia_plan once, fia_execute twice: the claim counter re-arms itself
+    import decode_tile_scheduler_gb300 as fia
+    p = fi.make_fia(B=2, QN=8, KVN=2, D=128, q_lens=[300, 129], kv_lens=[300, 129],
+                    layout=fi.LAYOUT_TND, block_size=64, mask_mode=3, with_sinks=True, seed=31,
+                    device=dev)
+    c = fia.FiaCall(p, with_lse=True)
+    c.plan()
+    outs = []
+    for _ in range(2):
+        c.out.fill_(float("nan"))
+        c.execute()
+        torch.cuda.synchronize()
+        assert c.error_word() == 0
+        outs.append((c.out.clone(), c.lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    ro, rl = oracle.fia(p.to("cpu"))
+    check_close(outs[1][0], outs[1][1], ro, rl, "plan reuse")

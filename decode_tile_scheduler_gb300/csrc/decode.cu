@@ -19,8 +19,8 @@
 // always small pieces.  CTAs claim chunks from the queue with one atomic each:
 // an SM that streams faster simply takes more chunks.  A unit cut into several
 // chunks is split-KV: each chunk writes its (m, l, acc) partial to the slot
-// of its (unit, chunk index), and a combine kernel, launched next on the
-// stream, folds them in chunk order (deterministic, whichever CTAs ran them).
+// of its (unit, chunk index), and a combine kernel chained behind the decode
+// kernel folds them in chunk order (deterministic, whichever CTAs ran them).
 //
 // Decode kernel: one producer warp streams K and V pages with TMA (page rows
 // from block_table) into a ring of shared-memory stages; eight consumer warps
@@ -169,7 +169,8 @@ __device__ __forceinline__ int64_t batch_cost(const DecodeArgs& a, int b) {
 }
 
 // largest b with prefix[b] <= g (prefix[0] = 0 <= g < prefix[B])
-__device__ __forceinline__ int find_batch(const int64_t* prefix, int B, int64_t g) {
+template <typename T>
+__device__ __forceinline__ int find_batch(const T* prefix, int B, int64_t g) {
   int lo = 0, hi = B;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -235,13 +236,13 @@ __device__ __forceinline__ void finish_head(const DecodeArgs& a, int h, float M,
 // ---------------------------------------------------------------------------
 // scheduler
 // ---------------------------------------------------------------------------
-// Block-wide exclusive scan of three counters over the 1024 threads; returns
+// Block-wide exclusive scan of four counters over the 1024 threads; returns
 // the block totals in tot[] (every thread).
-__device__ __forceinline__ void scan3(int64_t (&x)[3], int64_t (&tot)[3], int64_t (*ws)[3]) {
+__device__ __forceinline__ void scan4(int64_t (&x)[4], int64_t (&tot)[4], int64_t (*ws)[4]) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int64_t incl[3];
+  int64_t incl[4];
 #pragma unroll
-  for (int k = 0; k < 3; ++k) {
+  for (int k = 0; k < 4; ++k) {
     int64_t v = x[k];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -254,7 +255,7 @@ __device__ __forceinline__ void scan3(int64_t (&x)[3], int64_t (&tot)[3], int64_
   __syncthreads();
   if (wid == 0) {
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
+    for (int k = 0; k < 4; ++k) {
       int64_t v = lane < (int)(blockDim.x >> 5) ? ws[lane][k] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -266,7 +267,7 @@ __device__ __forceinline__ void scan3(int64_t (&x)[3], int64_t (&tot)[3], int64_
   }
   __syncthreads();
 #pragma unroll
-  for (int k = 0; k < 3; ++k) {
+  for (int k = 0; k < 4; ++k) {
     const int64_t before = wid ? ws[wid - 1][k] : 0;
     tot[k] = ws[31][k];
     x[k] = before + incl[k] - x[k];
@@ -274,63 +275,84 @@ __device__ __forceinline__ void scan3(int64_t (&x)[3], int64_t (&tot)[3], int64_
   __syncthreads();
 }
 
-constexpr int kSchedSmemBatches = 2048;  // queue prefixes kept in shared memory up to this B
+constexpr int kSchedSmemBatches = 2048;  // per-batch values kept in shared memory up to this B
 
 __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs a) {
-  __shared__ int64_t ws[32][3];
+  __shared__ int64_t ws[32][4];
   __shared__ int64_t s_total;
-  __shared__ int64_t sR[2][kSchedSmemBatches + 1];
+  // up to kSchedSmemBatches batches: lengths, costs and queue prefixes stay in
+  // shared memory, so the batch arrays are read from global memory once
+  __shared__ int s_cost[kSchedSmemBatches], s_kv[kSchedSmemBatches], s_qrow[kSchedSmemBatches];
+  __shared__ int sR[2][kSchedSmemBatches + 1];
   const int tid = threadIdx.x, lane = tid & 31;
   pdl_trigger();  // the decode kernel may set up while the plan is built
   const int B = a.B;
+  const bool small = B <= kSchedSmemBatches;
   const int UPB = a.KVN * a.HG;
   int64_t* sched = a.sched;
-  int64_t* Q = sched + 4;            // [B+1] partial slots before batch b
-  int64_t* R1 = Q + (B + 1);         // [B+1] big-chunk queue positions
-  int64_t* R2 = R1 + (B + 1);        // [B+1] small-chunk queue positions
+  int64_t* Q = sched + kSchedHeader;  // [B+1] partial slots before batch b
+  int64_t* R1 = Q + (B + 1);          // [B+1] big-chunk queue positions
+  int64_t* R2 = R1 + (B + 1);         // [B+1] small-chunk queue positions
+  int64_t* SB = R2 + (B + 1);         // [B] batches cut into several chunks, then -1
 
-  // total cost
+  // total cost (and, for small B, each batch's lengths and cost)
   int64_t part = 0;
-  for (int b = tid; b < B; b += blockDim.x) part += batch_cost(a, b);
+  for (int b = tid; b < B; b += blockDim.x) {
+    SB[b] = -1;
+    int64_t qrow, ql, kv_len;
+    batch_lengths(a, b, &qrow, &ql, &kv_len);
+    const UnitInfo r = unit_from(a, b, 0, qrow, ql, kv_len);
+    const int64_t cost = ql > 0 ? max(1, r.ntiles) : 0;
+    part += cost;
+    if (small) {
+      s_cost[b] = (int)cost;
+      s_kv[b] = (int)kv_len;
+      s_qrow[b] = (int)qrow;
+    }
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
   if (tid == 0) s_total = 0;
   __syncthreads();
   if (lane == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&s_total),
                            (unsigned long long)part);
-  __syncthreads();
+  __syncthreads();  // also orders the SB fill before the scatter below
   const int64_t T = s_total * UPB;
   const int64_t per = (int64_t)a.num_ctas * a.chunks_per_cta;
   const int64_t C = max((int64_t)1, (T + per - 1) / per);
   const int64_t c2 = (C + 1) / 2;
 
-  // per batch: chunks of each unit (all, big, small) -> three exclusive scans
-  int64_t carry[3] = {0, 0, 0};
+  // per batch: chunks of each unit (all, big, small) and whether the batch is
+  // split -> four exclusive scans
+  int64_t carry[4] = {0, 0, 0, 0};
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + tid;
-    int64_t x[3] = {0, 0, 0};
+    int64_t x[4] = {0, 0, 0, 0};
     if (b < B) {
-      const int64_t cost = batch_cost(a, b);
+      const int64_t cost = small ? s_cost[b] : batch_cost(a, b);
       if (cost > 0) {
         const ChunkGeom gm = chunk_geom(cost, C, c2);
         x[0] = (int64_t)gm.nch * UPB;
         x[1] = (int64_t)gm.n1 * UPB;
         x[2] = (int64_t)(gm.nch - gm.n1) * UPB;
+        x[3] = gm.nch > 1;
       }
     }
-    int64_t tot[3];
-    scan3(x, tot, ws);
+    const bool is_split = x[3] != 0;
+    int64_t tot[4];
+    scan4(x, tot, ws);
+    if (b < B && is_split) SB[carry[3] + x[3]] = b;
     if (b < B) {
       Q[b] = carry[0] + x[0];
       R1[b] = carry[1] + x[1];
       R2[b] = carry[2] + x[2];
-      if (B <= kSchedSmemBatches) {
-        sR[0][b] = R1[b];
-        sR[1][b] = R2[b];
+      if (small) {
+        sR[0][b] = (int)(carry[1] + x[1]);
+        sR[1][b] = (int)(carry[2] + x[2]);
       }
     }
 #pragma unroll
-    for (int k = 0; k < 3; ++k) carry[k] += tot[k];
+    for (int k = 0; k < 4; ++k) carry[k] += tot[k];
   }
   // N <= n*W + 4*U always holds (the workspace bound); a plan that broke it
   // would run nothing and say so in the error word
@@ -340,39 +362,99 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
     Q[B] = carry[0];
     R1[B] = carry[1];
     R2[B] = carry[2];
-    if (B <= kSchedSmemBatches) {
-      sR[0][B] = carry[1];
-      sR[1][B] = carry[2];
+    if (small) {
+      sR[0][B] = (int)carry[1];
+      sR[1][B] = (int)carry[2];
     }
     sched[0] = C;
     sched[1] = c2;
     sched[2] = N;
     sched[3] = F;
-    a.claim[0] = 0;
-    a.claim[1] = 0;
+    sched[4] = fits ? carry[3] : 0;  // split batches
+    sched[5] = sched[6] = sched[7] = 0;
+    a.claim[0] = a.claim[1] = 0;
     *a.err = fits ? 0 : 2;  // error word of this plan's execution
   }
   __syncthreads();
   // the claim queue: big chunks, then small chunks
-  const int64_t* P1 = B <= kSchedSmemBatches ? sR[0] : R1;
-  const int64_t* P2 = B <= kSchedSmemBatches ? sR[1] : R2;
   for (int64_t g = tid; g < N; g += blockDim.x) {
     int b, ci, w;
+    int64_t local;
     if (g < F) {
-      b = find_batch(P1, B, g);
-      const int64_t local = g - P1[b];
+      b = small ? find_batch(sR[0], B, g) : find_batch(R1, B, g);
+      local = g - (small ? sR[0][b] : R1[b]);
       ci = (int)(local / UPB);
-      w = (int)(local % UPB);
     } else {
-      b = find_batch(P2, B, g - F);
-      const int64_t local = g - F - P2[b];
-      const int n1 = (int)((P1[b + 1] - P1[b]) / UPB);
-      ci = n1 + (int)(local / UPB);
-      w = (int)(local % UPB);
+      b = small ? find_batch(sR[1], B, g - F) : find_batch(R2, B, g - F);
+      local = g - F - (small ? sR[1][b] : R2[b]);
+      const int64_t r1 = small ? sR[0][b + 1] - sR[0][b] : R1[b + 1] - R1[b];
+      ci = (int)(r1 / UPB + local / UPB);
     }
-    int64_t qrow, ql, kv_len;
-    batch_lengths(a, b, &qrow, &ql, &kv_len);
-    a.queue[g] = make_int4(b, (ci << 10) | w, (int)kv_len, (int)qrow);
+    w = (int)(local % UPB);
+    int kv_len, qrow;
+    if (small) {
+      kv_len = s_kv[b];
+      qrow = s_qrow[b];
+    } else {
+      int64_t q64, ql, kv64;
+      batch_lengths(a, b, &q64, &ql, &kv64);
+      kv_len = (int)kv64;
+      qrow = (int)q64;
+    }
+    a.queue[g] = make_int4(b, (ci << 10) | w, kv_len, qrow);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// split-KV combine helpers: the partials of a unit's chunks are folded in a
+// fixed order (deterministic), then the sink and the final normalisation are
+// applied.
+// ---------------------------------------------------------------------------
+// Fold chunk partials k = k0, k0 + step, ... (< nch) of one (unit, head) into
+// (M, L, o0, o1) for the d-pair at d, eight loads in flight at a time.
+template <int D>
+__device__ __forceinline__ void fold_chunks(const float* base, int64_t kstride, int d, int k0,
+                                            int step, int nch, float& M, float& L, float& o0,
+                                            float& o1) {
+  constexpr int NB = 8;  // partials in flight per thread
+  for (int kb = k0; kb < nch; kb += NB * step) {
+    float2 ml[NB], ov[NB];
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      const int kk = kb + k * step;
+      ml[k] = make_float2(-INFINITY, 0.f);
+      ov[k] = make_float2(0.f, 0.f);
+      if (kk < nch) {
+        const float* pp = base + kk * kstride;
+        ml[k] = __ldcg(reinterpret_cast<const float2*>(pp + D));  // (m, l)
+        ov[k] = __ldcg(reinterpret_cast<const float2*>(pp + d));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      if (ml[k].x == -INFINITY) continue;
+      const float Mn = fmaxf(M, ml[k].x);
+      const float fo = M == -INFINITY ? 0.f : exp2f(M - Mn);
+      const float fn = exp2f(ml[k].x - Mn);
+      L = L * fo + ml[k].y * fn;
+      o0 = o0 * fo + ov[k].x * fn;
+      o1 = o1 * fo + ov[k].y * fn;
+      M = Mn;
+    }
+  }
+}
+
+__device__ __forceinline__ void combine_store(const DecodeArgs& a, const UnitInfo& r, int head,
+                                              int D, int d, float M, float L, float o0,
+                                              float o1) {
+  const int h = r.h0 + head;
+  float scl, lse;
+  finish_head(a, h, M, L, &scl, &lse);
+  uint16_t* o = a.out + r.qrow * a.out_stride + (int64_t)h * D + d;
+  *reinterpret_cast<uint32_t*>(o) = pack_bf16(o0 * scl, o1 * scl);
+  if (a.lse && d == 0) {
+    const int64_t li = a.layout == 1 ? r.qrow * a.QN + h : ((int64_t)r.b * a.QN + h) * a.S_q;
+    a.lse[li] = lse;
   }
 }
 
@@ -584,7 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait_or_abort(&qfull[qs], (ucount >> 1) & 1, a.err, misc);
     if (msg[qs].done || *reinterpret_cast<volatile int*>(misc)) break;
     const UnitInfo r = msg[qs].r;
-    const int64_t slot0 = a.sched[4 + r.b] + (msg[qs].u - (int64_t)r.b * a.KVN * a.HG);
+    const int64_t u = msg[qs].u;
+    const int64_t slot0 = a.sched[kSchedHeader + r.b] + (u - (int64_t)r.b * a.KVN * a.HG);
     const int t_begin = msg[qs].t_begin, t_end = msg[qs].t_end;
     const int ci = msg[qs].ci, nch = msg[qs].nch;
     const bool split = nch > 1;
@@ -1008,119 +1091,82 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// split-KV combine: one CTA per unit cut into several chunks; the partials of
-// its chunks are folded in chunk order (deterministic), then the sink and the
-// final normalisation are applied.
+// split-KV combine, launched right after the decode kernel: one item per
+// (batch with several chunks per unit, unit, head), found from the schedule's
+// list of such batches; the partials are folded in chunk order.
 // ---------------------------------------------------------------------------
-// Fold chunk partials k = k0, k0 + step, ... (< nch) of one (unit, head) into
-// (M, L, o0, o1) for the d-pair at d, eight loads in flight at a time.
-template <int D>
-__device__ __forceinline__ void fold_chunks(const float* base, int64_t kstride, int d, int k0,
-                                            int step, int nch, float& M, float& L, float& o0,
-                                            float& o1) {
-  constexpr int NB = 4;  // partials in flight per thread
-  for (int kb = k0; kb < nch; kb += NB * step) {
-    float2 ml[NB], ov[NB];
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-      const int kk = kb + k * step;
-      ml[k] = make_float2(-INFINITY, 0.f);
-      ov[k] = make_float2(0.f, 0.f);
-      if (kk < nch) {
-        const float* pp = base + kk * kstride;
-        ml[k] = __ldcg(reinterpret_cast<const float2*>(pp + D));  // (m, l)
-        ov[k] = __ldcg(reinterpret_cast<const float2*>(pp + d));
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-      if (ml[k].x == -INFINITY) continue;
-      const float Mn = fmaxf(M, ml[k].x);
-      const float fo = M == -INFINITY ? 0.f : exp2f(M - Mn);
-      const float fn = exp2f(ml[k].x - Mn);
-      L = L * fo + ml[k].y * fn;
-      o0 = o0 * fo + ov[k].x * fn;
-      o1 = o1 * fo + ov[k].y * fn;
-      M = Mn;
-    }
-  }
-}
+struct CombineItem {
+  UnitInfo r;  // h0, b, qrow are used
+  int head, nch;
+  const float* base;
+};
 
-// Unit and head of combine item pr, and whether it needs combining: returns
-// the number of chunks (0 when the item is skipped) and the partial base.
-__device__ __forceinline__ int combine_item(const DecodeArgs& a, int64_t pr, int D, UnitInfo* r,
-                                            int* head, const float** base) {
+__device__ __forceinline__ bool combine_item(const DecodeArgs& a, int64_t pr, int D,
+                                             CombineItem* it) {
   const int64_t UPB = (int64_t)a.KVN * a.HG;
-  const int64_t u = pr / a.GH;
-  *head = (int)(pr % a.GH);
-  const int b = (int)(u / UPB), w = (int)(u % UPB);
-  if (*head >= min(a.GH, a.G - (w % a.HG) * a.GH)) return 0;  // past the group's heads
-  int64_t qrow, ql, kv_len;
-  batch_lengths(a, b, &qrow, &ql, &kv_len);
-  if (ql <= 0) return 0;
-  *r = unit_from(a, b, w, qrow, ql, kv_len);
-  const ChunkGeom gm = chunk_geom(max(1, r->ntiles), a.sched[0], a.sched[1]);
-  if (gm.nch <= 1) return 0;  // written by the decode kernel itself
-  *base = a.partials + (a.sched[4 + b] + w) * (int64_t)a.GH * (D + 2) + *head * (D + 2);
-  return gm.nch;
+  const int64_t* Q = a.sched + kSchedHeader;
+  const int64_t* SB = Q + 3 * ((int64_t)a.B + 1);
+  it->head = (int)(pr % a.GH);
+  const int64_t bw = pr / a.GH;
+  const int w = (int)(bw % UPB);
+  const int hg = w % a.HG;
+  if (it->head >= min(a.GH, a.G - hg * a.GH)) return false;  // past the group's heads
+  const int b = (int)SB[bw / UPB];
+  it->nch = (int)((Q[b + 1] - Q[b]) / UPB);
+  it->r.b = b;
+  it->r.h0 = (w / a.HG) * a.G + hg * a.GH;
+  it->r.qrow = a.layout == 1 ? (int64_t)a.cu_seqlens_q[b] : (int64_t)b * a.S_q;
+  it->base = a.partials + (Q[b] + w) * (int64_t)a.GH * (D + 2) + it->head * (D + 2);
+  return true;
 }
 
-__device__ __forceinline__ void combine_store(const DecodeArgs& a, const UnitInfo& r, int head,
-                                              int D, int d, float M, float L, float o0,
-                                              float o1) {
-  const int h = r.h0 + head;
-  float scl, lse;
-  finish_head(a, h, M, L, &scl, &lse);
-  uint16_t* o = a.out + r.qrow * a.out_stride + (int64_t)h * D + d;
-  *reinterpret_cast<uint32_t*>(o) = pack_bf16(o0 * scl, o1 * scl);
-  if (a.lse && d == 0) {
-    const int64_t li = a.layout == 1 ? r.qrow * a.QN + h : ((int64_t)r.b * a.QN + h) * a.S_q;
-    a.lse[li] = lse;
-  }
-}
-
-// Few chunks per unit: one thread per (unit, head, d-pair), chunks folded in
-// order.
+// Few chunks per unit: one thread per (item, d-pair), chunks folded in order.
 template <int D>
 __global__ void __launch_bounds__(256, 4) decode_combine_flat(const DecodeArgs a) {
   constexpr int TPP = D / 2, PPB = 256 / TPP;
-  pdl_wait();  // every partial of the decode kernel is written
-  const int64_t pr = (int64_t)blockIdx.x * PPB + threadIdx.x / TPP;
-  if (pr >= a.num_units * a.GH) return;
-  const int d = 2 * (threadIdx.x % TPP);
-  UnitInfo r;
-  int head;
-  const float* base;
-  const int nch = combine_item(a, pr, D, &r, &head, &base);
-  if (nch == 0) return;
+  // The schedule was complete before the decode kernel started its work, so
+  // the first item is located while the decode kernel still runs; only the
+  // partials need its completion.
+  const int64_t items = a.sched[4] * a.KVN * a.HG * a.GH;
   const int64_t kstride = (int64_t)a.KVN * a.HG * a.GH * (D + 2);
-  float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f;
-  fold_chunks<D>(base, kstride, d, 0, 1, nch, M, L, o0, o1);
-  combine_store(a, r, head, D, d, M, L, o0, o1);
+  const int d = 2 * (threadIdx.x % TPP);
+  int64_t pr = (int64_t)blockIdx.x * PPB + threadIdx.x / TPP;
+  CombineItem it;
+  bool have = pr < items && combine_item(a, pr, D, &it);
+  pdl_wait();  // every partial of the decode kernel is written
+  while (pr < items) {
+    if (have) {
+      float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f;
+      fold_chunks<D>(it.base, kstride, d, 0, 1, it.nch, M, L, o0, o1);
+      combine_store(a, it.r, it.head, D, d, M, L, o0, o1);
+    }
+    pr += (int64_t)gridDim.x * PPB;
+    have = pr < items && combine_item(a, pr, D, &it);
+  }
 }
 
-// Many chunks per unit: one CTA per (unit, head); NGRP thread groups fold
-// every NGRP-th chunk, then group 0 folds the groups in order.
+// Many chunks per unit: one CTA per item; NGRP thread groups fold every
+// NGRP-th chunk, then group 0 folds the groups in order.
 template <int D>
 __global__ void __launch_bounds__(256, 4) decode_combine_grouped(const DecodeArgs a) {
   constexpr int TPP = D / 2, NGRP = 256 / TPP;
   __shared__ float4 st[NGRP][TPP];
-  pdl_wait();  // every partial of the decode kernel is written
-  const int grp = threadIdx.x / TPP, d = 2 * (threadIdx.x % TPP);
+  const int64_t items = a.sched[4] * a.KVN * a.HG * a.GH;
   const int64_t kstride = (int64_t)a.KVN * a.HG * a.GH * (D + 2);
-  for (int64_t pr = blockIdx.x; pr < a.num_units * a.GH; pr += gridDim.x) {
-    UnitInfo r;
-    int head;
-    const float* base;
-    const int nch = combine_item(a, pr, D, &r, &head, &base);  // uniform over the CTA
-    if (nch == 0) continue;
+  const int grp = threadIdx.x / TPP, t = threadIdx.x % TPP, d = 2 * t;
+  int64_t pr = blockIdx.x;
+  CombineItem it;
+  bool have = pr < items && combine_item(a, pr, D, &it);  // the schedule is complete
+  pdl_wait();  // every partial of the decode kernel is written
+  for (; pr < items; pr += gridDim.x, have = pr < items && combine_item(a, pr, D, &it)) {
+    if (!have) continue;  // uniform over the CTA
     float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f;
-    fold_chunks<D>(base, kstride, d, grp, NGRP, nch, M, L, o0, o1);
-    st[grp][threadIdx.x % TPP] = make_float4(M, L, o0, o1);
+    fold_chunks<D>(it.base, kstride, d, grp, NGRP, it.nch, M, L, o0, o1);
+    st[grp][t] = make_float4(M, L, o0, o1);
     __syncthreads();
     if (grp == 0) {
       for (int g2 = 1; g2 < NGRP; ++g2) {
-        const float4 x = st[g2][threadIdx.x % TPP];
+        const float4 x = st[g2][t];
         if (x.x == -INFINITY) continue;
         const float Mn = fmaxf(M, x.x);
         const float fo = M == -INFINITY ? 0.f : exp2f(M - Mn);
@@ -1130,7 +1176,7 @@ __global__ void __launch_bounds__(256, 4) decode_combine_grouped(const DecodeArg
         o1 = o1 * fo + x.w * fn;
         M = Mn;
       }
-      combine_store(a, r, head, D, d, M, L, o0, o1);
+      combine_store(a, it.r, it.head, D, d, M, L, o0, o1);
     }
     __syncthreads();
   }
@@ -1201,18 +1247,17 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUte
   cudaError_t e = launch_decode_main(a, tk, tv, fp8, s);
   if (e != cudaSuccess) return e;
   // The plan bounds the chunks by n*W + 4*U, so a unit has about n*W/U + 4;
-  // with more than 16 a (unit, head) gets a whole CTA.  The choice depends on
-  // shapes only, so results stay deterministic.
-  const int64_t pairs = a.num_units * a.GH;
-  if (pairs <= 0) return cudaSuccess;
+  // with more than 16 an item gets a whole CTA.  The choice depends on shapes
+  // only, so results stay deterministic.
+  const int64_t items = a.num_units * a.GH;  // bound: every batch split
   const int64_t est = (int64_t)a.num_ctas * a.chunks_per_cta / a.num_units + 4;
   if (est > 16) {
-    const int grid = (int)std::min<int64_t>(pairs, (int64_t)a.num_ctas * 16);
+    const int grid = (int)std::min<int64_t>(items, (int64_t)a.num_ctas * 8);
     if (a.D == 64) return launch_pdl(decode_combine_grouped<64>, dim3(grid), dim3(256), 0, s, a);
     return launch_pdl(decode_combine_grouped<128>, dim3(grid), dim3(256), 0, s, a);
   }
   const int ppb = 256 / (a.D / 2);
-  const int grid = (int)((pairs + ppb - 1) / ppb);
+  const int grid = (int)std::min<int64_t>((items + ppb - 1) / ppb, (int64_t)a.num_ctas * 8);
   if (a.D == 64) return launch_pdl(decode_combine_flat<64>, dim3(grid), dim3(256), 0, s, a);
   return launch_pdl(decode_combine_flat<128>, dim3(grid), dim3(256), 0, s, a);
 }

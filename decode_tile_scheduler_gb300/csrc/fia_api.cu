@@ -157,8 +157,7 @@ struct DecodePlan {
 };
 
 // Decode workspace: [0, 256) error word (offset 0) and the claim counters
-// (offset 16); the schedule header and prefixes; the claim queue; the partial
-// slots.  A unit of cost c gets at most c/C big chunks
+// (offset 16); the schedule; the claim queue; the partial slots.  A unit of cost c gets at most c/C big chunks
 // (so at most n*W over all units) and at most 4 small ones, hence
 // max_chunks = n*W + 4*U bounds the chunks of any lengths.
 fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
@@ -173,7 +172,7 @@ fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
   pl->max_chunks = (int64_t)n * kDecodeChunksPerCta + 4 * pl->U;
   int64_t off = kAlign;
   pl->off_sched = off;
-  off = align_up(off + 8 * (4 + 3 * ((int64_t)p->batch + 1)));
+  off = align_up(off + 8 * (kSchedHeader + 3 * ((int64_t)p->batch + 1) + p->batch));
   pl->off_queue = off;
   off = align_up(off + 16 * pl->max_chunks);
   pl->off_part = off;

@@ -40,16 +40,18 @@ struct DecodeArgs {
   int chunks_per_cta;          // W: the chunk size aims at W chunks per CTA
   int64_t num_units;           // B * KVN * HG
   int64_t max_chunks;          // partial slots: a bound on the number of chunks
-  int64_t* sched;              // [4 + 3(B+1)]: C, c2, chunks, big chunks, then the
-                               // partial-slot prefix Q and the queue prefixes R1, R2
+  int64_t* sched;              // [8 + 3(B+1) + B]: C, c2, chunks, big chunks, split
+                               // batches, 3 zeros; the partial-slot prefix Q, the queue
+                               // prefixes R1, R2; the split batches (then -1)
   int4* queue;                 // [max_chunks] (b, chunk << 10 | unit of b, kv_len, qrow)
-  int* claim;                  // [2]: next queue entry, CTAs done claiming
+  int* claim;                  // [2]: next queue entry, CTAs done with the queue
   float* partials;             // [max_chunks][GH][D + 2]: acc, then m and l
   int* err;
 };
 
 // Target number of big chunks per persistent CTA in the decode schedule.
-constexpr int kDecodeChunksPerCta = 8;
+constexpr int kDecodeChunksPerCta = 6;
+constexpr int kSchedHeader = 8;  // int64 header words of the decode schedule
 
 struct PrefillArgs {
   int B, QN, KVN, D, G, npairs, per_pair;  // per_pair query heads per unit (2, or 1 if G odd)

@@ -204,9 +204,10 @@ fia_status fia_decode_run_noalloc(const fia_params *p, void *stream);
  * chunks per CTA, C = max(1, ceil(T / (n W))) and c2 = ceil(C / 2).  A unit
  * of cost c gets n1 = max(0, floor(c/C) - 1) chunks of C tiles, then chunks
  * of c2 tiles over the rest.  sched holds int64 {C, c2, chunks N, big chunks
- * F}, then Q[B+1] (partial slots before batch b: chunk i of unit w of batch b
- * owns slot Q[b] + i*UPB + w, UPB = units per batch), then R1[B+1] and
- * R2[B+1] (big and small chunks before batch b).  The claim queue lists the
+ * F, split batches M, 0, 0, 0}, then Q[B+1] (partial slots before batch b:
+ * chunk i of unit w of batch b owns slot Q[b] + i*UPB + w, UPB = units per
+ * batch), then R1[B+1] and R2[B+1] (big and small chunks before batch b),
+ * then the M batches whose units have several chunks (ascending; -1 after).  The claim queue lists the
  * big chunks, batch-major then chunk then unit, followed by the small chunks
  * in the same order; entry = four int32 (b, i << 10 | w, KV length of b,
  * first query row of b). */
@@ -215,7 +216,7 @@ typedef struct fia_plan_layout {
     int32_t num_ctas;         /* persistent CTAs                               */
     int64_t num_units;        /* decode: units; prefill: bound on units        */
     int64_t max_chunks;       /* decode: partial slots, bound on chunks        */
-    int64_t sched_off;        /* decode: int64 [4 + 3(B+1)] schedule           */
+    int64_t sched_off;        /* decode: int64 [8 + 3(B+1) + B] schedule       */
     int64_t queue_off;        /* decode: int32 [max_chunks][4] claim queue     */
     int64_t unit_list_off;    /* prefill: int32 [num_units][2] ordered units   */
     int64_t total_bytes;

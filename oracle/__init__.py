@@ -278,14 +278,14 @@ def bf16_to_double(bits: int) -> float:
 
 
 def decode_schedule(p, num_ctas: int, per_cta: int):
-    """(sched int64 [4 + 3(B+1)], queue int32 [N, 4]) of the decode chunk
+    """(sched int64 [8 + 3(B+1) + B], queue int32 [N, 4]) of the decode chunk
     schedule for n CTAs and W = per_cta chunks per CTA."""
     s, keep = _fia_struct(p)
     G = p.QN // p.KVN
     HG = -(-G // (8 if G <= 8 else 16))
     U = p.B * p.KVN * HG
     cap = num_ctas * per_cta + 4 * U
-    sched = np.zeros(4 + 3 * (p.B + 1), dtype=np.int64)
+    sched = np.zeros(8 + 3 * (p.B + 1) + p.B, dtype=np.int64)
     queue = np.zeros((max(cap, 1), 4), dtype=np.int32)
     n = lib().oracle_decode_schedule(ctypes.byref(s), num_ctas, per_cta, sched.ctypes.data,
                                      queue.ctypes.data, cap)

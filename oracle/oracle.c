@@ -511,9 +511,12 @@ static int64_t or_tiles(int64_t lo, int64_t hi)
  *   a unit of cost c has n1 = max(0, floor(c/C) - 1) big chunks of C tiles,
  *   then its remaining c - n1*C tiles in small chunks of c2 tiles (the last
  *   one shorter), n2 of them.
- * Outputs (int64 sched[4 + 3(B+1)]): C, c2, N (all chunks), F (big chunks),
+ * Outputs (int64 sched[8 + 3(B+1) + B]): C, c2, N (all chunks), F (big
+ * chunks), M (batches whose units have more than one chunk), three zeros;
  * Q[b] = sum over b' < b of (n1+n2)(b')*UPB, then R1[b] (big) and R2[b]
- * (small) the same sums of n1*UPB and n2*UPB; each array has B+1 entries.
+ * (small) the same sums of n1*UPB and n2*UPB, each array with B+1 entries;
+ * then the M batches with more than one chunk per unit in increasing order,
+ * followed by -1 up to B entries.
  * The queue (N entries of four int32) lists for b = 0..B-1, chunk i =
  * 0..n1-1, unit w = 0..UPB-1 the entry (b, i << 10 | w, kv_len(b), first
  * query row of b), then the small chunks in the same nesting with i =
@@ -525,7 +528,8 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
     int HG = (int)or_ceil_div(G, G <= 8 ? 8 : 16);
     int64_t UPB = (int64_t)a->KVN * HG;
     int B = a->B, b;
-    int64_t *Q = sched + 4, *R1 = Q + (B + 1), *R2 = R1 + (B + 1);
+    int64_t *Q = sched + 8, *R1 = Q + (B + 1), *R2 = R1 + (B + 1), *SB = R2 + (B + 1);
+    int64_t nsplit = 0;
     int64_t *cost = (int64_t *)malloc(sizeof(int64_t) * (B > 0 ? B : 1));
     int64_t T = 0, C, c2, q = 0, r1 = 0, r2 = 0, n = 0;
     for (b = 0; b < B; ++b) {
@@ -551,6 +555,8 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
         Q[b] = q;
         R1[b] = r1;
         R2[b] = r2;
+        SB[b] = -1;
+        if (n1 + n2 > 1) SB[nsplit++] = b;
         q += (n1 + n2) * UPB;
         r1 += n1 * UPB;
         r2 += n2 * UPB;
@@ -562,6 +568,8 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
     sched[1] = c2;
     sched[2] = q;
     sched[3] = r1;
+    sched[4] = nsplit;
+    sched[5] = sched[6] = sched[7] = 0;
     if (q > cap) {
         free(cost);
         return -1;

@@ -93,13 +93,36 @@ def test_schedule_metadata_bit_exact():
         ws = c.ws.cpu()
         U = lay.num_units
         per_cta = (lay.max_chunks - 4 * U) // n
-        nsched = 4 + 3 * (p.B + 1)
+        nsched = 8 + 3 * (p.B + 1) + p.B
         sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
         rs, rq = oracle.decode_schedule(p.to("cpu"), n, per_cta)
         assert np.array_equal(sched, rs)
         N = int(sched[2])
         queue = ws[lay.queue_off: lay.queue_off + 16 * N].view(torch.int32).numpy().reshape(N, 4)
         assert np.array_equal(queue, rq)
+
+
+def test_schedule_many_batches_bit_exact_and_parity():
+    # more batches than the scheduler keeps in shared memory: the global path
+    import decode_tile_scheduler_gb300 as fia
+    g = np.random.default_rng(41)
+    B = 2100
+    kv = [int(x) for x in g.integers(0, 600, B)]
+    p = fi.make_fia(B=B, QN=8, KVN=2, D=128, q_lens=[1] * B, kv_lens=kv, block_size=64,
+                    seed=43, device=dev)
+    c, out, lse = _run(p, 152)
+    lay = c.plan_layout()
+    ws = c.ws.cpu()
+    per_cta = (lay.max_chunks - 4 * lay.num_units) // 152
+    nsched = 8 + 3 * (B + 1) + B
+    sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
+    rs, rq = oracle.decode_schedule(p.to("cpu"), 152, per_cta)
+    assert np.array_equal(sched, rs)
+    N = int(sched[2])
+    queue = ws[lay.queue_off: lay.queue_off + 16 * N].view(torch.int32).numpy().reshape(N, 4)
+    assert np.array_equal(queue, rq)
+    ro, rl = _ref(p)
+    check_close(out, lse, ro, rl, "2100 batches")
 
 
 def test_execute_reuses_one_plan():

@@ -466,11 +466,15 @@ def test_decode_schedule_chunks_cover_each_unit_once(ctas, per_cta):
     T = UPB * sum(costs)
     C = max(1, -(-T // (ctas * per_cta)))
     c2 = -(-C // 2)
-    assert list(sched[:2]) == [C, c2]
+    assert list(sched[:2]) == [C, c2] and list(sched[5:8]) == [0, 0, 0]
     N, F = int(sched[2]), int(sched[3])
     assert N == queue.shape[0] and 0 <= F <= N
     assert N <= ctas * per_cta + 4 * B * UPB             # the workspace bound
-    Q = sched[4:4 + B + 1]
+    Q = sched[8:8 + B + 1]
+    # batches whose units need a split-KV combine, in order, then -1
+    split = [b for b in range(B) if (Q[b + 1] - Q[b]) // UPB > 1]
+    SB = sched[8 + 3 * (B + 1):]
+    assert sched[4] == len(split) and list(SB) == split + [-1] * (B - len(split))
     chunks = _unit_chunks(sched, queue, B, UPB)
     for b in range(B):
         for w in range(UPB):
@@ -500,7 +504,7 @@ def test_decode_schedule_band_counts_window_tiles_only():
     # row position 999 sees [799, 999] -> tiles 6..7; position 99 sees [0, 99] -> tile 0
     # T = 3 tiles over 24 chunk slots: C = 1, so each tile is one chunk
     assert sched[0] == 1
-    Q = sched[4:7]
+    Q = sched[8:11]
     assert list(np.diff(Q)) == [2, 1]
 
 

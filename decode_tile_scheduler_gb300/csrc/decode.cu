@@ -179,24 +179,22 @@ __device__ __forceinline__ int find_batch(const T* prefix, int B, int64_t g) {
   return lo;
 }
 
-__device__ __forceinline__ int64_t phys_row(const DecodeArgs& a, int b, int64_t j) {
-  if (a.block_table) {
-    const int64_t blk = a.block_table[(int64_t)b * a.max_blocks + j / a.block_size];
-    return blk * a.block_size + j % a.block_size;
-  }
-  return (int64_t)b * a.S_kv + j;
+// Physical page holding logical KV row j of batch b (0 for a contiguous cache).
+__device__ __forceinline__ int64_t page_of(const DecodeArgs& a, int b, int64_t j) {
+  return a.block_table ? (int64_t)a.block_table[(int64_t)b * a.max_blocks + j / a.block_size] : 0;
 }
-
-// Row of the FP8 scale arrays for logical KV row j of batch b, KV head hk:
-// scales are stored head-major inside each page, [pages, KV_N, page rows,
-// D/64] (the paged per-token, per-head scale shape (blockNum, N, blockSize) of
-// the FIA dequantisation parameters, with the 64-element tiles last).
-__device__ __forceinline__ int64_t scale_row(const DecodeArgs& a, int b, int hk, int64_t j) {
-  if (a.block_table) {
-    const int64_t blk = a.block_table[(int64_t)b * a.max_blocks + j / a.block_size];
-    return (blk * a.KVN + hk) * a.block_size + j % a.block_size;
-  }
-  return ((int64_t)b * a.KVN + hk) * a.S_kv + j;
+// Pool row and FP8 scale row of logical KV row j of batch b, KV head hk, in
+// page blk.  FP8 scales are stored head-major inside each page, [pages, KV_N,
+// page rows, D/64] (the paged per-token, per-head scale shape (blockNum, N,
+// blockSize) of the FIA dequantisation parameters, with the 64-element tiles
+// last).
+__device__ __forceinline__ int64_t pool_row(const DecodeArgs& a, int b, int64_t blk, int64_t j) {
+  return a.block_table ? blk * a.block_size + j % a.block_size : (int64_t)b * a.S_kv + j;
+}
+__device__ __forceinline__ int64_t scale_row_in(const DecodeArgs& a, int b, int hk, int64_t blk,
+                                                int64_t j) {
+  return a.block_table ? (blk * a.KVN + hk) * a.block_size + j % a.block_size
+                       : ((int64_t)b * a.KVN + hk) * a.S_kv + j;
 }
 
 // Bounded barrier wait; after the first time-out in the CTA every later wait
@@ -552,19 +550,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++ucount;
       }
+      // lane roles for the boxes of a tile: K or V, 128-byte column slice,
+      // page piece
+      const int nrb = kKvTile / a.box_rows;
+      const int nbox = nrb * Cfg::kNsub * 2;  // <= 32: one box per lane
+      const int isv = lane & 1;
+      const int sub = (lane >> 1) % Cfg::kNsub;
+      const int rb = (lane >> 1) / Cfg::kNsub;
       for (int t = t_begin; r.ntiles > 0 && t < t_end; ++t, ++it) {
         const int s = it % S;
         const uint32_t par = ((it / S) & 1) ^ 1;
         const int64_t j0 = (int64_t)(r.tile0 + t) * kKvTile;
-        const int nrb = kKvTile / a.box_rows;
-        const int nbox = nrb * Cfg::kNsub * 2;  // <= 32: one box per lane
-        // page lookups first: their latency overlaps the wait for the slot
-        const int isv = lane & 1;
-        const int sub = (lane >> 1) % Cfg::kNsub;
-        const int rb = (lane >> 1) / Cfg::kNsub;
         const int64_t jb = j0 + (int64_t)rb * a.box_rows;
         const bool mine = lane < nbox && jb < r.kv_len;
-        const int64_t prow = mine ? phys_row(a, r.b, jb) : 0;
+        const int64_t blk = mine ? page_of(a, r.b, jb) : 0;  // latency overlaps the slot wait
+        const int64_t prow = mine ? pool_row(a, r.b, blk, jb) : 0;
         constexpr int NT = D / 64;
         // FP8: the scales of one head inside a page are contiguous rows of NT
         // floats, so each (K or V, page piece) is one bulk copy next to its
@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t srow = 0;
         int srows = a.box_rows;
         if constexpr (FP8) {
-          if (mine) srow = scale_row(a, r.b, r.hk, jb);
+          if (mine) srow = scale_row_in(a, r.b, r.hk, blk, jb);
           if (!a.block_table) srows = (int)min((int64_t)a.box_rows, (int64_t)a.S_kv - jb);
         }
         int nvalid = 0, scale_rows = 0;
@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       m_r[ng][0] = m_r[ng][1] = -INFINITY;
       l_r[ng][0] = l_r[ng][1] = 0.f;
     }
-    float vref[2] = {1.f, 1.f};  // FP8: V scale reference per d-tile
+    int vexp[2] = {0, 0};  // FP8: exponent of the V scale reference per d-tile (0: none yet)
 
     const int ntile_here = r.ntiles == 0 ? 0 : (t_end - t_begin);
     for (int tt = 0; tt < ntile_here; ++tt, ++it) {
@@ -810,9 +810,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mn = fmaxf(m_r[ng][e], mx);
+          // the reference moves only when the maximum passes it by more than
+          // 8 (log2 units): p <= 2^8 stays exact enough in 16-bit P, and the
+          // accumulators are rarely rescaled
+          const float mold = m_r[ng][e];
+          const float mn = mx > mold + 8.f ? mx : mold;
           const float mu = mn == -INFINITY ? 0.f : mn;
-          corr[ng][e] = m_r[ng][e] == -INFINITY ? 0.f : fast_exp2(m_r[ng][e] - mu);
+          corr[ng][e] = mn == mold ? 1.f : (mold == -INFINITY ? 0.f : fast_exp2(mold - mu));
           m_r[ng][e] = mn;
           const float p0 = fast_exp2(x0 - mu), p1 = fast_exp2(x1 - mu);
           sc[ng][e] = p0;
@@ -830,15 +834,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           pb[ng][0] = movmatrix_t(pack_bf16(sc[ng][0], sc[ng][1]));
           pb[ng][1] = movmatrix_t(pack_bf16(sc[ng][2], sc[ng][3]));
         }
+        bool resc = false;
 #pragma unroll
-        for (int i = 0; i < MT; ++i)
+        for (int ng = 0; ng < NG; ++ng) resc |= (corr[ng][0] != 1.f) | (corr[ng][1] != 1.f);
+        if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-          for (int ng = 0; ng < NG; ++ng) {
-            acc[i][ng][0] *= corr[ng][0];
-            acc[i][ng][1] *= corr[ng][1];
-            acc[i][ng][2] *= corr[ng][0];
-            acc[i][ng][3] *= corr[ng][1];
-          }
+          for (int i = 0; i < MT; ++i)
+#pragma unroll
+            for (int ng = 0; ng < NG; ++ng) {
+              acc[i][ng][0] *= corr[ng][0];
+              acc[i][ng][1] *= corr[ng][1];
+              acc[i][ng][2] *= corr[ng][0];
+              acc[i][ng][3] *= corr[ng][1];
+            }
+        }
         // rows past kv_len may hold anything (even NaN): zero their V lanes
         bool z0 = false, z1 = false, z2 = false, z3 = false;
         if (tail) {
@@ -879,35 +888,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (jg0 >= r.kv_len) v0 = make_float2(0.f, 0.f);
           if (jg1 >= r.kv_len) v1 = make_float2(0.f, 0.f);
         }
-        // warp-wide reference per d-tile keeps P^T * scale / ref in (0, 1]
-        float vmax[2] = {fmaxf(v0.x, v1.x), fmaxf(v0.y, v1.y)};
+        // Warp-wide power-of-two reference per d-tile: 2^(e-127) with e the
+        // largest exponent of a V scale seen so far (positive floats order
+        // like their bit patterns, so one warp max over the bits finds it).
+        // P^T * scale / ref then stays below 2^9 in fp16, and moving the
+        // reference rescales the accumulators by an exact power of two.
+        float ratio[2], iv[2];
+        bool resc = false;
 #pragma unroll
         for (int t2 = 0; t2 < 2; ++t2) {
-          vmax[t2] = fmaxf(vmax[t2], __shfl_xor_sync(0xffffffffu, vmax[t2], 4));
-          vmax[t2] = fmaxf(vmax[t2], __shfl_xor_sync(0xffffffffu, vmax[t2], 8));
-          vmax[t2] = fmaxf(vmax[t2], __shfl_xor_sync(0xffffffffu, vmax[t2], 16));
-          if (!(vmax[t2] > 0.f)) vmax[t2] = vref[t2];
+          const uint32_t bits = max(__float_as_uint(t2 ? v0.y : v0.x), __float_as_uint(t2 ? v1.y : v1.x));
+          const int e = (int)(__reduce_max_sync(0xffffffffu, bits) >> 23);
+          const int en = max(vexp[t2], e);
+          ratio[t2] = (en == vexp[t2] || vexp[t2] == 0) ? 1.f : ldexpf(1.f, vexp[t2] - en);
+          resc |= ratio[t2] != 1.f;
+          vexp[t2] = en;
+          iv[t2] = en > 0 ? ldexpf(1.f, 127 - en) : 1.f;
         }
-        const float ratio[2] = {vref[0] / vmax[0], vref[1] / vmax[1]};
-        vref[0] = vmax[0];
-        vref[1] = vmax[1];
 #pragma unroll
-        for (int i = 0; i < MT; ++i) {
-          const int t2 = i >> 2;
+        for (int ng = 0; ng < NG; ++ng) resc |= (corr[ng][0] != 1.f) | (corr[ng][1] != 1.f);
+        if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-          for (int ng = 0; ng < NG; ++ng) {
-            acc[i][ng][0] *= corr[ng][0] * ratio[t2];
-            acc[i][ng][1] *= corr[ng][1] * ratio[t2];
-            acc[i][ng][2] *= corr[ng][0] * ratio[t2];
-            acc[i][ng][3] *= corr[ng][1] * ratio[t2];
+          for (int i = 0; i < MT; ++i) {
+            const int t2 = i >> 2;
+#pragma unroll
+            for (int ng = 0; ng < NG; ++ng) {
+              acc[i][ng][0] *= corr[ng][0] * ratio[t2];
+              acc[i][ng][1] *= corr[ng][1] * ratio[t2];
+              acc[i][ng][2] *= corr[ng][0] * ratio[t2];
+              acc[i][ng][3] *= corr[ng][1] * ratio[t2];
+            }
           }
         }
         // P^T per d-tile with the V scales folded in
         uint32_t pb[2][NG][2];
 #pragma unroll
         for (int t2 = 0; t2 < 2; ++t2) {
-          const float iv = 1.f / vref[t2];
-          const float fa = (t2 ? v0.y : v0.x) * iv, fb = (t2 ? v1.y : v1.x) * iv;
+          const float fa = (t2 ? v0.y : v0.x) * iv[t2], fb = (t2 ? v1.y : v1.x) * iv[t2];
 #pragma unroll
           for (int ng = 0; ng < NG; ++ng) {
             pb[t2][ng][0] = movmatrix_t(pack_f16(sc[ng][0] * fa, sc[ng][1] * fa));
@@ -963,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (FP8) {
 #pragma unroll
       for (int i = 0; i < MT; ++i) {
-        const float f = vref[i >> 2];
+        const float f = vexp[i >> 2] > 0 ? ldexpf(1.f, vexp[i >> 2] - 127) : 1.f;
 #pragma unroll
         for (int ng = 0; ng < NG; ++ng) {
           acc[i][ng][0] *= f; acc[i][ng][1] *= f; acc[i][ng][2] *= f; acc[i][ng][3] *= f;

@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(const PrefillArg
 // ---------------------------------------------------------------------------
 // attention kernel
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool NEG>  // NEG: the softmax scale is negative
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tq,
                    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
@@ -316,9 +316,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
   tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[1]);
   const int64_t num_units = *a.num_units;
+  // Register split by warpgroup (each role branch below starts with its
+  // part): the producer / MMA / guard warpgroup gives registers to the two
+  // softmax warpgroups, which keep a whole row of S (128 fp32) in registers.
+  // 128 x 72 + 256 x 216 = 384 x 168, the launch's total.
 
   if (warp == 0) {
     // ============================ producer ============================
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
@@ -411,6 +416,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false);
       constexpr uint32_t kIdO = idesc_bf16(128, D, true);
@@ -512,6 +518,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncwarp();
   } else if (warp == 2) {
     // ============================ V guard ============================
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
     int ucnt = 0, kv_it = 0;
     while (true) {
       const int ms = ucnt & 1;
@@ -541,8 +548,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (lane == 0) mbar_arrive(&vready[vs]);
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp == 3) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");  // no role
+  } else {
     // ============================ softmax + epilogue ============================
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
     const int s = (warp - 4) >> 2;      // slot
     const int row = tid - 128 - 128 * s;  // query row of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -577,37 +587,35 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int c1 = (int)min(max(hi - j0 + 1, (int64_t)0), (int64_t)kKvTile);
         const bool all_full = __all_sync(0xffffffffu, c0 == 0 && c1 == kKvTile);
         const float sl = a.scale_log2;
-        const float hole = sl >= 0.f ? -INFINITY : INFINITY;  // masked score
-        // pass 1: row maximum of the raw scores (minimum for a negative scale),
-        // 64 columns per TMEM round trip, four three-input chains
-        float pm[4] = {hole, hole, hole, hole};
+        // masked score: -inf after the scaling for either sign of the scale
+        const uint32_t hole = __float_as_uint(NEG ? INFINITY : -INFINITY);
+        // the row's 128 scores: four TMEM loads, one wait; they stay in
+        // registers for the maximum and the exponentials
+        uint32_t v[kKvTile];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[64];
-          tmem_ld32(tS + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          tmem_ld32(tS + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_wait_ld();
-          if (!all_full) {
+        for (int c = 0; c < kKvTile / 32; ++c)
+          tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+        tmem_wait_ld();
+        if (!all_full) {
 #pragma unroll
-            for (int e = 0; e < 64; ++e)
-              if (64 * c + e < c0 || 64 * c + e >= c1) v[e] = __float_as_uint(hole);
-          }
-          if (sl >= 0.f) {
-#pragma unroll
-            for (int e = 0; e < 64; e += 8)
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                pm[k] = fmax3(pm[k], __uint_as_float(v[e + k]), __uint_as_float(v[e + 4 + k]));
-          } else {
-#pragma unroll
-            for (int e = 0; e < 64; e += 8)
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                pm[k] = fmin3(pm[k], __uint_as_float(v[e + k]), __uint_as_float(v[e + 4 + k]));
-          }
+          for (int e = 0; e < kKvTile; ++e)
+            if (e < c0 || e >= c1) v[e] = hole;
         }
-        const float best = sl >= 0.f ? fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]))
-                                     : fminf(fminf(pm[0], pm[1]), fminf(pm[2], pm[3]));
+        // row maximum of the raw scores (minimum for a negative scale), four
+        // three-input chains
+        float pm[4] = {__uint_as_float(hole), __uint_as_float(hole), __uint_as_float(hole),
+                       __uint_as_float(hole)};
+#pragma unroll
+        for (int e = 0; e < kKvTile; e += 8)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if constexpr (NEG)
+              pm[k] = fmin3(pm[k], __uint_as_float(v[e + k]), __uint_as_float(v[e + 4 + k]));
+            else
+              pm[k] = fmax3(pm[k], __uint_as_float(v[e + k]), __uint_as_float(v[e + 4 + k]));
+          }
+        const float best = NEG ? fminf(fminf(pm[0], pm[1]), fminf(pm[2], pm[3]))
+                               : fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
         const float mx = isinf(best) ? -INFINITY : best * sl;  // all masked -> -inf
         // lazily moved reference maximum: a row moves it when the new maximum
         // exceeds it by more than 2^8 (or on its first visible key); rows
@@ -635,29 +643,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         if (move) m_used = mx;
         const float nbase = m_used == -INFINITY ? 0.f : -m_used;
-        // pass 2: p = 2^(s * scale * log2e - m), two columns per packed FMA,
-        // masked columns give 0, packed to bf16 pairs over the first 64 columns
+        // p = 2^(s * scale * log2e - m), two columns per packed FMA; masked
+        // columns hold -inf after the scaling and give 0; P goes back to the
+        // first 64 TMEM columns of S as bf16 pairs
         float2 ps[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) ps[k] = make_float2(0.f, 0.f);
         const float2 sl2 = make_float2(sl, sl), nb2 = make_float2(nbase, nbase);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t v[64];
-          tmem_ld32(tS + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          tmem_ld32(tS + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_wait_ld();
           uint32_t pv[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float2 x = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+            const float2 x = ffma2(make_float2(__uint_as_float(v[64 * c + 2 * e]),
+                                               __uint_as_float(v[64 * c + 2 * e + 1])),
                                    sl2, nb2);
-            float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            if (!all_full) {
-              const int ca = 64 * c + 2 * e;
-              pp.x = (ca >= c0 && ca < c1) ? pp.x : 0.f;
-              pp.y = (ca + 1 >= c0 && ca + 1 < c1) ? pp.y : 0.f;
-            }
+            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             ps[e & 3] = fadd2(ps[e & 3], pp);
             pv[e] = pack_bf16(pp.x, pp.y);
           }
@@ -735,12 +736,12 @@ cudaError_t launch_prefill_schedule(const PrefillArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool NEG>
 static cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& tq,
                                     const CUtensorMap& tk, const CUtensorMap& tv,
                                     cudaStream_t s) {
   using Cfg = PrefillCfg<D>;
-  auto kern = prefill_kernel<D>;
+  auto kern = prefill_kernel<D, NEG>;
   static std::atomic<uint64_t> done_mask[4];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -757,7 +758,11 @@ static cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& tq,
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t s) {
-  return a.D == 64 ? launch_prefill_t<64>(a, tq, tk, tv, s) : launch_prefill_t<128>(a, tq, tk, tv, s);
+  const bool neg = a.scale_log2 < 0.f;
+  if (a.D == 64) return neg ? launch_prefill_t<64, true>(a, tq, tk, tv, s)
+                            : launch_prefill_t<64, false>(a, tq, tk, tv, s);
+  return neg ? launch_prefill_t<128, true>(a, tq, tk, tv, s)
+             : launch_prefill_t<128, false>(a, tq, tk, tv, s);
 }
 
 }  // namespace fia

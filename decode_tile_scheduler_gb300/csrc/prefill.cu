@@ -15,9 +15,11 @@
 // Kernel roles (12 warps, one CTA per SM, all 512 TMEM columns):
 //   warp 0      producer: TMA loads of the Q tiles and of K/V tiles whose rows
 //               come from block_table (128-byte swizzled boxes)
-//   warp 1      MMA issuer (one thread): S = Q K^T (both operands in shared
-//               memory) and O += P V (P in TMEM, V in shared memory), fp32
-//               accumulators in TMEM, ordered so that the two slots ping-pong
+//   warps 1, 3  MMA issuers, one thread each, for query slots 0 and 1:
+//               S = Q K^T (both operands in shared memory) and O += P V (P in
+//               TMEM, V in shared memory), fp32 accumulators in TMEM; the two
+//               slots ping-pong, and each thread's commits and waits overlap
+//               the other slot's MMAs
 //   warp 2      V guard: zeroes V rows past kv_len in a tail tile, so that a
 //               zero probability never meets a NaN in unused cache rows
 //   warps 4-7   softmax of slot 0; warps 8-11 softmax of slot 1: one TMEM lane
@@ -43,15 +45,15 @@ template <int D>
 struct PrefillCfg {
   static constexpr int kNsub = D / 64;                    // 128-byte slices per row
   static constexpr int kTileBytes = kNsub * 128 * 128;    // a 128-row tile of Q, K or V
-  static constexpr int kKStages = D == 128 ? 3 : 4;
-  static constexpr int kVStages = D == 128 ? 2 : 4;
+  static constexpr int kKStages = D == 128 ? 2 : 4;
+  static constexpr int kVStages = D == 128 ? 3 : 4;
   static constexpr int kOffQ = 0;                         // 2 slots
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   // barriers: mfull[2] mempty[2] qfull qempty kfull[KS] kempty[KS] vfull[VS]
-  // vready[VS] vempty[VS] sfull[2] pfull[2] ofull[2] ofree[2] drain
-  static constexpr int kNumBars = 4 + 2 + 2 * kKStages + 3 * kVStages + 8 + 1;
+  // vready[VS] vempty[VS] sfull[2] pfull[2] ofull[2] ofree[2] drain[2] tok[2]
+  static constexpr int kNumBars = 4 + 2 + 2 * kKStages + 3 * kVStages + 8 + 2 + 2;
   static constexpr int kOffMsg = kOffBar + 8 * kNumBars;
   static constexpr int kOffMisc = kOffMsg + 2 * 64;
   static constexpr int kSmem = kOffMisc + 64 + 1024;
@@ -278,7 +280,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* pfull = sfull + 2;
   uint64_t* ofull = pfull + 2;
   uint64_t* ofree = ofull + 2;
-  uint64_t* drain = ofree + 2;
+  uint64_t* drain = ofree + 2;  // [2], one per MMA thread
+  uint64_t* tok = drain + 2;    // [2], MMA issue turn of each slot
   PMsg* msg = reinterpret_cast<PMsg*>(smem + Cfg::kOffMsg);
   int* misc = reinterpret_cast<int*>(smem + Cfg::kOffMisc);  // [0] abort, [1] tmem base
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -286,24 +289,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(&mfull[s], 1);
-      mbar_init(&mempty[s], 4);
+      mbar_init(&mempty[s], 5);  // two MMA threads, the V guard, two softmax warpgroups
       mbar_init(&sfull[s], 1);
       mbar_init(&pfull[s], 4);  // one arrival per softmax warp
       mbar_init(&ofull[s], 1);
       mbar_init(&ofree[s], 4);
     }
     mbar_init(qfull, 1);
-    mbar_init(qempty, 1);
+    mbar_init(qempty, 2);  // one commit (or arrival) per MMA thread
     for (int s = 0; s < KS; ++s) {
       mbar_init(&kfull[s], 1);
-      mbar_init(&kempty[s], 1);
+      mbar_init(&kempty[s], 2);
     }
     for (int s = 0; s < VS; ++s) {
       mbar_init(&vfull[s], 1);
       mbar_init(&vready[s], 1);
-      mbar_init(&vempty[s], 1);
+      mbar_init(&vempty[s], 2);
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
+    mbar_init(&tok[0], 1);
+    mbar_init(&tok[1], 1);
     misc[0] = 0;
     fence_barrier_init();
   }
@@ -414,43 +420,64 @@ __global__ void __launch_bounds__(kPThreads, 1)
                       &tv, &vfull[vs], m.hk * D + sub * 64, (int)prow);
       }
     }
-  } else if (warp == 1) {
-    // ============================ MMA issuer ============================
+  } else if (warp == 1 || warp == 3) {
+    // ========================= MMA issuers =========================
+    // Warp 1 issues the MMAs of query slot 0, warp 3 those of slot 1 (one
+    // thread each).  tcgen05.mma issue blocks at about the rate the tensor
+    // core executes, so a single issuing thread leaves the tensor core idle
+    // while it commits and waits between batches; with one thread per slot,
+    // one slot's bookkeeping overlaps the other slot's MMAs.  K, V and Q
+    // buffers are released when both threads have committed (count 2).
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
+    const int s = warp == 3 ? 1 : 0;
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false);
       constexpr uint32_t kIdO = idesc_bf16(128, D, true);
       const uint32_t sq = smem_u32(smem + Cfg::kOffQ);
       const uint32_t sk = smem_u32(smem + Cfg::kOffK);
       const uint32_t sv = smem_u32(smem + Cfg::kOffV);
-      int ucnt = 0, kv_it = 0, q_cnt = 0;
-      int s_it[2] = {0, 0}, u_cnt[2] = {0, 0};
+      int ucnt = 0, kv_it = 0, q_cnt = 0, p_it = 0, u_cnt = 0;
+      // Issue turns: in units with two slots the threads issue their MMA
+      // batches strictly alternately (slot 0, slot 1, slot 0, ...), which
+      // keeps the two softmax warpgroups half a period apart (ping-pong);
+      // a thread hands the turn over right after its last MMA of a batch.
+      int turn = 0;  // batches issued in two-slot units
+      auto take_turn = [&](bool paired) {
+        if (!paired) return;
+        if (s == 0) {
+          if (turn > 0) pwait(&tok[0], (uint32_t)((turn - 1) & 1), a.err, misc);
+        } else {
+          pwait(&tok[1], (uint32_t)(turn & 1), a.err, misc);
+        }
+      };
+      auto pass_turn = [&](bool paired) {
+        if (!paired) return;
+        mbar_arrive(&tok[1 - s]);
+        ++turn;
+      };
       // descriptors of every operand buffer, built once; a k-step only adds
       // its byte offset (>> 4) to the start-address field
-      const uint64_t qd0 = smem_desc_sw128(sq, 16, 1024);
+      const uint64_t qd = smem_desc_sw128(sq, 16, 1024) + (uint64_t)s * (Cfg::kTileBytes >> 4);
       const uint64_t kd0 = smem_desc_sw128(sk, 16, 1024);
       // V is the MN-major B operand of P V: 64-column swizzle atoms 16 KB apart
       // (leading byte offset), 8-row groups along K 1 KB apart (stride offset)
       const uint64_t vd0 = smem_desc_sw128(sv, 16384, 1024);
       constexpr uint64_t kTileUnits = Cfg::kTileBytes >> 4;
-      auto issue_qk = [&](int s, int ks) {
-        const uint32_t d = tmem + 256 * s;
-        const uint64_t qd = qd0 + (uint64_t)s * kTileUnits;
+      const uint32_t tS = tmem + 256 * s, tO = tmem + 256 * s + 128;
+      auto issue_qk = [&](int ks) {
         const uint64_t kd = kd0 + (uint64_t)ks * kTileUnits;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_ss(d, qd + off, kd + off, kIdS, kk > 0);
+          mma_ss(tS, qd + off, kd + off, kIdS, kk > 0);
         }
       };
-      auto issue_pv = [&](int s, int vs, bool first_tile) {
-        const uint32_t p = tmem + 256 * s;
-        const uint32_t o = tmem + 256 * s + 128;
+      auto issue_pv = [&](int vs, bool first_tile) {
         const uint64_t vd = vd0 + (uint64_t)vs * kTileUnits;
 #pragma unroll
         for (int kk = 0; kk < kKvTile / 16; ++kk) {
           const uint64_t off = (uint64_t)((kk * 2048) >> 4);
-          mma_ts(o, p + kk * 8, vd + off, kIdO, (!first_tile || kk > 0) ? 1u : 0u);
+          mma_ts(tO, tS + kk * 8, vd + off, kIdO, (!first_tile || kk > 0) ? 1u : 0u);
         }
       };
       while (true) {
@@ -460,60 +487,69 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const PMsg m = msg[ms];
         mbar_arrive(&mempty[ms]);
         if (m.done || *reinterpret_cast<volatile int*>(misc)) break;
-        const int n = m.ntiles, ns = m.nslots;
+        const int n = m.ntiles;
         if (n == 0) continue;  // no MMA work: the softmax warps write the zeros
-        // O of each slot is free once the previous unit's epilogue read it.
+        if (s >= m.nslots) {
+          // this slot is idle in the unit (odd GQA group): give the shared
+          // buffers this thread's release once each is filled for the unit
+          pwait(qfull, q_cnt & 1, a.err, misc);
+          ++q_cnt;
+          mbar_arrive(qempty);
+          for (int j = 0; j < n; ++j) {
+            const int it = kv_it + j;
+            pwait(&kfull[it % KS], (it / KS) & 1, a.err, misc);
+            mbar_arrive(&kempty[it % KS]);
+            pwait(&vready[it % VS], (it / VS) & 1, a.err, misc);
+            mbar_arrive(&vempty[it % VS]);
+          }
+          kv_it += n;
+          continue;
+        }
+        // O of the slot is free once the previous unit's epilogue read it.
         // Only units with tiles take part in this handshake, so the softmax
         // side can never run two phases ahead of these waits.
-        for (int s = 0; s < ns; ++s) {
-          pwait(&ofree[s], (u_cnt[s] & 1) ^ 1, a.err, misc);
-          ++u_cnt[s];
-        }
+        pwait(&ofree[s], (u_cnt & 1) ^ 1, a.err, misc);
+        ++u_cnt;
         pwait(qfull, q_cnt & 1, a.err, misc);
         ++q_cnt;
+        const bool paired = m.nslots == 2;
         {
           const int ks0 = kv_it % KS;
           pwait(&kfull[ks0], (kv_it / KS) & 1, a.err, misc);
+          take_turn(paired);
           tc_fence_after();
-          for (int s = 0; s < ns; ++s) {
-            issue_qk(s, ks0);
-            tc_commit(&sfull[s]);
-          }
+          issue_qk(ks0);
+          pass_turn(paired);
+          tc_commit(&sfull[s]);
           tc_commit(&kempty[ks0]);
           if (n == 1) tc_commit(qempty);
         }
         for (int j = 0; j < n; ++j) {
           const int it = kv_it + j;
           const int vs = it % VS;
+          const int itn = it + 1, ksn = itn % KS;
           pwait(&vready[vs], (it / VS) & 1, a.err, misc);
+          if (j + 1 < n) pwait(&kfull[ksn], (itn / KS) & 1, a.err, misc);
+          pwait(&pfull[s], p_it & 1, a.err, misc);
+          ++p_it;
+          take_turn(paired);
           tc_fence_after();
-          for (int s = 0; s < ns; ++s) {
-            pwait(&pfull[s], s_it[s] & 1, a.err, misc);
-            ++s_it[s];
-            tc_fence_after();
-            issue_pv(s, vs, j == 0);
-            if (j == n - 1) tc_commit(&ofull[s]);
-            if (j + 1 < n) {
-              const int itn = it + 1, ksn = itn % KS;
-              if (s == 0) {
-                pwait(&kfull[ksn], (itn / KS) & 1, a.err, misc);
-                tc_fence_after();
-              }
-              issue_qk(s, ksn);
-              tc_commit(&sfull[s]);
-              if (s == ns - 1) {
-                tc_commit(&kempty[ksn]);
-                if (j + 1 == n - 1) tc_commit(qempty);
-              }
-            }
-          }
+          issue_pv(vs, j == 0);
+          if (j + 1 < n) issue_qk(ksn);
+          pass_turn(paired);
+          if (j == n - 1) tc_commit(&ofull[s]);
           tc_commit(&vempty[vs]);
+          if (j + 1 < n) {
+            tc_commit(&sfull[s]);
+            tc_commit(&kempty[ksn]);
+            if (j + 1 == n - 1) tc_commit(qempty);
+          }
         }
         kv_it += n;
       }
-      // everything issued has finished before the TMEM is released
-      tc_commit(drain);
-      mbar_wait(drain, 0, a.err);
+      // everything this thread issued has finished before the TMEM is released
+      tc_commit(&drain[s]);
+      mbar_wait(&drain[s], 0, a.err);
     }
     __syncwarp();
   } else if (warp == 2) {
@@ -548,8 +584,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (lane == 0) mbar_arrive(&vready[vs]);
       }
     }
-  } else if (warp == 3) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");  // no role
   } else {
     // ============================ softmax + epilogue ============================
     asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");

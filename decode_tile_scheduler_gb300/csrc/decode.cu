@@ -800,21 +800,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok0 = !(edge || tail) || (jg0 >= r.lo && jg0 <= r.hi);
       const bool ok1 = !(edge || tail) || (jg1 >= r.lo && jg1 <= r.hi);
       float corr[NG][2];
+      // the reference moves only when a score passes it by more than 8 (log2
+      // units): p <= 2^8 stays exact enough in 16-bit P, and the
+      // accumulators are rarely rescaled.  One warp vote finds out whether
+      // any head needs that; only then are the row maxima reduced.
+      float xs[NG][4];
+      bool over = false;
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          xs[ng][e] = ok0 ? sc[ng][e] * a.scale_log2 : -INFINITY;
+          xs[ng][2 + e] = ok1 ? sc[ng][2 + e] * a.scale_log2 : -INFINITY;
+          over |= fmaxf(xs[ng][e], xs[ng][2 + e]) > m_r[ng][e] + 8.f;
+        }
+      const bool any_over = __any_sync(0xffffffffu, over);
 #pragma unroll
       for (int ng = 0; ng < NG; ++ng) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float x0 = ok0 ? sc[ng][e] * a.scale_log2 : -INFINITY;
-          const float x1 = ok1 ? sc[ng][2 + e] * a.scale_log2 : -INFINITY;
-          float mx = fmaxf(x0, x1);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          // the reference moves only when the maximum passes it by more than
-          // 8 (log2 units): p <= 2^8 stays exact enough in 16-bit P, and the
-          // accumulators are rarely rescaled
+          const float x0 = xs[ng][e], x1 = xs[ng][2 + e];
           const float mold = m_r[ng][e];
-          const float mn = mx > mold + 8.f ? mx : mold;
+          float mn = mold;
+          if (any_over) {
+            float mx = fmaxf(x0, x1);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            mn = mx > mold + 8.f ? mx : mold;
+          }
           const float mu = mn == -INFINITY ? 0.f : mn;
           corr[ng][e] = mn == mold ? 1.f : (mold == -INFINITY ? 0.f : fast_exp2(mold - mu));
           m_r[ng][e] = mn;

@@ -505,11 +505,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
           kv_it += n;
           continue;
         }
-        // O of the slot is free once the previous unit's epilogue read it.
-        // Only units with tiles take part in this handshake, so the softmax
-        // side can never run two phases ahead of these waits.
-        pwait(&ofree[s], (u_cnt & 1) ^ 1, a.err, misc);
-        ++u_cnt;
         pwait(qfull, q_cnt & 1, a.err, misc);
         ++q_cnt;
         const bool paired = m.nslots == 2;
@@ -532,6 +527,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (j + 1 < n) pwait(&kfull[ksn], (itn / KS) & 1, a.err, misc);
           pwait(&pfull[s], p_it & 1, a.err, misc);
           ++p_it;
+          if (j == 0) {
+            // O of the slot is free once the previous unit's epilogue read
+            // it (the first QK above already overlapped that epilogue).
+            // Only units with tiles take part in this handshake, so the
+            // softmax side can never run two phases ahead of these waits.
+            pwait(&ofree[s], (u_cnt & 1) ^ 1, a.err, misc);
+            ++u_cnt;
+          }
           take_turn(paired);
           tc_fence_after();
           issue_pv(vs, j == 0);

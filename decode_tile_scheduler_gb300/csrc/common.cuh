@@ -187,8 +187,16 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 // is representable in fp16).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
   uint32_t out;
-  asm volatile("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(codes));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(codes));
   return out;
+}
+// Four E4M3 codes (one 32-bit word) to two fp16 pairs: lo from bytes 0-1,
+// hi from bytes 2-3 (the 16-bit halves are taken in place).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes));
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -723,6 +723,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int vexp[2] = {0, 0};  // FP8: exponent of the V scale reference per d-tile (0: none yet)
 
+    // FP8: the P V of each tile runs one tile late, beside the next tile's
+    // Q K^T and softmax (two independent instruction streams per warp)
+    struct PendingPV {
+      bool valid;
+      int s;
+      int64_t jw;
+      bool tail;
+      uint32_t pb[2][NG][2];
+      float fct[2][NG][2];
+    } prev;
+    prev.valid = false;
+    auto pv_fp8 = [&](const PendingPV& pp) {
+      bool resc = false;
+#pragma unroll
+      for (int t2 = 0; t2 < 2; ++t2)
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) resc |= (pp.fct[t2][ng][0] != 1.f) | (pp.fct[t2][ng][1] != 1.f);
+      if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+          const int t2 = i >> 2;
+#pragma unroll
+          for (int ng = 0; ng < NG; ++ng) {
+            acc[i][ng][0] *= pp.fct[t2][ng][0];
+            acc[i][ng][1] *= pp.fct[t2][ng][1];
+            acc[i][ng][2] *= pp.fct[t2][ng][0];
+            acc[i][ng][3] *= pp.fct[t2][ng][1];
+          }
+        }
+      }
+      // V codes of KV slots 2q, 2q+1, 2q+8, 2q+9: 8 bytes per d-tile at
+      // d = 64*tile + 8*g .. +7 (m-tile i covers d = 64*(i/4) + 8*g + (i%4)
+      // in fragment rows 0-7 and +4 in rows 8-15); rows past kv_len -> 0
+      const uint8_t* vt = smem + pp.s * Cfg::kStageBytes + Cfg::kTileBytes;
+      uint2 w[4][2];
+#pragma unroll
+      for (int sl = 0; sl < 4; ++sl) {
+        const int slot = 2 * q4 + (sl & 1) + (sl >> 1) * 8;
+        const int row = R0 + rho16(slot);
+        const bool ok = !pp.tail || (pp.jw + rho16(slot) < r.kv_len);
+#pragma unroll
+        for (int t2 = 0; t2 < 2; ++t2) {
+          uint2 x = *reinterpret_cast<const uint2*>(vt + sw128(row, 4 * t2 + (g >> 1)) + 8 * (g & 1));
+          if (!ok) { x.x = 0u; x.y = 0u; }
+          w[sl][t2] = x;
+        }
+      }
+#pragma unroll
+      for (int t2 = 0; t2 < 2; ++t2) {
+#pragma unroll
+        for (int ip = 0; ip < 4; ip += 2) {  // m-tiles 4*t2 + ip, +1
+          // bytes ip, ip+1 (fragment rows 0-7) and 4+ip, 5+ip (rows 8-15)
+          const uint32_t sel = (uint32_t)(ip | (4 + ip) << 4 | (ip + 1) << 8 | (5 + ip) << 12);
+          const uint32_t p_lo01 = __byte_perm(w[0][t2].x, w[1][t2].x, sel);  // slots 2q,2q+1
+          const uint32_t p_hi01 = __byte_perm(w[0][t2].y, w[1][t2].y, sel);
+          const uint32_t p_lo89 = __byte_perm(w[2][t2].x, w[3][t2].x, sel);  // slots 2q+8,2q+9
+          const uint32_t p_hi89 = __byte_perm(w[2][t2].y, w[3][t2].y, sel);
+          uint32_t va[2][4];  // [h2]: the low and the high halves of the four words
+          e4m3x4_to_f16x2x2(p_lo01, va[0][0], va[1][0]);
+          e4m3x4_to_f16x2x2(p_hi01, va[0][1], va[1][1]);
+          e4m3x4_to_f16x2x2(p_lo89, va[0][2], va[1][2]);
+          e4m3x4_to_f16x2x2(p_hi89, va[0][3], va[1][3]);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+            for (int ng = 0; ng < NG; ++ng)
+              mma_f16(acc[4 * t2 + ip + h2][ng], va[h2], pp.pb[t2][ng][0], pp.pb[t2][ng][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[pp.s]);
+    };
+
     const int ntile_here = r.ntiles == 0 ? 0 : (t_end - t_begin);
     for (int tt = 0; tt < ntile_here; ++tt, ++it) {
       const int t = t_begin + tt;
@@ -768,10 +841,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint32_t ka[4];
-            ka[0] = e4m3x2_to_f16x2((uint16_t)(va[j] & 0xffffu));
-            ka[1] = e4m3x2_to_f16x2((uint16_t)(vb[j] & 0xffffu));
-            ka[2] = e4m3x2_to_f16x2((uint16_t)(va[j] >> 16));
-            ka[3] = e4m3x2_to_f16x2((uint16_t)(vb[j] >> 16));
+            e4m3x4_to_f16x2x2(va[j], ka[0], ka[2]);
+            e4m3x4_to_f16x2x2(vb[j], ka[1], ka[3]);
 #pragma unroll
             for (int ng = 0; ng < NG; ++ng) {
               if (tile == 0) mma_f16(sc[ng], ka, qb[ng][tile * 4 + j][0], qb[ng][tile * 4 + j][1]);
@@ -908,34 +979,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P^T * scale / ref then stays below 2^9 in fp16, and moving the
         // reference rescales the accumulators by an exact power of two.
         float ratio[2], iv[2];
-        bool resc = false;
 #pragma unroll
         for (int t2 = 0; t2 < 2; ++t2) {
           const uint32_t bits = max(__float_as_uint(t2 ? v0.y : v0.x), __float_as_uint(t2 ? v1.y : v1.x));
           const int e = (int)(__reduce_max_sync(0xffffffffu, bits) >> 23);
           const int en = max(vexp[t2], e);
-          ratio[t2] = (en == vexp[t2] || vexp[t2] == 0) ? 1.f : ldexpf(1.f, vexp[t2] - en);
-          resc |= ratio[t2] != 1.f;
+          // 2^(old - new) and 2^(127 - new) built from their exponent bits
+          // (a jump past 2^-126 leaves a negligible old sum and gives 0)
+          ratio[t2] = (en == vexp[t2] || vexp[t2] == 0)
+                          ? 1.f
+                          : __int_as_float(max(127 + vexp[t2] - en, 0) << 23);
           vexp[t2] = en;
-          iv[t2] = en > 0 ? ldexpf(1.f, 127 - en) : 1.f;
+          iv[t2] = (en > 0 && en < 254) ? __int_as_float((254 - en) << 23) : 1.f;
         }
-#pragma unroll
-        for (int ng = 0; ng < NG; ++ng) resc |= (corr[ng][0] != 1.f) | (corr[ng][1] != 1.f);
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int i = 0; i < MT; ++i) {
-            const int t2 = i >> 2;
-#pragma unroll
-            for (int ng = 0; ng < NG; ++ng) {
-              acc[i][ng][0] *= corr[ng][0] * ratio[t2];
-              acc[i][ng][1] *= corr[ng][1] * ratio[t2];
-              acc[i][ng][2] *= corr[ng][0] * ratio[t2];
-              acc[i][ng][3] *= corr[ng][1] * ratio[t2];
-            }
-          }
-        }
-        // P^T per d-tile with the V scales folded in
+        // P^T of this tile with the V scales folded in, and the factors the
+        // accumulators take before its P V is added
         uint32_t pb[2][NG][2];
+        float fct[2][NG][2];
 #pragma unroll
         for (int t2 = 0; t2 < 2; ++t2) {
           const float fa = (t2 ? v0.y : v0.x) * iv[t2], fb = (t2 ? v1.y : v1.x) * iv[t2];
@@ -943,58 +1003,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ng = 0; ng < NG; ++ng) {
             pb[t2][ng][0] = movmatrix_t(pack_f16(sc[ng][0] * fa, sc[ng][1] * fa));
             pb[t2][ng][1] = movmatrix_t(pack_f16(sc[ng][2] * fb, sc[ng][3] * fb));
+            fct[t2][ng][0] = corr[ng][0] * ratio[t2];
+            fct[t2][ng][1] = corr[ng][1] * ratio[t2];
           }
         }
-        // V codes of KV slots 2q, 2q+1, 2q+8, 2q+9: 8 bytes per d-tile at
-        // d = 64*tile + 8*g .. +7 (m-tile i covers d = 64*(i/4) + 8*g + (i%4)
-        // in fragment rows 0-7 and +4 in rows 8-15)
-        const uint8_t* vt = stp + Cfg::kTileBytes;
-        uint2 w[4][2];
+        // P V of the previous tile: independent of this tile's work above, so
+        // the two interleave (the previous stage is released after it)
+        if (prev.valid) pv_fp8(prev);
+        prev.valid = true;
+        prev.s = s;
+        prev.jw = jw;
+        prev.tail = tail;
 #pragma unroll
-        for (int sl = 0; sl < 4; ++sl) {
-          const int slot = 2 * q4 + (sl & 1) + (sl >> 1) * 8;
-          const int row = R0 + rho16(slot);
-          const bool ok = !tail || (jw + rho16(slot) < r.kv_len);
+        for (int t2 = 0; t2 < 2; ++t2)
 #pragma unroll
-          for (int t2 = 0; t2 < 2; ++t2) {
-            uint2 x = *reinterpret_cast<const uint2*>(vt + sw128(row, 4 * t2 + (g >> 1)) + 8 * (g & 1));
-            if (!ok) { x.x = 0u; x.y = 0u; }
-            w[sl][t2] = x;
+          for (int ng = 0; ng < NG; ++ng) {
+            prev.pb[t2][ng][0] = pb[t2][ng][0];
+            prev.pb[t2][ng][1] = pb[t2][ng][1];
+            prev.fct[t2][ng][0] = fct[t2][ng][0];
+            prev.fct[t2][ng][1] = fct[t2][ng][1];
           }
-        }
-#pragma unroll
-        for (int t2 = 0; t2 < 2; ++t2) {
-#pragma unroll
-          for (int ip = 0; ip < 4; ip += 2) {  // m-tiles 4*t2 + ip, +1
-            // bytes ip, ip+1 (fragment rows 0-7) and 4+ip, 5+ip (rows 8-15)
-            const uint32_t sel = (uint32_t)(ip | (4 + ip) << 4 | (ip + 1) << 8 | (5 + ip) << 12);
-            const uint32_t p_lo01 = __byte_perm(w[0][t2].x, w[1][t2].x, sel);  // slots 2q,2q+1
-            const uint32_t p_hi01 = __byte_perm(w[0][t2].y, w[1][t2].y, sel);
-            const uint32_t p_lo89 = __byte_perm(w[2][t2].x, w[3][t2].x, sel);  // slots 2q+8,2q+9
-            const uint32_t p_hi89 = __byte_perm(w[2][t2].y, w[3][t2].y, sel);
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              uint32_t va[4];
-              va[0] = e4m3x2_to_f16x2((uint16_t)(h2 ? (p_lo01 >> 16) : (p_lo01 & 0xffffu)));
-              va[1] = e4m3x2_to_f16x2((uint16_t)(h2 ? (p_hi01 >> 16) : (p_hi01 & 0xffffu)));
-              va[2] = e4m3x2_to_f16x2((uint16_t)(h2 ? (p_lo89 >> 16) : (p_lo89 & 0xffffu)));
-              va[3] = e4m3x2_to_f16x2((uint16_t)(h2 ? (p_hi89 >> 16) : (p_hi89 & 0xffffu)));
-#pragma unroll
-              for (int ng = 0; ng < NG; ++ng)
-                mma_f16(acc[4 * t2 + ip + h2][ng], va, pb[t2][ng][0], pb[t2][ng][1]);
-            }
-          }
-        }
+        continue;  // the stage stays held until its P V ran
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if constexpr (FP8) {
+      if (prev.valid) pv_fp8(prev);  // the chunk's last tile
     }
 
     // ---------------- merge the eight warps' states ----------------
     if constexpr (FP8) {
 #pragma unroll
       for (int i = 0; i < MT; ++i) {
-        const float f = vexp[i >> 2] > 0 ? ldexpf(1.f, vexp[i >> 2] - 127) : 1.f;
+        const float f = vexp[i >> 2] > 0 ? __int_as_float(vexp[i >> 2] << 23) : 1.f;  // 2^(e-127)
 #pragma unroll
         for (int ng = 0; ng < NG; ++ng) {
           acc[i][ng][0] *= f; acc[i][ng][1] *= f; acc[i][ng][2] *= f; acc[i][ng][3] *= f;

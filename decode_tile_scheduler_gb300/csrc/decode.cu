@@ -557,13 +557,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int isv = lane & 1;
       const int sub = (lane >> 1) % Cfg::kNsub;
       const int rb = (lane >> 1) / Cfg::kNsub;
+      // The chunk's page ids, one per lane, with one coalesced load when the
+      // chunk spans at most 32 pages: each tile then finds its pages by a
+      // shuffle instead of a dependent global load.
+      int64_t pg0 = 0;
+      int npg = 0, mypage = 0;
+      if (a.block_table && r.ntiles > 0 && t_begin < t_end) {
+        const int64_t jlo = (int64_t)(r.tile0 + t_begin) * kKvTile;
+        const int64_t jhi = min((int64_t)(r.tile0 + t_end) * kKvTile, r.kv_len);
+        pg0 = jlo / a.block_size;
+        npg = (int)((jhi - 1) / a.block_size - pg0 + 1);
+        if (npg <= 32 && lane < npg)
+          mypage = a.block_table[(int64_t)r.b * a.max_blocks + pg0 + lane];
+      }
+      const bool pages_in_regs = npg > 0 && npg <= 32;
       for (int t = t_begin; r.ntiles > 0 && t < t_end; ++t, ++it) {
         const int s = it % S;
         const uint32_t par = ((it / S) & 1) ^ 1;
         const int64_t j0 = (int64_t)(r.tile0 + t) * kKvTile;
         const int64_t jb = j0 + (int64_t)rb * a.box_rows;
         const bool mine = lane < nbox && jb < r.kv_len;
-        const int64_t blk = mine ? page_of(a, r.b, jb) : 0;  // latency overlaps the slot wait
+        int64_t blk;
+        if (pages_in_regs) {
+          const int pidx = mine ? (int)(jb / a.block_size - pg0) : 0;
+          blk = __shfl_sync(0xffffffffu, mypage, pidx);
+        } else {
+          blk = mine ? page_of(a, r.b, jb) : 0;  // latency overlaps the slot wait
+        }
         const int64_t prow = mine ? pool_row(a, r.b, blk, jb) : 0;
         constexpr int NT = D / 64;
         // FP8: the scales of one head inside a page are contiguous rows of NT

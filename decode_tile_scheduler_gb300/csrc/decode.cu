@@ -179,21 +179,25 @@ __device__ __forceinline__ int find_batch(const T* prefix, int B, int64_t g) {
   return lo;
 }
 
-// Physical page holding logical KV row j of batch b (0 for a contiguous cache).
-__device__ __forceinline__ int64_t page_of(const DecodeArgs& a, int b, int64_t j) {
-  return a.block_table ? (int64_t)a.block_table[(int64_t)b * a.max_blocks + j / a.block_size] : 0;
+// Page index of logical KV row j (0 <= j < 2^31) of a paged cache: j / block_size
+// as one wide multiply and a shift (the multiplier and shift come with the
+// arguments).  The producer finds a page per tile, and a 64-bit division there
+// costs more issue time than the rest of its per-tile work.
+__device__ __forceinline__ int64_t page_index(const DecodeArgs& a, int64_t j) {
+  return (int64_t)(((uint64_t)(uint32_t)j * a.bs_magic) >> a.bs_shift);
 }
 // Pool row and FP8 scale row of logical KV row j of batch b, KV head hk, in
-// page blk.  FP8 scales are stored head-major inside each page, [pages, KV_N,
-// page rows, D/64] (the paged per-token, per-head scale shape (blockNum, N,
-// blockSize) of the FIA dequantisation parameters, with the 64-element tiles
-// last).
-__device__ __forceinline__ int64_t pool_row(const DecodeArgs& a, int b, int64_t blk, int64_t j) {
-  return a.block_table ? blk * a.block_size + j % a.block_size : (int64_t)b * a.S_kv + j;
+// page blk, with jp = j - block_size * page_index(j) (j's row in its page).
+// FP8 scales are stored head-major inside each page, [pages, KV_N, page rows,
+// D/64] (the paged per-token, per-head scale shape (blockNum, N, blockSize) of
+// the FIA dequantisation parameters, with the 64-element tiles last).
+__device__ __forceinline__ int64_t pool_row(const DecodeArgs& a, int b, int64_t blk, int64_t j,
+                                            int64_t jp) {
+  return a.block_table ? blk * a.block_size + jp : (int64_t)b * a.S_kv + j;
 }
 __device__ __forceinline__ int64_t scale_row_in(const DecodeArgs& a, int b, int hk, int64_t blk,
-                                                int64_t j) {
-  return a.block_table ? (blk * a.KVN + hk) * a.block_size + j % a.block_size
+                                                int64_t j, int64_t jp) {
+  return a.block_table ? (blk * a.KVN + hk) * a.block_size + jp
                        : ((int64_t)b * a.KVN + hk) * a.S_kv + j;
 }
 
@@ -565,8 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (a.block_table && r.ntiles > 0 && t_begin < t_end) {
         const int64_t jlo = (int64_t)(r.tile0 + t_begin) * kKvTile;
         const int64_t jhi = min((int64_t)(r.tile0 + t_end) * kKvTile, r.kv_len);
-        pg0 = jlo / a.block_size;
-        npg = (int)((jhi - 1) / a.block_size - pg0 + 1);
+        pg0 = page_index(a, jlo);
+        npg = (int)(page_index(a, jhi - 1) - pg0 + 1);
         if (npg <= 32 && lane < npg)
           mypage = a.block_table[(int64_t)r.b * a.max_blocks + pg0 + lane];
       }
@@ -577,14 +581,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t j0 = (int64_t)(r.tile0 + t) * kKvTile;
         const int64_t jb = j0 + (int64_t)rb * a.box_rows;
         const bool mine = lane < nbox && jb < r.kv_len;
-        int64_t blk;
-        if (pages_in_regs) {
-          const int pidx = mine ? (int)(jb / a.block_size - pg0) : 0;
-          blk = __shfl_sync(0xffffffffu, mypage, pidx);
+        int64_t blk, jp = 0;
+        if (a.block_table) {
+          const int64_t pj = mine ? page_index(a, jb) : 0;
+          jp = jb - pj * a.block_size;
+          if (pages_in_regs) {
+            blk = __shfl_sync(0xffffffffu, mypage, (int)(pj - pg0));
+          } else {
+            blk = mine ? (int64_t)a.block_table[(int64_t)r.b * a.max_blocks + pj] : 0;
+          }
         } else {
-          blk = mine ? page_of(a, r.b, jb) : 0;  // latency overlaps the slot wait
+          blk = 0;
         }
-        const int64_t prow = mine ? pool_row(a, r.b, blk, jb) : 0;
+        const int64_t prow = mine ? pool_row(a, r.b, blk, jb, jp) : 0;
         constexpr int NT = D / 64;
         // FP8: the scales of one head inside a page are contiguous rows of NT
         // floats, so each (K or V, page piece) is one bulk copy next to its
@@ -594,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t srow = 0;
         int srows = a.box_rows;
         if constexpr (FP8) {
-          if (mine) srow = scale_row_in(a, r.b, r.hk, blk, jb);
+          if (mine) srow = scale_row_in(a, r.b, r.hk, blk, jb, jp);
           if (!a.block_table) srows = (int)min((int64_t)a.box_rows, (int64_t)a.S_kv - jb);
         }
         int nvalid = 0, scale_rows = 0;

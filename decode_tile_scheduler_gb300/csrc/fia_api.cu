@@ -28,6 +28,16 @@ int gcd_i(int a, int b) {
   return a;
 }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Multiplier and shift with j / d == (j * magic) >> shift for 0 <= j < 2^31,
+// 1 <= d <= 2^20: l = ceil(log2 d), magic = floor(2^(31+l) / d) + 1 (the
+// round-up method; magic * d - 2^(31+l) <= d <= 2^l keeps it exact, and
+// magic < 2^32).
+void fast_divisor(int d, uint32_t* magic, int* shift) {
+  int l = 0;
+  while ((1 << l) < d) ++l;
+  *magic = (uint32_t)(((uint64_t)1 << (31 + l)) / (uint64_t)d + 1);
+  *shift = 31 + l;
+}
 
 // ---------------------------------------------------------------------------
 // device properties and the tensor-map encoder (driver entry point)
@@ -206,6 +216,7 @@ DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
   a.max_blocks = p->max_blocks_per_seq;
   a.block_size = p->block_table ? p->block_size : 1;
   a.box_rows = p->block_table ? gcd_i(p->block_size, kKvTile) : kKvTile;
+  fast_divisor(a.block_size, &a.bs_magic, &a.bs_shift);
   a.k_scale = p->k_scale;
   a.v_scale = p->v_scale;
   a.scale_log2 = p->scale * 1.4426950408889634f;

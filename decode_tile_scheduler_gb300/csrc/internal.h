@@ -30,6 +30,8 @@ struct DecodeArgs {
   int S_kv;
   const int32_t* block_table;  // null: contiguous
   int max_blocks, block_size, box_rows;
+  uint32_t bs_magic;           // j / block_size == (j * bs_magic) >> bs_shift, 0 <= j < 2^31
+  int bs_shift;
   const float* k_scale;
   const float* v_scale;
   float scale_log2;      // scale * log2(e)

@@ -51,6 +51,11 @@ CASES = {
                            pre_tokens=1000, next_tokens=0),
     "fp8_contiguous": dict(B=2, QN=8, KVN=2, D=128, kv_lens=[100, 300], paged=False,
                            kv_dtype=fi.KV_FP8_E4M3),
+    # pages of 96 and 272 rows: tiles straddle pages, and the page index of a
+    # row is not a shift
+    "fp8_bs96": dict(B=3, QN=16, KVN=2, D=128, kv_lens=[1500, 95, 97], block_size=96,
+                     kv_dtype=fi.KV_FP8_E4M3),
+    "gqa4_bs272": dict(B=2, QN=8, KVN=2, D=64, kv_lens=[2000, 273], block_size=272),
 }
 
 

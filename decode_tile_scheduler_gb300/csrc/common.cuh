@@ -135,8 +135,28 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32).
+// Bounded barrier wait; after the first time-out in the CTA every later wait
+// returns at once, so a broken pipeline ends the kernel instead of hanging it.
+__device__ __forceinline__ void wait_or_abort(uint64_t* bar, uint32_t parity, int* err,
+                                              int* misc) {
+  if (*reinterpret_cast<volatile int*>(misc)) return;
+  if (!mbar_wait(bar, parity, err)) *reinterpret_cast<volatile int*>(misc) = 1;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Named barrier that also ORs a predicate over its threads: every thread gets
+// the same answer, so a decision taken with it is uniform.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool c) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)c), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ---------------------------------------------------------------------------

@@ -201,14 +201,6 @@ __device__ __forceinline__ int64_t scale_row_in(const DecodeArgs& a, int b, int 
                        : ((int64_t)b * a.KVN + hk) * a.S_kv + j;
 }
 
-// Bounded barrier wait; after the first time-out in the CTA every later wait
-// returns at once, so a broken pipeline ends the kernel instead of hanging it.
-__device__ __forceinline__ void wait_or_abort(uint64_t* bar, uint32_t parity, int* err,
-                                              int* misc) {
-  if (*reinterpret_cast<volatile int*>(misc)) return;
-  if (!mbar_wait(bar, parity, err)) *reinterpret_cast<volatile int*>(misc) = 1;
-}
-
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -693,7 +685,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   while (true) {
     const int qs = ucount & 1;
     wait_or_abort(&qfull[qs], (ucount >> 1) & 1, a.err, misc);
-    if (msg[qs].done || *reinterpret_cast<volatile int*>(misc)) break;
+    // every consumer warp leaves together (the merge meets at a named
+    // barrier), so the stop decision is one barrier OR over the consumers
+    if (named_bar_or(1, nthr, msg[qs].done || *reinterpret_cast<volatile int*>(misc))) break;
     const UnitInfo r = msg[qs].r;
     const int64_t u = msg[qs].u;
     const int64_t slot0 = a.sched[kSchedHeader + r.b] + (u - (int64_t)r.b * a.KVN * a.HG);

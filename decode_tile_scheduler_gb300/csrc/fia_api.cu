@@ -337,11 +337,11 @@ fia_status q_map(const fia_params* p, CUtensorMap* tq) {
 // ---------------------------------------------------------------------------
 // shared-KV sparse attention ("kv_quant_sparse_attn_sharedkv" constraints)
 // ---------------------------------------------------------------------------
-constexpr int kSparseChunk = 64;
-constexpr int kSparseMaxCtas = 503;  // (1024 - 16) / 2 - 1 begins fit the metadata
+constexpr int kSparseHeads = 8;     // query heads per work item
+constexpr int kSparseMaxCtas = 1007;  // 1024 - 16 - 1 begins fit the metadata
 
 struct SparsePlan {
-  int n, mode, max_chunks;
+  int n, mode;
   int64_t rows, total;
 };
 
@@ -362,6 +362,7 @@ fia_status sparse_validate(const sparse_attn_params* p) {
   if (p->ori_block_size <= 0 || p->ori_block_size % 16 || p->ori_block_size > 1024)
     return FIA_ERR_BAD_SHAPE;
   if (p->ori_max_blocks <= 0 || p->ori_num_blocks <= 0) return FIA_ERR_BAD_SHAPE;
+  if ((int64_t)p->ori_max_blocks * p->ori_block_size > INT32_MAX) return FIA_ERR_BAD_SHAPE;
   if (p->ori_win_left < 0 || p->ori_win_right < 0 ||
       (int64_t)p->ori_win_left + p->ori_win_right + 1 > 65536)
     return FIA_ERR_BAD_SHAPE;
@@ -373,6 +374,7 @@ fia_status sparse_validate(const sparse_attn_params* p) {
     if (p->cmp_block_size <= 0 || p->cmp_block_size % 16 || p->cmp_block_size > 1024)
       return FIA_ERR_BAD_SHAPE;
     if (p->cmp_max_blocks <= 0 || p->cmp_num_blocks <= 0) return FIA_ERR_BAD_SHAPE;
+    if ((int64_t)p->cmp_max_blocks * p->cmp_block_size > INT32_MAX) return FIA_ERR_BAD_SHAPE;
     if (p->cmp_ratio < 1) return FIA_ERR_BAD_SHAPE;
     if (p->cmp_sparse_indices && (p->topk < 1 || p->topk > 2048)) return FIA_ERR_BAD_SHAPE;
   } else if (p->cmp_sparse_indices) {
@@ -392,13 +394,15 @@ fia_status sparse_plan(const sparse_attn_params* p, SparsePlan* pl) {
   pl->mode = !p->cmp_kv ? 0 : (p->cmp_sparse_indices ? 1 : 2);
   pl->rows = p->layout == FIA_LAYOUT_TND ? (int64_t)p->total_q
                                          : (int64_t)p->batch * p->max_seqlen_q;
+  // the metadata holds the item count and the total item weight as int32
   const int64_t W = (int64_t)p->ori_win_left + p->ori_win_right + 1;
   int64_t kc = 0;
   if (pl->mode == 1) kc = p->topk;
   else if (pl->mode == 2) kc = (int64_t)p->cmp_max_blocks * p->cmp_block_size;
-  pl->max_chunks = (int)(ceil_div(W, kSparseChunk) + ceil_div(kc, kSparseChunk));
-  pl->total = align_up(kAlign + 4 * pl->rows * pl->max_chunks * (int64_t)p->num_q_heads *
-                                    (p->head_dim + 2));
+  const int64_t items = pl->rows * ((p->num_q_heads + kSparseHeads - 1) / kSparseHeads);
+  if (items * (ceil_div(W, 64) + ceil_div(kc, 64)) > INT32_MAX) return FIA_ERR_BAD_SHAPE;
+  // workspace: the status word only (a row's chunks all run in one CTA)
+  pl->total = kAlign;
   return FIA_OK;
 }
 
@@ -417,6 +421,8 @@ SparseArgs sparse_args(const sparse_attn_params* p, const SparsePlan& pl, void* 
   a.ori_block_table = p->ori_block_table;
   a.ori_max_blocks = p->ori_max_blocks;
   a.ori_block_size = p->ori_block_size;
+  a.ori_num_blocks = p->ori_num_blocks;
+  a.cmp_num_blocks = p->cmp_kv ? p->cmp_num_blocks : 0;
   a.cmp_kv = static_cast<const uint16_t*>(p->cmp_kv);
   a.cmp_block_table = p->cmp_block_table;
   a.cmp_max_blocks = p->cmp_max_blocks;
@@ -432,14 +438,11 @@ SparseArgs sparse_args(const sparse_attn_params* p, const SparsePlan& pl, void* 
   a.win_right = p->ori_win_right;
   a.mode = pl.mode;
   a.rows = pl.rows;
-  a.chunk = kSparseChunk;
-  a.max_chunks = pl.max_chunks;
+  a.hgs = (p->num_q_heads + kSparseHeads - 1) / kSparseHeads;
+  fast_divisor(p->ori_block_size, &a.ori_magic, &a.ori_shift);
+  fast_divisor(a.cmp_block_size, &a.cmp_magic, &a.cmp_shift);
   a.num_ctas = pl.n;
-  if (ws) {
-    char* w = static_cast<char*>(ws);
-    a.err = reinterpret_cast<int*>(w);
-    a.partials = reinterpret_cast<float*>(w + kAlign);
-  }
+  if (ws) a.err = reinterpret_cast<int*>(ws);
   return a;
 }
 

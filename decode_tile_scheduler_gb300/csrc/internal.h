@@ -89,9 +89,11 @@ struct SparseArgs {
   const uint16_t* ori_kv;
   const int32_t* ori_block_table;
   int ori_max_blocks, ori_block_size;
+  int64_t ori_num_blocks;
   const uint16_t* cmp_kv;
   const int32_t* cmp_block_table;
   int cmp_max_blocks, cmp_block_size;
+  int64_t cmp_num_blocks;
   const int32_t* cmp_sparse_indices;
   int K2;
   const int32_t* cu_seqlens_q;
@@ -101,9 +103,9 @@ struct SparseArgs {
   int cmp_ratio, win_left, win_right;
   int mode;              // 0 SWA, 1 CSA, 2 HCA
   int64_t rows;
-  int chunk;
-  int max_chunks;        // partial slots per row
-  float* partials;       // [rows][max_chunks][N1][D + 2]
+  int64_t hgs;           // groups of 8 query heads per row (work items per row)
+  uint32_t ori_magic, cmp_magic;  // j / block_size == (j * magic) >> shift, 0 <= j < 2^31
+  int ori_shift, cmp_shift;
   int* err;
   int num_ctas;
 };

@@ -3,15 +3,18 @@
 // SWA, CSA and HCA modes and the metadata pre-step), bf16 KV.
 //
 // K~ of a query row is the band window of the original KV followed by the
-// compressed rows (the listed top-k indices for CSA, every causally visible
-// compressed row for HCA).  It is cut into fixed chunks of kChunk logical
-// positions; the metadata kernel balances the (query row, chunk) items over
-// the CTAs; the attention kernel gathers each chunk's rows with one bulk copy
-// per row (the index -> block_table -> pool row indirection happens in the
-// kernel), computes the chunk's (m, l, acc) for all heads with mma.sync, and
-// the combine kernel folds the chunks of a row in chunk order and applies the
-// sink.  Chunk boundaries do not depend on the rest of the batch, so results
-// are batch invariant as well as deterministic.
+// compressed rows (the listed top-k indices for CSA, scanned up to the first
+// -1 and kept when causally visible; every visible compressed row for HCA).
+// A work item is (query row, group of 8 query heads); the metadata kernel
+// hands each CTA a contiguous run of items of balanced weight.  In a CTA one
+// producer warp gathers K~ in 64-row chunks (index -> block table -> pool
+// row, one bulk copy per row) into a ring of shared-memory stages, and eight
+// consumer warps run the whole item: S^T = K~ Q^T and O^T += V~^T P^T with
+// mma.sync (the K~ rows are the M dimension, the 8 heads N), the online
+// softmax across chunks in the exp2 domain, and the sink and normalisation at
+// the end.  A row's chunks all run in one CTA, in order, so nothing is
+// combined through global memory and the result does not depend on the rest
+// of the batch.
 #include <atomic>
 
 #include "common.cuh"
@@ -21,16 +24,19 @@ namespace fia {
 
 namespace {
 
-constexpr int kChunk = 64;          // K~ rows per item
-constexpr int kSThreads = 256;      // 8 warps: 4 head groups of 16 x 2 halves of D
-constexpr int kHeadsPerCta = 64;
-constexpr int kMdCtaBase = 16;      // metadata: CTA begins from this entry
+constexpr int kChunk = 64;                // K~ rows per stage
+constexpr int kHeads = 8;                 // query heads per work item (mma N)
+constexpr int kSCons = 8;                 // consumer warps
+constexpr int kSThreads = 32 * (1 + kSCons);
+constexpr int kMdBase = 16;               // metadata: CTA begins from this entry
+constexpr int32_t kMdMagic = 0x46534D32;
+constexpr int kMaxK2 = 2048;              // longest index list (validated on the host)
 
 struct SparseRow {
   int b;
   int64_t i, q_len, S2, p;
-  int ncmp_vis;  // visible compressed rows (before the top-k cap)
-  int nchunks;
+  int64_t vis;  // visible compressed rows, floor((p + 1) / cmp_ratio)
+  int cost;     // balancing weight: window chunks + capped compressed chunks
 };
 
 __device__ __forceinline__ SparseRow sparse_row(const SparseArgs& a, int64_t u) {
@@ -51,45 +57,55 @@ __device__ __forceinline__ SparseRow sparse_row(const SparseArgs& a, int64_t u) 
   }
   r.S2 = a.seqused_kv[r.b];
   r.p = r.S2 - r.q_len + r.i;
-  const int64_t vis = (r.p + 1) >= 0 ? (r.p + 1) / a.cmp_ratio : 0;
-  r.ncmp_vis = (int)vis;
+  r.vis = (r.p + 1) >= 0 ? (r.p + 1) / a.cmp_ratio : 0;
   int64_t kc = 0;
-  if (a.mode == 1) kc = min(vis, (int64_t)a.K2);
-  else if (a.mode == 2) kc = vis;
+  if (a.mode == 1) kc = min(r.vis, (int64_t)a.K2);
+  else if (a.mode == 2) kc = r.vis;
   const int64_t W = (int64_t)a.win_left + a.win_right + 1;
-  r.nchunks = (int)((W + kChunk - 1) / kChunk + (kc + kChunk - 1) / kChunk);
+  r.cost = (int)((W + kChunk - 1) / kChunk + (kc + kChunk - 1) / kChunk);
   return r;
+}
+
+// j / d for 0 <= j < 2^31 with the host's multiplier and shift
+__device__ __forceinline__ int64_t fast_div(int64_t j, uint32_t magic, int shift) {
+  return (int64_t)(((uint64_t)(uint32_t)j * magic) >> shift);
 }
 
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// metadata: per-row chunk counts -> balanced (row, chunk) begins of every CTA
+// metadata: item weights -> the first item of every CTA
 // ---------------------------------------------------------------------------
+// Items k = u * G + g (query row u, head group g, G groups per row) weigh
+// cost(u); with P_k the weight before item k and T the total, CTA c begins at
+// #{k : P_k < floor(c T / n)}.  Row u's items start at A = G * pre(u) and
+// item g of the row at A + g * cost(u), so a threshold t in (A, A + G cost]
+// gives the begin u * G + ceil((t - A) / cost).
 __global__ void __launch_bounds__(1024) sparse_metadata_kernel(const SparseArgs a, int32_t* md) {
   __shared__ int64_t warp_sums[32];
   __shared__ int64_t carry;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nthr = blockDim.x;
-  const int n = a.num_ctas;
+  const int64_t n = a.num_ctas, G = a.hgs;
   for (int k = tid; k < 1024; k += nthr) md[k] = 0;
-  // pass 1: total number of chunks
+  // pass 1: total weight
   if (tid == 0) carry = 0;
   __syncthreads();
   int64_t part = 0;
-  for (int64_t u = tid; u < a.rows; u += nthr) part += sparse_row(a, u).nchunks;
+  for (int64_t u = tid; u < a.rows; u += nthr) part += sparse_row(a, u).cost;
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
   if (lane == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&carry), (unsigned long long)part);
   __syncthreads();
-  const int64_t total = carry;
+  const int64_t T = carry * G;
   __syncthreads();
-  // pass 2: running prefix; every row writes the begins that fall inside it
+  // pass 2: running row prefix; each row writes the begins whose threshold
+  // falls on its items
   if (tid == 0) carry = 0;
   __syncthreads();
   for (int64_t base = 0; base < a.rows; base += nthr) {
     const int64_t u = base + tid;
-    const int64_t nch = u < a.rows ? sparse_row(a, u).nchunks : 0;
-    int64_t x = nch;
+    const int64_t cost = u < a.rows ? sparse_row(a, u).cost : 0;
+    int64_t x = cost;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
@@ -107,27 +123,26 @@ __global__ void __launch_bounds__(1024) sparse_metadata_kernel(const SparseArgs 
       warp_sums[lane] = w;
     }
     __syncthreads();
-    const int64_t pre = carry + (wid ? warp_sums[wid - 1] : 0) + x - nch;
-    if (u < a.rows && nch > 0 && total > 0) {
-      // CTAs c with floor(c * total / n) in [pre, pre + nch)
-      int64_t c = (pre * n + total - 1) / total;
-      for (; c < n; ++c) {
-        const int64_t g = c * total / n;
-        if (g >= pre + nch) break;
-        md[kMdCtaBase + 2 * c] = (int32_t)u;
-        md[kMdCtaBase + 2 * c + 1] = (int32_t)(g - pre);
+    const int64_t pre = carry + (wid ? warp_sums[wid - 1] : 0) + x - cost;
+    if (u < a.rows && T > 0) {
+      const int64_t A = pre * G, E = A + G * cost;
+      // thresholds floor(c T / n) in (A, E]: c from ceil((A + 1) n / T)
+      for (int64_t c = ((A + 1) * n + T - 1) / T; c <= n; ++c) {
+        const int64_t t = c * T / n;
+        if (t > E) break;
+        md[kMdBase + c] = (int32_t)(u * G + (t - A + cost - 1) / cost);
       }
     }
     __syncthreads();
-    if (tid == nthr - 1) carry = pre + nch;
+    if (tid == nthr - 1) carry = pre + cost;
     __syncthreads();
   }
   if (tid == 0) {
-    md[0] = 0x46534D31;
-    md[1] = n;
+    md[0] = kMdMagic;
+    md[1] = (int32_t)n;
     md[2] = (int32_t)a.rows;
     md[3] = kChunk;
-    md[4] = (int32_t)total;
+    md[4] = (int32_t)T;
     md[5] = a.B;
     md[6] = a.N1;
     md[7] = a.K2;
@@ -135,320 +150,420 @@ __global__ void __launch_bounds__(1024) sparse_metadata_kernel(const SparseArgs 
     md[9] = a.win_left;
     md[10] = a.win_right;
     md[11] = a.mode;
-    md[kMdCtaBase + 2 * n] = (int32_t)a.rows;
-    md[kMdCtaBase + 2 * n + 1] = 0;
-    if (total == 0)
-      for (int c = 0; c < n; ++c) {
-        md[kMdCtaBase + 2 * c] = (int32_t)a.rows;
-        md[kMdCtaBase + 2 * c + 1] = 0;
-      }
+    md[12] = kHeads;
+    md[13] = (int32_t)(a.rows * G);
   }
 }
 
 // ---------------------------------------------------------------------------
-// attention over one (row, chunk) item at a time
+// attention: one (query row, 8 heads) item at a time, K~ streamed in chunks
 // ---------------------------------------------------------------------------
 template <int D>
 struct SparseCfg {
-  static constexpr int kRowBytes = D * 2 + 16;  // padded: ldmatrix rows hit distinct banks
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kHeadsPerCta * kRowBytes;
-  static constexpr int kOffS = kOffK + kChunk * kRowBytes;          // [8 warps][16][64] fp32
-  static constexpr int kOffRows = kOffS + 8 * 16 * kChunk * 4;     // [64] int64 pool offsets
-  static constexpr int kOffBar = kOffRows + kChunk * 8;
-  static constexpr int kOffMisc = kOffBar + 16;
-  static constexpr int kSmem = kOffMisc + 64;
+  static constexpr int kRowBytes = D * 2 + 16;  // padded rows: ldmatrix without bank conflicts
+  static constexpr int kStageBytes = kChunk * kRowBytes;
+  static constexpr int kStages = D == 512 ? 3 : (D == 256 ? 6 : 8);
+  static constexpr int kPtStride = kChunk + 8;  // bf16 per head row of P^T (padded)
+  static constexpr int kOffQ = kStages * kStageBytes;
+  static constexpr int kOffSx = kOffQ + kHeads * kRowBytes;        // [8 warps][4][32] fp32
+  static constexpr int kOffMx = kOffSx + kSCons * 4 * 32 * 4;      // [4 row groups][8 heads]
+  static constexpr int kOffL = kOffMx + 4 * kHeads * 4;            // [4 row groups][8 heads]
+  static constexpr int kOffPt = kOffL + 4 * kHeads * 4;            // [8 heads][kPtStride] bf16
+  static constexpr int kOffList = kOffPt + kHeads * kPtStride * 2; // [K2] int32 CSA rows
+  static constexpr int kOffHdr = kOffList + kMaxK2 * 4;            // per stage: valid rows, last
+  static constexpr int kOffBar = kOffHdr + kStages * 16;
+  static constexpr int kOffMisc = kOffBar + 8 * (2 * kStages + 2);
+  static constexpr int kSmem = kOffMisc + 16;
+  static_assert(kStageBytes % 16 == 0 && kOffQ % 16 == 0, "bulk-copy alignment");
+  static_assert(kOffBar % 8 == 0, "mbarrier alignment");
   static_assert(kSmem <= 232448, "shared memory");
+};
+
+struct StageHdr {
+  uint64_t valid;  // bit r: row r holds a K~ row
+  int32_t last;    // the item's last chunk
+  int32_t pad;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kSThreads, 1)
     sparse_attn_kernel(const SparseArgs a, const int32_t* __restrict__ md) {
   using Cfg = SparseCfg<D>;
-  constexpr int DH = D / 2;      // d range of one warp
-  constexpr int KS = DH / 16;    // k-steps of Q K^T over a half
-  constexpr int NT = DH / 8;     // n-tiles of P V over a half
+  constexpr int S = Cfg::kStages;
   extern __shared__ __align__(128) uint8_t sm[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Cfg::kOffBar);
-  int64_t* rowoff = reinterpret_cast<int64_t*>(sm + Cfg::kOffRows);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Cfg::kOffBar);
+  uint64_t* empty = full + S;
+  uint64_t* qfull = empty + S;
+  uint64_t* qempty = qfull + 1;
+  StageHdr* hdr = reinterpret_cast<StageHdr*>(sm + Cfg::kOffHdr);
   int* misc = reinterpret_cast<int*>(sm + Cfg::kOffMisc);
-  float* sx = reinterpret_cast<float*>(sm + Cfg::kOffS);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q4 = lane & 3;
-  const int hgrp = warp & 3, half = warp >> 2;  // 16 heads x D/2
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
-  const int head0 = blockIdx.y * kHeadsPerCta;
-  const int nheads = min(kHeadsPerCta, a.N1 - head0);
-  if (md[0] != 0x46534D31 || md[1] != a.num_ctas || md[2] != (int32_t)a.rows ||
-      md[5] != a.B || md[6] != a.N1 || md[7] != a.K2) {
+  if (md[0] != kMdMagic || md[1] != a.num_ctas || md[2] != (int32_t)a.rows || md[5] != a.B ||
+      md[6] != a.N1 || md[7] != a.K2 || md[12] != kHeads || md[13] != (int32_t)(a.rows * a.hgs)) {
     if (tid == 0) atomicExch(a.err, 2);
     return;
   }
-  int64_t u = md[kMdCtaBase + 2 * c];
-  int ch = md[kMdCtaBase + 2 * c + 1];
-  const int64_t u_end = md[kMdCtaBase + 2 * c + 2];
-  const int ch_end = md[kMdCtaBase + 2 * c + 3];
+  const int64_t k_begin = md[kMdBase + c], k_end = md[kMdBase + c + 1];
   if (tid == 0) {
-    mbar_init(bar, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kSCons);
+    }
+    mbar_init(qfull, 1);
+    mbar_init(qempty, kSCons);
     misc[0] = 0;
     fence_barrier_init();
   }
   __syncthreads();
-  const uint32_t sq = smem_u32(sm + Cfg::kOffQ), sk = smem_u32(sm + Cfg::kOffK);
-  const int64_t W = (int64_t)a.win_left + a.win_right + 1;
-  int phase = 0;
-  while (u < u_end || (u == u_end && ch < ch_end)) {
-    const SparseRow r = sparse_row(a, u);
-    if (ch >= r.nchunks) {  // next row
-      ++u;
-      ch = 0;
-      continue;
-    }
-    // ---- first -1 of the index list up to this chunk (CSA scan rule) ----
-    int first_neg = 0x7fffffff;
-    if (a.mode == 1) {
-      const int lim = (int)min((int64_t)a.K2, (int64_t)(ch + 1) * kChunk - W);
-      const int32_t* ix = a.cmp_sparse_indices + u * (int64_t)a.K2;
-      for (int t = tid; t < lim; t += kSThreads)
-        if (ix[t] < 0) first_neg = min(first_neg, t);
+  if (k_begin >= k_end) return;
+
+  if (warp == 0) {
+    // ======================= producer =======================
+    int32_t* list = reinterpret_cast<int32_t*>(sm + Cfg::kOffList);
+    int it = 0, qn = 0;
+    bool aborted = false;
+    // Gathers chunk positions [base, base + 64) of one part of the row's K~:
+    // the window (rows lo + pos of the original cache) or the compressed
+    // rows (list entries for CSA, rows 0.. for HCA); cnt = the part's length.
+    auto issue_chunk = [&](const SparseRow& r, bool cmp, int64_t lo, int base, int cnt,
+                           bool last) {
+      const int s = it % S;
+      wait_or_abort(&empty[s], ((it / S) & 1) ^ 1, a.err, misc);
+      if (*reinterpret_cast<volatile int*>(misc)) {
+        aborted = true;
+        return;
+      }
+      uint8_t* st = sm + s * Cfg::kStageBytes;
+      int64_t off[2];
+      bool ok[2];
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) first_neg = min(first_neg, __shfl_xor_sync(0xffffffffu, first_neg, o));
-      if (lane == 0) misc[1 + warp] = first_neg;
-      __syncthreads();
-      first_neg = misc[1];
-      for (int w2 = 1; w2 < 8; ++w2) first_neg = min(first_neg, misc[1 + w2]);
-    }
-    // ---- gather: pool offsets of the chunk's 64 K~ rows (-1: no row) ----
-    if (tid < kChunk) {
-      const int64_t pos = (int64_t)ch * kChunk + tid;
-      int64_t off = -1;
-      if (pos < W) {
-        const int64_t j = r.p - a.win_left + pos;
-        if (j >= 0 && j < r.S2) {
-          const int64_t blk = a.ori_block_table[(int64_t)r.b * a.ori_max_blocks + j / a.ori_block_size];
-          off = (blk * a.ori_block_size + j % a.ori_block_size) * (int64_t)D;
-        }
-      } else if (a.mode != 0) {
-        const int64_t t = pos - W;
-        int64_t idx = -1;
-        if (a.mode == 1) {
-          if (t < a.K2 && t < first_neg) idx = a.cmp_sparse_indices[u * (int64_t)a.K2 + t];
-        } else {
-          idx = t;
-        }
-        if (idx >= 0 && idx < r.ncmp_vis) {
-          const int64_t blk = a.cmp_block_table[(int64_t)r.b * a.cmp_max_blocks + idx / a.cmp_block_size];
-          // compressed rows are flagged by bit 62 so the copy picks the right pool
-          off = ((blk * a.cmp_block_size + idx % a.cmp_block_size) * (int64_t)D) | (1ll << 62);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int pos = base + lane + 32 * h2;
+        ok[h2] = pos < cnt;
+        off[h2] = 0;
+        if (ok[h2]) {
+          // a row whose page lies outside the block table or the pool (a
+          // length or table entry that breaks the caller's contract) is
+          // left out instead of read
+          if (!cmp) {
+            const int64_t j = lo + pos;
+            const int64_t pg = fast_div(j, a.ori_magic, a.ori_shift);
+            const int64_t blk = pg < a.ori_max_blocks
+                                    ? a.ori_block_table[(int64_t)r.b * a.ori_max_blocks + pg] : -1;
+            ok[h2] = blk >= 0 && blk < a.ori_num_blocks;
+            off[h2] = (blk * a.ori_block_size + (j - pg * a.ori_block_size)) * D;
+          } else {
+            const int64_t cr = a.mode == 1 ? (int64_t)list[pos] : (int64_t)pos;
+            const int64_t pg = fast_div(cr, a.cmp_magic, a.cmp_shift);
+            const int64_t blk = pg < a.cmp_max_blocks
+                                    ? a.cmp_block_table[(int64_t)r.b * a.cmp_max_blocks + pg] : -1;
+            ok[h2] = blk >= 0 && blk < a.cmp_num_blocks;
+            off[h2] = (blk * a.cmp_block_size + (cr - pg * a.cmp_block_size)) * D;
+          }
         }
       }
-      rowoff[tid] = off;
-    }
-    __syncthreads();
-    // ---- bulk copies: Q rows of the head group and the valid K~ rows ----
-    if (warp == 0) {
-      // earlier generic-proxy reads and zero-fills of these rows precede the
-      // async-proxy copies below
+      const uint64_t valid = (uint64_t)__ballot_sync(0xffffffffu, ok[0]) |
+                             ((uint64_t)__ballot_sync(0xffffffffu, ok[1]) << 32);
+      // rows without a K~ row are zeroed: their P is 0, and a zero row keeps
+      // P V exact whatever an earlier chunk left there
+      for (uint64_t inval = ~valid; inval; inval &= inval - 1) {
+        const int rr = __ffsll((long long)inval) - 1;
+        for (int x = lane; x < D / 8; x += 32)
+          *reinterpret_cast<uint4*>(st + rr * Cfg::kRowBytes + x * 16) = make_uint4(0, 0, 0, 0);
+      }
+      if (lane == 0) {
+        hdr[s].valid = valid;
+        hdr[s].last = last ? 1 : 0;
+      }
+      // the zero rows (generic proxy) precede later bulk copies into them
       fence_proxy_async_smem();
-      int nvalid = 0;
-      for (int rr = 0; rr < kChunk; ++rr) nvalid += rowoff[rr] >= 0;
-      if (lane == 0)
-        mbar_arrive_expect_tx(bar, (uint32_t)((nheads + nvalid) * D * 2));
       __syncwarp();
-      const uint16_t* qrow = a.q + (u * a.N1 + head0) * (int64_t)D;
-      for (int h = lane; h < nheads; h += 32)
-        bulk_load(sm + Cfg::kOffQ + h * Cfg::kRowBytes, qrow + (int64_t)h * D, D * 2, bar);
-      for (int rr = lane; rr < kChunk; rr += 32) {
-        const int64_t off = rowoff[rr];
-        if (off >= 0) {
-          const uint16_t* src = (off >> 62) ? a.cmp_kv + (off & ((1ll << 62) - 1)) : a.ori_kv + off;
-          bulk_load(sm + Cfg::kOffK + rr * Cfg::kRowBytes, src, D * 2, bar);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(__popcll(valid) * D * 2));
+      __syncwarp();
+      const uint16_t* src = cmp ? a.cmp_kv : a.ori_kv;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2)
+        if (ok[h2]) bulk_load(st + (lane + 32 * h2) * Cfg::kRowBytes, src + off[h2], D * 2, &full[s]);
+      ++it;
+    };
+
+    for (int64_t k = k_begin; k < k_end && !aborted; ++k, ++qn) {
+      const int64_t u = k / a.hgs;
+      const int head0 = (int)(k - u * a.hgs) * kHeads;
+      const int nh = min(kHeads, a.N1 - head0);
+      const SparseRow r = sparse_row(a, u);
+      // ---- the item's query rows (once the consumers hold the last item's) ----
+      wait_or_abort(qempty, (qn & 1) ^ 1, a.err, misc);
+      if (*reinterpret_cast<volatile int*>(misc)) break;
+      uint8_t* qs = sm + Cfg::kOffQ;
+      for (int h = nh; h < kHeads; ++h)  // heads past N1 read as zeros
+        for (int x = lane; x < D / 8; x += 32)
+          *reinterpret_cast<uint4*>(qs + h * Cfg::kRowBytes + x * 16) = make_uint4(0, 0, 0, 0);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(qfull, (uint32_t)(nh * D * 2));
+      __syncwarp();
+      if (lane < nh)
+        bulk_load(qs + lane * Cfg::kRowBytes, a.q + (u * a.N1 + head0 + lane) * (int64_t)D, D * 2,
+                  qfull);
+      // ---- window rows [lo, hi] of the original cache ----
+      const int64_t lo = max((int64_t)0, r.p - a.win_left);
+      const int64_t hi = min(r.S2 - 1, r.p + a.win_right);
+      const int nw = (int)max((int64_t)0, hi - lo + 1);
+      const int nwch = (nw + kChunk - 1) / kChunk;
+      // the last window chunk ends the item when no compressed rows follow
+      // (known up front except for CSA, whose list is compacted below)
+      const bool win_ends = a.mode == 0 || (a.mode == 2 && r.vis == 0);
+      bool ended = false;
+      for (int ch = 0; ch < nwch && !aborted; ++ch) {
+        const bool last = win_ends && ch == nwch - 1;
+        issue_chunk(r, false, lo, ch * kChunk, nw, last);
+        ended |= last;
+      }
+      if (aborted) break;
+      // ---- compressed rows ----
+      int nk = 0;
+      if (a.mode == 1) {
+        // CSA: the list up to the first negative entry, visible entries kept
+        // in order (warp compaction into shared memory)
+        const int32_t* ix = a.cmp_sparse_indices + u * (int64_t)a.K2;
+        bool stop = false;
+        for (int t0 = 0; t0 < a.K2 && !stop; t0 += 32 * 8) {
+          int v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int t = t0 + 32 * j + lane;
+            v[j] = t < a.K2 ? ix[t] : -1;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (!stop) {
+              const uint32_t neg = __ballot_sync(0xffffffffu, v[j] < 0);
+              const int first = neg ? __ffs(neg) - 1 : 32;
+              const bool keep = lane < first && (int64_t)v[j] < r.vis;
+              const uint32_t km = __ballot_sync(0xffffffffu, keep);
+              if (keep) list[nk + __popc(km & ((1u << lane) - 1u))] = v[j];
+              nk += __popc(km);
+              stop = neg != 0;
+            }
+          }
+        }
+        __syncwarp();  // the list is read by other lanes below
+      } else if (a.mode == 2) {
+        nk = (int)r.vis;
+      }
+      const int nkch = (nk + kChunk - 1) / kChunk;
+      for (int ch = 0; ch < nkch && !aborted; ++ch) {
+        const bool last = ch == nkch - 1;
+        issue_chunk(r, true, 0, ch * kChunk, nk, last);
+        ended |= last;
+      }
+      if (!ended && !aborted) issue_chunk(r, true, 0, 0, 0, true);  // nothing visible: one empty chunk
+    }
+    return;
+  }
+
+  // ======================= consumers =======================
+  // Warp cw: QK rows 16 rg .. 16 rg + 15 of each chunk over half hf of D
+  // (the two halves' partial scores are summed through shared memory), and
+  // P V for output columns cw * D/8 .. + D/8 over all 64 rows.
+  constexpr int KS = D / 32;             // k-steps over half of D
+  constexpr int DW = D / kSCons;         // output columns of a warp
+  constexpr int MTW = DW / 16;           // their m-tiles
+  constexpr int nthr = 32 * kSCons;
+  const int cw = warp - 1, rg = cw & 3, hf = cw >> 2;
+  const int g = lane >> 2, q4 = lane & 3;
+  float* sx = reinterpret_cast<float*>(sm + Cfg::kOffSx);
+  float* mxs = reinterpret_cast<float*>(sm + Cfg::kOffMx);
+  float* lsum = reinterpret_cast<float*>(sm + Cfg::kOffL);
+  uint16_t* pt = reinterpret_cast<uint16_t*>(sm + Cfg::kOffPt);
+  const uint32_t sm_base = smem_u32(sm);
+  const int r0 = 16 * rg + g, r1 = r0 + 8;  // chunk rows of fragment rows g, g+8
+  int it = 0, qn = 0;
+  for (int64_t k = k_begin; k < k_end; ++k, ++qn) {
+    const int64_t u = k / a.hgs;
+    const int head0 = (int)(k - u * a.hgs) * kHeads;
+    const int nh = min(kHeads, a.N1 - head0);
+    // ---- Q^T fragments of this warp's half of D (mma B: k = d, n = head) ----
+    wait_or_abort(qfull, qn & 1, a.err, misc);
+    uint32_t qb[KS][2];
+    {
+      const uint16_t* qsm = reinterpret_cast<const uint16_t*>(sm + Cfg::kOffQ);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const int d0 = hf * (D / 2) + kk * 16 + 2 * q4;
+        qb[kk][0] = *reinterpret_cast<const uint32_t*>(qsm + g * (Cfg::kRowBytes / 2) + d0);
+        qb[kk][1] = *reinterpret_cast<const uint32_t*>(qsm + g * (Cfg::kRowBytes / 2) + d0 + 8);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(qempty);
+
+    float acc[MTW][4];
+#pragma unroll
+    for (int i = 0; i < MTW; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY};  // running maxima of heads 2q, 2q+1 (exp2 domain)
+    float l[2] = {0.f, 0.f};              // this lane's share of the sums (row-group warps)
+    bool stop = false;
+    while (true) {
+      const int s = it % S;
+      wait_or_abort(&full[s], (it / S) & 1, a.err, misc);
+      const uint64_t valid = hdr[s].valid;
+      const bool last = hdr[s].last != 0;
+      const uint32_t st = sm_base + s * Cfg::kStageBytes;
+      // ---- partial S^T = K~ Q^T: rows of this row group, half hf of D ----
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        // A: matrices (rows 0-7, d lo8), (rows 8-15, d lo8), (rows 0-7, hi8), (rows 8-15, hi8)
+        const int mi = lane >> 3;
+        const int row = 16 * rg + (mi & 1) * 8 + (lane & 7);
+        const int col = hf * (D / 2) + kk * 16 + (mi >> 1) * 8;
+        uint32_t ka[4];
+        ldsm_x4(st + row * Cfg::kRowBytes + col * 2, ka[0], ka[1], ka[2], ka[3]);
+        mma_bf16(sc, ka, qb[kk][0], qb[kk][1]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sx[(cw * 4 + e) * 32 + lane] = sc[e];
+      // the two halves meet; a time-out anywhere stops every consumer warp here
+      if (named_bar_or(1, nthr, *reinterpret_cast<volatile int*>(misc) != 0)) {
+        stop = true;
+        break;
+      }
+      float x[4];
+      {
+        const bool v0 = (valid >> r0) & 1, v1 = (valid >> r1) & 1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float o = sx[((cw ^ 4) * 4 + e) * 32 + lane];
+          const float sfull = hf ? o + sc[e] : sc[e] + o;  // the same sum in both warps
+          x[e] = ((e < 2) ? v0 : v1) ? sfull * a.scale_log2 : -INFINITY;
         }
       }
-    } else {
-      // zero the rows that hold no K~ row (and head rows past N1)
-      for (int x = tid - 32; x < kChunk * (D / 8); x += kSThreads - 32) {
-        const int rr = x / (D / 8), k = x % (D / 8);
-        if (rowoff[rr] < 0)
-          *reinterpret_cast<uint4*>(sm + Cfg::kOffK + rr * Cfg::kRowBytes + k * 16) = make_uint4(0, 0, 0, 0);
+      // ---- chunk maxima per head: 16 rows here, then the 4 row groups ----
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float mx = fmaxf(x[e], x[2 + e]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (hf == 0 && g == 0) mxs[rg * kHeads + 2 * q4 + e] = mx;
       }
-      for (int x = tid - 32; x < (kHeadsPerCta - nheads) * (D / 8); x += kSThreads - 32) {
-        const int h = nheads + x / (D / 8), k = x % (D / 8);
-        *reinterpret_cast<uint4*>(sm + Cfg::kOffQ + h * Cfg::kRowBytes + k * 16) = make_uint4(0, 0, 0, 0);
+      named_bar_sync(1, nthr);
+      float corr[2], mu[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float mc = mxs[2 * q4 + e];
+#pragma unroll
+        for (int r2 = 1; r2 < 4; ++r2) mc = fmaxf(mc, mxs[r2 * kHeads + 2 * q4 + e]);
+        const float mn = fmaxf(m[e], mc);
+        mu[e] = mn == -INFINITY ? 0.f : mn;
+        corr[e] = mn == m[e] ? 1.f : (m[e] == -INFINITY ? 0.f : fast_exp2(m[e] - mu[e]));
+        m[e] = mn;
       }
+      // ---- P = exp2(x - m): the row-group warps keep the sums and publish P^T ----
+      if (hf == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float p0 = fast_exp2(x[e] - mu[e]), p1 = fast_exp2(x[2 + e] - mu[e]);
+          l[e] = l[e] * corr[e] + p0 + p1;
+          const __nv_bfloat16 b0 = __float2bfloat16_rn(p0), b1 = __float2bfloat16_rn(p1);
+          pt[(2 * q4 + e) * Cfg::kPtStride + r0] = *reinterpret_cast<const uint16_t*>(&b0);
+          pt[(2 * q4 + e) * Cfg::kPtStride + r1] = *reinterpret_cast<const uint16_t*>(&b1);
+        }
+      }
+      named_bar_sync(1, nthr);
+      // ---- O^T += V~^T P^T over this warp's columns ----
+      if (__any_sync(0xffffffffu, corr[0] != 1.f || corr[1] != 1.f)) {
+#pragma unroll
+        for (int i = 0; i < MTW; ++i) {
+          acc[i][0] *= corr[0]; acc[i][1] *= corr[1];
+          acc[i][2] *= corr[0]; acc[i][3] *= corr[1];
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < kChunk / 16; ++kk) {
+        // B = P^T (k = rows, n = head): rows 2q, 2q+1 and 2q+8, 2q+9 of head g
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(pt + g * Cfg::kPtStride + kk * 16 + 2 * q4);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(pt + g * Cfg::kPtStride + kk * 16 + 2 * q4 + 8);
+#pragma unroll
+        for (int i = 0; i < MTW; ++i) {
+          // A = V^T (m = d, k = rows), transposed by ldmatrix: matrices
+          // (rows 0-7, d lo8), (rows 0-7, d hi8), (rows 8-15, d lo8), (rows 8-15, d hi8)
+          const int mi = lane >> 3;
+          const int row = kk * 16 + (mi >> 1) * 8 + (lane & 7);
+          const int col = cw * DW + i * 16 + (mi & 1) * 8;
+          uint32_t va[4];
+          ldsm_x4_t(st + row * Cfg::kRowBytes + col * 2, va[0], va[1], va[2], va[3]);
+          mma_bf16(acc[i], va, b0, b1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      ++it;
+      if (last) break;
     }
-    if (!mbar_wait(bar, phase, a.err)) misc[0] = 1;
-    phase ^= 1;
-    __syncthreads();
+    if (stop) break;
 
-    // ---- partial S = Q K~^T over this warp's half of D (16 heads x 64 rows) ----
-    float sc[8][4];
+    // ---- sink, normalisation, O and lse ----
+    if (hf == 0) {
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-      const int d0 = half * DH + kk * 16;
-      uint32_t qa[4];
-      {
-        // A: rows = heads (16), k = d: matrices (h 0-7, d lo), (h 8-15, d lo), (h 0-7, d hi), (h 8-15, d hi)
-        const int mi = lane >> 3;
-        const int hr = hgrp * 16 + (mi & 1) * 8 + (lane & 7);
-        const uint32_t addr = sq + hr * Cfg::kRowBytes + (d0 + (mi >> 1) * 8) * 2;
-        ldsm_x4(addr, qa[0], qa[1], qa[2], qa[3]);
-      }
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        // B: n = K~ rows, k = d: matrices (rows 8np.., d lo), (.., d hi), (rows 8np+8.., lo), (.., hi)
-        const int mi = lane >> 3;
-        const int rr = np * 16 + (mi >> 1) * 8 + (lane & 7);
-        const uint32_t addr = sk + rr * Cfg::kRowBytes + (d0 + (mi & 1) * 8) * 2;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(addr, b0, b1, b2, b3);
-        mma_bf16(sc[2 * np], qa, b0, b1);
-        mma_bf16(sc[2 * np + 1], qa, b2, b3);
+      for (int e = 0; e < 2; ++e) {
+        float t = l[e];
+        t += __shfl_xor_sync(0xffffffffu, t, 4);
+        t += __shfl_xor_sync(0xffffffffu, t, 8);
+        t += __shfl_xor_sync(0xffffffffu, t, 16);
+        if (g == 0) lsum[rg * kHeads + 2 * q4 + e] = t;
       }
     }
-    // exchange halves: S = S_half0 + S_half1
-    float* mine = sx + (size_t)warp * 16 * kChunk;
-    const float* other = sx + (size_t)(warp ^ 4) * 16 * kChunk;
+    named_bar_sync(1, nthr);
+    float scl[2], lse[2];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      mine[g * kChunk + nt * 8 + 2 * q4] = sc[nt][0];
-      mine[g * kChunk + nt * 8 + 2 * q4 + 1] = sc[nt][1];
-      mine[(g + 8) * kChunk + nt * 8 + 2 * q4] = sc[nt][2];
-      mine[(g + 8) * kChunk + nt * 8 + 2 * q4 + 1] = sc[nt][3];
-    }
-    __syncthreads();
+    for (int e = 0; e < 2; ++e) {
+      const int hl = 2 * q4 + e;
+      float L = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      sc[nt][0] += other[g * kChunk + nt * 8 + 2 * q4];
-      sc[nt][1] += other[g * kChunk + nt * 8 + 2 * q4 + 1];
-      sc[nt][2] += other[(g + 8) * kChunk + nt * 8 + 2 * q4];
-      sc[nt][3] += other[(g + 8) * kChunk + nt * 8 + 2 * q4 + 1];
-    }
-    // ---- softmax of the chunk per head (exp2 domain) ----
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int col = nt * 8 + 2 * q4 + (e & 1);
-        const float x = rowoff[col] >= 0 ? sc[nt][e] * a.scale_log2 : -INFINITY;
-        sc[nt][e] = x;
-        mx[e >> 1] = fmaxf(mx[e >> 1], x);
-      }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 1));
-      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 2));
-    }
-    float lsum[2] = {0.f, 0.f};
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float base = mx[e >> 1] == -INFINITY ? 0.f : mx[e >> 1];
-        const float pv = fast_exp2(sc[nt][e] - base);
-        sc[nt][e] = pv;
-        lsum[e >> 1] += pv;
-      }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      lsum[hh] += __shfl_xor_sync(0xffffffffu, lsum[hh], 1);
-      lsum[hh] += __shfl_xor_sync(0xffffffffu, lsum[hh], 2);
-    }
-    // ---- acc = P V over this warp's half of D ----
-    float acc[NT][4];
-#pragma unroll
-    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < kChunk / 16; ++kk) {
-      uint32_t pa[4];
-      pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-      pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-      pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-      pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-#pragma unroll
-      for (int np = 0; np < NT / 2; ++np) {
-        // B = V rows (k = K~ row, n = d), transposed by ldmatrix:
-        // matrices (rows 0-7, d lo), (rows 8-15, d lo), (rows 0-7, d hi), (rows 8-15, d hi)
-        const int mi = lane >> 3;
-        const int rr = kk * 16 + (mi & 1) * 8 + (lane & 7);
-        const int dd = half * DH + np * 16 + (mi >> 1) * 8;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sk + rr * Cfg::kRowBytes + dd * 2, b0, b1, b2, b3);
-        mma_bf16(acc[2 * np], pa, b0, b1);
-        mma_bf16(acc[2 * np + 1], pa, b2, b3);
+      for (int r2 = 0; r2 < 4; ++r2) L += lsum[r2 * kHeads + hl];
+      scl[e] = 0.f;
+      lse[e] = INFINITY;
+      if (m[e] != -INFINITY) {
+        float Mp = m[e];
+        if (a.sinks && hl < nh) {
+          const float sk = a.sinks[head0 + hl] * 1.4426950408889634f;
+          Mp = fmaxf(m[e], sk);
+          L = L * exp2f(m[e] - Mp) + exp2f(sk - Mp);
+        }
+        scl[e] = exp2f(m[e] - Mp) / L;
+        lse[e] = (Mp + log2f(L)) * 0.6931471805599453f;
       }
     }
-    // ---- partial of this item: [N1][D + 2] at slot (row, chunk) ----
-    float* pp = a.partials + ((size_t)u * a.max_chunks + ch) * (size_t)a.N1 * (D + 2);
+    // acc[i][0..1]: column d = cw*DW + 16i + g, heads 2q, 2q+1; [2..3]: d + 8.
+    // Lanes g and g^1 hold neighbouring columns: even g writes head 2q at
+    // (d, d+1), odd g head 2q+1 at (d-1, d), as bf16 pairs.
+    uint16_t* orow = a.out + (u * a.N1 + head0) * (int64_t)D;
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int hl = hgrp * 16 + g + 8 * hh;
-      if (hl >= nheads) continue;
-      float* ph = pp + (size_t)(head0 + hl) * (D + 2);
+    for (int i = 0; i < MTW; ++i)
 #pragma unroll
-      for (int i = 0; i < NT; ++i) {
-        const int d = half * DH + i * 8 + 2 * q4;
-        *reinterpret_cast<float2*>(ph + d) = make_float2(acc[i][2 * hh], acc[i][2 * hh + 1]);
+      for (int hr = 0; hr < 2; ++hr) {
+        const float v0 = acc[i][2 * hr] * scl[0], v1 = acc[i][2 * hr + 1] * scl[1];
+        const float w0 = __shfl_xor_sync(0xffffffffu, v0, 4);
+        const float w1 = __shfl_xor_sync(0xffffffffu, v1, 4);
+        const int d = cw * DW + 16 * i + 8 * hr + g;
+        if ((g & 1) == 0) {
+          if (2 * q4 < nh)
+            *reinterpret_cast<uint32_t*>(orow + (2 * q4) * D + d) = pack_bf16(v0, w0);
+        } else {
+          if (2 * q4 + 1 < nh)
+            *reinterpret_cast<uint32_t*>(orow + (2 * q4 + 1) * D + d - 1) = pack_bf16(w1, v1);
+        }
       }
-      if (half == 0 && q4 == 0) {
-        ph[D] = mx[hh];
-        ph[D + 1] = lsum[hh];
-      }
+    if (a.lse && cw == 0 && g == 0) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        if (2 * q4 + e < nh) a.lse[u * a.N1 + head0 + 2 * q4 + e] = lse[e];
     }
-    __syncthreads();  // shared buffers are reused by the next item
-    if (*reinterpret_cast<volatile int*>(misc)) break;
-    ++ch;
   }
-}
-
-// ---------------------------------------------------------------------------
-// combine: fold a row's chunk partials in chunk order, sink, normalise
-// ---------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(128) sparse_combine_kernel(const SparseArgs a,
-                                                              const int32_t* __restrict__ md) {
-  if (md[0] != 0x46534D31 || md[1] != a.num_ctas || md[2] != (int32_t)a.rows ||
-      md[5] != a.B || md[6] != a.N1 || md[7] != a.K2)
-    return;  // the attention kernel has set the status word
-  const int64_t u = blockIdx.x;
-  const int h = blockIdx.y;
-  const SparseRow r = sparse_row(a, u);
-  const float* base = a.partials + ((size_t)u * a.max_chunks) * (size_t)a.N1 * (D + 2) +
-                      (size_t)h * (D + 2);
-  const size_t cstride = (size_t)a.N1 * (D + 2);
-  float M = -INFINITY;
-  for (int ch = 0; ch < r.nchunks; ++ch) M = fmaxf(M, base[ch * cstride + D]);
-  const float Mu = M == -INFINITY ? 0.f : M;
-  float L = 0.f;
-  for (int ch = 0; ch < r.nchunks; ++ch) {
-    const float mc = base[ch * cstride + D];
-    if (mc != -INFINITY) L += base[ch * cstride + D + 1] * exp2f(mc - Mu);
-  }
-  float scl = 0.f, lse = INFINITY;
-  if (M != -INFINITY) {
-    float Mp = M;
-    if (a.sinks) {
-      const float sk = a.sinks[h] * 1.4426950408889634f;
-      Mp = fmaxf(M, sk);
-      L = L * exp2f(M - Mp) + exp2f(sk - Mp);
-    }
-    scl = exp2f(M - Mp) / L;
-    lse = (Mp + log2f(L)) * 0.6931471805599453f;
-  }
-  for (int d = threadIdx.x * 2; d < D; d += 256) {
-    float o0 = 0.f, o1 = 0.f;
-    for (int ch = 0; ch < r.nchunks; ++ch) {
-      const float mc = base[ch * cstride + D];
-      if (mc == -INFINITY) continue;
-      const float f = exp2f(mc - Mu);
-      o0 += base[ch * cstride + d] * f;
-      o1 += base[ch * cstride + d + 1] * f;
-    }
-    *reinterpret_cast<uint32_t*>(a.out + (u * a.N1 + h) * (int64_t)D + d) = pack_bf16(o0 * scl, o1 * scl);
-  }
-  if (a.lse && threadIdx.x == 0) a.lse[u * a.N1 + h] = lse;
 }
 
 // ---------------------------------------------------------------------------
@@ -473,12 +588,7 @@ static cudaError_t launch_sparse_t(const SparseArgs& a, const int32_t* md, cudaS
     if (e != cudaSuccess) return e;
     done_mask[(dev >> 6) & 3].fetch_or(bit);
   }
-  dim3 grid(a.num_ctas, (a.N1 + kHeadsPerCta - 1) / kHeadsPerCta);
-  kern<<<grid, kSThreads, Cfg::kSmem, s>>>(a, md);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  dim3 cgrid((unsigned)a.rows, a.N1);
-  sparse_combine_kernel<D><<<cgrid, 128, 0, s>>>(a, md);
+  kern<<<a.num_ctas, kSThreads, Cfg::kSmem, s>>>(a, md);
   return cudaGetLastError();
 }
 

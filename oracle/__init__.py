@@ -117,7 +117,7 @@ def lib():
                                                ctypes.c_void_p, ctypes.c_int64]
             L.oracle_prefill_units.restype = ctypes.c_int64
             L.oracle_sparse_metadata.argtypes = [ctypes.POINTER(_SparseArgs), ctypes.c_int32,
-                                                 ctypes.c_int32, ctypes.c_void_p]
+                                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
             L.oracle_sparse_metadata.restype = ctypes.c_int
             L.oracle_sparse_rows.argtypes = [ctypes.POINTER(_SparseArgs), ctypes.c_int,
                                              ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64]
@@ -308,9 +308,9 @@ def prefill_units(p):
     return units[:n].copy(), cost[:n].copy()
 
 
-def sparse_metadata(p, num_ctas: int, chunk: int = 64):
+def sparse_metadata(p, num_ctas: int, chunk: int = 64, heads: int = 8):
     s, keep = _sparse_struct(p)
     md = np.zeros(1024, dtype=np.int32)
-    rc = lib().oracle_sparse_metadata(ctypes.byref(s), num_ctas, chunk, md.ctypes.data)
+    rc = lib().oracle_sparse_metadata(ctypes.byref(s), num_ctas, chunk, heads, md.ctypes.data)
     assert rc == 0
     return md

@@ -655,30 +655,33 @@ int64_t oracle_prefill_units(const oracle_fia_args *a, int32_t *units, int64_t *
 }
 
 /* Sparse metadata ([SFMLA] sparse_flash_mla_metadata; fixed [1024] int32).
- * Units are query rows in row order.  The concatenated K~ of a unit is cut
- * into fixed chunks of `chunk` logical positions: ceil(W/chunk) window chunks
- * (W = win_left + win_right + 1) followed by ceil(kc/chunk) compressed
- * chunks, kc = visible compressed rows capped at K2 (CSA) or all visible
- * compressed rows (HCA), 0 for SWA.  CTA c owns the chunk interval
- * [floor(c*total/n), floor((c+1)*total/n)) of the row-major (unit, chunk)
- * sequence.  Layout:
- *   [0] 0x46534D31  [1] n  [2] units  [3] chunk  [4] total  [5] B  [6] N1
- *   [7] K2  [8] cmp_ratio  [9] win_left  [10] win_right  [11] mode
- *   (0 SWA, 1 CSA, 2 HCA)  [12..15] 0
- *   [16+2c], [17+2c]: (unit, chunk) where CTA c begins, c = 0..n
- *   the rest 0.  Returns 0, or -1 if n does not fit. */
+ * Work items are (query row u, group g of `heads` consecutive query heads),
+ * numbered k = u * G + g with G = ceil(N1 / heads).  The weight of an item is
+ * its row's chunk count: ceil(W/chunk) window chunks (W = win_left +
+ * win_right + 1) plus ceil(kc/chunk) compressed chunks, kc = the visible
+ * compressed rows capped at K2 (CSA), all of them (HCA), 0 (SWA).  With P_k
+ * the summed weight of the items before k and T the total weight, CTA c
+ * takes the items with floor(c*T/n) <= P_k < floor((c+1)*T/n); it begins at
+ * item #{k : P_k < floor(c*T/n)}.  Layout:
+ *   [0] 0x46534D32  [1] n  [2] rows  [3] chunk  [4] T  [5] B  [6] N1  [7] K2
+ *   [8] cmp_ratio (1 without a compressed cache)  [9] win_left
+ *   [10] win_right  [11] mode (0 SWA, 1 CSA, 2 HCA)  [12] heads  [13] items
+ *   [14..15] 0
+ *   [16 + c]: first item of CTA c, c = 0..n;  the rest 0.
+ * Returns 0, or -1 if n does not fit. */
 int oracle_sparse_metadata(const oracle_sparse_args *a, int32_t num_ctas, int32_t chunk,
-                           int32_t *md)
+                           int32_t heads, int32_t *md)
 {
     int64_t rows = a->layout == OR_LAYOUT_TND ? a->T1 : (int64_t)a->B * a->S1;
-    int64_t W = (int64_t)a->win_left + a->win_right + 1, total = 0, u, c;
-    int64_t *pre;
+    int64_t W = (int64_t)a->win_left + a->win_right + 1, total = 0, u, c, k;
+    int64_t G = or_ceil_div(a->N1, heads), items = rows * G;
+    int64_t *P;
     int mode = !a->cmp_kv ? 0 : (a->cmp_sparse_indices ? 1 : 2);
-    if (16 + 2 * ((int64_t)num_ctas + 1) > 1024) return -1;
-    pre = (int64_t *)malloc(sizeof(int64_t) * (size_t)(rows + 1));
+    if (num_ctas < 1 || 17 + (int64_t)num_ctas > 1024) return -1;
+    P = (int64_t *)malloc(sizeof(int64_t) * (size_t)(items + 1));
     for (u = 0; u < rows; ++u) {
         int b = 0;
-        int64_t ql, qs, i, p, kc = 0, nch;
+        int64_t ql, qs, i, p, kc = 0, nch, g;
         if (a->layout == OR_LAYOUT_TND) {
             while (b + 1 <= a->B && a->cu_seqlens_q[b + 1] <= u) ++b;
             qs = a->cu_seqlens_q[b];
@@ -695,12 +698,14 @@ int oracle_sparse_metadata(const oracle_sparse_args *a, int32_t num_ctas, int32_
             if (mode == 1 && kc > a->K2) kc = a->K2;
         }
         nch = or_ceil_div(W, chunk) + or_ceil_div(kc, chunk);
-        pre[u] = total;
-        total += nch;
+        for (g = 0; g < G; ++g) {
+            P[u * G + g] = total;
+            total += nch;
+        }
     }
-    pre[rows] = total;
+    P[items] = total;
     memset(md, 0, sizeof(int32_t) * 1024);
-    md[0] = 0x46534D31;
+    md[0] = 0x46534D32;
     md[1] = num_ctas;
     md[2] = (int32_t)rows;
     md[3] = chunk;
@@ -708,26 +713,18 @@ int oracle_sparse_metadata(const oracle_sparse_args *a, int32_t num_ctas, int32_
     md[5] = a->B;
     md[6] = a->N1;
     md[7] = a->K2;
-    md[8] = a->cmp_ratio;
+    md[8] = a->cmp_kv ? a->cmp_ratio : 1;  /* no compressed cache: 1 */
     md[9] = a->win_left;
     md[10] = a->win_right;
     md[11] = mode;
+    md[12] = heads;
+    md[13] = (int32_t)items;
     for (c = 0; c <= num_ctas; ++c) {
-        int64_t g = c * total / num_ctas, lo = 0, hi = rows;
-        /* unit containing chunk g: largest u with pre[u] <= g (g == total: rows) */
-        if (g >= total) {
-            md[16 + 2 * c] = (int32_t)rows;
-            md[17 + 2 * c] = 0;
-            continue;
-        }
-        while (hi - lo > 1) {
-            int64_t mid = (lo + hi) / 2;
-            if (pre[mid] <= g) lo = mid; else hi = mid;
-        }
-        md[16 + 2 * c] = (int32_t)lo;
-        md[17 + 2 * c] = (int32_t)(g - pre[lo]);
+        int64_t theta = c * total / num_ctas, cnt = 0;
+        for (k = 0; k < items; ++k) cnt += P[k] < theta;
+        md[16 + c] = (int32_t)cnt;
     }
-    free(pre);
+    free(P);
     return 0;
 }
 

@@ -518,27 +518,45 @@ def test_prefill_units_enumerate_every_tile_and_head_pair():
         assert c == 1 + t + 1
 
 
-def test_sparse_metadata_covers_every_chunk_in_order():
-    sp = fi.make_sparse(B=3, N1=4, D=32, q_lens=[2, 2, 2], kv_lens=[600, 40, 3000], mode="csa",
+def test_sparse_metadata_worked_example():
+    """SWA with a 128-row band: every row weighs 2 chunks; N1 = 16 gives two
+    8-head items per row.  Three rows -> item weights 2 x 6, T = 12; over 4
+    CTAs the thresholds are 0, 3, 6, 9, 12 and the item offsets 0, 2, ..., 10,
+    so the CTAs begin at items 0, 2, 3, 5 and the list ends at 6."""
+    sp = fi.make_sparse(B=3, N1=16, D=32, q_lens=[1, 1, 1], kv_lens=[500, 7, 130], mode="swa",
+                        ori_block_size=16, seed=62)
+    md = oracle.sparse_metadata(sp, 4, 64, 8)
+    assert list(md[:14]) == [0x46534D32, 4, 3, 64, 12, 3, 16, 0, 1, 127, 0, 0, 8, 6]
+    assert list(md[16:21]) == [0, 2, 3, 5, 6]
+    assert np.all(md[21:] == 0) and md[14] == 0 and md[15] == 0
+
+
+def test_sparse_metadata_covers_every_item_in_order():
+    sp = fi.make_sparse(B=3, N1=16, D=32, q_lens=[2, 2, 2], kv_lens=[600, 40, 3000], mode="csa",
                         K2=64, ori_block_size=16, cmp_block_size=16, seed=61)
-    for n in (1, 5, 152, 503):
-        md = oracle.sparse_metadata(sp, n, 64)
-        assert md[0] == 0x46534D31 and md[1] == n and md[2] == sp.rows and md[3] == 64
-        total = md[4]
-        # per-unit chunk counts from the definition
-        counts = []
-        for b in range(sp.B):
-            for i in range(2):
-                p = sp.kv_lens[b] - 2 + i
-                kc = min(64, (p + 1) // 4)
-                counts.append(2 + -(-kc // 64))
-        assert total == sum(counts)
-        pre = np.concatenate([[0], np.cumsum(counts)])
-        begins = [pre[md[16 + 2 * c]] + md[17 + 2 * c] for c in range(n + 1)]
-        assert begins[0] == 0 and begins[-1] == total
-        assert all(y >= x for x, y in zip(begins, begins[1:]))
-        sizes = np.diff(begins)
-        assert sizes.max() - sizes.min() <= 1
-        assert np.all(md[16 + 2 * (n + 1):] == 0)
+    G = 2
+    # per-row chunk counts from the definition: 2 window chunks (band 128)
+    # plus the capped visible compressed rows in chunks of 64
+    counts = []
+    for b in range(sp.B):
+        for i in range(2):
+            p = sp.kv_lens[b] - 2 + i
+            kc = min(64, (p + 1) // 4)
+            counts.append(2 + -(-kc // 64))
+    weights = np.repeat(counts, G)
+    for n in (1, 5, 13, 152, 1007):
+        md = oracle.sparse_metadata(sp, n, 64, 8)
+        assert md[0] == 0x46534D32 and md[1] == n and md[2] == sp.rows and md[3] == 64
+        assert md[4] == weights.sum() and md[13] == len(weights)
+        begins = md[16:17 + n]
+        # contiguous, ordered, every item exactly once
+        assert begins[0] == 0 and begins[-1] == len(weights)
+        assert np.all(np.diff(begins) >= 0)
+        # balance: a CTA's weight exceeds its share by less than one item
+        pre = np.concatenate([[0], np.cumsum(weights)])
+        load = pre[begins[1:]] - pre[begins[:-1]]
+        share = weights.sum() / n
+        assert load.max() < share + weights.max()
+        assert np.all(md[17 + n:] == 0)
     with pytest.raises(AssertionError):
-        oracle.sparse_metadata(sp, 504, 64)
+        oracle.sparse_metadata(sp, 1008, 64, 8)

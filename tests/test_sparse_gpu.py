@@ -45,6 +45,14 @@ CASES = {
     "csa_no_sinks_window_right": dict(B=2, N1=8, D=128, q_lens=[4, 4], kv_lens=[200, 90],
                                       mode="csa", K2=64, win_left=30, win_right=2,
                                       with_sinks=False, ori_block_size=16, cmp_block_size=16),
+    # pages of 48 and 80 rows (the page index is not a shift), one head group
+    # of 2 heads, a long HCA list (several compressed chunks)
+    "hca_odd_pages_two_heads": dict(B=2, N1=2, D=256, q_lens=[2, 1], kv_lens=[9000, 333],
+                                    layout=fi.LAYOUT_TND, mode="hca", cmp_ratio=16,
+                                    ori_block_size=48, cmp_block_size=80),
+    "csa_odd_pages": dict(B=3, N1=32, D=128, q_lens=[1, 1, 1], kv_lens=[2500, 64, 700],
+                          mode="csa", K2=300, cmp_ratio=4, ori_block_size=80,
+                          cmp_block_size=48),
 }
 
 
@@ -72,7 +80,7 @@ def test_sparse_trailing_invalid_indices_and_duplicates():
     check_close(out, lse, ro, rl, "trailing -1")
 
 
-@pytest.mark.parametrize("num_sms", [1, 7, 152, 503])
+@pytest.mark.parametrize("num_sms", [1, 7, 152, 503, 1007])
 def test_sparse_metadata_bit_exact(num_sms):
     import decode_tile_scheduler_gb300 as fia
     sp = fi.make_sparse(B=4, N1=8, D=128, q_lens=[3, 1, 2, 5], kv_lens=[600, 10, 3000, 128],
@@ -82,6 +90,20 @@ def test_sparse_metadata_bit_exact(num_sms):
     torch.cuda.synchronize()
     ref = oracle.sparse_metadata(sp.to("cpu"), num_sms, 64)
     assert np.array_equal(c.metadata.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("mode", ["swa", "hca"])
+def test_sparse_metadata_bit_exact_other_modes(mode):
+    import decode_tile_scheduler_gb300 as fia
+    sp = fi.make_sparse(B=3, N1=32, D=128, q_lens=[1, 4, 2], kv_lens=[4000, 7, 900],
+                        layout=fi.LAYOUT_TND, mode=mode, cmp_ratio=16, cmp_block_size=64,
+                        seed=15, device=dev)
+    for n in (3, 152):
+        c = fia.SparseCall(sp, num_sms=n)
+        c.plan()
+        torch.cuda.synchronize()
+        ref = oracle.sparse_metadata(sp.to("cpu"), n, 64)
+        assert np.array_equal(c.metadata.cpu().numpy(), ref)
 
 
 def test_sparse_batch_invariance():

@@ -279,32 +279,33 @@ typedef struct sparse_attn_params {
 } sparse_attn_params;
 
 /* Metadata step ("sparse_flash_mla_metadata": generates, before the main call,
- * the task list of every core: where in (batch/query row, KV chunk) its work
- * starts and ends; "kv_quant_sparse_attn_sharedkv": metadata int32 [1024]).
- * Validates p, launches the scheduler kernel on `stream`, which writes
- * `metadata` (device int32 [1024]), and stores the workspace size that
- * sparse_attn_run needs in *workspace_bytes (host).  Layout of metadata:
- *   [0] 0x46534D31  [1] n = CTAs  [2] units (query rows)  [3] chunk rows
- *   [4] total chunks  [5] B  [6] N1  [7] topk  [8] cmp_ratio  [9] win_left
- *   [10] win_right  [11] mode (0 SWA, 1 CSA, 2 HCA)  [12..15] 0
- *   [16+2c], [17+2c]: (query row, chunk) where CTA c begins, c = 0..n
- *   remaining entries 0.
- * The concatenated K~ of a query row is cut into fixed chunks of `chunk`
- * logical positions: ceil(W/chunk) window chunks (W = win_left + win_right
- * + 1) then ceil(kc/chunk) compressed chunks (kc = visible compressed rows,
- * capped at topk for CSA; 0 for SWA).  CTA c takes the chunk interval
- * [floor(c*total/n), floor((c+1)*total/n)).  Chunk boundaries do not depend
- * on the other rows of the batch, so results are batch invariant
- * ("sparse_flash_mla": deterministic and batch invariant by default).  n is
- * capped at 503 so that the list fits. */
+ * the task list of every core; "kv_quant_sparse_attn_sharedkv": metadata
+ * int32 [1024]).  Validates p, launches the scheduler kernel on `stream`,
+ * which writes `metadata` (device int32 [1024]), and stores the workspace
+ * size that sparse_attn_run needs in *workspace_bytes (host; the status word
+ * only).  A work item is (query row u, group g of 8 query heads), numbered
+ * k = u * G + g with G = ceil(N1 / 8); it weighs its row's chunk count
+ * ceil(W/64) + ceil(kc/64) (W = win_left + win_right + 1, kc = visible
+ * compressed rows, capped at topk for CSA, 0 for SWA).  With P_k the weight
+ * before item k and T the total, CTA c takes the items with
+ * floor(c*T/n) <= P_k < floor((c+1)*T/n).  Layout of metadata:
+ *   [0] 0x46534D32  [1] n = CTAs  [2] query rows  [3] chunk rows (64)
+ *   [4] T  [5] B  [6] N1  [7] topk  [8] cmp_ratio (1 without cmp_kv)
+ *   [9] win_left  [10] win_right  [11] mode (0 SWA, 1 CSA, 2 HCA)
+ *   [12] heads per item (8)  [13] items  [14..15] 0
+ *   [16 + c]: first item of CTA c, c = 0..n;  remaining entries 0.
+ * A query row's K~ is processed whole by one CTA, in order, so results do
+ * not depend on the other rows of the batch ("sparse_flash_mla":
+ * deterministic and batch invariant by default).  n is capped at 1007 so
+ * that the list fits. */
 fia_status sparse_attn_metadata(const sparse_attn_params *p, int32_t *metadata,
                                 size_t *workspace_bytes, void *stream);
 
-/* Main call: launches the gather-attention kernel and the chunk combine on
- * `stream`; `workspace` needs the size sparse_attn_metadata reported.
+/* Main call: launches the gather-attention kernel on `stream`; `workspace`
+ * needs the size sparse_attn_metadata reported.
  * `metadata` must come from sparse_attn_metadata with the same shapes.  The
- * kernels check its header (magic, CTA count, rows, B, N1, topk) on the
- * device; on a mismatch they write nothing to out/lse and set the int32
+ * kernel checks its header (magic, CTA count, rows, B, N1, topk, heads per
+ * item, items) on the device; on a mismatch it writes nothing to out/lse and set the int32
  * status word at workspace offset 0 to FIA_ERR_BAD_SHAPE (0 otherwise; read
  * it with any device-to-host copy after the call). */
 fia_status sparse_attn_run(const sparse_attn_params *p, const int32_t *metadata,

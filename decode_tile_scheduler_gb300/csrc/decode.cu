@@ -365,7 +365,9 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
     sched[2] = N;
     sched[3] = F;
     sched[4] = fits ? carry[3] : 0;  // split batches
-    sched[5] = sched[6] = sched[7] = 0;
+    sched[5] = kDecodePlanMark;  // this plan's mark, B and CTA count
+    sched[6] = B;
+    sched[7] = a.num_ctas;
     a.claim[0] = a.claim[1] = 0;
     *a.err = fits ? 0 : 2;  // error word of this plan's execution
   }
@@ -496,13 +498,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ======================= producer =======================
-    const int64_t C = a.sched[0], c2 = a.sched[1], N = a.sched[2];
+    // A plan of these arguments carries the scheduler's mark, B and CTA
+    // count; without one (execute on a workspace never planned) nothing runs
+    // and the error word says 2.  Queue entries are range-checked as well,
+    // so a plan of other lengths cannot send a load or store out of bounds.
+    const bool plan_ok = a.sched[5] == kDecodePlanMark && a.sched[6] == a.B &&
+                         a.sched[7] == a.num_ctas && a.sched[0] >= 1 && a.sched[1] >= 1 &&
+                         a.sched[2] >= 0 && a.sched[2] <= a.max_chunks;
+    if (!plan_ok && lane == 0 && blockIdx.x == 0) atomicExch(a.err, 2);
+    const int64_t C = plan_ok ? a.sched[0] : 1, c2 = plan_ok ? a.sched[1] : 1;
+    const int64_t N = plan_ok ? a.sched[2] : 0;
     const int UPB = a.KVN * a.HG;
     int it = 0, ucount = 0;
     // claim the first chunk; every later claim is issued one chunk ahead and
     // only read after the chunk's tiles are queued, so its latency hides
     int64_t g = 0;
-    if (lane == 0) g = atomicAdd(a.claim, 1);
+    if (lane == 0 && plan_ok) g = atomicAdd(a.claim, 1);
     g = __shfl_sync(0xffffffffu, g, 0);
     int4 ent = g < N ? a.queue[g] : make_int4(0, 0, 0, 0);
     bool aborted = false;
@@ -515,6 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int4 ent_n = make_int4(0, 0, 0, 0);
       bool fetched = false;
       const int b = ent.x, ci = ent.y >> 10, w = ent.y & 1023;
+      const bool ent_ok = b >= 0 && b < a.B && ci >= 0 && w < UPB && ent.z >= 0 &&
+                          ent.z <= a.S_kv && ent.w >= 0 && ent.w < a.q_rows;
+      if (!ent_ok && lane == 0) atomicExch(a.err, 2);
       const int64_t u = (int64_t)b * UPB + w;
       const UnitInfo r = unit_from(a, b, w, ent.w, 1, ent.z);
       const int64_t cost = max(1, r.ntiles);
@@ -527,7 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         t_begin = (int)(gm.n1 * C + (ci - gm.n1) * c2);
         t_end = (int)min(cost, t_begin + c2);
       }
-      {  // chunk description + query rows of the group (one bulk copy)
+      if (!ent_ok || ci >= gm.nch) t_begin = t_end = 0;  // nothing of a bad entry runs
+      if (ent_ok && ci < gm.nch) {  // chunk description + query rows of the group (one bulk copy)
         const int qs = ucount & 1;
         wait_or_abort(&qempty[qs], ((ucount >> 1) & 1) ^ 1, a.err, misc);
         if (lane == 0) {
@@ -592,26 +607,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // TMA box.  Pieces are even-length at even rows (block sizes are
         // multiples of 32; contiguous caches have an even length), hence
         // 16-byte aligned.
+        // (a page id outside the pool reads zeros through TMA; its FP8
+        // scales, which come by plain bulk copy, are not read at all)
         int64_t srow = 0;
         int srows = a.box_rows;
+        bool scale_ok = false;
         if constexpr (FP8) {
-          if (mine) srow = scale_row_in(a, r.b, r.hk, blk, jb, jp);
+          scale_ok = mine && (!a.block_table || (blk >= 0 && blk < a.num_blocks));
+          if (scale_ok) srow = scale_row_in(a, r.b, r.hk, blk, jb, jp);
           if (!a.block_table) srows = (int)min((int64_t)a.box_rows, (int64_t)a.S_kv - jb);
         }
-        int nvalid = 0, scale_rows = 0;
-        for (int q = 0; q < nrb; ++q) {
-          const int64_t jq = j0 + (int64_t)q * a.box_rows;
-          if (jq < r.kv_len) {
-            ++nvalid;
-            scale_rows += a.block_table ? a.box_rows : (int)min((int64_t)a.box_rows, (int64_t)a.S_kv - jq);
-          }
-        }
+        int nvalid = 0;
+        for (int q = 0; q < nrb; ++q)
+          if (j0 + (int64_t)q * a.box_rows < r.kv_len) ++nvalid;
+        uint32_t scale_bytes = 0;
+        if constexpr (FP8)
+          scale_bytes = __reduce_add_sync(0xffffffffu, scale_ok ? (uint32_t)(srows * NT * 4) : 0u);
         wait_or_abort(&empty[s], par, a.err, misc);
         if (*reinterpret_cast<volatile int*>(misc)) break;  // issue nothing after a time-out
         uint8_t* st = smem + s * Cfg::kStageBytes;
         if (lane == 0) {
           uint32_t bytes = (uint32_t)(2 * nvalid * Cfg::kNsub * a.box_rows * 128);
-          if constexpr (FP8) bytes += (uint32_t)(2 * scale_rows * NT * 4);
+          if constexpr (FP8) bytes += scale_bytes;
           mbar_arrive_expect_tx(&full[s], bytes);
         }
         __syncwarp();
@@ -622,8 +639,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (FP8) {
             float* sdst = reinterpret_cast<float*>(st + 2 * Cfg::kTileBytes) +
                           isv * (kKvTile * NT) + rb * a.box_rows * NT;
-            bulk_load(sdst, (isv ? a.v_scale : a.k_scale) + srow * NT,
-                      (uint32_t)(srows * NT * 4), &full[s]);
+            if (scale_ok)
+              bulk_load(sdst, (isv ? a.v_scale : a.k_scale) + srow * NT,
+                        (uint32_t)(srows * NT * 4), &full[s]);
           }
         }
         if (!fetched) {
@@ -652,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_trigger();  // this CTA loads nothing more: the combine kernel may launch
     // this CTA claims no more: the last CTA out resets the queue for the
     // next fia_execute with the same plan
-    if (lane == 0) {
+    if (lane == 0 && plan_ok) {
       __threadfence();  // this CTA's last claim is performed before it counts out
       if (atomicAdd(a.claim + 1, 1) == a.num_ctas - 1) {
         a.claim[0] = 0;
@@ -1219,6 +1237,9 @@ __device__ __forceinline__ bool combine_item(const DecodeArgs& a, int64_t pr, in
 // Few chunks per unit: one thread per (item, d-pair), chunks folded in order.
 template <int D>
 __global__ void __launch_bounds__(256, 4) decode_combine_flat(const DecodeArgs a) {
+  if (a.sched[5] != kDecodePlanMark || a.sched[6] != a.B || a.sched[7] != a.num_ctas ||
+      a.sched[4] < 0 || a.sched[4] > a.B)
+    return;  // no plan of these arguments: the decode kernel has reported it
   constexpr int TPP = D / 2, PPB = 256 / TPP;
   // The schedule was complete before the decode kernel started its work, so
   // the first item is located while the decode kernel still runs; only the
@@ -1245,6 +1266,9 @@ __global__ void __launch_bounds__(256, 4) decode_combine_flat(const DecodeArgs a
 // NGRP-th chunk, then group 0 folds the groups in order.
 template <int D>
 __global__ void __launch_bounds__(256, 4) decode_combine_grouped(const DecodeArgs a) {
+  if (a.sched[5] != kDecodePlanMark || a.sched[6] != a.B || a.sched[7] != a.num_ctas ||
+      a.sched[4] < 0 || a.sched[4] > a.B)
+    return;  // no plan of these arguments: the decode kernel has reported it
   constexpr int TPP = D / 2, NGRP = 256 / TPP;
   __shared__ float4 st[NGRP][TPP];
   const int64_t items = a.sched[4] * a.KVN * a.HG * a.GH;

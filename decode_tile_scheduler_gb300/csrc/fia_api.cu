@@ -212,6 +212,9 @@ DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
   a.cu_seqlens_q = p->cu_seqlens_q;
   a.seqused_kv = p->seqused_kv;
   a.S_kv = p->block_table ? (int)kv_capacity(p) : p->max_seqlen_kv;
+  a.q_rows = p->layout == FIA_LAYOUT_TND ? (int64_t)p->total_q
+                                         : (int64_t)p->batch * p->max_seqlen_q;
+  a.num_blocks = p->block_table ? p->num_blocks : 0;
   a.block_table = p->block_table;
   a.max_blocks = p->max_blocks_per_seq;
   a.block_size = p->block_table ? p->block_size : 1;
@@ -276,7 +279,8 @@ fia_status prefill_plan(const fia_params* p, PrefillPlan* pl) {
                              : (int64_t)p->batch * ceil_div(p->max_seqlen_q, kQTile);
   pl->U_max = qtiles * H;
   pl->max_cost = (int)(1 + ceil_div(kv_capacity(p), kKvTile));
-  int64_t off = kAlign;  // [0,4) error word, [8,16) units, [16,24) claim counters
+  int64_t off = kAlign;  // [0,4) error word, [8,16) units, [16,24) claim counters,
+                         // [24,48) the plan's mark, B and CTA count
   pl->off_seq = off;
   off = align_up(off + 8 * ((int64_t)p->batch + 1));
   pl->off_hist = off;
@@ -323,6 +327,7 @@ PrefillArgs prefill_args(const fia_params* p, const PrefillPlan& pl, void* ws) {
   a.seq_prefix = reinterpret_cast<int64_t*>(w + pl.off_seq);
   a.hist = reinterpret_cast<int*>(w + pl.off_hist);
   a.unit_list = reinterpret_cast<int2*>(w + pl.off_list);
+  a.max_units = pl.U_max;
   return a;
 }
 

@@ -28,6 +28,8 @@ struct DecodeArgs {
   const int32_t* cu_seqlens_q;
   const int32_t* seqused_kv;  // may be null (contiguous: S_kv for every batch)
   int S_kv;
+  int64_t q_rows;              // query rows of q/out (B * S_q, or T for TND)
+  int64_t num_blocks;          // pages in the pool (paged caches)
   const int32_t* block_table;  // null: contiguous
   int max_blocks, block_size, box_rows;
   uint32_t bs_magic;           // j / block_size == (j * bs_magic) >> bs_shift, 0 <= j < 2^31
@@ -54,6 +56,11 @@ struct DecodeArgs {
 // Target number of big chunks per persistent CTA in the decode schedule.
 constexpr int kDecodeChunksPerCta = 6;
 constexpr int kSchedHeader = 8;  // int64 header words of the decode schedule
+// header word 5 of a decode plan written by the scheduler (words 6, 7: B and
+// the CTA count): fia_execute runs nothing on a workspace without it
+constexpr int64_t kDecodePlanMark = 0x4649414445434F44LL;
+// the same for a prefill plan, at workspace bytes [24, 48): mark, B, CTA count
+constexpr int64_t kPrefillPlanMark = 0x4649415052454649LL;
 
 struct PrefillArgs {
   int B, QN, KVN, D, G, npairs, per_pair;  // per_pair query heads per unit (2, or 1 if G odd)
@@ -79,6 +86,7 @@ struct PrefillArgs {
   int2* unit_list;        // [units] (b, q_tile | hk << 18 | pair << 26), cost-descending
   int* claim;             // [2]: next unit to claim, CTAs done claiming
   int* err;
+  int64_t max_units;      // bound on the plan's unit count (the unit list's length)
 };
 
 struct SparseArgs {

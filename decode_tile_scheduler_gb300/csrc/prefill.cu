@@ -248,6 +248,9 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(const PrefillArg
   }
   if (tid == 0) {
     *a.num_units = U;
+    a.num_units[2] = kPrefillPlanMark;  // workspace bytes [24, 48): mark, B, CTA count
+    a.num_units[3] = a.B;
+    a.num_units[4] = a.num_ctas;
     a.claim[0] = 0;
     a.claim[1] = 0;
     *a.err = 0;
@@ -321,7 +324,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[1]);
-  const int64_t num_units = *a.num_units;
+  // a plan of these arguments carries the scheduler's mark, B and CTA count;
+  // without one (execute on a workspace never planned) nothing runs and the
+  // error word says 2
+  const bool plan_ok = a.num_units[2] == kPrefillPlanMark && a.num_units[3] == a.B &&
+                       a.num_units[4] == a.num_ctas && *a.num_units >= 0 &&
+                       *a.num_units <= a.max_units;
+  if (!plan_ok && tid == 0 && blockIdx.x == 0) atomicExch(a.err, 2);
+  const int64_t num_units = plan_ok ? *a.num_units : 0;
   // Register split by warpgroup (each role branch below starts with its
   // part): the producer / MMA / guard warpgroup gives registers to the two
   // softmax warpgroups, which keep a whole row of S (128 fp32) in registers.
@@ -343,9 +353,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int ms = ucnt & 1;
       pwait(&mempty[ms], ((ucnt >> 1) & 1) ^ 1, a.err, misc);
       ++ucnt;
-      if (idx >= num_units || *reinterpret_cast<volatile int*>(misc)) {
+      if (idx < 0 || idx >= num_units || *reinterpret_cast<volatile int*>(misc)) {
         if (lane == 0) {
-          if (idx >= num_units) {
+          if (plan_ok && idx >= num_units) {
             // this CTA claims no more: the last CTA out re-arms the counter
             // for the next fia_execute with the same plan
             __threadfence();

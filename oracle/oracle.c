@@ -512,7 +512,9 @@ static int64_t or_tiles(int64_t lo, int64_t hi)
  *   then its remaining c - n1*C tiles in small chunks of c2 tiles (the last
  *   one shorter), n2 of them.
  * Outputs (int64 sched[8 + 3(B+1) + B]): C, c2, N (all chunks), F (big
- * chunks), M (batches whose units have more than one chunk), three zeros;
+ * chunks), M (batches whose units have more than one chunk), the plan's
+ * mark 0x4649414445434F44, B and the CTA count (so that execute can tell a
+ * plan of its arguments from anything else in the workspace);
  * Q[b] = sum over b' < b of (n1+n2)(b')*UPB, then R1[b] (big) and R2[b]
  * (small) the same sums of n1*UPB and n2*UPB, each array with B+1 entries;
  * then the M batches with more than one chunk per unit in increasing order,
@@ -569,7 +571,9 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
     sched[2] = q;
     sched[3] = r1;
     sched[4] = nsplit;
-    sched[5] = sched[6] = sched[7] = 0;
+    sched[5] = 0x4649414445434F44LL;  /* the plan's mark, then B and the CTA count */
+    sched[6] = B;
+    sched[7] = num_ctas;
     if (q > cap) {
         free(cost);
         return -1;

@@ -189,3 +189,28 @@ def test_fp8_long_decode_workload_sampled():
     err = np.abs(o[rows, heads] - ro)
     assert err.max() <= 2e-2 and err.mean() <= 2e-3
     assert np.abs(l[rows, heads] - rl).max() <= 1e-3
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_execute_without_a_plan_runs_nothing(fp8):
+    """fia_execute on a workspace that holds no plan of these arguments (never
+    planned, or overwritten) finds no plan mark: nothing is loaded or written,
+    and the error word reports 2."""
+    import decode_tile_scheduler_gb300 as fia
+    kw = dict(kv_dtype=fi.KV_FP8_E4M3) if fp8 else {}
+    p = fi.make_fia(B=3, QN=16, KVN=2, D=128, q_lens=[1] * 3, kv_lens=[700, 5, 2000],
+                    block_size=64, seed=31, device=dev, **kw)
+    c = fia.FiaCall(p)
+    for fill in (0x00, 0x5A):
+        c.ws.fill_(fill)
+        c.out.fill_(7.0)
+        c.execute()
+        torch.cuda.synchronize()
+        assert c.error_word() == 2
+        assert bool(torch.all(c.out == 7.0))
+    # a plan makes the same workspace usable again
+    c.run()
+    torch.cuda.synchronize()
+    assert c.error_word() == 0
+    ro, rl = oracle.fia(p.to("cpu"))
+    check_close(c.out, c.lse, ro, rl, "after a fresh plan")

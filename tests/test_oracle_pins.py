@@ -466,7 +466,7 @@ def test_decode_schedule_chunks_cover_each_unit_once(ctas, per_cta):
     T = UPB * sum(costs)
     C = max(1, -(-T // (ctas * per_cta)))
     c2 = -(-C // 2)
-    assert list(sched[:2]) == [C, c2] and list(sched[5:8]) == [0, 0, 0]
+    assert list(sched[:2]) == [C, c2] and list(sched[5:8]) == [0x4649414445434F44, p.B, ctas]
     N, F = int(sched[2]), int(sched[3])
     assert N == queue.shape[0] and 0 <= F <= N
     assert N <= ctas * per_cta + 4 * B * UPB             # the workspace bound

@@ -145,3 +145,21 @@ def test_execute_reuses_one_plan():
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
     ro, rl = oracle.fia(p.to("cpu"))
     check_close(outs[1][0], outs[1][1], ro, rl, "plan reuse")
+
+
+def test_execute_without_a_plan_runs_nothing():
+    """The prefill kernel, too, runs nothing without its plan's mark."""
+    import decode_tile_scheduler_gb300 as fia
+    p = fi.make_fia(B=2, QN=8, KVN=2, D=128, q_lens=[300, 77], kv_lens=[300, 77],
+                    layout=fi.LAYOUT_TND, block_size=64, mask_mode=3, seed=33, device=dev)
+    c = fia.FiaCall(p)
+    for fill in (0x00, 0x5A):
+        c.ws.fill_(fill)
+        c.out.fill_(7.0)
+        c.execute()
+        torch.cuda.synchronize()
+        assert c.error_word() == 2
+        assert bool(torch.all(c.out == 7.0))
+    c.run()
+    torch.cuda.synchronize()
+    assert c.error_word() == 0

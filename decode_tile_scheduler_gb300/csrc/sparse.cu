@@ -27,7 +27,8 @@ namespace {
 constexpr int kChunk = 64;                // K~ rows per stage
 constexpr int kHeads = 8;                 // query heads per work item (mma N)
 constexpr int kSCons = 8;                 // consumer warps
-constexpr int kSThreads = 32 * (1 + kSCons);
+constexpr int kSProd = 4;                 // producer warps (warp w gathers the rows r of a chunk with r mod kSProd = w)
+constexpr int kSThreads = 32 * (kSProd + kSCons);
 constexpr int kMdBase = 16;               // metadata: CTA begins from this entry
 constexpr int32_t kMdMagic = 0x46534D32;
 constexpr int kMaxK2 = 2048;              // longest index list (validated on the host)
@@ -173,7 +174,7 @@ struct SparseCfg {
   static constexpr int kOffHdr = kOffList + kMaxK2 * 4;            // per stage: valid rows, last
   static constexpr int kOffBar = kOffHdr + kStages * 16;
   static constexpr int kOffMisc = kOffBar + 8 * (2 * kStages + 2);
-  static constexpr int kSmem = kOffMisc + 16;
+  static constexpr int kSmem = kOffMisc + 16;  // misc: abort flag, -, CSA list length
   static_assert(kStageBytes % 16 == 0 && kOffQ % 16 == 0, "bulk-copy alignment");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
   static_assert(kSmem <= 232448, "shared memory");
@@ -218,8 +219,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __syncthreads();
   if (k_begin >= k_end) return;
 
-  if (warp == 0) {
-    // ======================= producer =======================
+  if (warp < kSProd) {
+    // ======================= producers =======================
+    // Every producer warp walks the same items and chunks; warp pw issues
+    // the copies of the rows r = pw mod kSProd of each chunk (the copies of one
+    // warp are issued one after another, so more warps keep more rows in
+    // flight), warp 0 also the query rows, the CSA compaction and the
+    // stage header.
+    const int pw = warp;
     int32_t* list = reinterpret_cast<int32_t*>(sm + Cfg::kOffList);
     int it = 0, qn = 0;
     bool aborted = false;
@@ -267,46 +274,53 @@ __global__ void __launch_bounds__(kSThreads, 1)
                              ((uint64_t)__ballot_sync(0xffffffffu, ok[1]) << 32);
       // rows without a K~ row are zeroed: their P is 0, and a zero row keeps
       // P V exact whatever an earlier chunk left there
-      for (uint64_t inval = ~valid; inval; inval &= inval - 1) {
+      // (warp 0 alone, so that its arrival orders the zeros for the consumers)
+      for (uint64_t inval = pw == 0 ? ~valid : 0ull; inval; inval &= inval - 1) {
         const int rr = __ffsll((long long)inval) - 1;
         for (int x = lane; x < D / 8; x += 32)
           *reinterpret_cast<uint4*>(st + rr * Cfg::kRowBytes + x * 16) = make_uint4(0, 0, 0, 0);
       }
-      if (lane == 0) {
+      if (pw == 0 && lane == 0) {
         hdr[s].valid = valid;
         hdr[s].last = last ? 1 : 0;
       }
       // the zero rows (generic proxy) precede later bulk copies into them
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(__popcll(valid) * D * 2));
+      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(__popcll(valid) * D * 2));
       __syncwarp();
       const uint16_t* src = cmp ? a.cmp_kv : a.ori_kv;
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2)
-        if (ok[h2]) bulk_load(st + (lane + 32 * h2) * Cfg::kRowBytes, src + off[h2], D * 2, &full[s]);
+        if (ok[h2] && (lane + 32 * h2) % kSProd == pw)
+          bulk_load(st + (lane + 32 * h2) * Cfg::kRowBytes, src + off[h2], D * 2, &full[s]);
       ++it;
     };
 
-    for (int64_t k = k_begin; k < k_end && !aborted; ++k, ++qn) {
+    // (for CSA every producer warp reaches the item's barriers, aborted or not)
+    for (int64_t k = k_begin; k < k_end && (a.mode == 1 || !aborted); ++k, ++qn) {
       const int64_t u = k / a.hgs;
       const int head0 = (int)(k - u * a.hgs) * kHeads;
       const int nh = min(kHeads, a.N1 - head0);
       const SparseRow r = sparse_row(a, u);
       // ---- the item's query rows (once the consumers hold the last item's) ----
-      wait_or_abort(qempty, (qn & 1) ^ 1, a.err, misc);
-      if (*reinterpret_cast<volatile int*>(misc)) break;
-      uint8_t* qs = sm + Cfg::kOffQ;
-      for (int h = nh; h < kHeads; ++h)  // heads past N1 read as zeros
-        for (int x = lane; x < D / 8; x += 32)
-          *reinterpret_cast<uint4*>(qs + h * Cfg::kRowBytes + x * 16) = make_uint4(0, 0, 0, 0);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(qfull, (uint32_t)(nh * D * 2));
-      __syncwarp();
-      if (lane < nh)
-        bulk_load(qs + lane * Cfg::kRowBytes, a.q + (u * a.N1 + head0 + lane) * (int64_t)D, D * 2,
-                  qfull);
+      if (pw == 0) {
+        wait_or_abort(qempty, (qn & 1) ^ 1, a.err, misc);
+        if (*reinterpret_cast<volatile int*>(misc)) aborted = true;
+        uint8_t* qs = sm + Cfg::kOffQ;
+        for (int h = nh; h < kHeads; ++h)  // heads past N1 read as zeros
+          for (int x = lane; x < D / 8; x += 32)
+            *reinterpret_cast<uint4*>(qs + h * Cfg::kRowBytes + x * 16) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (!aborted) {
+          if (lane == 0) mbar_arrive_expect_tx(qfull, (uint32_t)(nh * D * 2));
+          __syncwarp();
+          if (lane < nh)
+            bulk_load(qs + lane * Cfg::kRowBytes, a.q + (u * a.N1 + head0 + lane) * (int64_t)D,
+                      D * 2, qfull);
+        }
+      }
       // ---- window rows [lo, hi] of the original cache ----
       const int64_t lo = max((int64_t)0, r.p - a.win_left);
       const int64_t hi = min(r.S2 - 1, r.p + a.win_right);
@@ -321,10 +335,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
         issue_chunk(r, false, lo, ch * kChunk, nw, last);
         ended |= last;
       }
-      if (aborted) break;
+      // (for CSA the producer warps stop together at the barriers below)
+      if (aborted && a.mode != 1) break;
       // ---- compressed rows ----
       int nk = 0;
       if (a.mode == 1) {
+        // every producer warp is done with the previous item's list (and
+        // all stop together after a time-out)
+        if (named_bar_or(3, 32 * kSProd, aborted)) break;
+      }
+      if (a.mode == 1 && pw == 0) {
         // CSA: the list up to the first negative entry, visible entries kept
         // in order (warp compaction into shared memory)
         const int32_t* ix = a.cmp_sparse_indices + u * (int64_t)a.K2;
@@ -349,7 +369,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
             }
           }
         }
-        __syncwarp();  // the list is read by other lanes below
+        if (lane == 0) misc[2] = nk;
+      }
+      if (a.mode == 1) {
+        // the list and its length are ready for every producer warp
+        if (named_bar_or(3, 32 * kSProd, aborted)) break;
+        nk = *reinterpret_cast<volatile int*>(misc + 2);
       } else if (a.mode == 2) {
         nk = (int)r.vis;
       }
@@ -372,7 +397,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   constexpr int DW = D / kSCons;         // output columns of a warp
   constexpr int MTW = DW / 16;           // their m-tiles
   constexpr int nthr = 32 * kSCons;
-  const int cw = warp - 1, rg = cw & 3, hf = cw >> 2;
+  const int cw = warp - kSProd, rg = cw & 3, hf = cw >> 2;
   const int g = lane >> 2, q4 = lane & 3;
   float* sx = reinterpret_cast<float*>(sm + Cfg::kOffSx);
   float* mxs = reinterpret_cast<float*>(sm + Cfg::kOffMx);

@@ -510,18 +510,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t N = plan_ok ? a.sched[2] : 0;
     const int UPB = a.KVN * a.HG;
     int it = 0, ucount = 0;
-    // claim the first chunk; every later claim is issued one chunk ahead and
-    // only read after the chunk's tiles are queued, so its latency hides
-    int64_t g = 0;
-    if (lane == 0 && plan_ok) g = atomicAdd(a.claim, 1);
-    g = __shfl_sync(0xffffffffu, g, 0);
+    // CTA c starts with queue entry c (no claim on the way to the first
+    // loads); the entries after the first gridDim.x are claimed with the
+    // counter, each claim issued one chunk ahead and read only after the
+    // chunk's tiles are queued, so its latency hides
+    int64_t g = plan_ok ? (int64_t)blockIdx.x : N;
     int4 ent = g < N ? a.queue[g] : make_int4(0, 0, 0, 0);
     bool aborted = false;
     while (g < N) {
       // claim the next chunk now; its result and queue entry are read once
       // the first tile of this chunk is queued, so neither latency is exposed
       int gn_l = 0;
-      if (lane == 0) gn_l = atomicAdd(a.claim, 1);
+      if (lane == 0) gn_l = (int)gridDim.x + atomicAdd(a.claim, 1);
       int64_t gn = N;
       int4 ent_n = make_int4(0, 0, 0, 0);
       bool fetched = false;

@@ -51,6 +51,11 @@ CASES = {
                            pre_tokens=1000, next_tokens=0),
     "fp8_contiguous": dict(B=2, QN=8, KVN=2, D=128, kv_lens=[100, 300], paged=False,
                            kv_dtype=fi.KV_FP8_E4M3),
+    # FP8 with 16 query heads per KV head (two head groups per unit) and with 2
+    "fp8_gqa16": dict(B=2, QN=32, KVN=2, D=128, kv_lens=[900, 130], block_size=128,
+                      kv_dtype=fi.KV_FP8_E4M3, with_sinks=True),
+    "fp8_gqa2": dict(B=3, QN=4, KVN=2, D=128, kv_lens=[700, 1, 64], block_size=32,
+                     kv_dtype=fi.KV_FP8_E4M3),
     # pages of 96 and 272 rows: tiles straddle pages, and the page index of a
     # row is not a shift
     "fp8_bs96": dict(B=3, QN=16, KVN=2, D=128, kv_lens=[1500, 95, 97], block_size=96,

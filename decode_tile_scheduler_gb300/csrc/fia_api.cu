@@ -603,7 +603,7 @@ fia_status sparse_attn_run(const sparse_attn_params* p, const int32_t* metadata,
   SparseArgs a = sparse_args(p, pl, ws);
   if (a.rows == 0) return FIA_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return FIA_ERR_CUDA;
+  // (the kernel clears the status word itself once the metadata checks out)
   return launch_sparse(a, metadata, s) == cudaSuccess ? FIA_OK : FIA_ERR_CUDA;
 }
 

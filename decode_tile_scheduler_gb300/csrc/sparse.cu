@@ -205,6 +205,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (tid == 0) atomicExch(a.err, 2);
     return;
   }
+  // the status word of this call: cleared here (a time-out, the only other
+  // error, is reported seconds later), set to 2 above on a metadata mismatch
+  if (c == 0 && tid == 0) *reinterpret_cast<volatile int*>(a.err) = 0;
   const int64_t k_begin = md[kMdBase + c], k_end = md[kMdBase + c + 1];
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {

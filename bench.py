@@ -135,12 +135,21 @@ def _barrier(ws):
 
 
 def _max_over_ranks(x, ws):
+    """The largest x over the ranks (a step is as slow as its slowest rank)."""
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _job_rate(units_per_rank, step_ms_max, ws):
+    """Whole-job throughput: every rank processes its own replica of the
+    workload (weak scaling), so the job moves ws * units in the slowest
+    rank's step time."""
+    return ws * units_per_rank / (step_ms_max / 1e3)
 
 
 class L2Flush:
@@ -351,7 +360,7 @@ def run_fia(args):
     _barrier(ws)
     ms = _max_over_ranks(statistics.mean(step_ms), ws)
     kern_ms = _max_over_ranks(statistics.mean(exec_ms), ws)
-    value = ws * by / (ms / 1e3) / 1e9
+    value = _job_rate(by, ms, ws) / 1e9
     achieved = by / (kern_ms / 1e3) / 1e9
 
     # ---- end to end through the C ABI with host buffers ----
@@ -394,7 +403,7 @@ def run_fia(args):
             e2e_ms.append(e0.elapsed_time(e1))
     h2d = host_in.numel()
     d2h = host_res.numel()
-    e2e = ws * by / (_max_over_ranks(statistics.mean(e2e_ms), ws) / 1e3) / 1e9
+    e2e = _job_rate(by, _max_over_ranks(statistics.mean(e2e_ms), ws), ws) / 1e9
 
     extras = {}
     if rank == 0 and not args.no_extras:

@@ -78,6 +78,7 @@ EXPORTS = (
     "fia_status_string", "fia_abi_version", "fia_sizeof_params", "fia_sizeof_sparse_params",
     "fia_get_workspace_size", "fia_plan", "fia_execute", "fia_run", "fia_get_plan_layout",
     "sparse_attn_metadata", "sparse_attn_run", "fia_decode_run_noalloc",
+    "fia_selftest_bounded_wait",
 )
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -126,6 +127,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.sparse_attn_run.argtypes = [ctypes.POINTER(SparseParams), _P, _P, ctypes.c_size_t,
                                           _P]
             L.fia_decode_run_noalloc.argtypes = [ctypes.POINTER(FiaParams), _P]
+            L.fia_selftest_bounded_wait.argtypes = [_P, ctypes.c_uint64, _P]
             for f in EXPORTS:
                 if f not in ("fia_status_string", "fia_abi_version", "fia_sizeof_params",
                              "fia_sizeof_sparse_params"):
@@ -181,6 +183,10 @@ def sparse_attn_metadata(p: SparseParams, metadata: int, stream: int = 0) -> int
     _check(lib().sparse_attn_metadata(ctypes.byref(p), metadata, ctypes.byref(n), stream),
            "sparse_attn_metadata")
     return n.value
+
+
+def selftest_bounded_wait(status: int, limit_ns: int, stream: int = 0):
+    _check(lib().fia_selftest_bounded_wait(status, limit_ns, stream), "fia_selftest_bounded_wait")
 
 
 def sparse_attn_run(p: SparseParams, metadata: int, ws: int, nbytes: int, stream: int = 0):

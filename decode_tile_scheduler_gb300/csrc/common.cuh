@@ -70,16 +70,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // that no kernel of this library can spin forever.
 // The global timer is read only every 256 polls: reading it is slow, and a
 // thread busy reading it would notice a completed phase late.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, int* err,
+                                             uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 255u) == 0 && globaltimer_ns() - t0 > FIA_WAIT_TIMEOUT_NS) {
+    if ((n & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
       if (err) atomicExch(err, 1);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  return mbar_wait_ns(bar, parity, err, FIA_WAIT_TIMEOUT_NS);
 }
 
 // ---------------------------------------------------------------------------

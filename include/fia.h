@@ -196,6 +196,18 @@ fia_status fia_run(const fia_params *p, void *workspace, size_t workspace_bytes,
 #define FIA_NOALLOC_SCRATCH_BYTES (8u << 20)
 fia_status fia_decode_run_noalloc(const fia_params *p, void *stream);
 
+/* Self-test of the bounded wait that every pipeline barrier of this library
+ * uses (failure detection without a GPU fault): launches, on `stream`, one
+ * warp that waits on a shared-memory barrier nothing ever completes, with a
+ * time limit of `limit_ns` (1 ms .. 1 s) instead of the pipelines' 2 s.
+ * `status` (device int32 [3], caller-owned) receives: [0] the error word
+ * (1 = the wait gave up, as the pipelines report it), [1] microseconds
+ * waited, [2] 1 if the wait had completed (never).  The kernel returns after
+ * the time-out and the context stays usable.  FIA_ERR_NULL_ARG for a null
+ * status, FIA_ERR_BAD_SHAPE for a limit out of range, FIA_ERR_CUDA if the
+ * launch fails. */
+fia_status fia_selftest_bounded_wait(int32_t *status, uint64_t limit_ns, void *stream);
+
 /* Workspace layout of the plan, for inspection (host-only).
  *
  * Decode schedule (written by fia_plan): work unit u = (b, kv head, head

@@ -219,3 +219,25 @@ def test_execute_without_a_plan_runs_nothing(fp8):
     assert c.error_word() == 0
     ro, rl = oracle.fia(p.to("cpu"))
     check_close(c.out, c.lse, ro, rl, "after a fresh plan")
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable():
+    """Failure detection without a GPU fault: the bounded wait that every
+    pipeline barrier uses gives up on a barrier that nothing completes, sets
+    the error word to 1 and returns; the next launches run normally."""
+    import decode_tile_scheduler_gb300 as fia
+    from decode_tile_scheduler_gb300 import _abi
+    status = torch.full((3,), -1, dtype=torch.int32, device=dev)
+    _abi.selftest_bounded_wait(status.data_ptr(), 20_000_000, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    err, waited_us, completed = status.tolist()
+    assert err == 1 and completed == 0
+    assert 20_000 <= waited_us < 1_000_000          # the 20 ms limit, not longer than a second
+    p = fi.make_fia(B=2, QN=8, KVN=2, D=128, q_lens=[1, 1], kv_lens=[300, 77], block_size=64,
+                    seed=41, device=dev)
+    c = fia.FiaCall(p)
+    c.run()
+    torch.cuda.synchronize()
+    assert c.error_word() == 0
+    ro, rl = oracle.fia(p.to("cpu"))
+    check_close(c.out, c.lse, ro, rl, "after a timed-out wait")

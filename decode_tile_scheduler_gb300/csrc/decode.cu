@@ -369,6 +369,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
     sched[6] = B;
     sched[7] = a.num_ctas;
     a.claim[0] = a.claim[1] = 0;
+    *a.prefill_mark = 0;  // the workspace holds no prefill plan any more
     *a.err = fits ? 0 : 2;  // error word of this plan's execution
   }
   __syncthreads();
@@ -499,12 +500,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ======================= producer =======================
     // A plan of these arguments carries the scheduler's mark, B and CTA
-    // count; without one (execute on a workspace never planned) nothing runs
-    // and the error word says 2.  Queue entries are range-checked as well,
-    // so a plan of other lengths cannot send a load or store out of bounds.
+    // count, and no prefill plan has been written over the workspace since;
+    // without one (execute on a workspace never planned, or planned for the
+    // prefill branch last) nothing runs and the error word says 2.  Queue
+    // entries and partial slots are range-checked as well, so a plan of
+    // other lengths cannot send a load or store out of bounds.
     const bool plan_ok = a.sched[5] == kDecodePlanMark && a.sched[6] == a.B &&
                          a.sched[7] == a.num_ctas && a.sched[0] >= 1 && a.sched[1] >= 1 &&
-                         a.sched[2] >= 0 && a.sched[2] <= a.max_chunks;
+                         a.sched[2] >= 0 && a.sched[2] <= a.max_chunks &&
+                         *a.prefill_mark != kPrefillPlanMark;
     if (!plan_ok && lane == 0 && blockIdx.x == 0) atomicExch(a.err, 2);
     const int64_t C = plan_ok ? a.sched[0] : 1, c2 = plan_ok ? a.sched[1] : 1;
     const int64_t N = plan_ok ? a.sched[2] : 0;
@@ -1192,7 +1196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        float* pp = a.partials + (slot0 + ci * UPB) * pstride;
+        // (clamped: a plan of other lengths cannot move the write out of the
+        // partial slots; the combine rejects such a plan's prefixes)
+        const int64_t slot = min(max(slot0 + ci * UPB, (int64_t)0), a.max_chunks - 1);
+        float* pp = a.partials + slot * pstride;
         for (int idx = ctid; idx < nh * (D + 2); idx += nthr) {
           const int hh = idx / (D + 2), d = idx % (D + 2);
           const float v = d < D ? red[d * 8 + hh] : red_ml[hh * 2 + (d - D)];
@@ -1225,7 +1232,18 @@ __device__ __forceinline__ bool combine_item(const DecodeArgs& a, int64_t pr, in
   const int w = (int)(bw % UPB);
   const int hg = w % a.HG;
   if (it->head >= min(a.GH, a.G - hg * a.GH)) return false;  // past the group's heads
-  const int b = (int)SB[bw / UPB];
+  const int64_t b64 = SB[bw / UPB];
+  // an entry outside the batches or the partial slots (a plan of other
+  // lengths) is skipped: the decode kernel has reported the plan
+  if (b64 < 0 || b64 >= a.B) {
+    atomicExch(a.err, 2);
+    return false;
+  }
+  const int b = (int)b64;
+  if (Q[b] < 0 || Q[b + 1] < Q[b] + UPB || Q[b + 1] > a.max_chunks) {
+    atomicExch(a.err, 2);
+    return false;
+  }
   it->nch = (int)((Q[b + 1] - Q[b]) / UPB);
   it->r.b = b;
   it->r.h0 = (w / a.HG) * a.G + hg * a.GH;
@@ -1238,7 +1256,7 @@ __device__ __forceinline__ bool combine_item(const DecodeArgs& a, int64_t pr, in
 template <int D>
 __global__ void __launch_bounds__(256, 4) decode_combine_flat(const DecodeArgs a) {
   if (a.sched[5] != kDecodePlanMark || a.sched[6] != a.B || a.sched[7] != a.num_ctas ||
-      a.sched[4] < 0 || a.sched[4] > a.B)
+      a.sched[4] < 0 || a.sched[4] > a.B || *a.prefill_mark == kPrefillPlanMark)
     return;  // no plan of these arguments: the decode kernel has reported it
   constexpr int TPP = D / 2, PPB = 256 / TPP;
   // The schedule was complete before the decode kernel started its work, so
@@ -1267,7 +1285,7 @@ __global__ void __launch_bounds__(256, 4) decode_combine_flat(const DecodeArgs a
 template <int D>
 __global__ void __launch_bounds__(256, 4) decode_combine_grouped(const DecodeArgs a) {
   if (a.sched[5] != kDecodePlanMark || a.sched[6] != a.B || a.sched[7] != a.num_ctas ||
-      a.sched[4] < 0 || a.sched[4] > a.B)
+      a.sched[4] < 0 || a.sched[4] > a.B || *a.prefill_mark == kPrefillPlanMark)
     return;  // no plan of these arguments: the decode kernel has reported it
   constexpr int TPP = D / 2, NGRP = 256 / TPP;
   __shared__ float4 st[NGRP][TPP];

@@ -235,6 +235,7 @@ DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
   a.sched = reinterpret_cast<int64_t*>(w + pl.off_sched);
   a.queue = reinterpret_cast<int4*>(w + pl.off_queue);
   a.claim = reinterpret_cast<int*>(w + 16);
+  a.prefill_mark = reinterpret_cast<int64_t*>(w + kWsPrefillMarkOff);
   a.partials = reinterpret_cast<float*>(w + pl.off_part);
   a.err = reinterpret_cast<int*>(w);
   return a;

@@ -49,6 +49,7 @@ struct DecodeArgs {
                                // prefixes R1, R2; the split batches (then -1)
   int4* queue;                 // [max_chunks] (b, chunk << 10 | unit of b, kv_len, qrow)
   int* claim;                  // [2]: next queue entry, CTAs done with the queue
+  int64_t* prefill_mark;       // header word of a prefill plan: a decode plan clears it
   float* partials;             // [max_chunks][GH][D + 2]: acc, then m and l
   int* err;
 };
@@ -61,6 +62,13 @@ constexpr int kSchedHeader = 8;  // int64 header words of the decode schedule
 constexpr int64_t kDecodePlanMark = 0x4649414445434F44LL;
 // the same for a prefill plan, at workspace bytes [24, 48): mark, B, CTA count
 constexpr int64_t kPrefillPlanMark = 0x4649415052454649LL;
+// The first 256 bytes of a workspace are a header that both branches share:
+// [0, 4) error word, [8, 16) prefill unit count, [16, 24) claim counters,
+// [24, 48) prefill plan mark, B and CTA count.  A decode plan clears the
+// prefill mark, and a decode execute runs nothing while that mark is set, so
+// one workspace can serve both branches: an execute after the other branch's
+// plan reports 2 in the error word instead of reading a plan that is gone.
+constexpr int kWsPrefillMarkOff = 24;
 
 struct PrefillArgs {
   int B, QN, KVN, D, G, npairs, per_pair;  // per_pair query heads per unit (2, or 1 if G odd)

@@ -374,16 +374,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
       m.b = pk.x;
       m.t = pk.y & 0x3FFFF;
       m.hk = (pk.y >> 18) & 0xFF;
-      const int pr = (pk.y >> 26) & 0x3F;
+      int pr = (pk.y >> 26) & 0x3F;
+      // an entry that names no unit of these arguments (a unit list of other
+      // lengths) runs as an empty unit: nothing is loaded or written
+      const bool ent_ok = m.b >= 0 && m.b < a.B && m.hk < a.KVN && pr < a.npairs;
+      if (!ent_ok) {
+        if (lane == 0) atomicExch(a.err, 2);
+        m.b = 0;
+        m.hk = 0;
+        pr = 0;
+      }
       m.nslots = a.per_pair;
       m.h0 = m.hk * a.G + pr * a.per_pair;
       m.h1 = m.h0 + 1;
       int64_t qs, ql, kl;
       seq_lengths(a, m.b, &qs, &ql, &kl);
+      const int64_t i0 = (int64_t)m.t * kQTile, i1 = min(i0 + kQTile, ql) - 1;
+      if (!ent_ok || i0 >= ql) ql = 0;  // no query row of the tile exists
       m.q_len = (int)ql;
       m.kv_len = (int)kl;
-      const int64_t i0 = (int64_t)m.t * kQTile, i1 = min(i0 + kQTile, ql) - 1;
-      m.ntiles = tile_span(a, ql, kl, i0, i1, &m.tile0);
+      m.ntiles = ql > 0 ? tile_span(a, ql, kl, i0, i1, &m.tile0) : 0;
+      if (ql <= 0) m.tile0 = 0;
       m.q_row0 = qs + i0;
       m.done = 0;
       m.pad = 0;

@@ -156,6 +156,68 @@ def test_execute_reuses_one_plan():
     check_close(outs[0][0], outs[0][1], ro, rl, "plan reuse")
 
 
+def test_decode_and_prefill_share_a_workspace():
+    """One workspace for a decode and a prefill problem: each branch's plan
+    leaves the other's execute without a plan (the prefill mark in the
+    workspace header, which a decode plan clears), so fia_execute of the
+    branch whose plan was replaced runs nothing (error word 2), and fia_run
+    of either is right."""
+    import decode_tile_scheduler_gb300 as fia
+    pd = fi.make_fia(B=3, QN=16, KVN=2, D=128, q_lens=[1] * 3, kv_lens=[900, 2, 3000],
+                     block_size=64, seed=29, device=dev)
+    pp = fi.make_fia(B=2, QN=8, KVN=2, D=128, q_lens=[300, 64], kv_lens=[300, 64],
+                     layout=fi.LAYOUT_TND, block_size=64, mask_mode=3, seed=37, device=dev)
+    cd = fia.FiaCall(pd, with_lse=True)
+    cp = fia.FiaCall(pp, with_lse=True)
+    ws = torch.empty(max(cd.ws_bytes, cp.ws_bytes), dtype=torch.uint8, device=dev)
+    cd.ws = ws
+    cp.ws = ws
+    rdo, rdl = _ref(pd)
+    rpo, rpl = _ref(pp)
+    for _ in range(2):
+        cp.run()
+        torch.cuda.synchronize()
+        assert cp.error_word() == 0
+        check_close(cp.out, cp.lse, rpo, rpl, "prefill")
+        cd.out.fill_(7.0)
+        cd.execute()  # the decode plan was replaced by the prefill plan
+        torch.cuda.synchronize()
+        assert cd.error_word() == 2
+        assert bool(torch.all(cd.out == 7.0))
+        cd.run()
+        torch.cuda.synchronize()
+        assert cd.error_word() == 0
+        check_close(cd.out, cd.lse, rdo, rdl, "decode")
+        cp.out.fill_(7.0)
+        cp.execute()  # the prefill plan was replaced by the decode plan
+        torch.cuda.synchronize()
+        assert cp.error_word() == 2
+        assert bool(torch.all(cp.out == 7.0))
+
+
+def test_plan_with_slot_prefixes_outside_the_partials():
+    """A plan whose mark matches but whose partial-slot prefix Q points past
+    the partial slots: the split chunks' writes stay inside the slots, the
+    combine rejects every such batch, and the error word says 2.  A fresh
+    plan makes the workspace usable again."""
+    import decode_tile_scheduler_gb300 as fia
+    p = fi.make_fia(B=3, QN=16, KVN=2, D=128, q_lens=[1] * 3, kv_lens=[3000, 5, 2000],
+                    block_size=64, seed=41, device=dev)
+    c = fia.FiaCall(p, with_lse=True, num_sms=4)  # few CTAs: every long unit is split
+    c.plan()
+    lay = c.plan_layout()
+    q = c.ws[lay.sched_off + 64: lay.sched_off + 64 + 8 * (p.B + 1)].view(torch.int64)
+    q.copy_(torch.arange(p.B + 1, device=dev, dtype=torch.int64) + (1 << 40))
+    c.execute()
+    torch.cuda.synchronize()
+    assert c.error_word() == 2
+    c.run()
+    torch.cuda.synchronize()
+    assert c.error_word() == 0
+    ro, rl = _ref(p)
+    check_close(c.out, c.lse, ro, rl, "after a fresh plan")
+
+
 def test_deterministic_bitwise():
     p = fi.make_fia(B=5, QN=32, KVN=8, D=128, q_lens=[1] * 5, kv_lens=[4000, 700, 1, 129, 2500],
                     block_size=128, seed=9, device=dev)

@@ -163,3 +163,29 @@ def test_execute_without_a_plan_runs_nothing():
     c.run()
     torch.cuda.synchronize()
     assert c.error_word() == 0
+
+
+def test_unit_list_entries_outside_the_arguments_run_nothing():
+    """A plan whose mark matches but whose unit entries name no unit of these
+    arguments (batch, KV head or head pair out of range) runs every such
+    entry as an empty unit: nothing is loaded or written, and the error word
+    says 2.  A fresh plan makes the workspace usable again."""
+    import decode_tile_scheduler_gb300 as fia
+    p = fi.make_fia(B=2, QN=8, KVN=2, D=128, q_lens=[300, 77], kv_lens=[300, 77],
+                    layout=fi.LAYOUT_TND, block_size=64, mask_mode=3, seed=35, device=dev)
+    c = fia.FiaCall(p)
+    c.plan()
+    lay = c.plan_layout()
+    n = int(c.ws[8:16].view(torch.int64).item())  # units of the plan
+    assert n > 0
+    c.ws[lay.unit_list_off: lay.unit_list_off + 8 * n].fill_(0x7F)  # batch 0x7F7F7F7F
+    c.out.fill_(7.0)
+    c.execute()
+    torch.cuda.synchronize()
+    assert c.error_word() == 2
+    assert bool(torch.all(c.out == 7.0))
+    c.run()
+    torch.cuda.synchronize()
+    assert c.error_word() == 0
+    ro, rl = oracle.fia(p.to("cpu"))
+    check_close(c.out, c.lse, ro, rl, "after a fresh plan")

@@ -165,10 +165,15 @@ fia_status fia_plan(const fia_params *p, void *workspace, size_t workspace_bytes
  * Deterministic: the same inputs give bitwise the same outputs.
  * Device error word: the first int32 of the workspace is 0 after a clean
  * execute; 1 when a bounded wait inside a kernel gave up (about 2 s; the
- * kernel returned early and the outputs are undefined); 2 when a decode plan
- * held more chunks than the workspace bound (not reachable for validated
- * inputs; nothing ran).  Reading it needs a device-to-host copy after the
- * stream has reached the call. */
+ * kernel returned early and the outputs are undefined); 2 when the
+ * workspace holds no plan of these arguments (never planned, planned with
+ * other shapes, or planned for the other branch since: a decode plan clears
+ * the prefill plan's mark and a decode execute runs nothing while that mark
+ * is set; nothing ran), when a plan entry lies outside these arguments (that
+ * entry ran as empty, its loads and stores kept inside their buffers), or
+ * when a decode plan held more chunks than the workspace bound (not
+ * reachable for validated inputs).  Reading it needs a device-to-host copy
+ * after the stream has reached the call. */
 fia_status fia_execute(const fia_params *p, void *workspace, size_t workspace_bytes,
                        void *stream);
 

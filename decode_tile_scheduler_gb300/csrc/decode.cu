@@ -150,12 +150,19 @@ static_assert(sizeof(UnitMsg) <= 128, "message slot");
 struct ChunkGeom {
   int n1, nch;
 };
+// A unit's cost is below 2^31 and C, c2 matter only up to it, so 32-bit
+// divisions give the 64-bit results (a 64-bit division costs several times
+// more, and this sits on the path to a chunk's first load).
 __device__ __forceinline__ ChunkGeom chunk_geom(int64_t cost, int64_t C, int64_t c2) {
   ChunkGeom g;
-  const int64_t n1 = max((int64_t)0, cost / C - 1);
-  const int64_t rest = cost - n1 * C;
+  const uint32_t c = (uint32_t)cost;
+  const uint32_t Cc = (uint32_t)min(C, (int64_t)0x7fffffff);
+  const uint32_t c2c = (uint32_t)min(c2, (int64_t)0x7fffffff);
+  const uint32_t q = c / Cc;
+  const uint32_t n1 = q > 0 ? q - 1 : 0;
+  const uint32_t rest = c - n1 * Cc;
   g.n1 = (int)n1;
-  g.nch = (int)(n1 + (rest + c2 - 1) / c2);
+  g.nch = (int)(n1 + (rest + c2c - 1) / c2c);
   return g;
 }
 
@@ -230,40 +237,35 @@ __device__ __forceinline__ void finish_head(const DecodeArgs& a, int h, float M,
 // ---------------------------------------------------------------------------
 // scheduler
 // ---------------------------------------------------------------------------
-// Block-wide exclusive scan of four counters over the 1024 threads; returns
-// the block totals in tot[] (every thread).
-__device__ __forceinline__ void scan4(int64_t (&x)[4], int64_t (&tot)[4], int64_t (*ws)[4]) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int64_t incl[4];
+// Block-wide exclusive scan of three 32-bit counters; returns the block
+// totals in tot[] (every thread).  One barrier after the warp totals are
+// stored (each warp then sums the totals before it with a shuffle
+// reduction), one before `ws` is reused.
+__device__ __forceinline__ void scan3(uint32_t (&x)[3], uint32_t (&tot)[3], uint32_t (*ws)[3]) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
+  uint32_t incl[3];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    int64_t v = x[k];
+  for (int k = 0; k < 3; ++k) {
+    uint32_t v = x[k];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int64_t y = __shfl_up_sync(0xffffffffu, v, o);
+      const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
       if (lane >= o) v += y;
     }
     incl[k] = v;
     if (lane == 31) ws[wid][k] = v;
   }
   __syncthreads();
-  if (wid == 0) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      int64_t v = lane < (int)(blockDim.x >> 5) ? ws[lane][k] : 0;
+  for (int k = 0; k < 3; ++k) {
+    const uint32_t wv = lane < nw ? ws[lane][k] : 0u;
+    uint32_t before = lane < wid ? wv : 0u, all = wv;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
-      }
-      ws[lane][k] = v;
+    for (int o = 16; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+      all += __shfl_xor_sync(0xffffffffu, all, o);
     }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int64_t before = wid ? ws[wid - 1][k] : 0;
-    tot[k] = ws[31][k];
+    tot[k] = all;
     x[k] = before + incl[k] - x[k];
   }
   __syncthreads();
@@ -272,13 +274,13 @@ __device__ __forceinline__ void scan4(int64_t (&x)[4], int64_t (&tot)[4], int64_
 constexpr int kSchedSmemBatches = 2048;  // per-batch values kept in shared memory up to this B
 
 __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs a) {
-  __shared__ int64_t ws[32][4];
-  __shared__ int64_t s_total;
+  __shared__ uint32_t ws[32][3];
+  __shared__ int64_t ws_total[32];
   // up to kSchedSmemBatches batches: lengths, costs and queue prefixes stay in
   // shared memory, so the batch arrays are read from global memory once
   __shared__ int s_cost[kSchedSmemBatches], s_kv[kSchedSmemBatches], s_qrow[kSchedSmemBatches];
   __shared__ int sR[2][kSchedSmemBatches + 1];
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   pdl_trigger();  // the decode kernel may set up while the plan is built
   const int B = a.B;
   const bool small = B <= kSchedSmemBatches;
@@ -292,7 +294,6 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
   // total cost (and, for small B, each batch's lengths and cost)
   int64_t part = 0;
   for (int b = tid; b < B; b += blockDim.x) {
-    SB[b] = -1;
     int64_t qrow, ql, kv_len;
     batch_lengths(a, b, &qrow, &ql, &kv_len);
     const UnitInfo r = unit_from(a, b, 0, qrow, ql, kv_len);
@@ -306,65 +307,73 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if (tid == 0) s_total = 0;
-  __syncthreads();
-  if (lane == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&s_total),
-                           (unsigned long long)part);
-  __syncthreads();  // also orders the SB fill before the scatter below
-  const int64_t T = s_total * UPB;
+  if (lane == 0) ws_total[wid] = part;
+  __syncthreads();  // (also publishes the shared-memory batch values)
+  int64_t total = lane < (int)(blockDim.x >> 5) ? ws_total[lane] : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+  const int64_t T = total * UPB;
   const int64_t per = (int64_t)a.num_ctas * a.chunks_per_cta;
-  const int64_t C = max((int64_t)1, (T + per - 1) / per);
+  // C = max(1, ceil(T / per)), with a 32-bit division whenever T allows
+  int64_t C = 1;
+  if (T > 0)
+    C = (T - 1 <= 0xffffffffLL && per <= 0xffffffffLL)
+            ? (int64_t)((uint32_t)(T - 1) / (uint32_t)per) + 1
+            : (T - 1) / per + 1;
   const int64_t c2 = (C + 1) / 2;
 
-  // per batch: chunks of each unit (all, big, small) and whether the batch is
-  // split -> four exclusive scans
-  int64_t carry[4] = {0, 0, 0, 0};
+  // per batch: big and small chunks of its units and whether it is split ->
+  // three exclusive scans (all chunks before b = big + small before b)
+  int64_t carry[3] = {0, 0, 0};
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + tid;
-    int64_t x[4] = {0, 0, 0, 0};
+    uint32_t x[3] = {0u, 0u, 0u};
     if (b < B) {
       const int64_t cost = small ? s_cost[b] : batch_cost(a, b);
       if (cost > 0) {
         const ChunkGeom gm = chunk_geom(cost, C, c2);
-        x[0] = (int64_t)gm.nch * UPB;
-        x[1] = (int64_t)gm.n1 * UPB;
-        x[2] = (int64_t)(gm.nch - gm.n1) * UPB;
-        x[3] = gm.nch > 1;
+        x[0] = (uint32_t)gm.n1 * (uint32_t)UPB;
+        x[1] = (uint32_t)(gm.nch - gm.n1) * (uint32_t)UPB;
+        x[2] = gm.nch > 1;
       }
     }
-    const bool is_split = x[3] != 0;
-    int64_t tot[4];
-    scan4(x, tot, ws);
-    if (b < B && is_split) SB[carry[3] + x[3]] = b;
+    const bool is_split = x[2] != 0;
+    uint32_t tot[3];
+    scan3(x, tot, ws);
+    if (b < B && is_split) SB[carry[2] + x[2]] = b;
     if (b < B) {
-      Q[b] = carry[0] + x[0];
-      R1[b] = carry[1] + x[1];
-      R2[b] = carry[2] + x[2];
+      const int64_t r1 = carry[0] + x[0], r2 = carry[1] + x[1];
+      Q[b] = r1 + r2;
+      R1[b] = r1;
+      R2[b] = r2;
       if (small) {
-        sR[0][b] = (int)(carry[1] + x[1]);
-        sR[1][b] = (int)(carry[2] + x[2]);
+        sR[0][b] = (int)r1;
+        sR[1][b] = (int)r2;
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) carry[k] += tot[k];
+    for (int k = 0; k < 3; ++k) carry[k] += tot[k];
   }
+  // the list of split batches ends with -1 entries
+  for (int64_t b = carry[2] + tid; b < B; b += blockDim.x) SB[b] = -1;
   // N <= n*W + 4*U always holds (the workspace bound); a plan that broke it
   // would run nothing and say so in the error word
-  const bool fits = carry[0] <= a.max_chunks;
-  const int64_t F = fits ? carry[1] : 0, N = fits ? carry[0] : 0;
+  const int64_t n_all = carry[0] + carry[1];
+  const bool fits = n_all <= a.max_chunks;
+  const int64_t F = fits ? carry[0] : 0, N = fits ? n_all : 0;
   if (tid == 0) {
-    Q[B] = carry[0];
-    R1[B] = carry[1];
-    R2[B] = carry[2];
+    Q[B] = n_all;
+    R1[B] = carry[0];
+    R2[B] = carry[1];
     if (small) {
-      sR[0][B] = (int)carry[1];
-      sR[1][B] = (int)carry[2];
+      sR[0][B] = (int)carry[0];
+      sR[1][B] = (int)carry[1];
     }
     sched[0] = C;
     sched[1] = c2;
     sched[2] = N;
     sched[3] = F;
-    sched[4] = fits ? carry[3] : 0;  // split batches
+    sched[4] = fits ? carry[2] : 0;  // split batches
     sched[5] = kDecodePlanMark;  // this plan's mark, B and CTA count
     sched[6] = B;
     sched[7] = a.num_ctas;
@@ -373,21 +382,29 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
     *a.err = fits ? 0 : 2;  // error word of this plan's execution
   }
   __syncthreads();
-  // the claim queue: big chunks, then small chunks
+  // the claim queue: big chunks, then small chunks (queue positions below
+  // 2^31, as the workspace bound implies, take 32-bit arithmetic)
+  const uint32_t upb = (uint32_t)UPB;
   for (int64_t g = tid; g < N; g += blockDim.x) {
-    int b, ci, w;
-    int64_t local;
+    int b;
+    int64_t local, r1 = 0;
     if (g < F) {
       b = small ? find_batch(sR[0], B, g) : find_batch(R1, B, g);
       local = g - (small ? sR[0][b] : R1[b]);
-      ci = (int)(local / UPB);
     } else {
       b = small ? find_batch(sR[1], B, g - F) : find_batch(R2, B, g - F);
       local = g - F - (small ? sR[1][b] : R2[b]);
-      const int64_t r1 = small ? sR[0][b + 1] - sR[0][b] : R1[b + 1] - R1[b];
+      r1 = small ? sR[0][b + 1] - sR[0][b] : R1[b + 1] - R1[b];
+    }
+    int ci, w;
+    if (N <= 0x7fffffffLL) {
+      const uint32_t qd = (uint32_t)local / upb;
+      w = (int)((uint32_t)local - qd * upb);
+      ci = (int)((uint32_t)r1 / upb + qd);
+    } else {
+      w = (int)(local % UPB);
       ci = (int)(r1 / UPB + local / UPB);
     }
-    w = (int)(local % UPB);
     int kv_len, qrow;
     if (small) {
       kv_len = s_kv[b];
@@ -1323,23 +1340,6 @@ __global__ void __launch_bounds__(256, 4) decode_combine_grouped(const DecodeArg
 // ---------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------
-// Launch with programmatic stream serialization: the kernel may begin while
-// the previous kernel on the stream finishes, and waits in pdl_wait().
-template <typename... KArgs, typename... Args>
-static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                              cudaStream_t s, const Args&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
 size_t decode_smem_bytes(int D, int fp8) {
   if (fp8) return DecodeCfg<128, true>::kSmem;
   return D == 64 ? DecodeCfg<64, false>::kSmem : DecodeCfg<128, false>::kSmem;

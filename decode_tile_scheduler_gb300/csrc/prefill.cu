@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(const PrefillArg
   __shared__ int64_t warp_sums[32];
   __shared__ int64_t carry;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  pdl_trigger();  // the prefill kernel may set up while the plan is built
   const int nthr = blockDim.x;
   const int H = a.KVN * a.npairs;
   int64_t* seq_prefix = a.seq_prefix;
@@ -324,6 +325,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[1]);
+  // launched behind the scheduler with programmatic serialization: the
+  // set-up above overlaps it; the plan and the inputs are read from here on
+  pdl_wait();
   // a plan of these arguments carries the scheduler's mark, B and CTA count;
   // without one (execute on a workspace never planned) nothing runs and the
   // error word says 2
@@ -810,8 +814,7 @@ static cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& tq,
     if (e != cudaSuccess) return e;
     done_mask[(dev >> 6) & 3].fetch_or(bit);
   }
-  kern<<<a.num_ctas, kPThreads, Cfg::kSmem, s>>>(a, tq, tk, tv);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.num_ctas), dim3(kPThreads), Cfg::kSmem, s, a, tq, tk, tv);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(1024) sparse_metadata_kernel(const SparseArgs 
   __shared__ int64_t carry;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nthr = blockDim.x;
   const int64_t n = a.num_ctas, G = a.hgs;
+  pdl_trigger();  // the attention kernel may set up while the metadata is built
   for (int k = tid; k < 1024; k += nthr) md[k] = 0;
   // pass 1: total weight
   if (tid == 0) carry = 0;
@@ -188,7 +189,7 @@ struct StageHdr {
 
 template <int D>
 __global__ void __launch_bounds__(kSThreads, 1)
-    sparse_attn_kernel(const SparseArgs a, const int32_t* __restrict__ md) {
+    sparse_attn_kernel(const SparseArgs a, const int32_t* md) {
   using Cfg = SparseCfg<D>;
   constexpr int S = Cfg::kStages;
   extern __shared__ __align__(128) uint8_t sm[];
@@ -200,15 +201,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
   int* misc = reinterpret_cast<int*>(sm + Cfg::kOffMisc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
-  if (md[0] != kMdMagic || md[1] != a.num_ctas || md[2] != (int32_t)a.rows || md[5] != a.B ||
-      md[6] != a.N1 || md[7] != a.K2 || md[12] != kHeads || md[13] != (int32_t)(a.rows * a.hgs)) {
-    if (tid == 0) atomicExch(a.err, 2);
-    return;
-  }
-  // the status word of this call: cleared here (a time-out, the only other
-  // error, is reported seconds later), set to 2 above on a metadata mismatch
-  if (c == 0 && tid == 0) *reinterpret_cast<volatile int*>(a.err) = 0;
-  const int64_t k_begin = md[kMdBase + c], k_end = md[kMdBase + c + 1];
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -220,6 +212,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
     fence_barrier_init();
   }
   __syncthreads();
+  // launched behind the metadata kernel with programmatic serialization: the
+  // set-up above overlaps it, everything below reads its result (and the
+  // inputs of earlier work on the stream).  `md` is a plain pointer: marked
+  // __restrict__ its loads could be hoisted above this wait.
+  pdl_wait();
+  if (md[0] != kMdMagic || md[1] != a.num_ctas || md[2] != (int32_t)a.rows || md[5] != a.B ||
+      md[6] != a.N1 || md[7] != a.K2 || md[12] != kHeads || md[13] != (int32_t)(a.rows * a.hgs)) {
+    if (tid == 0) atomicExch(a.err, 2);
+    return;
+  }
+  // the status word of this call: cleared here (a time-out, the only other
+  // error, is reported seconds later), set to 2 above on a metadata mismatch
+  if (c == 0 && tid == 0) *reinterpret_cast<volatile int*>(a.err) = 0;
+  const int64_t k_begin = md[kMdBase + c], k_end = md[kMdBase + c + 1];
   if (k_begin >= k_end) return;
 
   if (warp < kSProd) {
@@ -616,8 +622,7 @@ static cudaError_t launch_sparse_t(const SparseArgs& a, const int32_t* md, cudaS
     if (e != cudaSuccess) return e;
     done_mask[(dev >> 6) & 3].fetch_or(bit);
   }
-  kern<<<a.num_ctas, kSThreads, Cfg::kSmem, s>>>(a, md);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.num_ctas), dim3(kSThreads), Cfg::kSmem, s, a, md);
 }
 
 cudaError_t launch_sparse(const SparseArgs& a, const int32_t* md, cudaStream_t s) {

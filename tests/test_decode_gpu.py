@@ -218,6 +218,27 @@ def test_plan_with_slot_prefixes_outside_the_partials():
     check_close(c.out, c.lse, ro, rl, "after a fresh plan")
 
 
+def test_execute_waits_for_its_plan_when_queued_behind_busy_work():
+    """The decode kernel is launched behind the scheduler with programmatic
+    serialization and may start while the plan is being written.  Queued
+    behind a busy stream over a poisoned workspace, it still reads only the
+    finished plan: error word 0 and the oracle's outputs, every time."""
+    import decode_tile_scheduler_gb300 as fia
+    p = fi.make_fia(B=5, QN=32, KVN=8, D=128, q_lens=[1] * 5, kv_lens=[4000, 700, 1, 129, 2500],
+                    block_size=128, with_sinks=True, seed=47, device=dev)
+    ro, rl = _ref(p)
+    c = fia.FiaCall(p, with_lse=True)
+    for _ in range(3):
+        c.ws.fill_(0x5A)
+        c.out.fill_(float("nan"))
+        torch.cuda._sleep(2_000_000)
+        c.plan()
+        c.execute()
+        torch.cuda.synchronize()
+        assert c.error_word() == 0
+        check_close(c.out, c.lse, ro, rl, "queued behind busy work")
+
+
 def test_deterministic_bitwise():
     p = fi.make_fia(B=5, QN=32, KVN=8, D=128, q_lens=[1] * 5, kv_lens=[4000, 700, 1, 129, 2500],
                     block_size=128, seed=9, device=dev)

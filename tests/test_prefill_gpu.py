@@ -189,3 +189,25 @@ def test_unit_list_entries_outside_the_arguments_run_nothing():
     assert c.error_word() == 0
     ro, rl = oracle.fia(p.to("cpu"))
     check_close(c.out, c.lse, ro, rl, "after a fresh plan")
+
+
+def test_execute_waits_for_its_plan_when_queued_behind_busy_work():
+    """The prefill kernel is launched behind its scheduler with programmatic
+    serialization and may start while the unit list is being written.
+    Queued behind a busy stream over a poisoned workspace, it still reads
+    only the finished plan: error word 0 and the oracle's outputs."""
+    import decode_tile_scheduler_gb300 as fia
+    p = fi.make_fia(B=3, QN=8, KVN=2, D=128, q_lens=[400, 50, 260], kv_lens=[400, 50, 260],
+                    layout=fi.LAYOUT_TND, block_size=64, mask_mode=3, with_sinks=True, seed=49,
+                    device=dev)
+    ro, rl = oracle.fia(p.to("cpu"))
+    c = fia.FiaCall(p, with_lse=True)
+    for _ in range(3):
+        c.ws.fill_(0x5A)
+        c.out.fill_(float("nan"))
+        torch.cuda._sleep(2_000_000)
+        c.plan()
+        c.execute()
+        torch.cuda.synchronize()
+        assert c.error_word() == 0
+        check_close(c.out, c.lse, ro, rl, "queued behind busy work")

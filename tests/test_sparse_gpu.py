@@ -144,3 +144,25 @@ def test_sparse_metadata_mismatch_is_reported():
     torch.cuda.synchronize()
     assert int(cb.ws[:4].view(torch.int32).item()) == fia.FIA_ERR_BAD_SHAPE
     assert torch.count_nonzero(cb.out) == 0
+
+
+def test_attention_waits_for_its_metadata_when_queued_behind_busy_work():
+    """The attention kernel is launched behind the metadata kernel with
+    programmatic serialization, so it may start while the metadata is still
+    being written.  Queued behind a busy stream (the early start then really
+    happens) over poisoned metadata, it still reads only the finished
+    metadata: status 0 and the oracle's outputs, every time."""
+    import decode_tile_scheduler_gb300 as fia
+    sp = fi.make_sparse(device=dev, seed=61, **CASES["csa_odd_pages"])
+    ro, rl = oracle.sparse(sp.to("cpu"))
+    c = fia.SparseCall(sp, with_lse=True)
+    c.plan()
+    for _ in range(3):
+        c.metadata.fill_(0x5A5A5A5A)
+        c.out.fill_(float("nan"))
+        torch.cuda._sleep(2_000_000)
+        c.plan()
+        c.run()
+        torch.cuda.synchronize()
+        assert int(c.ws[:4].view(torch.int32).item()) == 0
+        check_close(c.out, c.lse, ro, rl, "queued behind busy work")

@@ -13,7 +13,7 @@
 // the chunk size is C = ceil(T / (n * W)) tiles (W chunks per CTA, at least
 // one tile), and a unit of cost c is cut into n1 = max(0, floor(c/C) - 1) big
 // chunks of C tiles followed by the remaining r = c - n1*C tiles (C <= r < 2C
-// unless c < C) in small chunks of c2 = ceil(C/2) tiles.  The claim queue
+// unless c < C) in small chunks of c2 = ceil(C/3) tiles.  The claim queue
 // lists every big chunk (batch-major, then chunk, then unit of the batch)
 // before every small chunk (same order), so the work left at the end is
 // always small pieces.  CTAs claim chunks from the queue with one atomic each:
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
     C = (T - 1 <= 0xffffffffLL && per <= 0xffffffffLL)
             ? (int64_t)((uint32_t)(T - 1) / (uint32_t)per) + 1
             : (T - 1) / per + 1;
-  const int64_t c2 = (C + 1) / 2;
+  const int64_t c2 = (C + 2) / 3;
 
   // per batch: big and small chunks of its units and whether it is split ->
   // three exclusive scans (all chunks before b = big + small before b)
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
   }
   // the list of split batches ends with -1 entries
   for (int64_t b = carry[2] + tid; b < B; b += blockDim.x) SB[b] = -1;
-  // N <= n*W + 4*U always holds (the workspace bound); a plan that broke it
+  // N <= n*W + 6*U always holds (the workspace bound); a plan that broke it
   // would run nothing and say so in the error word
   const int64_t n_all = carry[0] + carry[1];
   const bool fits = n_all <= a.max_chunks;
@@ -1384,11 +1384,11 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUte
                           int fp8, cudaStream_t s) {
   cudaError_t e = launch_decode_main(a, tk, tv, fp8, s);
   if (e != cudaSuccess) return e;
-  // The plan bounds the chunks by n*W + 4*U, so a unit has about n*W/U + 4;
+  // The plan bounds the chunks by n*W + 6*U, so a unit has about n*W/U + 6;
   // with more than 16 an item gets a whole CTA.  The choice depends on shapes
   // only, so results stay deterministic.
   const int64_t items = a.num_units * a.GH;  // bound: every batch split
-  const int64_t est = (int64_t)a.num_ctas * a.chunks_per_cta / a.num_units + 4;
+  const int64_t est = (int64_t)a.num_ctas * a.chunks_per_cta / a.num_units + 6;
   if (est > 16) {
     const int grid = (int)std::min<int64_t>(items, (int64_t)a.num_ctas * 8);
     if (a.D == 64) return launch_pdl(decode_combine_grouped<64>, dim3(grid), dim3(256), 0, s, a);

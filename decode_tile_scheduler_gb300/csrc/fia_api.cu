@@ -168,8 +168,8 @@ struct DecodePlan {
 
 // Decode workspace: [0, 256) error word (offset 0) and the claim counters
 // (offset 16); the schedule; the claim queue; the partial slots.  A unit of cost c gets at most c/C big chunks
-// (so at most n*W over all units) and at most 4 small ones, hence
-// max_chunks = n*W + 4*U bounds the chunks of any lengths.
+// (so at most n*W over all units) and at most 6 small ones, hence
+// max_chunks = n*W + 6*U bounds the chunks of any lengths.
 fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
   int n;
   fia_status st = sm_count(p->num_sms, &n);
@@ -179,7 +179,7 @@ fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
   const int HG = (int)ceil_div(G, GH);
   pl->n = n;
   pl->U = (int64_t)p->batch * p->num_kv_heads * HG;
-  pl->max_chunks = (int64_t)n * kDecodeChunksPerCta + 4 * pl->U;
+  pl->max_chunks = (int64_t)n * kDecodeChunksPerCta + 6 * pl->U;
   int64_t off = kAlign;
   pl->off_sched = off;
   off = align_up(off + 8 * (kSchedHeader + 3 * ((int64_t)p->batch + 1) + p->batch));

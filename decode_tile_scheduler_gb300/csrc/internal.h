@@ -55,7 +55,7 @@ struct DecodeArgs {
 };
 
 // Target number of big chunks per persistent CTA in the decode schedule.
-constexpr int kDecodeChunksPerCta = 6;
+constexpr int kDecodeChunksPerCta = 5;
 constexpr int kSchedHeader = 8;  // int64 header words of the decode schedule
 // header word 5 of a decode plan written by the scheduler (words 6, 7: B and
 // the CTA count): fia_execute runs nothing on a workspace without it

@@ -218,7 +218,7 @@ fia_status fia_selftest_bounded_wait(int32_t *status, uint64_t limit_ns, void *s
  * Decode schedule (written by fia_plan): work unit u = (b, kv head, head
  * group); cost = KV tiles (128 positions) its query row sees, at least 1 (0
  * when the batch has no query row).  With T the total cost, n CTAs and W
- * chunks per CTA, C = max(1, ceil(T / (n W))) and c2 = ceil(C / 2).  A unit
+ * chunks per CTA, C = max(1, ceil(T / (n W))) and c2 = ceil(C / 3).  A unit
  * of cost c gets n1 = max(0, floor(c/C) - 1) chunks of C tiles, then chunks
  * of c2 tiles over the rest.  sched holds int64 {C, c2, chunks N, big chunks
  * F, split batches M, 0, 0, 0}, then Q[B+1] (partial slots before batch b:

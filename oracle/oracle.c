@@ -507,7 +507,7 @@ static int64_t or_tiles(int64_t lo, int64_t hi)
  * a batch has UPB = KVN*HG units, all with the same cost: 0 when the batch has
  * no query row, else the number of KV tiles its single query row can see, at
  * least 1.  With T the sum of all unit costs, n CTAs and W chunks per CTA:
- *   C  = max(1, ceil(T / (n*W))),  c2 = ceil(C/2);
+ *   C  = max(1, ceil(T / (n*W))),  c2 = ceil(C/3);
  *   a unit of cost c has n1 = max(0, floor(c/C) - 1) big chunks of C tiles,
  *   then its remaining c - n1*C tiles in small chunks of c2 tiles (the last
  *   one shorter), n2 of them.
@@ -546,7 +546,7 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
     }
     C = or_ceil_div(T, (int64_t)num_ctas * per_cta);
     if (C < 1) C = 1;
-    c2 = (C + 1) / 2;
+    c2 = (C + 2) / 3;
     for (b = 0; b < B; ++b) {
         int64_t n1 = 0, n2 = 0;
         if (cost[b] > 0) {

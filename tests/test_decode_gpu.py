@@ -102,7 +102,7 @@ def test_schedule_metadata_bit_exact():
         lay = c.plan_layout()
         ws = c.ws.cpu()
         U = lay.num_units
-        per_cta = (lay.max_chunks - 4 * U) // n
+        per_cta = (lay.max_chunks - 6 * U) // n
         nsched = 8 + 3 * (p.B + 1) + p.B
         sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
         rs, rq = oracle.decode_schedule(p.to("cpu"), n, per_cta)
@@ -123,7 +123,7 @@ def test_schedule_many_batches_bit_exact_and_parity():
     c, out, lse = _run(p, 152)
     lay = c.plan_layout()
     ws = c.ws.cpu()
-    per_cta = (lay.max_chunks - 4 * lay.num_units) // 152
+    per_cta = (lay.max_chunks - 6 * lay.num_units) // 152
     nsched = 8 + 3 * (B + 1) + B
     sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
     rs, rq = oracle.decode_schedule(p.to("cpu"), 152, per_cta)

@@ -465,11 +465,11 @@ def test_decode_schedule_chunks_cover_each_unit_once(ctas, per_cta):
     costs = [max(1, -(-k // 128)) for k in kv]          # no mask: every tile, at least 1
     T = UPB * sum(costs)
     C = max(1, -(-T // (ctas * per_cta)))
-    c2 = -(-C // 2)
+    c2 = -(-C // 3)
     assert list(sched[:2]) == [C, c2] and list(sched[5:8]) == [0x4649414445434F44, p.B, ctas]
     N, F = int(sched[2]), int(sched[3])
     assert N == queue.shape[0] and 0 <= F <= N
-    assert N <= ctas * per_cta + 4 * B * UPB             # the workspace bound
+    assert N <= ctas * per_cta + 6 * B * UPB             # the workspace bound
     Q = sched[8:8 + B + 1]
     # batches whose units need a split-KV combine, in order, then -1
     split = [b for b in range(B) if (Q[b + 1] - Q[b]) // UPB > 1]

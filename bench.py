@@ -167,10 +167,12 @@ class L2Flush:
     def zero_(self):
         self.w.zero_()
         torch.sum(self.r, dim=0, out=self.sink[0])
-        # Hold the stream for ~50 us after the flush so that the host has
-        # queued the whole step before its first event runs: the events then
-        # time device work only, never the host's launch latency.
-        torch.cuda._sleep(100_000)
+        # Hold the stream for ~100 us after the flush so that the host has
+        # queued the whole step (two or three C-ABI calls, ~15-20 us each on
+        # the GPU machine's host) before its first event runs: the events then
+        # time device work only, never the host's launch latency (which the
+        # e2e figure includes).
+        torch.cuda._sleep(200_000)
 
 
 def _flush_buf():

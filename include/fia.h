@@ -217,11 +217,12 @@ fia_status fia_selftest_bounded_wait(int32_t *status, uint64_t limit_ns, void *s
  *
  * Decode schedule (written by fia_plan): work unit u = (b, kv head, head
  * group); cost = KV tiles (128 positions) its query row sees, at least 1 (0
- * when the batch has no query row).  With T the total cost, n CTAs and W
+ * when the batch has no query row).  With T the total cost, n CTAs and W = 5
  * chunks per CTA, C = max(1, ceil(T / (n W))) and c2 = ceil(C / 3).  A unit
  * of cost c gets n1 = max(0, floor(c/C) - 1) chunks of C tiles, then chunks
- * of c2 tiles over the rest.  sched holds int64 {C, c2, chunks N, big chunks
- * F, split batches M, 0, 0, 0}, then Q[B+1] (partial slots before batch b:
+ * of c2 tiles over the rest (at most 6), so n W + 6 U bounds the chunks of U
+ * units.  sched holds int64 {C, c2, chunks N, big chunks F, split batches M,
+ * plan mark 0x4649414445434F44, B, CTA count}, then Q[B+1] (partial slots before batch b:
  * chunk i of unit w of batch b owns slot Q[b] + i*UPB + w, UPB = units per
  * batch), then R1[B+1] and R2[B+1] (big and small chunks before batch b),
  * then the M batches whose units have several chunks (ascending; -1 after).  The claim queue lists the

@@ -728,6 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier), so the stop decision is one barrier OR over the consumers
     if (named_bar_or(1, nthr, msg[qs].done || *reinterpret_cast<volatile int*>(misc))) break;
     const UnitInfo r = msg[qs].r;
+    const int kvl = (int)r.kv_len, lo32 = (int)r.lo, hi32 = (int)r.hi;
     const int64_t u = msg[qs].u;
     const int64_t slot0 = a.sched[kSchedHeader + r.b] + (u - (int64_t)r.b * a.KVN * a.HG);
     const int t_begin = msg[qs].t_begin, t_end = msg[qs].t_end;
@@ -790,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     struct PendingPV {
       bool valid;
       int s;
-      int64_t jw;
+      int jw;
       bool tail;
       uint32_t pb[2][NG][2];
       float fct[2][NG][2];
@@ -824,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int sl = 0; sl < 4; ++sl) {
         const int slot = 2 * q4 + (sl & 1) + (sl >> 1) * 8;
         const int row = R0 + rho16(slot);
-        const bool ok = !pp.tail || (pp.jw + rho16(slot) < r.kv_len);
+        const bool ok = !pp.tail || (pp.jw + rho16(slot) < kvl);
 #pragma unroll
         for (int t2 = 0; t2 < 2; ++t2) {
           uint2 x = *reinterpret_cast<const uint2*>(vt + sw128(row, 4 * t2 + (g >> 1)) + 8 * (g & 1));
@@ -865,11 +866,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_or_abort(&full[s], (it / S) & 1, a.err, misc);
       const uint32_t st = smem_base + s * Cfg::kStageBytes;
       const uint8_t* stp = smem + s * Cfg::kStageBytes;
-      const int64_t jw = (int64_t)(r.tile0 + t) * kKvTile + R0;  // first KV row of this warp
-      const bool edge = (jw < r.lo) || (jw + kRowsPerWarp - 1 > r.hi);
-      const bool tail = (jw + kRowsPerWarp > r.kv_len);
+      // KV positions in 32 bits: lengths are int32, so every position and
+      // bound here is below 2^31
+      const int jw = (r.tile0 + t) * kKvTile + R0;  // first KV row of this warp
+      const bool edge = (jw < lo32) || (jw + kRowsPerWarp - 1 > hi32);
+      const bool tail = (jw + kRowsPerWarp > kvl);
       // KV positions of fragment rows g and g+8
-      const int64_t jg0 = jw + rho16(g), jg1 = jw + rho16(g + 8);
+      const int jg0 = jw + rho16(g), jg1 = jw + rho16(g + 8);
 
       // ---------------- S^T = K Q^T  (m = 16 KV rows, n = 8 heads) ----------------
       float sc[NG][4];
@@ -917,8 +920,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 k0 = *reinterpret_cast<const float2*>(ks + rowa * NT);
         float2 k1 = *reinterpret_cast<const float2*>(ks + rowb * NT);
         if (tail) {
-          if (jg0 >= r.kv_len) k0 = make_float2(0.f, 0.f);
-          if (jg1 >= r.kv_len) k1 = make_float2(0.f, 0.f);
+          if (jg0 >= kvl) k0 = make_float2(0.f, 0.f);
+          if (jg1 >= kvl) k1 = make_float2(0.f, 0.f);
         }
 #pragma unroll
         for (int ng = 0; ng < NG; ++ng) {
@@ -930,8 +933,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // ---------------- mask + online softmax per head ----------------
-      const bool ok0 = !(edge || tail) || (jg0 >= r.lo && jg0 <= r.hi);
-      const bool ok1 = !(edge || tail) || (jg1 >= r.lo && jg1 <= r.hi);
+      const bool ok0 = !(edge || tail) || (jg0 >= lo32 && jg0 <= hi32);
+      const bool ok1 = !(edge || tail) || (jg1 >= lo32 && jg1 <= hi32);
       float corr[NG][2];
       // the reference moves only when a score passes it by more than 8 (log2
       // units): p <= 2^8 stays exact enough in 16-bit P, and the
@@ -998,10 +1001,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rows past kv_len may hold anything (even NaN): zero their V lanes
         bool z0 = false, z1 = false, z2 = false, z3 = false;
         if (tail) {
-          z0 = jw + rho16(2 * q4) >= r.kv_len;
-          z1 = jw + rho16(2 * q4 + 1) >= r.kv_len;
-          z2 = jw + rho16(2 * q4 + 8) >= r.kv_len;
-          z3 = jw + rho16(2 * q4 + 9) >= r.kv_len;
+          z0 = jw + rho16(2 * q4) >= kvl;
+          z1 = jw + rho16(2 * q4 + 1) >= kvl;
+          z2 = jw + rho16(2 * q4 + 8) >= kvl;
+          z3 = jw + rho16(2 * q4 + 9) >= kvl;
         }
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
@@ -1032,8 +1035,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 v0 = *reinterpret_cast<const float2*>(vs + rowa * NT);
         float2 v1 = *reinterpret_cast<const float2*>(vs + rowb * NT);
         if (tail) {
-          if (jg0 >= r.kv_len) v0 = make_float2(0.f, 0.f);
-          if (jg1 >= r.kv_len) v1 = make_float2(0.f, 0.f);
+          if (jg0 >= kvl) v0 = make_float2(0.f, 0.f);
+          if (jg1 >= kvl) v1 = make_float2(0.f, 0.f);
         }
         // Warp-wide power-of-two reference per d-tile: 2^(e-127) with e the
         // largest exponent of a V scale seen so far (positive floats order

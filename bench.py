@@ -212,25 +212,100 @@ def _time_steps(fn_plan, fn_exec, steps, flush):
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle baseline
+# CPU oracle baselines (bounded samples of each workload)
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(prob_cpu, bytes_per_run, min_seconds=10.0):
-    import oracle
-    cores = len(os.sched_getaffinity(0))
-    oracle.fia(prob_cpu, cores)  # build + warm
+def _cores():
+    return len(os.sched_getaffinity(0))
+
+
+def _timed_repeats(fn, min_seconds):
+    """Run fn until min_seconds have passed (at least once): (runs, seconds)."""
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle.fia(prob_cpu, cores)
+        fn()
         n += 1
         if time.perf_counter() - t0 >= min_seconds:
             break
-    dt = time.perf_counter() - t0
+    return n, time.perf_counter() - t0
+
+
+def cpu_baseline(prob_cpu, bytes_per_run, min_seconds=10.0):
+    import oracle
+    cores = _cores()
+    oracle.fia(prob_cpu, cores)  # build + warm
+    n, dt = _timed_repeats(lambda: oracle.fia(prob_cpu, cores), min_seconds)
     return {"value": bytes_per_run * n / dt / 1e9, "unit": "GB/s", "cores": cores,
             "kind": "oracle",
             "sample": f"the whole paged GQA decode batch, repeated {n}x ({dt:.1f} s, fp64, "
                       f"OpenMP over output rows)"}
+
+
+def cpu_single_thread(prob_cpu, bytes_per_run):
+    """The same oracle on one thread, one whole pass."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.fia(prob_cpu, 1)
+    dt = time.perf_counter() - t0
+    return {"value": bytes_per_run / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"the whole batch once ({dt:.1f} s)"}
+
+
+def _sample_rows_heads(p, n_pairs, seed):
+    import numpy as np
+    g = np.random.default_rng(seed)
+    rows = g.integers(0, p.rows, n_pairs)
+    heads = g.integers(0, p.QN, n_pairs)
+    return rows, heads
+
+
+def _row_kv(p, rows):
+    """Visible keys of each sampled query row (for the work it stands for)."""
+    out = []
+    cu = None if p.cu_seqlens_q is None else p.cu_seqlens_q.tolist()
+    for r in rows.tolist():
+        if cu is None:
+            b, i = divmod(r, p.S_q)
+        else:
+            b = max(k for k in range(p.B) if cu[k] <= r)
+            i = r - cu[b]
+        ql, kl = p.q_lens[b], p.kv_lens[b]
+        hi = kl - ql + i if p.mask_mode == 3 else kl - 1
+        out.append(max(0, min(hi, kl - 1) + 1))
+    return out
+
+
+def cpu_fp8_decode(p_cpu, min_seconds):
+    """Oracle on a sample of (batch, head) rows of the long FP8 decode; the
+    rate counts the KV bytes those rows stand for (a row's share of its KV
+    head's bytes: 1/G of them)."""
+    import oracle
+    cores = _cores()
+    rows, heads = _sample_rows_heads(p_cpu, 32, 5)
+    G = p_cpu.QN // p_cpu.KVN
+    per_tok = 2 * (p_cpu.D + 4 * (p_cpu.D // 64))
+    by = sum(per_tok * k for k in _row_kv(p_cpu, rows)) / G
+    n, dt = _timed_repeats(lambda: oracle.fia_sample(p_cpu, rows, heads, cores), min_seconds)
+    return {"value": by * n / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"32 (batch, head) rows, repeated {n}x ({dt:.1f} s)"}
+
+
+def cpu_prefill(p_cpu, min_seconds):
+    import oracle
+    cores = _cores()
+    rows, heads = _sample_rows_heads(p_cpu, 256, 7)
+    fl = sum(4 * p_cpu.D * k for k in _row_kv(p_cpu, rows))
+    n, dt = _timed_repeats(lambda: oracle.fia_sample(p_cpu, rows, heads, cores), min_seconds)
+    return {"value": fl * n / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"256 (query row, head) pairs, repeated {n}x ({dt:.1f} s)"}
+
+
+def cpu_sparse(sp_cpu, by, nthreads, min_seconds):
+    import oracle
+    n, dt = _timed_repeats(lambda: oracle.sparse(sp_cpu, nthreads), min_seconds)
+    return {"value": by * n / dt / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"the whole sparse CSA batch, {n}x ({dt:.1f} s)"}
 
 
 # ---------------------------------------------------------------------------
@@ -241,11 +316,14 @@ def _bench_call(call, steps, warmup, flush):
     for _ in range(warmup):
         call.run()
     torch.cuda.synchronize()
-    st, ex = _time_steps(call.plan, call.execute, steps, flush)
-    return statistics.mean(st), statistics.mean(ex)
+    return _time_steps(call.plan, call.execute, steps, flush)
 
 
-def extra_workloads(steps, warmup, flush, peaks):
+def _stats(xs):
+    return statistics.mean(xs), statistics.median(xs)
+
+
+def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds):
     import decode_tile_scheduler_gb300 as fia
     import fia_inputs as fi
     res = {}
@@ -253,14 +331,17 @@ def extra_workloads(steps, warmup, flush, peaks):
     try:
         p = fi.workload_fp8_long_decode(device="cuda")
         call = fia.FiaCall(p, with_lse=True)
-        ms, ex = _bench_call(call, steps, warmup, flush)
+        st, ex = _bench_call(call, steps, warmup, flush)
+        (ms, ms_med), (kms, kms_med) = _stats(st), _stats(ex)
         by = p.kv_bytes_visible()
         res["fp8_long_decode"] = {
             "workload": "B=4, Q_N=64, KV_N=8, D=128, E4M3 KV + fp32/64 scales, kv len ~ "
                         "U[32768,131072], block 128",
-            "ms_per_step": ms, "kernel_ms": ex, "GB/s": by / ms / 1e6,
-            "kernel_GB/s": by / ex / 1e6, "frac_of_hbm": by / ex / 1e6 / peaks["hbm_gbs"],
-            "algorithmic_bytes": by}
+            "ms_per_step": ms, "ms_median": ms_med, "kernel_ms": kms, "kernel_ms_median": kms_med,
+            "GB/s": by / ms / 1e6, "kernel_GB/s": by / kms / 1e6,
+            "frac_of_hbm": by / kms / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": by}
+        if with_cpu:
+            res["fp8_long_decode"]["cpu_baseline"] = cpu_fp8_decode(p.to("cpu"), cpu_seconds)
         del call, p
     except Exception as e:  # not built yet
         res["fp8_long_decode"] = {"unavailable": str(e)[:200]}
@@ -268,14 +349,17 @@ def extra_workloads(steps, warmup, flush, peaks):
     try:
         p = fi.workload_varlen_prefill(device="cuda")
         call = fia.FiaCall(p, with_lse=True)
-        ms, ex = _bench_call(call, steps, warmup, flush)
+        st, ex = _bench_call(call, steps, warmup, flush)
+        (ms, ms_med), (kms, kms_med) = _stats(st), _stats(ex)
         fl = 4 * p.D * p.QN * sum(L * (L + 1) // 2 for L in p.q_lens)
         res["varlen_causal_prefill"] = {
             "workload": "TND B=8, L ~ U[256,4096], Q_N=32, KV_N=8, D=128, paged block 128, "
                         "right-down causal, sinks",
-            "ms_per_step": ms, "kernel_ms": ex, "TFLOP/s": fl / ms / 1e9,
-            "kernel_TFLOP/s": fl / ex / 1e9,
-            "frac_of_bf16": fl / ex / 1e9 / peaks["bf16_tflops"], "flops": fl}
+            "ms_per_step": ms, "ms_median": ms_med, "kernel_ms": kms, "kernel_ms_median": kms_med,
+            "TFLOP/s": fl / ms / 1e9, "kernel_TFLOP/s": fl / kms / 1e9,
+            "frac_of_bf16": fl / kms / 1e9 / peaks["bf16_tflops"], "flops": fl}
+        if with_cpu:
+            res["varlen_causal_prefill"]["cpu_baseline"] = cpu_prefill(p.to("cpu"), cpu_seconds)
         del call, p
     except Exception as e:
         res["varlen_causal_prefill"] = {"unavailable": str(e)[:200]}
@@ -288,14 +372,31 @@ def extra_workloads(steps, warmup, flush, peaks):
             call.run()
         torch.cuda.synchronize()
         st, ex = _time_steps(call.plan, call.run, steps, flush)
+        (ms, ms_med), (kms, kms_med) = _stats(st), _stats(ex)
         by = sp.B * (sp.win_left + 1 + sp.K2) * sp.D * 2
         res["sparse_csa_decode"] = {
             "workload": "B=16, N1=64, D=512, ori 8192 band 127/0, cmp 2048 (ratio 4), top-512",
-            "ms_per_step": statistics.mean(st), "kernel_ms": statistics.mean(ex),
-            "GB/s": by / statistics.mean(st) / 1e6, "kernel_GB/s": by / statistics.mean(ex) / 1e6,
-            "algorithmic_bytes": by}
+            "ms_per_step": ms, "ms_median": ms_med, "kernel_ms": kms, "kernel_ms_median": kms_med,
+            "GB/s": by / ms / 1e6, "kernel_GB/s": by / kms / 1e6,
+            "frac_of_hbm": by / kms / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": by}
+        if with_cpu:
+            spc = sp.to("cpu")
+            res["sparse_csa_decode"]["cpu_baseline"] = cpu_sparse(spc, by, _cores(), cpu_seconds)
+            res["sparse_csa_decode"]["cpu_single_thread"] = cpu_sparse(spc, by, 1, 0.0)
     except Exception as e:
         res["sparse_csa_decode"] = {"unavailable": str(e)[:200]}
+    if with_cpu:
+        try:
+            import oracle
+            t = fi.workload_tiny_prefill(device="cpu")
+            fl = 4 * t.D * t.QN * sum(L * (L + 1) // 2 for L in t.q_lens)
+            oracle.fia(t, 1)
+            n, dt = _timed_repeats(lambda: oracle.fia(t, 1), 1.0)
+            res["tiny_prefill_cpu_single_thread"] = {
+                "value": fl * n / dt / 1e9, "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+                "sample": f"the whole tiny prefill, {n}x ({dt:.1f} s)"}
+        except Exception as e:
+            res["tiny_prefill_cpu_single_thread"] = {"unavailable": str(e)[:200]}
     return res
 
 
@@ -362,6 +463,8 @@ def run_fia(args):
     _barrier(ws)
     ms = _max_over_ranks(statistics.mean(step_ms), ws)
     kern_ms = _max_over_ranks(statistics.mean(exec_ms), ws)
+    ms_med = _max_over_ranks(statistics.median(step_ms), ws)
+    kern_ms_med = _max_over_ranks(statistics.median(exec_ms), ws)
     value = _job_rate(by, ms, ws) / 1e9
     achieved = by / (kern_ms / 1e3) / 1e9
 
@@ -389,31 +492,38 @@ def run_fia(args):
     call_e2e = fia.FiaCall(p, with_lse=True, out=v_out, lse=v_lse)
     host_in = dev_in.cpu().pin_memory()
     host_res = torch.empty(dev_out.numel(), dtype=torch.uint8).pin_memory()
+    # Host wall clock around each step: the copy in, fia_run (host-side
+    # validation, tensor-map encoding and launches through the C ABI) and the
+    # copy out, ending with a stream synchronise.  L2 is flushed and the
+    # stream drained before the clock starts, so nothing queued earlier runs
+    # inside the timed region and no device sleep hides the host's cost.
     s = torch.cuda.current_stream()
     e2e_ms = []
     for i in range(args.warmup + args.steps):
         flush.zero_()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(s)
+        s.synchronize()
+        t0 = time.perf_counter()
         dev_in.copy_(host_in, non_blocking=True)
         call_e2e.run()
         host_res.copy_(dev_out, non_blocking=True)
-        e1.record(s)
-        e1.synchronize()
+        s.synchronize()
+        t1 = time.perf_counter()
         if i >= args.warmup:
-            e2e_ms.append(e0.elapsed_time(e1))
+            e2e_ms.append(1e3 * (t1 - t0))
     h2d = host_in.numel()
     d2h = host_res.numel()
     e2e = _job_rate(by, _max_over_ranks(statistics.mean(e2e_ms), ws), ws) / 1e9
 
     extras = {}
     if rank == 0 and not args.no_extras:
-        extras = extra_workloads(max(3, min(args.steps, 10)), 3, flush, peaks)
+        extras = extra_workloads(max(3, min(args.steps, 50)), 3, flush, peaks,
+                                 not args.no_cpu, min(3.0, args.cpu_seconds))
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        cpu = cpu_baseline(p.to("cpu"), by, min_seconds=args.cpu_seconds)
+        pc = p.to("cpu")
+        cpu = cpu_baseline(pc, by, min_seconds=args.cpu_seconds)
+        cpu["single_thread"] = cpu_single_thread(pc, by)
 
     traffic = _ncu_traffic("decode_kernel_bf16_d128", ["decode.cu", "common.cuh", "internal.h"], by)
     if rank == 0:
@@ -429,7 +539,13 @@ def run_fia(args):
                          "traffic": traffic, "kernel": "decode_kernel<128,bf16> + decode_combine_flat (fia_execute)",
                          "peak_source": peaks["source"] + " (burst copy)"},
             "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "clock": "host wall clock (perf_counter) around "
+                    "H2D copy + fia_run + D2H copy + stream synchronise",
+                    "ms_per_step": statistics.mean(e2e_ms),
+                    "ms_median": statistics.median(e2e_ms)},
+            "timing": {"step_ms_median": ms_med, "kernel_ms_mean": kern_ms,
+                       "kernel_ms_median": kern_ms_med,
+                       "note": "value and ms_per_step: mean of the K timed steps; medians beside"},
             "gpu_launches": 3 * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
@@ -444,7 +560,7 @@ def run_fia(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="fia", choices=["fia", "reference"])
     ap.add_argument("--no-extras", action="store_true")

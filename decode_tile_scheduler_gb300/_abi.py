@@ -25,8 +25,17 @@ LAYOUT_TND = 1
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
 MASK_NONE = 0
+MASK_ALL = 1
+MASK_LEFT_UP_CAUSAL = 2
 MASK_RIGHT_DOWN_CAUSAL = 3
 MASK_BAND = 4
+KV_LAYOUT_BNBSH = 0
+KV_LAYOUT_BNNBSD = 1
+SPARSE_KV_BF16 = 0
+SPARSE_KV_FP8_PACKED = 1
+SPARSE_PACKED_ROW_BYTES = 640
+COMBINE_MAX_PARTS = 16
+ABI_VERSION = 3
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
@@ -47,7 +56,9 @@ class FiaParams(ctypes.Structure):
         ("cu_seqlens_q", _P), ("seqused_kv", _P),
         ("scale", ctypes.c_float), ("mask_mode", _I), ("pre_tokens", _I), ("next_tokens", _I),
         ("sinks", _P),
-        ("num_sms", _I), ("reserved", _I * 7),
+        ("num_sms", _I), ("kv_layout", _I),
+        ("atten_mask", _P), ("mask_batch_stride", _L), ("mask_row_stride", _L),
+        ("reserved", _I * 8),
     ]
 
 
@@ -62,7 +73,17 @@ class SparseParams(ctypes.Structure):
         ("cmp_max_blocks", _I), ("cmp_block_size", _I), ("cmp_num_blocks", _I), ("topk", _I),
         ("cmp_sparse_indices", _P), ("cu_seqlens_q", _P), ("seqused_kv", _P), ("sinks", _P),
         ("softmax_scale", ctypes.c_float), ("cmp_ratio", _I), ("ori_win_left", _I),
-        ("ori_win_right", _I), ("num_sms", _I), ("reserved", _I * 7),
+        ("ori_win_right", _I), ("num_sms", _I), ("kv_dtype", _I), ("tile_size", _I),
+        ("rope_head_dim", _I), ("reserved", _I * 8),
+    ]
+
+
+class CombineParams(ctypes.Structure):
+    _fields_ = [
+        ("n_parts", _I), ("layout", _I), ("batch", _I), ("seqlen_q", _I), ("total_q", _I),
+        ("num_heads", _I), ("head_dim", _I), ("pad0_", _I),
+        ("o_parts", ctypes.POINTER(_P)), ("lse_parts", ctypes.POINTER(_P)),
+        ("out", _P), ("lse", _P), ("reserved", _I * 8),
     ]
 
 
@@ -76,9 +97,10 @@ class FiaPlanLayout(ctypes.Structure):
 # every symbol include/fia.h declares
 EXPORTS = (
     "fia_status_string", "fia_abi_version", "fia_sizeof_params", "fia_sizeof_sparse_params",
+    "fia_sizeof_combine_params",
     "fia_get_workspace_size", "fia_plan", "fia_execute", "fia_run", "fia_get_plan_layout",
     "sparse_attn_metadata", "sparse_attn_run", "fia_decode_run_noalloc",
-    "fia_selftest_bounded_wait",
+    "fia_selftest_bounded_wait", "fia_lse_combine",
 )
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -116,6 +138,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.fia_abi_version.restype = _I
             L.fia_sizeof_params.restype = ctypes.c_size_t
             L.fia_sizeof_sparse_params.restype = ctypes.c_size_t
+            L.fia_sizeof_combine_params.restype = ctypes.c_size_t
             L.fia_get_workspace_size.argtypes = [ctypes.POINTER(FiaParams),
                                                  ctypes.POINTER(ctypes.c_size_t)]
             L.fia_get_plan_layout.argtypes = [ctypes.POINTER(FiaParams),
@@ -126,16 +149,21 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
                                                ctypes.POINTER(ctypes.c_size_t), _P]
             L.sparse_attn_run.argtypes = [ctypes.POINTER(SparseParams), _P, _P, ctypes.c_size_t,
                                           _P]
-            L.fia_decode_run_noalloc.argtypes = [ctypes.POINTER(FiaParams), _P]
+            L.fia_decode_run_noalloc.argtypes = [ctypes.POINTER(FiaParams), _P, _P]
+            L.fia_lse_combine.argtypes = [ctypes.POINTER(CombineParams), _P]
             L.fia_selftest_bounded_wait.argtypes = [_P, ctypes.c_uint64, _P]
             for f in EXPORTS:
                 if f not in ("fia_status_string", "fia_abi_version", "fia_sizeof_params",
-                             "fia_sizeof_sparse_params"):
+                             "fia_sizeof_sparse_params", "fia_sizeof_combine_params"):
                     getattr(L, f).restype = ctypes.c_int
+            if L.fia_abi_version() != ABI_VERSION:
+                raise RuntimeError("libfia ABI version differs from the binding's")
             if L.fia_sizeof_params() != ctypes.sizeof(FiaParams):
                 raise RuntimeError("fia_params layout mismatch between fia.h and the binding")
             if L.fia_sizeof_sparse_params() != ctypes.sizeof(SparseParams):
                 raise RuntimeError("sparse_attn_params layout mismatch")
+            if L.fia_sizeof_combine_params() != ctypes.sizeof(CombineParams):
+                raise RuntimeError("fia_combine_params layout mismatch")
             _lib = L
     return _lib
 
@@ -174,8 +202,15 @@ def fia_run(p: FiaParams, ws: int, nbytes: int, stream: int = 0):
     _check(lib().fia_run(ctypes.byref(p), ws, nbytes, stream), "fia_run")
 
 
-def fia_decode_run_noalloc(p: FiaParams, stream: int = 0):
-    _check(lib().fia_decode_run_noalloc(ctypes.byref(p), stream), "fia_decode_run_noalloc")
+def fia_decode_run_noalloc(p: FiaParams, status: int = 0, stream: int = 0):
+    """`status`: device address of an int32 that receives the run's error word
+    (0 = clean), or 0 for none."""
+    _check(lib().fia_decode_run_noalloc(ctypes.byref(p), status or None, stream),
+           "fia_decode_run_noalloc")
+
+
+def fia_lse_combine(p: CombineParams, stream: int = 0):
+    _check(lib().fia_lse_combine(ctypes.byref(p), stream), "fia_lse_combine")
 
 
 def sparse_attn_metadata(p: SparseParams, metadata: int, stream: int = 0) -> int:

@@ -44,7 +44,12 @@ def make_fia_params(*, q: torch.Tensor, out: torch.Tensor, k_cache: torch.Tensor
                     cu_seqlens_q: Optional[torch.Tensor] = None,
                     seqused_kv: Optional[torch.Tensor] = None, scale: Optional[float] = None,
                     mask_mode: int = _abi.MASK_NONE, pre_tokens: int = 0, next_tokens: int = 0,
-                    sinks: Optional[torch.Tensor] = None, num_sms: int = 0) -> FiaParams:
+                    sinks: Optional[torch.Tensor] = None, num_sms: int = 0,
+                    kv_layout: int = _abi.KV_LAYOUT_BNBSH,
+                    atten_mask: Optional[torch.Tensor] = None) -> FiaParams:
+    """`atten_mask`: int8/uint8/bool [B or 1, rows, cols] (nonzero = masked
+    out), rows >= the query length, cols a multiple of 16 >= the KV capacity;
+    a first dimension of 1 is shared by every batch."""
     for name, t in (("q", q), ("out", out), ("k_cache", k_cache), ("v_cache", v_cache)):
         _contig(t, name)
     p = FiaParams()
@@ -63,6 +68,14 @@ def make_fia_params(*, q: torch.Tensor, out: torch.Tensor, k_cache: torch.Tensor
     p.mask_mode, p.pre_tokens, p.next_tokens = mask_mode, pre_tokens, next_tokens
     p.sinks = _ptr(sinks)
     p.num_sms = num_sms
+    p.kv_layout = kv_layout
+    if atten_mask is not None:
+        _contig(atten_mask, "atten_mask")
+        if atten_mask.dim() != 3 or atten_mask.element_size() != 1:
+            raise ValueError("atten_mask must be a 3-d tensor of 1-byte elements")
+        p.atten_mask = _ptr(atten_mask)
+        p.mask_row_stride = int(atten_mask.stride(1))
+        p.mask_batch_stride = 0 if atten_mask.shape[0] == 1 else int(atten_mask.stride(0))
     return p
 
 
@@ -79,7 +92,8 @@ def params_from_problem(prob, out: torch.Tensor, lse: Optional[torch.Tensor],
         max_seqlen_kv=0 if prob.block_table is not None else prob.S_kv,
         cu_seqlens_q=prob.cu_seqlens_q, seqused_kv=prob.seqused_kv, scale=prob.scale,
         mask_mode=prob.mask_mode, pre_tokens=prob.pre_tokens, next_tokens=prob.next_tokens,
-        sinks=prob.sinks, num_sms=num_sms)
+        sinks=prob.sinks, num_sms=num_sms, kv_layout=getattr(prob, "kv_layout", 0),
+        atten_mask=getattr(prob, "atten_mask", None))
 
 
 def lse_shape(prob):
@@ -148,6 +162,9 @@ def sparse_params_from_problem(sp, out: torch.Tensor, lse: Optional[torch.Tensor
     p.cmp_ratio = sp.cmp_ratio if sp.cmp_kv is not None else 1
     p.ori_win_left, p.ori_win_right = sp.win_left, sp.win_right
     p.num_sms = num_sms
+    p.kv_dtype = getattr(sp, "kv_dtype", _abi.SPARSE_KV_BF16)
+    if p.kv_dtype == _abi.SPARSE_KV_FP8_PACKED:
+        p.tile_size, p.rope_head_dim = 64, 64
     return p
 
 
@@ -177,3 +194,33 @@ class SparseCall:
         _abi.sparse_attn_run(self.params, self.metadata.data_ptr(), self.ws.data_ptr(),
                              self.ws_bytes, _stream(stream))
         return self.out, self.lse
+
+
+# ----------------------------------------------------------------------------
+# log-sum-exp combine of partial results (context parallelism over the keys)
+# ----------------------------------------------------------------------------
+
+def lse_combine(outs, lses, *, layout: int, num_heads: int, batch: int = 0, seqlen_q: int = 0,
+                total_q: int = 0, out: Optional[torch.Tensor] = None,
+                lse: Optional[torch.Tensor] = None, stream=None):
+    """Combine results of the same query rows against disjoint key sets with
+    fia_lse_combine.  `outs` are bf16 tensors in the FIA out layout, `lses`
+    the matching fp32 lse tensors.  Returns (out, lse)."""
+    import ctypes
+    n = len(outs)
+    if n != len(lses) or not 1 <= n <= _abi.COMBINE_MAX_PARTS:
+        raise ValueError("one lse per part, 1..16 parts")
+    for t in list(outs) + list(lses):
+        _contig(t, "part")
+    out = torch.empty_like(outs[0]) if out is None else out
+    lse = torch.empty_like(lses[0]) if lse is None else lse
+    c = _abi.CombineParams()
+    c.n_parts, c.layout, c.batch, c.seqlen_q, c.total_q = n, layout, batch, seqlen_q, total_q
+    c.num_heads, c.head_dim = num_heads, int(outs[0].shape[-1])
+    o_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in outs])
+    l_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in lses])
+    c.o_parts = ctypes.cast(o_arr, ctypes.POINTER(ctypes.c_void_p))
+    c.lse_parts = ctypes.cast(l_arr, ctypes.POINTER(ctypes.c_void_p))
+    c.out, c.lse = _ptr(out), _ptr(lse)
+    _abi.fia_lse_combine(c, _stream(stream))
+    return out, lse

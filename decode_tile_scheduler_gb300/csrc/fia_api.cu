@@ -96,9 +96,13 @@ fia_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, in
 // ---------------------------------------------------------------------------
 bool is_decode(const fia_params* p) { return p->max_seqlen_q == 1; }
 
+int64_t kv_capacity_of(const fia_params* p) {
+  return p->block_table ? (int64_t)p->max_blocks_per_seq * p->block_size : p->max_seqlen_kv;
+}
+
 fia_status validate(const fia_params* p) {
   if (!p) return FIA_ERR_NULL_ARG;
-  for (int i = 0; i < 7; ++i)
+  for (int i = 0; i < 8; ++i)
     if (p->reserved[i] != 0) return FIA_ERR_BAD_SHAPE;
   if (p->batch < 1 || p->batch > 65536) return FIA_ERR_BAD_SHAPE;
   if (p->num_q_heads < 1 || p->num_q_heads > 256) return FIA_ERR_BAD_SHAPE;
@@ -113,9 +117,19 @@ fia_status validate(const fia_params* p) {
     if (!p->cu_seqlens_q) return FIA_ERR_NULL_ARG;
   }
   if (p->kv_dtype != FIA_KV_BF16 && p->kv_dtype != FIA_KV_FP8_E4M3) return FIA_ERR_BAD_DTYPE;
-  if (p->mask_mode != FIA_MASK_NONE && p->mask_mode != FIA_MASK_RIGHT_DOWN_CAUSAL &&
-      p->mask_mode != FIA_MASK_BAND)
+  if (p->mask_mode < FIA_MASK_NONE || p->mask_mode > FIA_MASK_BAND) return FIA_ERR_BAD_SHAPE;
+  // an explicit mask goes with modes 0 and 1 only; mode 1 needs one
+  if (p->mask_mode == FIA_MASK_ALL && !p->atten_mask) return FIA_ERR_NULL_ARG;
+  if (p->atten_mask && p->mask_mode != FIA_MASK_NONE && p->mask_mode != FIA_MASK_ALL)
     return FIA_ERR_BAD_SHAPE;
+  if (p->atten_mask) {
+    if (!aligned16(p->atten_mask) || p->mask_row_stride <= 0 || p->mask_row_stride % 16 ||
+        p->mask_batch_stride < 0)
+      return FIA_ERR_BAD_SHAPE;
+  }
+  if (p->kv_layout != FIA_KV_LAYOUT_BNBSH && p->kv_layout != FIA_KV_LAYOUT_BNNBSD)
+    return FIA_ERR_BAD_SHAPE;
+  if (p->kv_layout == FIA_KV_LAYOUT_BNNBSD && !p->block_table) return FIA_ERR_BAD_SHAPE;
   if (p->mask_mode == FIA_MASK_BAND && (int64_t)p->pre_tokens + p->next_tokens < 0)
     return FIA_ERR_BAD_SHAPE;
   if (!std::isfinite(p->scale)) return FIA_ERR_BAD_SHAPE;
@@ -149,16 +163,21 @@ fia_status validate(const fia_params* p) {
     if (p->max_seqlen_kv < 0 || p->max_seqlen_kv > 20971520) return FIA_ERR_BAD_SHAPE;
     if ((int64_t)p->batch * p->max_seqlen_kv > INT32_MAX) return FIA_ERR_BAD_SHAPE;
   }
+  if (p->atten_mask) {
+    // every row of a sequence reaches the mask row of its query index, and
+    // every key position below the KV capacity
+    if (p->mask_row_stride < kv_capacity_of(p)) return FIA_ERR_BAD_SHAPE;
+  }
   // what is built
   if (p->head_dim != 64 && p->head_dim != 128) return FIA_ERR_UNSUPPORTED;
+  if (p->atten_mask || p->mask_mode == FIA_MASK_ALL || p->mask_mode == FIA_MASK_LEFT_UP_CAUSAL ||
+      p->kv_layout != FIA_KV_LAYOUT_BNBSH)
+    return FIA_ERR_UNSUPPORTED;
   if (p->kv_dtype == FIA_KV_FP8_E4M3 && (p->head_dim != 128 || !is_decode(p)))
     return FIA_ERR_UNSUPPORTED;
   return FIA_OK;
 }
 
-int64_t kv_capacity(const fia_params* p) {
-  return p->block_table ? (int64_t)p->max_blocks_per_seq * p->block_size : p->max_seqlen_kv;
-}
 
 struct DecodePlan {
   int n;
@@ -211,7 +230,7 @@ DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
   a.lse = p->lse;
   a.cu_seqlens_q = p->cu_seqlens_q;
   a.seqused_kv = p->seqused_kv;
-  a.S_kv = p->block_table ? (int)kv_capacity(p) : p->max_seqlen_kv;
+  a.S_kv = p->block_table ? (int)kv_capacity_of(p) : p->max_seqlen_kv;
   a.q_rows = p->layout == FIA_LAYOUT_TND ? (int64_t)p->total_q
                                          : (int64_t)p->batch * p->max_seqlen_q;
   a.num_blocks = p->block_table ? p->num_blocks : 0;
@@ -279,7 +298,7 @@ fia_status prefill_plan(const fia_params* p, PrefillPlan* pl) {
                              ? ceil_div(p->total_q, kQTile) + p->batch
                              : (int64_t)p->batch * ceil_div(p->max_seqlen_q, kQTile);
   pl->U_max = qtiles * H;
-  pl->max_cost = (int)(1 + ceil_div(kv_capacity(p), kKvTile));
+  pl->max_cost = (int)(1 + ceil_div(kv_capacity_of(p), kKvTile));
   int64_t off = kAlign;  // [0,4) error word, [8,16) units, [16,24) claim counters,
                          // [24,48) the plan's mark, B and CTA count
   pl->off_seq = off;
@@ -309,7 +328,7 @@ PrefillArgs prefill_args(const fia_params* p, const PrefillPlan& pl, void* ws) {
   a.lse = p->lse;
   a.cu_seqlens_q = p->cu_seqlens_q;
   a.seqused_kv = p->seqused_kv;
-  a.S_kv = p->block_table ? (int)kv_capacity(p) : p->max_seqlen_kv;
+  a.S_kv = p->block_table ? (int)kv_capacity_of(p) : p->max_seqlen_kv;
   a.block_table = p->block_table;
   a.max_blocks = p->max_blocks_per_seq;
   a.block_size = p->block_table ? p->block_size : 1;
@@ -353,8 +372,13 @@ struct SparsePlan {
 
 fia_status sparse_validate(const sparse_attn_params* p) {
   if (!p) return FIA_ERR_NULL_ARG;
-  for (int i = 0; i < 7; ++i)
+  for (int i = 0; i < 8; ++i)
     if (p->reserved[i] != 0) return FIA_ERR_BAD_SHAPE;
+  if (p->kv_dtype != FIA_SPARSE_KV_BF16 && p->kv_dtype != FIA_SPARSE_KV_FP8_PACKED)
+    return FIA_ERR_BAD_DTYPE;
+  if (p->kv_dtype == FIA_SPARSE_KV_FP8_PACKED &&
+      (p->head_dim != 512 || p->tile_size != 64 || p->rope_head_dim != 64))
+    return FIA_ERR_BAD_SHAPE;
   if (p->batch < 1 || p->batch > 65536) return FIA_ERR_BAD_SHAPE;
   if (p->num_q_heads < 1 || p->num_q_heads > 128 || (p->num_q_heads & (p->num_q_heads - 1)))
     return FIA_ERR_BAD_SHAPE;
@@ -387,6 +411,7 @@ fia_status sparse_validate(const sparse_attn_params* p) {
     return FIA_ERR_BAD_SHAPE;  // indices without a compressed cache
   }
   if (p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512) return FIA_ERR_UNSUPPORTED;
+  if (p->kv_dtype == FIA_SPARSE_KV_FP8_PACKED) return FIA_ERR_UNSUPPORTED;
   return FIA_OK;
 }
 

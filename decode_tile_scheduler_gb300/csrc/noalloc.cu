@@ -17,45 +17,47 @@
 // (the scheduler kernel resets the error word and the claim counters), so
 // a stale plan never leaks into a new call; but two calls whose work
 // overlaps on the GPU (different streams without ordering) race on the array.
-#include <mutex>
-
+// The array's first int32 is the run's error word; the caller gets a copy of
+// it through `status`, since it has no address of its own for the array.
 #include "../../include/fia.h"
 
 namespace {
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[FIA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 256;
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address has to come from
-// cudaGetSymbolAddress, looked up once per device with that device current.
+// Device address of the scratch array in the current context.  In host code
+// the array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress.  It is looked up on every call: after a device reset
+// or in another context on the same device the module is loaded again, at
+// another address, and a cached pointer would dangle.
 fia_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FIA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return FIA_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FIA_ERR_CUDA;
-    g_noalloc_addr[dev] = p;
-  }
-  *out = g_noalloc_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FIA_ERR_CUDA;
+  *out = p;
   return FIA_OK;
 }
 
 }  // namespace
 
-extern "C" fia_status fia_decode_run_noalloc(const fia_params* p, void* stream) {
+extern "C" fia_status fia_decode_run_noalloc(const fia_params* p, int32_t* status, void* stream) {
   fia_plan_layout lay;
   fia_status st = fia_get_plan_layout(p, &lay);
   if (st != FIA_OK) return st;
-  if (lay.branch != 1 && lay.total_bytes > 256) return FIA_ERR_UNSUPPORTED;  // decode only
+  if (lay.branch == 2) return FIA_ERR_UNSUPPORTED;  // decode only
   if (lay.total_bytes > (int64_t)FIA_NOALLOC_SCRATCH_BYTES) return FIA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (lay.branch == 0) {  // no query row: nothing runs, and nothing failed
+    if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess)
+      return FIA_ERR_CUDA;
+    return FIA_OK;
+  }
   void* scratch = nullptr;
   st = scratch_address(&scratch);
   if (st != FIA_OK) return st;
-  return fia_run(p, scratch, FIA_NOALLOC_SCRATCH_BYTES, stream);
+  st = fia_run(p, scratch, FIA_NOALLOC_SCRATCH_BYTES, stream);
+  if (st != FIA_OK) return st;
+  if (status && cudaMemcpyAsync(status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=
+                    cudaSuccess)
+    return FIA_ERR_CUDA;
+  return FIA_OK;
 }

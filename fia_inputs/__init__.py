@@ -31,8 +31,14 @@ LAYOUT_TND = 1
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
 MASK_NONE = 0
+MASK_ALL = 1
+MASK_LEFT_UP_CAUSAL = 2
 MASK_RIGHT_DOWN_CAUSAL = 3
 MASK_BAND = 4
+KV_LAYOUT_BNBSH = 0
+KV_LAYOUT_BNNBSD = 1
+SPARSE_KV_BF16 = 0
+SPARSE_KV_FP8_PACKED = 1
 
 N_SPARE_BLOCKS = 8
 FP8_TILE = 64
@@ -68,6 +74,8 @@ class FiaProblem:
     sinks: Optional[torch.Tensor] = None   # fp32 [QN]
     q_lens: Optional[list] = None          # host copy of query lengths
     kv_lens: Optional[list] = None         # host copy of KV lengths
+    kv_layout: int = KV_LAYOUT_BNBSH       # paged pools: [nb,bs,KVN,D] or [nb,KVN,bs,D]
+    atten_mask: Optional[torch.Tensor] = None  # uint8 [B or 1, rows, cols], 1 = hidden
 
     @property
     def max_blocks(self) -> int:
@@ -100,9 +108,10 @@ class FiaProblem:
             if ql == 0 or kl == 0:
                 out.append(0)
                 continue
-            p0, p1 = kl - ql, kl - 1
+            off = 0 if self.mask_mode == MASK_LEFT_UP_CAUSAL else kl - ql
+            p0, p1 = off, off + ql - 1
             lo = p0 - self.pre_tokens if self.mask_mode == MASK_BAND else 0
-            hi = (p1 if self.mask_mode == MASK_RIGHT_DOWN_CAUSAL else
+            hi = (p1 if self.mask_mode in (MASK_RIGHT_DOWN_CAUSAL, MASK_LEFT_UP_CAUSAL) else
                   p1 + self.next_tokens if self.mask_mode == MASK_BAND else kl - 1)
             lo, hi = max(lo, 0), min(hi, kl - 1)
             out.append(max(0, hi - lo + 1))
@@ -136,6 +145,7 @@ class SparseProblem:
     win_right: int = 0
     q_lens: Optional[list] = None
     kv_lens: Optional[list] = None
+    kv_dtype: int = SPARSE_KV_BF16   # packed FP8: uint8 pools [nb, bs, 1, 640]
 
     @property
     def rows(self) -> int:
@@ -177,6 +187,33 @@ def quantize_e4m3_per_tile(x: torch.Tensor, tile: int = FP8_TILE):
     y = (xt / scale.unsqueeze(-1)).clamp_(-FP8_MAX, FP8_MAX)
     codes = y.to(torch.float8_e4m3fn).view(torch.uint8).reshape(shp)
     return codes.contiguous(), scale.contiguous()
+
+
+def pack_fp8_sparse_rows(x: torch.Tensor) -> torch.Tensor:
+    """Pack bf16 K~ rows [..., 512] into the 640-byte shared-KV rows of the
+    kv_quant_sparse_attn_sharedkv format: the first 64 values (rope) kept as
+    bf16 (128 bytes), the other 448 (nope) as E4M3 codes (448 bytes) with one
+    E8M0 scale per 64 of them (7 bytes: 2^(e - 127)), zero padding after.
+    The scale of a tile is the smallest power of two s with amax / s <= 448
+    (1 for an all-zero tile); codes are RNE(x / s) in fp32 from the bf16
+    source.  This is the cache-write side of the format."""
+    shp = x.shape
+    assert shp[-1] == 512
+    xf = x.float().reshape(-1, 512)
+    rows = xf.shape[0]
+    out = torch.zeros((rows, 640), dtype=torch.uint8, device=x.device)
+    out[:, :128] = x.reshape(-1, 512)[:, :64].contiguous().view(torch.uint8).reshape(rows, 128)
+    nope = xf[:, 64:].reshape(rows, 7, 64)
+    amax = nope.abs().amax(dim=-1)
+    e = torch.where(amax > 0, torch.ceil(torch.log2(amax / FP8_MAX)), torch.zeros_like(amax))
+    # log2 may round: make sure amax / 2^e <= 448 and amax / 2^(e-1) > 448
+    e = torch.where((amax > 0) & (amax / torch.exp2(e) > FP8_MAX), e + 1, e)
+    e = torch.where((amax > 0) & (amax / torch.exp2(e - 1) <= FP8_MAX), e - 1, e)
+    e = e.clamp(-127, 127)
+    y = (nope / torch.exp2(e).unsqueeze(-1)).clamp(-FP8_MAX, FP8_MAX)
+    out[:, 128:576] = y.to(torch.float8_e4m3fn).view(torch.uint8).reshape(rows, 448)
+    out[:, 576:583] = (e + 127).to(torch.uint8)
+    return out.reshape(*shp[:-1], 640)
 
 
 def scales_head_major(scales: torch.Tensor) -> torch.Tensor:
@@ -227,10 +264,19 @@ def _valid_row_mask(kv_lens, block_size, placed, num_blocks):
 def make_fia(*, B, QN, KVN, D, q_lens, kv_lens, layout=LAYOUT_BSND, paged=True,
              block_size=128, kv_dtype=KV_BF16, mask_mode=MASK_NONE, pre_tokens=0,
              next_tokens=0, with_sinks=False, scale=None, seed=0, device="cpu",
-             poison=True, max_blocks=None, S_kv=None) -> FiaProblem:
+             poison=True, max_blocks=None, S_kv=None, q_mult=None, kv_layout=KV_LAYOUT_BNBSH,
+             mask_density=None, mask_shared=False, mask_full_rows=0) -> FiaProblem:
     """Build one FIA problem.  `q_lens`/`kv_lens` are host lists of length B
     (for BSND all q_lens must be equal).  `paged=False` gives a contiguous
-    BSND KV cache [B, S_kv, KVN, D]."""
+    BSND KV cache [B, S_kv, KVN, D].  `q_mult` (a power of two, or one per
+    query head) multiplies Q after it is drawn and rounded: powers of two
+    scale bf16 exactly, so the draws and every other tensor stay the same.
+    `kv_layout=KV_LAYOUT_BNNBSD` stores paged pools as [nb, KVN, bs, D].
+    `mask_density` (modes 0/1) adds an explicit uint8 mask [B (or 1 with
+    `mask_shared`), max query length, KV capacity rounded up to 16] with that
+    fraction of ones (hidden keys), drawn after everything else from the CPU
+    generator; `mask_full_rows` of its rows (row i of batch 0, i = 0, 1, ...)
+    are then hidden entirely."""
     gen_cpu = torch.Generator().manual_seed(seed)
     gdev = _dev_gen(device, seed + 1)
     q_lens = [int(x) for x in q_lens]
@@ -246,6 +292,12 @@ def make_fia(*, B, QN, KVN, D, q_lens, kv_lens, layout=LAYOUT_BSND, paged=True,
         S_q = max(q_lens) if q_lens else 0
         q = _normal_bf16((T, QN, D), gdev, device)
         cu = torch.tensor([0] + list(torch.tensor(q_lens).cumsum(0).tolist()), dtype=torch.int32)
+    if q_mult is not None:
+        m = torch.tensor(q_mult if isinstance(q_mult, (list, tuple)) else [q_mult] * QN,
+                         dtype=torch.float32, device=device)
+        for x in m.tolist():
+            assert x > 0 and math.frexp(x)[0] == 0.5, "q_mult must be a power of two"
+        q = (q.float() * m.view(QN, 1)).to(torch.bfloat16)
     if paged:
         table, nb, placed = _paged_layout(kv_lens, block_size, gen_cpu, max_blocks)
         rows = nb * block_size
@@ -284,6 +336,21 @@ def make_fia(*, B, QN, KVN, D, q_lens, kv_lens, layout=LAYOUT_BSND, paged=True,
             k_src.view(rows, -1)[inv] = float("nan")
             v_src.view(rows, -1)[inv] = float("nan")
         k_cache, v_cache, k_scale, v_scale = k_src, v_src, None, None
+    if kv_layout == KV_LAYOUT_BNNBSD:
+        assert paged, "head-major pages need a paged cache"
+        k_cache = k_cache.permute(0, 2, 1, 3).contiguous()
+        v_cache = v_cache.permute(0, 2, 1, 3).contiguous()
+    atten_mask = None
+    if mask_density is not None:
+        cap = skv
+        cols = (cap + 15) // 16 * 16
+        mrows = max(max(q_lens) if q_lens else 0, 1)
+        mb = 1 if mask_shared else B
+        atten_mask = (torch.rand((mb, mrows, cols), generator=gen_cpu) < mask_density).to(
+            torch.uint8)
+        for i in range(min(mask_full_rows, mrows)):
+            atten_mask[0, i, :] = 1
+        atten_mask = atten_mask.to(device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     return FiaProblem(B=B, QN=QN, KVN=KVN, D=D, layout=layout, S_q=S_q, T=T, q=q,
@@ -294,13 +361,14 @@ def make_fia(*, B, QN, KVN, D, q_lens, kv_lens, layout=LAYOUT_BSND, paged=True,
                       seqused_kv=seqused.to(device), scale=float(scale), mask_mode=mask_mode,
                       pre_tokens=pre_tokens, next_tokens=next_tokens,
                       sinks=None if sinks is None else sinks.to(device),
-                      q_lens=q_lens, kv_lens=kv_lens)
+                      q_lens=q_lens, kv_lens=kv_lens, kv_layout=kv_layout,
+                      atten_mask=atten_mask)
 
 
 def make_sparse(*, B, N1, D, q_lens, kv_lens, layout=LAYOUT_BSND, mode="csa", K2=512,
                 cmp_ratio=4, ori_block_size=128, cmp_block_size=128, win_left=127, win_right=0,
                 with_sinks=True, scale=None, seed=0, device="cpu", poison=True,
-                distinct=True) -> SparseProblem:
+                distinct=True, kv_dtype=SPARSE_KV_BF16) -> SparseProblem:
     """Build one shared-KV sparse attention problem.  mode: 'swa' (ori only),
     'csa' (ori window + top-K indexed compressed rows) or 'hca' (ori window +
     every causally visible compressed row)."""
@@ -319,20 +387,36 @@ def make_sparse(*, B, N1, D, q_lens, kv_lens, layout=LAYOUT_BSND, mode="csa", K2
         S1 = max(q_lens)
         q = _normal_bf16((T1, N1, D), gdev, device)
         cu = torch.tensor([0] + list(torch.tensor(q_lens).cumsum(0).tolist()), dtype=torch.int32)
+    def _store(src, valid):
+        # bf16 rows poisoned with NaN, or packed FP8 rows poisoned with NaN
+        # rope values, NaN codes (0x7F) and NaN scales (0xFF)
+        if kv_dtype == SPARSE_KV_BF16:
+            if valid is not None:
+                src.view(-1, D)[~valid] = float("nan")
+            return src
+        packed = pack_fp8_sparse_rows(src)
+        if valid is not None:
+            flat = packed.view(-1, 640)
+            bad = ~valid
+            flat[bad, 0:128] = torch.tensor([0xC0, 0x7F], dtype=torch.uint8,
+                                            device=packed.device).repeat(64)
+            flat[bad, 128:576] = 0x7F
+            flat[bad, 576:583] = 0xFF
+        return packed
+
     o_table, o_nb, o_placed = _paged_layout(kv_lens, ori_block_size, gen_cpu)
     ori = _normal_bf16((o_nb, ori_block_size, 1, D), gdev, device)
-    if poison:
-        ov = _valid_row_mask(kv_lens, ori_block_size, o_placed, o_nb).to(device)
-        ori.view(-1, D)[~ov] = float("nan")
+    ov = _valid_row_mask(kv_lens, ori_block_size, o_placed, o_nb).to(device) if poison else None
+    ori = _store(ori, ov)
     cmp_kv = c_table = idx = None
     if mode in ("csa", "hca"):
         cmp_lens = [l // cmp_ratio for l in kv_lens]
         c_table, c_nb, c_placed = _paged_layout([max(c, 0) for c in cmp_lens], cmp_block_size,
                                                 gen_cpu)
         cmp_kv = _normal_bf16((c_nb, cmp_block_size, 1, D), gdev, device)
-        if poison:
-            cv = _valid_row_mask(cmp_lens, cmp_block_size, c_placed, c_nb).to(device)
-            cmp_kv.view(-1, D)[~cv] = float("nan")
+        cv = (_valid_row_mask(cmp_lens, cmp_block_size, c_placed, c_nb).to(device)
+              if poison else None)
+        cmp_kv = _store(cmp_kv, cv)
     sinks = torch.randn((N1,), generator=gen_cpu, dtype=torch.float32) if with_sinks else None
     if mode == "csa":
         rows = T1
@@ -363,7 +447,7 @@ def make_sparse(*, B, N1, D, q_lens, kv_lens, layout=LAYOUT_BSND, mode="csa", K2
                          seqused_kv=torch.tensor(kv_lens, dtype=torch.int32).to(device),
                          sinks=None if sinks is None else sinks.to(device), scale=float(scale),
                          cmp_ratio=cmp_ratio, win_left=win_left, win_right=win_right,
-                         q_lens=q_lens, kv_lens=kv_lens)
+                         q_lens=q_lens, kv_lens=kv_lens, kv_dtype=kv_dtype)
 
 
 # ----------------------------------------------------------------------------

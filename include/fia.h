@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define FIA_ABI_VERSION 2
+#define FIA_ABI_VERSION 3
 
 /* Status codes ("...V5" two-phase API: the first phase validates the inputs
  * and reports errors before anything is launched). */
@@ -68,9 +68,26 @@ typedef int fia_status;
 #define FIA_KV_BF16 0
 #define FIA_KV_FP8_E4M3 1
 
+/* Mask modes ("...V5" Attention Mask group, sparseMode 0-4).  Row i of a
+ * sequence with q_len query rows and kv_len keys sees key j (0 <= j < kv_len)
+ * when:
+ *   0 NONE               every key; with atten_mask, where the mask byte is 0
+ *   1 ALL_MASK           where the mask byte is 0 (atten_mask required)
+ *   2 LEFT_UP_CAUSAL     j <= i            (the diagonal from the top-left)
+ *   3 RIGHT_DOWN_CAUSAL  j <= p, p = kv_len - q_len + i
+ *   4 BAND               p - pre_tokens <= j <= p + next_tokens
+ * Modes 2-4 are computed from positions; the pages pass them a fixed
+ * 2048 x 2048 mask that encodes the same rule, which this library neither
+ * needs nor reads (atten_mask must be NULL there). */
 #define FIA_MASK_NONE 0
+#define FIA_MASK_ALL 1
+#define FIA_MASK_LEFT_UP_CAUSAL 2
 #define FIA_MASK_RIGHT_DOWN_CAUSAL 3
 #define FIA_MASK_BAND 4
+
+/* Paged KV cache layouts ("...V5" Paged Attention group). */
+#define FIA_KV_LAYOUT_BNBSH 0  /* [num_blocks, block_size, KV_N, D] (H = KV_N*D)  */
+#define FIA_KV_LAYOUT_BNNBSD 1 /* [num_blocks, KV_N, block_size, D]             */
 
 /* Fused inference attention parameters.
  *
@@ -129,7 +146,14 @@ typedef struct fia_params {
     int32_t next_tokens;      /* band: keys after p;  pre + next >= 0          */
     const float *sinks;       /* fp32 [Q_N] or NULL                            */
     int32_t num_sms;          /* persistent CTAs; 0 = the device's SM count    */
-    int32_t reserved[7];      /* must be 0                                     */
+    int32_t kv_layout;        /* FIA_KV_LAYOUT_* (paged caches)                */
+    const uint8_t *atten_mask;    /* modes 0/1: int8/uint8/bool bytes, nonzero  */
+                              /* = masked out; element (b, i, j) at            */
+                              /* b*mask_batch_stride + i*mask_row_stride + j    */
+    int64_t mask_batch_stride;    /* bytes; 0 = one [S_q, S_kv] mask for all B  */
+    int64_t mask_row_stride;      /* bytes, a multiple of 16, >= the KV capacity */
+                              /* (paged: max_blocks_per_seq * block_size)        */
+    int32_t reserved[8];      /* must be 0                                     */
 } fia_params;
 
 /* Returns a static string naming a status code. */
@@ -138,10 +162,12 @@ const char *fia_status_string(fia_status s);
 /* Version of this ABI (FIA_ABI_VERSION). */
 int32_t fia_abi_version(void);
 
-/* sizeof(fia_params) and sizeof(sparse_attn_params) as compiled into the
- * library, so that a binding can check its mirror of the structs. */
+/* sizeof(fia_params), sizeof(sparse_attn_params) and sizeof(fia_combine_params)
+ * as compiled into the library, so that a binding can check its mirror of the
+ * structs. */
 size_t fia_sizeof_params(void);
 size_t fia_sizeof_sparse_params(void);
+size_t fia_sizeof_combine_params(void);
 
 /* Phase 1 ("...V5": the GetWorkspaceSize call validates the inputs and
  * computes the workspace).  Host-only, pure, idempotent: reads only the
@@ -185,21 +211,63 @@ fia_status fia_run(const fia_params *p, void *workspace, size_t workspace_bytes,
  * attention (a device fully owned by another component's memory pool, a host
  * process that forbids allocations after start-up, a latency-critical path
  * that must not touch the allocator).  It behaves like fia_run on the decode
- * branch (max_seqlen_q == 1) but keeps the scheduler's scratch -- the plan,
- * the split-KV counters and the partial slots -- in a device array of
- * FIA_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
- * loads libfia holds until the process exits.  It allocates nothing.
+ * branch but keeps the scheduler's scratch -- the plan, the split-KV counters
+ * and the partial slots -- in a device array of FIA_NOALLOC_SCRATCH_BYTES
+ * compiled into the library, which every GPU that loads libfia holds until
+ * the process exits.  It allocates nothing.
+ *  - status (nullable, a device int32 the caller owns): receives, in stream
+ *    order after the kernels, the error word fia_execute documents (0 clean,
+ *    1 a bounded wait gave up, 2 a plan problem); 0 when there was nothing to
+ *    run.  Without it a failure inside the kernels cannot be seen, since the
+ *    word lives in the library's array.
  *  - Returns FIA_ERR_WORKSPACE_TOO_SMALL, before launching anything, when the
  *    decode plan needs more than FIA_NOALLOC_SCRATCH_BYTES (what fia_get_
  *    workspace_size reports for the same params), FIA_ERR_UNSUPPORTED for the
  *    prefill branch, and any status fia_run returns.
- *  - The first call on a device looks up the array's device address (with
- *    that device current); make that first call before any stream capture.
+ *  - Every call looks up the array's device address in the current context;
+ *    the first call on a device loads the library's device code there, so
+ *    make that first call before any stream capture.
  *  - All calls on a device share the array and it keeps the last call's
  *    contents; every value that must start at zero is reset by the call.
  *    Calls that overlap on the GPU (unordered streams) race on the array. */
 #define FIA_NOALLOC_SCRATCH_BYTES (8u << 20)
-fia_status fia_decode_run_noalloc(const fia_params *p, void *stream);
+fia_status fia_decode_run_noalloc(const fia_params *p, int32_t *status, void *stream);
+
+/* Log-sum-exp combine of partial attention results over disjoint key sets:
+ * the use of softmax_lse that "...V2" names (softmax_lse restriction: the
+ * ring-attention algorithm), i.e. the exchange step of context parallelism
+ * with the KV cut across ranks ("sparse_flash_mla", CP example).  Given
+ * n_parts results (O_k, lse_k) of the same query rows against disjoint parts
+ * of the keys, it writes the result against their union:
+ *   lse = log sum_k exp(lse_k),   O = sum_k exp(lse_k - lse) * O_k.
+ * Parts with lse_k = +inf saw no key and are skipped; when every part is
+ * skipped, O = 0 and lse = +inf (the empty-row rule).  A sink belongs to one
+ * part only: run the other parts without sinks.
+ * Layouts are those of fia_params' out and lse: O bf16 [tokens, N, D] (BSND
+ * tokens = B * S_q, TND tokens = T) and lse fp32 BSND [B, N, S_q] or TND
+ * [T, N].  o_parts and lse_parts are HOST arrays of n_parts DEVICE pointers
+ * (16-byte aligned O, 4-byte aligned lse); out may alias none of the parts.
+ * Deterministic: parts are folded in index order.  Errors: FIA_ERR_NULL_ARG,
+ * FIA_ERR_BAD_SHAPE (n_parts outside 1..FIA_COMBINE_MAX_PARTS, D not a
+ * multiple of 8 or above 512, sizes out of range, misalignment),
+ * FIA_ERR_CUDA for a failed launch. */
+#define FIA_COMBINE_MAX_PARTS 16
+typedef struct fia_combine_params {
+    int32_t n_parts;
+    int32_t layout;           /* FIA_LAYOUT_BSND | FIA_LAYOUT_TND              */
+    int32_t batch;            /* BSND: B                                       */
+    int32_t seqlen_q;         /* BSND: S_q                                     */
+    int32_t total_q;          /* TND: T                                        */
+    int32_t num_heads;        /* N                                             */
+    int32_t head_dim;         /* D                                             */
+    int32_t pad0_;
+    const void *const *o_parts;     /* host array [n_parts] of device pointers */
+    const float *const *lse_parts;  /* host array [n_parts] of device pointers */
+    void *out;                /* bf16 [tokens, N, D]                           */
+    float *lse;               /* fp32, nullable                                */
+    int32_t reserved[8];      /* must be 0                                     */
+} fia_combine_params;
+fia_status fia_lse_combine(const fia_combine_params *p, void *stream);
 
 /* Self-test of the bounded wait that every pipeline barrier of this library
  * uses (failure detection without a GPU fault): launches, on `stream`, one
@@ -244,6 +312,20 @@ fia_status fia_get_plan_layout(const fia_params *p, fia_plan_layout *layout);
 /* ------------------------------------------------------------------------ */
 /* shared-KV sparse attention                                               */
 /* ------------------------------------------------------------------------ */
+
+/* KV row formats of the sparse variant ("kv_quant_sparse_attn_sharedkv",
+ * parameter table: kv_quant_mode 1 = per-tile quantised nope part, tile_size,
+ * rope_head_dim; constraint on the D of ori_kv / cmp_kv):
+ *  - BF16: a row is D bf16 values.
+ *  - FP8_PACKED: a row is 640 bytes for a query D of 512: the 64 rope values
+ *    as bf16 (128 bytes), then the 448 nope values as E4M3 codes (448 bytes),
+ *    then the 7 per-64 nope tile scales as E8M0 bytes (value 2^(e - 127),
+ *    e = 255 is NaN), then 57 bytes of padding.  Element d of the row is the
+ *    rope value for d < 64 and e4m3(code[d - 64]) * 2^(scale[(d - 64)/64] -
+ *    127) after.  The pool is bytes [num_blocks, block_size, 1, 640]. */
+#define FIA_SPARSE_KV_BF16 0
+#define FIA_SPARSE_KV_FP8_PACKED 1
+#define FIA_SPARSE_PACKED_ROW_BYTES 640
 
 /* Parameters ("kv_quant_sparse_attn_sharedkv" parameter table and
  * constraints; "sparse_flash_mla" modes):
@@ -293,7 +375,10 @@ typedef struct sparse_attn_params {
     int32_t ori_win_left;     /* 127 on the pages                              */
     int32_t ori_win_right;    /* 0 on the pages                                */
     int32_t num_sms;          /* CTAs of the split; 0 = the device's SM count  */
-    int32_t reserved[7];      /* must be 0                                     */
+    int32_t kv_dtype;         /* FIA_SPARSE_KV_* (ori_kv and cmp_kv alike)     */
+    int32_t tile_size;        /* packed FP8 rows: 64 (nope quantisation tile)  */
+    int32_t rope_head_dim;    /* packed FP8 rows: 64                           */
+    int32_t reserved[8];      /* must be 0                                     */
 } sparse_attn_params;
 
 /* Metadata step ("sparse_flash_mla_metadata": generates, before the main call,

@@ -35,7 +35,8 @@ def test_struct_layouts_agree():
     L = fia.lib()
     assert L.fia_sizeof_params() == ctypes.sizeof(_abi.FiaParams)
     assert L.fia_sizeof_sparse_params() == ctypes.sizeof(_abi.SparseParams)
-    assert L.fia_abi_version() == 2
+    assert L.fia_sizeof_combine_params() == ctypes.sizeof(_abi.CombineParams)
+    assert L.fia_abi_version() == 3
 
 
 def test_status_strings():
@@ -87,7 +88,10 @@ def test_valid_decode_params_size_the_workspace():
     ("block_size", 24, fia.FIA_ERR_BAD_SHAPE),       # multiple of 16
     ("block_size", 2048, fia.FIA_ERR_BAD_SHAPE),     # <= 1024
     ("kv_dtype", 7, fia.FIA_ERR_BAD_DTYPE),
-    ("mask_mode", 2, fia.FIA_ERR_BAD_SHAPE),
+    ("mask_mode", 5, fia.FIA_ERR_BAD_SHAPE),
+    ("mask_mode", -1, fia.FIA_ERR_BAD_SHAPE),
+    ("mask_mode", 1, fia.FIA_ERR_NULL_ARG),          # mode 1 needs an explicit mask
+    ("kv_layout", 2, fia.FIA_ERR_BAD_SHAPE),
     ("layout", 5, fia.FIA_ERR_BAD_SHAPE),
     ("q", FAKE + 8, fia.FIA_ERR_BAD_SHAPE),          # TMA needs 16-byte alignment
     ("q_token_stride", 1028, fia.FIA_ERR_BAD_SHAPE),  # multiple of 8 elements
@@ -218,3 +222,26 @@ def test_sparse_metadata_pointer_required():
     n = ctypes.c_size_t(0)
     assert fia.lib().sparse_attn_metadata(ctypes.byref(p), None, ctypes.byref(n), None) == \
         fia.FIA_ERR_NULL_ARG
+
+
+def test_explicit_mask_rules():
+    # an explicit mask goes with modes 0 and 1 only
+    for mode in (2, 3, 4):
+        assert _status(_decode_params(mask_mode=mode, atten_mask=FAKE, mask_row_stride=1024))[0] \
+            == fia.FIA_ERR_BAD_SHAPE
+    # 16-byte aligned, row stride a multiple of 16 covering the KV capacity
+    # (max_blocks_per_seq * block_size = 1024 here)
+    assert _status(_decode_params(atten_mask=FAKE + 8, mask_row_stride=1024))[0] == \
+        fia.FIA_ERR_BAD_SHAPE
+    assert _status(_decode_params(atten_mask=FAKE, mask_row_stride=1000))[0] == \
+        fia.FIA_ERR_BAD_SHAPE
+    assert _status(_decode_params(atten_mask=FAKE, mask_row_stride=1008))[0] == \
+        fia.FIA_ERR_BAD_SHAPE
+    assert _status(_decode_params(atten_mask=FAKE, mask_row_stride=1024,
+                                  mask_batch_stride=-16))[0] == fia.FIA_ERR_BAD_SHAPE
+
+
+def test_head_major_pages_need_a_block_table():
+    contig = dict(block_table=None, seqused_kv=None, max_blocks_per_seq=0, num_blocks=0,
+                  block_size=0, max_seqlen_kv=300)
+    assert _status(_decode_params(**contig, kv_layout=1))[0] == fia.FIA_ERR_BAD_SHAPE

@@ -264,19 +264,50 @@ def test_paged_gqa_decode_workload_full_size():
     check_close(out, lse, ro, rl, "paged GQA decode")
 
 
-def test_fp8_long_decode_workload_sampled():
+def test_fp8_long_decode_workload_every_row():
+    # all B x Q_N = 256 (batch, head) rows of the long FP8 decode workload
     p = fi.workload_fp8_long_decode(device=dev)
     _, out, lse = _run(p)
-    pc = p.to("cpu")
-    g = np.random.default_rng(0)
-    rows = g.integers(0, p.B, 24)
-    heads = g.integers(0, p.QN, 24)
-    ro, rl = oracle.fia_sample(pc, rows, heads)
-    o = out.float().cpu().numpy().reshape(p.B, p.QN, p.D)
-    l = lse.cpu().numpy().reshape(p.B, p.QN)
-    err = np.abs(o[rows, heads] - ro)
-    assert err.max() <= 2e-2 and err.mean() <= 2e-3
-    assert np.abs(l[rows, heads] - rl).max() <= 1e-3
+    ro, rl = oracle.fia(p.to("cpu"))
+    check_close(out, lse, ro, rl, "long FP8 decode, every row")
+
+
+# Query magnitudes across the whole bf16 range.  The FP8 products run in fp16,
+# so the kernel moves each head's query by a power of two before narrowing it;
+# the bf16 products see the query unchanged.  Powers of two keep the inputs
+# exact, and the scale brings the scores back to a moderate size.
+Q_RANGE = {
+    # |q| up to ~2^19, beyond fp16's largest finite value (65504)
+    "large": dict(q_mult=2.0 ** 17, scale=2.0 ** -17 / 11.3),
+    # |q| around 2^-20: fp16 subnormals would keep only a few bits
+    "tiny": dict(q_mult=2.0 ** -20, scale=2.0 ** 20 / 11.3),
+    # heads of one unit 2^6 apart: each head takes its own shift, so a head
+    # scaled with its neighbour's shift would be off by 64
+    "mixed_heads": dict(q_mult=[2.0 ** 3 if h % 2 else 2.0 ** -3 for h in range(16)],
+                        scale=1.0 / 11.3),
+}
+
+
+@pytest.mark.parametrize("kv_dtype", [fi.KV_BF16, fi.KV_FP8_E4M3])
+@pytest.mark.parametrize("name", sorted(Q_RANGE))
+def test_decode_query_range(name, kv_dtype):
+    p = fi.make_fia(B=3, QN=16, KVN=2, D=128, q_lens=[1] * 3, kv_lens=[900, 40, 257],
+                    block_size=64, kv_dtype=kv_dtype, with_sinks=True,
+                    seed=zlib.crc32(name.encode()) % 1000, device=dev, **Q_RANGE[name])
+    _, out, lse = _run(p)
+    ro, rl = _ref(p)
+    check_close(out, lse, ro, rl, f"{name} {kv_dtype}")
+
+
+def test_fp8_decode_query_range_gqa16():
+    # 16 query heads per KV head: two head groups per unit on the FP8 path
+    p = fi.make_fia(B=2, QN=32, KVN=2, D=128, q_lens=[1, 1], kv_lens=[700, 129],
+                    block_size=128, kv_dtype=fi.KV_FP8_E4M3, seed=77, device=dev,
+                    q_mult=[2.0 ** 17 if h % 3 else 2.0 ** 15 for h in range(32)],
+                    scale=2.0 ** -17 / 11.3)
+    _, out, lse = _run(p)
+    ro, rl = _ref(p)
+    check_close(out, lse, ro, rl, "fp8 gqa16 large q")
 
 
 @pytest.mark.parametrize("fp8", [False, True])

@@ -110,21 +110,32 @@ def test_prefill_deterministic_bitwise():
 
 
 def test_varlen_causal_prefill_workload_sampled():
+    # every 8th query row with all 32 heads, plus the first and the last row
+    # of every sequence (its shortest and longest rows), element by element
     p = fi.workload_varlen_prefill(device=dev)
     _, out, lse = _run(p)
     pc = p.to("cpu")
-    g = np.random.default_rng(0)
-    rows = g.integers(0, p.T, 48)
-    # the last row of every sequence and the first: the longest and shortest rows
     cu = pc.cu_seqlens_q.tolist()
-    rows = np.concatenate([rows, np.array(cu[1:]) - 1, np.array(cu[:-1])])
-    heads = g.integers(0, p.QN, rows.shape[0])
+    sel = sorted(set(range(0, p.T, 8)) | set(cu[:-1]) | set(c - 1 for c in cu[1:]))
+    rows = np.repeat(np.array(sel, dtype=np.int64), p.QN)
+    heads = np.tile(np.arange(p.QN, dtype=np.int32), len(sel))
     ro, rl = oracle.fia_sample(pc, rows, heads)
     o = out.float().cpu().numpy().reshape(p.T, p.QN, p.D)
     l = lse.cpu().numpy().reshape(p.T, p.QN)
     err = np.abs(o[rows, heads] - ro)
     assert err.max() <= 2e-2 and err.mean() <= 2e-3, (err.max(), err.mean())
     assert np.abs(l[rows, heads] - rl).max() <= 1e-3
+
+
+@pytest.mark.parametrize("q_mult,scale", [(2.0 ** 17, 2.0 ** -17 / 11.3),
+                                          (2.0 ** -20, 2.0 ** 20 / 11.3)])
+def test_prefill_query_range(q_mult, scale):
+    p = fi.make_fia(B=2, QN=8, KVN=2, D=128, q_lens=[200, 77], kv_lens=[200, 77],
+                    layout=fi.LAYOUT_TND, block_size=64, mask_mode=3, with_sinks=True,
+                    seed=83, device=dev, q_mult=q_mult, scale=scale)
+    _, out, lse = _run(p)
+    ro, rl = oracle.fia(p.to("cpu"))
+    check_close(out, lse, ro, rl, f"q x {q_mult}")
 
 
 def test_execute_reuses_one_plan():

@@ -32,6 +32,7 @@ balance; and the C code agrees with naive.py on tiny brute-force shapes.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 import threading
@@ -71,6 +72,9 @@ class _FiaArgs(ctypes.Structure):
         ("S_kv", ctypes.c_int32), ("seqused_kv", ctypes.c_void_p), ("scale", ctypes.c_double),
         ("mask_mode", ctypes.c_int32), ("pre_tokens", ctypes.c_int32),
         ("next_tokens", ctypes.c_int32), ("sinks", ctypes.c_void_p),
+        ("kv_layout", ctypes.c_int32), ("max_seqlen_q", ctypes.c_int32),
+        ("atten_mask", ctypes.c_void_p), ("mask_batch_stride", ctypes.c_int64),
+        ("mask_row_stride", ctypes.c_int64),
     ]
 
 
@@ -86,7 +90,7 @@ class _SparseArgs(ctypes.Structure):
         ("cmp_sparse_indices", ctypes.c_void_p), ("K2", ctypes.c_int32),
         ("seqused_kv", ctypes.c_void_p), ("sinks", ctypes.c_void_p), ("scale", ctypes.c_double),
         ("cmp_ratio", ctypes.c_int32), ("win_left", ctypes.c_int32),
-        ("win_right", ctypes.c_int32),
+        ("win_right", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
     ]
 
 
@@ -105,6 +109,8 @@ def lib():
             L.oracle_e4m3_to_double.restype = ctypes.c_double
             L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
             L.oracle_bf16_to_double.restype = ctypes.c_double
+            L.oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
+            L.oracle_e8m0_to_double.restype = ctypes.c_double
             L.oracle_fia_row_probs.argtypes = [ctypes.POINTER(_FiaArgs), ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
                                                ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
@@ -164,14 +170,22 @@ def _fia_struct(p):
         "v": _np(p.v_cache), "ks": _np(p.k_scale, np.float32), "vs": _np(p.v_scale, np.float32),
         "bt": _np(p.block_table, np.int32), "sk": _np(p.seqused_kv, np.int32),
         "sinks": _np(p.sinks, np.float32),
+        "mask": _np(getattr(p, "atten_mask", None)),
     }
+    mask = getattr(p, "atten_mask", None)
+    if mask is not None:
+        mrs, mbs = int(mask.shape[2]), (0 if mask.shape[0] == 1 else int(mask.shape[1] * mask.shape[2]))
+    else:
+        mrs = mbs = 0
     s = _FiaArgs(B=p.B, QN=p.QN, KVN=p.KVN, D=p.D, layout=p.layout, S_q=p.S_q, T=p.T,
                  q=_ptr(keep["q"]), cu_seqlens_q=_ptr(keep["cu"]), kv_dtype=p.kv_dtype,
                  k=_ptr(keep["k"]), v=_ptr(keep["v"]), k_scale=_ptr(keep["ks"]),
                  v_scale=_ptr(keep["vs"]), quant_tile=64, block_table=_ptr(keep["bt"]),
                  max_blocks=p.max_blocks, block_size=p.block_size or 1, S_kv=p.S_kv,
                  seqused_kv=_ptr(keep["sk"]), scale=p.scale, mask_mode=p.mask_mode,
-                 pre_tokens=p.pre_tokens, next_tokens=p.next_tokens, sinks=_ptr(keep["sinks"]))
+                 pre_tokens=p.pre_tokens, next_tokens=p.next_tokens, sinks=_ptr(keep["sinks"]),
+                 kv_layout=getattr(p, "kv_layout", 0), max_seqlen_q=max(p.S_q, 1),
+                 atten_mask=_ptr(keep["mask"]), mask_batch_stride=mbs, mask_row_stride=mrs)
     return s, keep
 
 
@@ -193,7 +207,8 @@ def _sparse_struct(p):
                     cmp_block_size=p.cmp_block_size or 1,
                     cmp_sparse_indices=_ptr(keep["idx"]), K2=p.K2, seqused_kv=_ptr(keep["sk"]),
                     sinks=_ptr(keep["sinks"]), scale=p.scale, cmp_ratio=p.cmp_ratio or 1,
-                    win_left=p.win_left, win_right=p.win_right)
+                    win_left=p.win_left, win_right=p.win_right,
+                    kv_dtype=getattr(p, "kv_dtype", 0))
     return s, keep
 
 
@@ -275,6 +290,36 @@ def e4m3_to_double(code: int) -> float:
 
 def bf16_to_double(bits: int) -> float:
     return lib().oracle_bf16_to_double(bits)
+
+
+def e8m0_to_double(code: int) -> float:
+    return lib().oracle_e8m0_to_double(code)
+
+
+def lse_combine(outs, lses):
+    """Attention over the union of disjoint key sets from the results over
+    each set ("aclnnFusedInferAttentionScoreV2", softmax_lse restriction: the
+    lse exists for ring attention, which joins partial results this way):
+        lse = log sum_k exp(lse_k),   O = sum_k exp(lse_k - lse) * O_k,
+    leaving out parts with lse_k = +inf (they saw no key); when every part is
+    left out, O = 0 and lse = +inf.  `outs[k]` is [..., D], `lses[k]` the
+    matching [...]; fp64 throughout, parts in the order given."""
+    outs = [np.asarray(o, dtype=np.float64) for o in outs]
+    lses = [np.asarray(l, dtype=np.float64) for l in lses]
+    shape = lses[0].shape
+    out = np.zeros(outs[0].shape, dtype=np.float64)
+    lse = np.full(shape, np.inf)
+    for idx in np.ndindex(*shape):
+        vals = [l[idx] for l in lses if not np.isinf(l[idx])]
+        if not vals:
+            continue
+        m = max(vals)
+        tot = m + math.log(sum(math.exp(v - m) for v in vals))
+        lse[idx] = tot
+        for o, l in zip(outs, lses):
+            if not np.isinf(l[idx]):
+                out[idx] += math.exp(l[idx] - tot) * o[idx]
+    return out, lse
 
 
 def decode_schedule(p, num_ctas: int, per_cta: int):

@@ -3,8 +3,9 @@
 TEST INFRASTRUCTURE (see oracle/__init__.py).  Written as matrices rather than
 rows: gather each sequence's K and V into dense [kv_len, KVN, D] arrays through
 the block table, form the whole score matrix S = scale * Q K^T per head, build
-the boolean visibility matrix of the mask mode with the query rows aligned to
-the bottom-right corner, and apply a textbook softmax with the sink as one
+the boolean visibility matrix of the mask mode (query rows aligned to the
+bottom-right corner, or to the top-left for the left-up causal mode; an
+explicit mask's ones removed), and apply a textbook softmax with the sink as one
 extra column that carries no value ("aclnnFusedInferAttentionScoreV5" formula
 section; "...V2" softmax_lse restriction; "...V4" empty-tensor rule).  Only for
 tiny shapes: it materialises every score.
@@ -38,6 +39,9 @@ def _as_np(t):
 
 def _dense_kv(p, b, which):
     pool = _as_np(p.k_cache if which == "k" else p.v_cache)
+    if getattr(p, "kv_layout", 0) == 1:
+        # head-major pages [nb, KVN, bs, D] -> token-major [nb, bs, KVN, D]
+        pool = pool.transpose(0, 2, 1, 3)
     kvl = p.kv_lens[b]
     if p.kv_dtype == 0:
         vals = _bf16_bits_to_f64(pool)
@@ -76,13 +80,17 @@ def fia(p):
         V = _dense_kv(p, b, "v")
         i = np.arange(ql)[:, None]
         j = np.arange(kl)[None, :]
-        pos = kl - ql + i
-        if p.mask_mode == 3:
+        pos = (0 if p.mask_mode == 2 else kl - ql) + i
+        if p.mask_mode in (2, 3):
             vis = j <= pos
         elif p.mask_mode == 4:
             vis = (j >= pos - p.pre_tokens) & (j <= pos + p.next_tokens)
         else:
             vis = np.ones((ql, kl), dtype=bool)
+        mask = getattr(p, "atten_mask", None)
+        if mask is not None:  # 1 = masked out
+            mk = _as_np(mask)
+            vis = vis & (mk[0 if mk.shape[0] == 1 else b, :ql, :kl] == 0)
         for h in range(p.QN):
             g = h // G
             S = p.scale * (q_all[qs:qs + ql, h, :] @ K[:, g, :].T)

@@ -66,13 +66,24 @@ double oracle_e4m3_to_double(uint8_t code)
 
 double oracle_bf16_to_double(uint16_t h) { return bf16_bits_to_double(h); }
 
+/* OCP E8M0 ("float8_e8m0fnu", the MX scale format [KQSAS] names for the
+ * nope_quant_scale): 8 exponent bits, no sign, no mantissa, bias 127; the
+ * value is 2^(e - 127) and e = 255 encodes NaN. */
+double oracle_e8m0_to_double(uint8_t e)
+{
+    if (e == 0xFF)
+        return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
 /* ------------------------------------------------------------------------ */
 /* fused inference attention (FIA)                                          */
 /* ------------------------------------------------------------------------ */
 
 enum { OR_LAYOUT_BSND = 0, OR_LAYOUT_TND = 1 };
 enum { OR_KV_BF16 = 0, OR_KV_E4M3 = 1 };
-enum { OR_MASK_NONE = 0, OR_MASK_RDC = 3, OR_MASK_BAND = 4 };
+enum { OR_MASK_NONE = 0, OR_MASK_ALL = 1, OR_MASK_LUC = 2, OR_MASK_RDC = 3, OR_MASK_BAND = 4 };
+enum { OR_KV_BNBSH = 0, OR_KV_BNNBSD = 1 };
 
 typedef struct {
     int32_t B, QN, KVN, D;
@@ -92,21 +103,28 @@ typedef struct {
     double scale;
     int32_t mask_mode, pre_tokens, next_tokens;
     const float *sinks;          /* [QN] fp32 or NULL                            */
+    int32_t kv_layout;           /* paged pools: 0 [nb,bs,KVN,D], 1 [nb,KVN,bs,D] */
+    int32_t max_seqlen_q;        /* rows per sequence the decode units cover     */
+    const uint8_t *atten_mask;   /* modes 0/1: byte (b, i, j) nonzero = hidden   */
+    int64_t mask_batch_stride;   /* bytes between batches (0: shared)            */
+    int64_t mask_row_stride;     /* bytes between query rows                     */
 } oracle_fia_args;
 
-/* Index of element d of logical KV row j of batch b, head g, in the KV storage
- * ([FIA-V2] page-attention scenario: blockTable holds block ids, K/V rows of a
- * block sit contiguously in one pool; KV cache layout BnBsH = [nb, bs, KVN*D]). */
+/* Index of the D-element vector of logical KV row j of batch b, head g, in the
+ * KV storage ([FIA-V2] page-attention scenario: blockTable holds block ids,
+ * the rows of a block sit contiguously in one pool; [FIA-V5] Paged Attention
+ * group: the cache is BnBsH = [nb, bs, KVN*D] or BnNBsD = [nb, KVN, bs, D]).
+ * Multiply by D for the first element. */
 static int64_t kv_row_base(const oracle_fia_args *a, int b, int64_t j, int g)
 {
-    int64_t phys_row;
     if (a->block_table) {
         int64_t blk = a->block_table[(int64_t)b * a->max_blocks + j / a->block_size];
-        phys_row = blk * a->block_size + j % a->block_size;
-    } else {
-        phys_row = (int64_t)b * a->S_kv + j;
+        int64_t jp = j % a->block_size;
+        if (a->kv_layout == OR_KV_BNNBSD)
+            return (blk * a->KVN + g) * a->block_size + jp;
+        return (blk * a->block_size + jp) * a->KVN + g;
     }
-    return phys_row * a->KVN + g; /* row-head index; multiply by D (or D/tile) */
+    return ((int64_t)b * a->S_kv + j) * a->KVN + g;
 }
 
 /* Index of the scale row of logical KV row j of batch b, head g.  The scales
@@ -152,29 +170,40 @@ static void fia_lengths(const oracle_fia_args *a, int b, int64_t *q_len, int64_t
     *kv_len = a->seqused_kv ? a->seqused_kv[b] : a->S_kv;
 }
 
-/* Visible KV interval [lo, hi] (inclusive) of query row i, per the mask mode.
- * The query row is aligned to the bottom-right corner of the (q_len x kv_len)
- * score matrix: its position is p = kv_len - q_len + i ([KQSAS] cmp_mask_mode 3
- * "rightDownCausal", split by the right vertex; the CP example in [SFMLA]
- * derives the query start as kv length minus q length).
- *   mode 0: all of [0, kv_len)
- *   mode 3: j <= p
- *   mode 4: p - pre_tokens <= j <= p + next_tokens  ([KQSAS] ori_mask_mode 4
- *           "band", ori_win_left / ori_win_right)
+/* Visible KV interval [lo, hi] (inclusive) of query row i, per the mask mode
+ * ([FIA-V5] Attention Mask group, sparseMode 0-4).  For modes 3 and 4 the
+ * query row is aligned to the bottom-right corner of the (q_len x kv_len)
+ * score matrix: its position is p = kv_len - q_len + i ([KQSAS] cmp_mask_mode
+ * 3 "rightDownCausal", split by the right vertex; the CP example in [SFMLA]
+ * derives the query start as kv length minus q length); mode 2 is the causal
+ * mask split by the left vertex, p = i.
+ *   modes 0, 1: all of [0, kv_len) (the explicit mask then hides single keys)
+ *   modes 2, 3: j <= p
+ *   mode 4:     p - pre_tokens <= j <= p + next_tokens  ([KQSAS] ori_mask_mode
+ *               4 "band", ori_win_left / ori_win_right)
  * Returns 0 when the interval is empty. */
 static int fia_visible(const oracle_fia_args *a, int64_t q_len, int64_t kv_len, int64_t i,
                        int64_t *lo, int64_t *hi)
 {
-    int64_t p = kv_len - q_len + i;
+    int64_t p = (a->mask_mode == OR_MASK_LUC ? 0 : kv_len - q_len) + i;
     *lo = 0;
     *hi = kv_len - 1;
-    if (a->mask_mode == OR_MASK_RDC) {
+    if (a->mask_mode == OR_MASK_RDC || a->mask_mode == OR_MASK_LUC) {
         if (p < *hi) *hi = p;
     } else if (a->mask_mode == OR_MASK_BAND) {
         if (p - a->pre_tokens > *lo) *lo = p - a->pre_tokens;
         if (p + a->next_tokens < *hi) *hi = p + a->next_tokens;
     }
     return *hi >= *lo;
+}
+
+/* Explicit mask ([FIA-V5] Attention Mask group: attenMask of shape
+ * [batch or 1, >= Q_S, >= KV_S], 1 = masked out, 0 = kept): nonzero when key
+ * j is hidden from query row i of batch b.  Modes 0 and 1 only. */
+static int fia_hidden(const oracle_fia_args *a, int b, int64_t i, int64_t j)
+{
+    if (!a->atten_mask) return 0;
+    return a->atten_mask[(int64_t)b * a->mask_batch_stride + i * a->mask_row_stride + j] != 0;
 }
 
 /* One output row: softmax over the visible scores (plus the sink logit, which
@@ -188,7 +217,7 @@ static void fia_row(const oracle_fia_args *a, int b, int h, int64_t q_row, int64
 {
     int D = a->D, G = a->QN / a->KVN, g = h / G;
     const uint16_t *qv = a->q + (q_row * a->QN + h) * (int64_t)D;
-    int64_t lo, hi, j, n;
+    int64_t lo, hi, j, n, nvis;
     double m, l;
     int d;
 
@@ -198,24 +227,37 @@ static void fia_row(const oracle_fia_args *a, int b, int h, int64_t q_row, int64
         return;
     }
     n = hi - lo + 1;
-    /* scores */
+    /* scores of the visible keys (an explicit mask hides single keys) */
     m = -INFINITY;
+    nvis = 0;
     for (j = 0; j < n; ++j) {
         double s = 0.0;
+        if (fia_hidden(a, b, i, lo + j)) {
+            s_buf[j] = -INFINITY;
+            continue;
+        }
+        ++nvis;
         for (d = 0; d < D; ++d)
             s += bf16_bits_to_double(qv[d]) * kv_value(a, a->k, a->k_scale, b, lo + j, g, d);
         s *= a->scale;
         s_buf[j] = s;
         if (s > m) m = s;
     }
+    if (nvis == 0) {
+        *lse = INFINITY;
+        return;
+    }
     if (a->sinks && (double)a->sinks[h] > m) m = (double)a->sinks[h];
     /* denominator */
     l = 0.0;
-    for (j = 0; j < n; ++j) l += exp(s_buf[j] - m);
+    for (j = 0; j < n; ++j)
+        if (s_buf[j] != -INFINITY) l += exp(s_buf[j] - m);
     if (a->sinks) l += exp((double)a->sinks[h] - m);
     /* numerator */
     for (j = 0; j < n; ++j) {
-        double w = exp(s_buf[j] - m) / l;
+        double w;
+        if (s_buf[j] == -INFINITY) continue;
+        w = exp(s_buf[j] - m) / l;
         for (d = 0; d < D; ++d)
             o[d] += w * kv_value(a, a->v, a->v_scale, b, lo + j, g, d);
     }
@@ -295,15 +337,25 @@ int64_t oracle_fia_row_probs(const oracle_fia_args *a, int b, int h, int64_t i, 
     qv = a->q + ((qs + i) * a->QN + h) * (int64_t)D;
     for (j = 0; j < n; ++j) {
         double s = 0.0;
+        if (fia_hidden(a, b, i, lo + j)) {
+            p[j] = -INFINITY;
+            continue;
+        }
         for (d = 0; d < D; ++d)
             s += bf16_bits_to_double(qv[d]) * kv_value(a, a->k, a->k_scale, b, lo + j, g, d);
         p[j] = s * a->scale;
         if (p[j] > m) m = p[j];
     }
+    if (m == -INFINITY) {  /* every key hidden: no probabilities */
+        for (j = 0; j < n; ++j) p[j] = 0.0;
+        *lo_out = lo;
+        return n;
+    }
     if (a->sinks && (double)a->sinks[h] > m) m = (double)a->sinks[h];
-    for (j = 0; j < n; ++j) l += exp(p[j] - m);
+    for (j = 0; j < n; ++j)
+        if (p[j] != -INFINITY) l += exp(p[j] - m);
     if (a->sinks) l += exp((double)a->sinks[h] - m);
-    for (j = 0; j < n; ++j) p[j] = exp(p[j] - m) / l;
+    for (j = 0; j < n; ++j) p[j] = p[j] == -INFINITY ? 0.0 : exp(p[j] - m) / l;
     if (a->sinks) *p_sink = exp((double)a->sinks[h] - m) / l;
     *lo_out = lo;
     return n;
@@ -319,10 +371,10 @@ typedef struct {
     int32_t S1, T1;
     const uint16_t *q;
     const int32_t *cu_seqlens_q; /* TND [B+1]                                   */
-    const uint16_t *ori_kv;      /* [nb1, bs1, 1, D] bf16                        */
+    const void *ori_kv;          /* [nb1, bs1, 1, D] bf16 or [nb1, bs1, 1, 640] B */
     const int32_t *ori_block_table;
     int32_t ori_max_blocks, ori_block_size;
-    const uint16_t *cmp_kv;      /* [nb2, bs2, 1, D] bf16, NULL for SWA          */
+    const void *cmp_kv;          /* the same for the compressed rows; NULL: SWA  */
     const int32_t *cmp_block_table;
     int32_t cmp_max_blocks, cmp_block_size;
     const int32_t *cmp_sparse_indices; /* [rows, 1, K2] or NULL (HCA)          */
@@ -331,7 +383,34 @@ typedef struct {
     const float *sinks;          /* [N1] or NULL                                 */
     double scale;
     int32_t cmp_ratio, win_left, win_right;
+    int32_t kv_dtype;            /* 0 bf16 rows of D; 1 packed FP8 rows of 640 B */
 } oracle_sparse_args;
+
+/* Bytes of one stored K~ row: D bf16 values, or the packed FP8 row of
+ * [KQSAS] (constraint on the D of ori_kv / cmp_kv: 640, the rope part, the
+ * nope part and its scales in that order, padded to a multiple of 128 B). */
+static int64_t sparse_row_bytes(const oracle_sparse_args *a)
+{
+    return a->kv_dtype == 1 ? 640 : 2 * (int64_t)a->D;
+}
+
+/* Element d of a stored K~ row.  Packed FP8 ([KQSAS] constraints: kv_rope
+ * bf16 with rope_head_dim 64, then kv_nope E4M3 with nope_head_dim 448, then
+ * nope_quant_scale E8M0 with 448 / tile_size = 7 entries, tile_size 64):
+ * d < 64 is the rope value; d >= 64 is the nope code times its tile scale. */
+static double sparse_value(const oracle_sparse_args *a, const uint8_t *row, int d)
+{
+    if (a->kv_dtype != 1) {
+        uint16_t h = (uint16_t)(row[2 * d] | (row[2 * d + 1] << 8));
+        return bf16_bits_to_double(h);
+    }
+    if (d < 64) {
+        uint16_t h = (uint16_t)(row[2 * d] | (row[2 * d + 1] << 8));
+        return bf16_bits_to_double(h);
+    }
+    return oracle_e4m3_to_double(row[128 + (d - 64)]) *
+           oracle_e8m0_to_double(row[128 + 448 + (d - 64) / 64]);
+}
 
 /* Logical rows of K~ (= V~) for query row i of batch b, in concatenation
  * order: the band window of the original KV, then the compressed rows.
@@ -371,17 +450,17 @@ static int64_t sparse_rows(const oracle_sparse_args *a, int b, int64_t q_len, in
     return n;
 }
 
-static const uint16_t *sparse_row_ptr(const oracle_sparse_args *a, int b, int64_t e)
+static const uint8_t *sparse_row_ptr(const oracle_sparse_args *a, int b, int64_t e)
 {
     int64_t r = e >> 1, phys;
     if (e & 1) {
         phys = (int64_t)a->cmp_block_table[(int64_t)b * a->cmp_max_blocks + r / a->cmp_block_size] *
                    a->cmp_block_size + r % a->cmp_block_size;
-        return a->cmp_kv + phys * a->D;
+        return (const uint8_t *)a->cmp_kv + phys * sparse_row_bytes(a);
     }
     phys = (int64_t)a->ori_block_table[(int64_t)b * a->ori_max_blocks + r / a->ori_block_size] *
                a->ori_block_size + r % a->ori_block_size;
-    return a->ori_kv + phys * a->D;
+    return (const uint8_t *)a->ori_kv + phys * sparse_row_bytes(a);
 }
 
 /* out: [rows, N1, D]; lse: [rows, N1] (= [B, N2=1, S1, N1] or [N2=1, T1, N1]).
@@ -434,10 +513,10 @@ int oracle_sparse(const oracle_sparse_args *a, double *out, double *lse, int nth
                 continue;
             }
             for (j = 0; j < n; ++j) {
-                const uint16_t *kr = sparse_row_ptr(a, bb, list[j]);
+                const uint8_t *kr = sparse_row_ptr(a, bb, list[j]);
                 double acc = 0.0;
                 for (d = 0; d < D; ++d)
-                    acc += bf16_bits_to_double(qv[d]) * bf16_bits_to_double(kr[d]);
+                    acc += bf16_bits_to_double(qv[d]) * sparse_value(a, kr, d);
                 s[j] = acc * a->scale;
                 if (s[j] > m) m = s[j];
             }
@@ -445,9 +524,9 @@ int oracle_sparse(const oracle_sparse_args *a, double *out, double *lse, int nth
             for (j = 0; j < n; ++j) l += exp(s[j] - m);
             if (a->sinks) l += exp((double)a->sinks[h] - m);
             for (j = 0; j < n; ++j) {
-                const uint16_t *vr = sparse_row_ptr(a, bb, list[j]);
+                const uint8_t *vr = sparse_row_ptr(a, bb, list[j]);
                 double w = exp(s[j] - m) / l;
-                for (d = 0; d < D; ++d) o[d] += w * bf16_bits_to_double(vr[d]);
+                for (d = 0; d < D; ++d) o[d] += w * sparse_value(a, vr, d);
             }
             if (lse) lse[t] = m + log(l);
         }
@@ -502,11 +581,17 @@ static int64_t or_tiles(int64_t lo, int64_t hi)
     return hi / OR_KV_TILE - lo / OR_KV_TILE + 1;
 }
 
-/* Decode schedule.  Units u = ((b*KVN + hk)*HG + hg): the G query heads of a
- * KV head are taken in groups of GH = 8 (G <= 8) or 16, HG = ceil(G/GH), so
- * a batch has UPB = KVN*HG units, all with the same cost: 0 when the batch has
- * no query row, else the number of KV tiles its single query row can see, at
- * least 1.  With T the sum of all unit costs, n CTAs and W chunks per CTA:
+/* Decode schedule (query rows per sequence S = max_seqlen_q, 1..16).  The
+ * columns of a KV head hk of batch b are its (query row i, query head h of
+ * the GQA group) pairs, numbered c = i*G + (h - hk*G); they are taken in
+ * groups of GH = 8 (S*G <= 8) or 16, HG = ceil(S*G/GH) groups per KV head,
+ * unit u = (b*KVN + hk)*HG + hg, UPB = KVN*HG units per batch.  Of these, the
+ * HA(b) = ceil(q_len(b)*G/GH) first groups of every KV head hold columns
+ * ("active"; A(b) = KVN*HA(b) of them, active index a = hk*HA(b) + hg).  All
+ * active units of a batch cost the same: 0 when the batch has no query row,
+ * else the number of KV tiles its rows can see together (the interval from
+ * the first row's lower bound to the last row's upper bound), at least 1.
+ * With T the sum of all active units' costs, n CTAs and W chunks per CTA:
  *   C  = max(1, ceil(T / (n*W))),  c2 = ceil(C/3);
  *   a unit of cost c has n1 = max(0, floor(c/C) - 1) big chunks of C tiles,
  *   then its remaining c - n1*C tiles in small chunks of c2 tiles (the last
@@ -515,40 +600,55 @@ static int64_t or_tiles(int64_t lo, int64_t hi)
  * chunks), M (batches whose units have more than one chunk), the plan's
  * mark 0x4649414445434F44, B and the CTA count (so that execute can tell a
  * plan of its arguments from anything else in the workspace);
- * Q[b] = sum over b' < b of (n1+n2)(b')*UPB, then R1[b] (big) and R2[b]
- * (small) the same sums of n1*UPB and n2*UPB, each array with B+1 entries;
- * then the M batches with more than one chunk per unit in increasing order,
- * followed by -1 up to B entries.
+ * Q[b] = sum over b' < b of (n1+n2)(b')*A(b'), then R1[b] (big) and R2[b]
+ * (small) the same sums of n1*A and n2*A, each array with B+1 entries; then
+ * the M batches with more than one chunk per unit in increasing order,
+ * followed by -1 up to B entries.  Chunk i of active unit a of batch b owns
+ * partial slot Q[b] + i*A(b) + a.
  * The queue (N entries of four int32) lists for b = 0..B-1, chunk i =
- * 0..n1-1, unit w = 0..UPB-1 the entry (b, i << 10 | w, kv_len(b), first
- * query row of b), then the small chunks in the same nesting with i =
- * n1..n1+n2-1.  Returns N, or -1 if N > cap. */
+ * 0..n1-1, active unit a = 0..A(b)-1 the entry (b, i << 16 | u - b*UPB,
+ * kv_len(b), first query row of b), then the small chunks in the same
+ * nesting with i = n1..n1+n2-1.  Query lengths above S count as S.  Returns
+ * N, or -1 if N > cap. */
 int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32_t per_cta,
                                int64_t *sched, int32_t *queue, int64_t cap)
 {
     int G = a->QN / a->KVN;
-    int HG = (int)or_ceil_div(G, G <= 8 ? 8 : 16);
-    int64_t UPB = (int64_t)a->KVN * HG;
+    int64_t S = a->max_seqlen_q;
+    int GH = S * G <= 8 ? 8 : 16;
+    int64_t HG = or_ceil_div(S * G, GH);
     int B = a->B, b;
     int64_t *Q = sched + 8, *R1 = Q + (B + 1), *R2 = R1 + (B + 1), *SB = R2 + (B + 1);
     int64_t nsplit = 0;
     int64_t *cost = (int64_t *)malloc(sizeof(int64_t) * (B > 0 ? B : 1));
+    int64_t *ha = (int64_t *)malloc(sizeof(int64_t) * (B > 0 ? B : 1));
     int64_t T = 0, C, c2, q = 0, r1 = 0, r2 = 0, n = 0;
     for (b = 0; b < B; ++b) {
-        int64_t ql, qs, kl, lo, hi, c = 0;
+        int64_t ql, qs, kl, lo, hi, lo1, hi1, c = 0;
         fia_lengths(a, b, &ql, &qs, &kl);
+        if (ql > S) ql = S;
+        ha[b] = ql > 0 ? or_ceil_div(ql * G, GH) : 0;
         if (ql > 0) {
-            if (kl > 0 && fia_visible(a, ql, kl, ql - 1, &lo, &hi)) c = or_tiles(lo, hi);
+            if (kl > 0) {
+                /* first row's lower bound, last row's upper bound */
+                int v0 = fia_visible(a, ql, kl, 0, &lo, &hi);
+                int v1 = fia_visible(a, ql, kl, ql - 1, &lo1, &hi1);
+                (void)v0;
+                (void)v1;
+                if (lo < 0) lo = 0;
+                if (hi1 > kl - 1) hi1 = kl - 1;
+                c = or_tiles(lo, hi1);
+            }
             if (c < 1) c = 1;
         }
         cost[b] = c;
-        T += c * UPB;
+        T += c * a->KVN * ha[b];
     }
     C = or_ceil_div(T, (int64_t)num_ctas * per_cta);
     if (C < 1) C = 1;
     c2 = (C + 2) / 3;
     for (b = 0; b < B; ++b) {
-        int64_t n1 = 0, n2 = 0;
+        int64_t n1 = 0, n2 = 0, A = a->KVN * ha[b];
         if (cost[b] > 0) {
             n1 = cost[b] / C - 1;
             if (n1 < 0) n1 = 0;
@@ -559,9 +659,9 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
         R2[b] = r2;
         SB[b] = -1;
         if (n1 + n2 > 1) SB[nsplit++] = b;
-        q += (n1 + n2) * UPB;
-        r1 += n1 * UPB;
-        r2 += n2 * UPB;
+        q += (n1 + n2) * A;
+        r1 += n1 * A;
+        r2 += n2 * A;
     }
     Q[B] = q;
     R1[B] = r1;
@@ -576,34 +676,37 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
     sched[7] = num_ctas;
     if (q > cap) {
         free(cost);
+        free(ha);
         return -1;
     }
     /* big chunks, then small chunks */
-    for (b = 0; b < B; ++b) {
-        int64_t n1 = (R1[b + 1] - R1[b]) / UPB, i, w, ql, qs, kl;
-        fia_lengths(a, b, &ql, &qs, &kl);
-        for (i = 0; i < n1; ++i)
-            for (w = 0; w < UPB; ++w) {
-                queue[4 * n] = b;
-                queue[4 * n + 1] = (int32_t)((i << 10) | w);
-                queue[4 * n + 2] = (int32_t)kl;
-                queue[4 * n + 3] = (int32_t)qs;
-                ++n;
-            }
-    }
-    for (b = 0; b < B; ++b) {
-        int64_t n1 = (R1[b + 1] - R1[b]) / UPB, n2 = (R2[b + 1] - R2[b]) / UPB, i, w, ql, qs, kl;
-        fia_lengths(a, b, &ql, &qs, &kl);
-        for (i = n1; i < n1 + n2; ++i)
-            for (w = 0; w < UPB; ++w) {
-                queue[4 * n] = b;
-                queue[4 * n + 1] = (int32_t)((i << 10) | w);
-                queue[4 * n + 2] = (int32_t)kl;
-                queue[4 * n + 3] = (int32_t)qs;
-                ++n;
+    {
+        int pass;
+        for (pass = 0; pass < 2; ++pass)
+            for (b = 0; b < B; ++b) {
+                int64_t A = a->KVN * ha[b], i, k, ql, qs, kl, i0, i1;
+                if (A == 0) continue;
+                fia_lengths(a, b, &ql, &qs, &kl);
+                if (pass == 0) {
+                    i0 = 0;
+                    i1 = (R1[b + 1] - R1[b]) / A;
+                } else {
+                    i0 = (R1[b + 1] - R1[b]) / A;
+                    i1 = i0 + (R2[b + 1] - R2[b]) / A;
+                }
+                for (i = i0; i < i1; ++i)
+                    for (k = 0; k < A; ++k) {
+                        int64_t w = (k / ha[b]) * HG + k % ha[b];
+                        queue[4 * n] = b;
+                        queue[4 * n + 1] = (int32_t)((i << 16) | w);
+                        queue[4 * n + 2] = (int32_t)kl;
+                        queue[4 * n + 3] = (int32_t)qs;
+                        ++n;
+                    }
             }
     }
     free(cost);
+    free(ha);
     return n;
 }
 
@@ -612,8 +715,9 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
  * when G is odd a pair holds one head).  The KV interval a 128-row query tile
  * [i0, i1] can see is bounded by its first and last rows: lo = max(0, lo(i0)),
  * hi = min(kv_len-1, hi(i1)) with lo(i) = p(i) - pre_tokens for the band mask
- * and 0 otherwise, hi(i) = p(i) for right-down causal, p(i) + next_tokens for
- * the band and kv_len-1 for no mask (p(i) = kv_len - q_len + i).  Both bounds
+ * and 0 otherwise, hi(i) = p(i) for the causal masks, p(i) + next_tokens for
+ * the band and kv_len-1 for modes 0 and 1 (p(i) = kv_len - q_len + i, or i for
+ * the left-up causal mask; an explicit mask does not narrow it).  Both bounds
  * are monotone in the row, so this is the union of the rows' intervals.  The
  * cost of a unit is 1 plus the number of KV tiles that interval touches.  The
  * GPU orders units by non-increasing cost (ties in any order).  Writes
@@ -635,10 +739,10 @@ int64_t oracle_prefill_units(const oracle_fia_args *a, int32_t *units, int64_t *
             int64_t p0, p1, lo, hi, c = 1;
             int hk, pr;
             if (i1 > ql - 1) i1 = ql - 1;
-            p0 = kl - ql + i0;
-            p1 = kl - ql + i1;
+            p0 = (a->mask_mode == OR_MASK_LUC ? 0 : kl - ql) + i0;
+            p1 = (a->mask_mode == OR_MASK_LUC ? 0 : kl - ql) + i1;
             lo = a->mask_mode == OR_MASK_BAND ? p0 - a->pre_tokens : 0;
-            hi = a->mask_mode == OR_MASK_RDC ? p1
+            hi = (a->mask_mode == OR_MASK_RDC || a->mask_mode == OR_MASK_LUC) ? p1
                : a->mask_mode == OR_MASK_BAND ? p1 + a->next_tokens : kl - 1;
             if (lo < 0) lo = 0;
             if (hi > kl - 1) hi = kl - 1;

@@ -449,7 +449,7 @@ def _unit_chunks(sched, queue, B, UPB):
     """{unit: [(queue position, chunk index)]} from the queue entries."""
     out = {}
     for pos, (b, y, _, _) in enumerate(queue.tolist()):
-        w, i = y & 1023, y >> 10
+        w, i = y & 0xFFFF, y >> 16
         assert 0 <= b < B and w < UPB
         out.setdefault(b * UPB + w, []).append((pos, i))
     return out
@@ -491,7 +491,7 @@ def test_decode_schedule_chunks_cover_each_unit_once(ctas, per_cta):
             if n1 > 0:
                 assert C <= rest < 2 * C                 # one big chunk left for the small ones
     # claim order: big chunks, then small, each batch-major, chunk, then unit
-    keys = [(b, y >> 10, y & 1023) for b, y, _, _ in queue.tolist()]
+    keys = [(b, y >> 16, y & 0xFFFF) for b, y, _, _ in queue.tolist()]
     assert keys[:F] == sorted(keys[:F]) and keys[F:] == sorted(keys[F:])
     # every entry carries its batch's KV length and query row (BSND: b * S_q)
     assert [(kl, qr) for b, _, kl, qr in queue.tolist()] == [(kv[b], b) for b, _, _, _ in queue.tolist()]
@@ -506,6 +506,54 @@ def test_decode_schedule_band_counts_window_tiles_only():
     assert sched[0] == 1
     Q = sched[8:11]
     assert list(np.diff(Q)) == [2, 1]
+
+
+@pytest.mark.parametrize("S,G,layout", [(4, 4, fi.LAYOUT_BSND), (2, 8, fi.LAYOUT_BSND),
+                                         (16, 2, fi.LAYOUT_TND), (3, 1, fi.LAYOUT_TND)])
+def test_decode_schedule_multi_row_units(S, G, layout):
+    """Several query rows per sequence: a KV head's columns are its (row,
+    head) pairs, S*G of them in groups of GH = 8 or 16; only the groups that
+    hold columns of the sequence's own rows are scheduled, every active unit
+    of a sequence costs the tiles its rows see together, and each of its
+    chunks owns the slot Q[b] + i * A(b) + a."""
+    kv = [700, 3, 129, 0, 1500]
+    ql = [S] * 5 if layout == fi.LAYOUT_BSND else [S, 1, 0, 2, S]
+    KVN = 2
+    p = fi.make_fia(B=5, QN=G * KVN, KVN=KVN, D=16, q_lens=ql, kv_lens=kv, layout=layout,
+                    block_size=16, mask_mode=3, seed=9)
+    p.S_q = S  # the rows every decode unit covers (max_seqlen_q)
+    GH = 8 if S * G <= 8 else 16
+    HG = -(-S * G // GH)
+    UPB = KVN * HG
+    for ctas, per in ((1, 5), (9, 5), (152, 5)):
+        sched, queue = oracle.decode_schedule(p, ctas, per)
+        B = p.B
+        Q = sched[8:8 + B + 1]
+        HA = [-(-q * G // GH) if q > 0 else 0 for q in ql]
+        A = [KVN * h for h in HA]
+        # cost: tiles from row 0's bound to the last row's bound (causal:
+        # keys 0 .. kv-1 for the last row), at least 1; none without rows
+        cost = [0 if q == 0 else max(1, -(-k // 128)) for q, k in zip(ql, kv)]
+        T = sum(c * a for c, a in zip(cost, A))
+        C = max(1, -(-T // (ctas * per)))
+        assert sched[0] == C
+        chunks = {}
+        for pos, (b, y, klen, qrow) in enumerate(queue.tolist()):
+            w, i = y & 0xFFFF, y >> 16
+            hk, hg = divmod(w, HG)
+            assert hg < HA[b] and hk < KVN          # only units with columns
+            assert klen == kv[b]
+            assert qrow == (b * S if layout == fi.LAYOUT_BSND else sum(ql[:b]))
+            chunks.setdefault((b, w), []).append(i)
+        for b in range(B):
+            for hk in range(KVN):
+                for hg in range(HA[b]):
+                    idx = sorted(chunks[(b, hk * HG + hg)])
+                    assert idx == list(range(len(idx)))
+                    assert Q[b + 1] - Q[b] == len(idx) * A[b]
+            assert Q[b + 1] - Q[b] == 0 or A[b] > 0
+        assert len(chunks) == sum(A)
+        assert queue.shape[0] <= ctas * per + 6 * B * UPB
 
 
 def test_prefill_units_enumerate_every_tile_and_head_pair():

@@ -83,7 +83,7 @@ class CombineParams(ctypes.Structure):
         ("n_parts", _I), ("layout", _I), ("batch", _I), ("seqlen_q", _I), ("total_q", _I),
         ("num_heads", _I), ("head_dim", _I), ("pad0_", _I),
         ("o_parts", ctypes.POINTER(_P)), ("lse_parts", ctypes.POINTER(_P)),
-        ("out", _P), ("lse", _P), ("reserved", _I * 8),
+        ("out", _P), ("lse", _P), ("sinks", _P), ("reserved", _I * 8),
     ]
 
 

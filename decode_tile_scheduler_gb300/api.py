@@ -202,10 +202,12 @@ class SparseCall:
 
 def lse_combine(outs, lses, *, layout: int, num_heads: int, batch: int = 0, seqlen_q: int = 0,
                 total_q: int = 0, out: Optional[torch.Tensor] = None,
-                lse: Optional[torch.Tensor] = None, stream=None):
+                lse: Optional[torch.Tensor] = None, sinks: Optional[torch.Tensor] = None,
+                stream=None):
     """Combine results of the same query rows against disjoint key sets with
     fia_lse_combine.  `outs` are bf16 tensors in the FIA out layout, `lses`
-    the matching fp32 lse tensors.  Returns (out, lse)."""
+    the matching fp32 lse tensors, computed without sinks; `sinks` (fp32
+    [num_heads]) enter here, once.  Returns (out, lse)."""
     import ctypes
     n = len(outs)
     if n != len(lses) or not 1 <= n <= _abi.COMBINE_MAX_PARTS:
@@ -221,6 +223,6 @@ def lse_combine(outs, lses, *, layout: int, num_heads: int, batch: int = 0, seql
     l_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in lses])
     c.o_parts = ctypes.cast(o_arr, ctypes.POINTER(ctypes.c_void_p))
     c.lse_parts = ctypes.cast(l_arr, ctypes.POINTER(ctypes.c_void_p))
-    c.out, c.lse = _ptr(out), _ptr(lse)
+    c.out, c.lse, c.sinks = _ptr(out), _ptr(lse), _ptr(sinks)
     _abi.fia_lse_combine(c, _stream(stream))
     return out, lse

@@ -4,9 +4,9 @@
 // "sparse_flash_mla", CP example: context parallelism across ranks).
 //
 // For one query row and head with part results (O_k, lse_k), k = 0..n-1:
-//   lse = log sum_k e^{lse_k},  O = sum_k e^{lse_k - lse} O_k,
-// parts with lse_k = +inf (no visible key) left out, and O = 0, lse = +inf
-// when every part is left out.  One warp per (token, head) row; each lane
+//   lse = log (sum_k e^{lse_k} + e^{sink}),  O = sum_k e^{lse_k - lse} O_k,
+// parts with lse_k = +inf (no visible key) left out, the sink term only with
+// a sink, and O = 0, lse = +inf when every part is left out.  One warp per (token, head) row; each lane
 // owns 8 consecutive elements of D per pass (16-byte loads and stores), and
 // the parts are folded in index order, so the result does not depend on the
 // launch shape.  HBM-bound: reads n rows of D bf16 and n lse values, writes
@@ -26,6 +26,7 @@ struct CombineArgs {
   const float* l[FIA_COMBINE_MAX_PARTS];
   uint16_t* out;
   float* lse;
+  const float* sinks;
   int n, layout, N, D, S_q;
   int64_t rows;  // tokens * N
 };
@@ -55,14 +56,20 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(const CombineArgs a) {
       lk[k] = k < a.n ? __ldg(a.l[k] + li) : INFINITY;
       if (lk[k] != INFINITY) M = fmaxf(M, lk[k]);
     }
+    // a sink is one more logit with no value, counted once when some part
+    // saw a key (a row that sees no key stays 0 / +inf, with a sink too)
+    const bool any = M != -INFINITY;
+    const float sk = (a.sinks && any) ? __ldg(a.sinks + h) : -INFINITY;
+    const float Mx = fmaxf(M, sk);
     float S = 0.f;
-    if (M != -INFINITY) {
+    if (any) {
 #pragma unroll
       for (int k = 0; k < FIA_COMBINE_MAX_PARTS; ++k)
-        if (lk[k] != INFINITY) S += expf(lk[k] - M);
+        if (lk[k] != INFINITY) S += expf(lk[k] - Mx);
+      if (sk != -INFINITY) S += expf(sk - Mx);
     }
-    const bool empty = M == -INFINITY || !(S > 0.f);
-    const float L = empty ? INFINITY : M + logf(S);
+    const bool empty = !any || !(S > 0.f);
+    const float L = empty ? INFINITY : Mx + logf(S);
     uint16_t* orow = a.out + r * a.D;
     for (int d0 = 8 * lane; d0 < a.D; d0 += 256) {
       float acc[8];
@@ -128,6 +135,7 @@ extern "C" fia_status fia_lse_combine(const fia_combine_params* p, void* stream)
     return FIA_ERR_BAD_SHAPE;
   a.out = static_cast<uint16_t*>(p->out);
   a.lse = p->lse;
+  a.sinks = p->sinks;
   a.n = p->n_parts;
   a.layout = p->layout;
   a.N = p->num_heads;

@@ -1,36 +1,44 @@
 // decode.cu -- the incremental-inference branch of fused inference attention
-// (query length 1; "aclnnFusedInferAttentionScoreV2": the IncreFlashAttention
-// branch runs when the query S is 1) over a paged KV cache, plus its tile
-// scheduler.
+// (a few query rows per sequence; "aclnnFusedInferAttentionScoreV2": the
+// IncreFlashAttention branch runs when the query S is 1; the quantised
+// Decode-MLA rules of "...V5" allow Q_S up to 16 for multi-token decode) over a
+// paged KV cache, plus its tile scheduler.
 //
-// Work unit: (batch b, KV head hk, head group hg).  The query heads of one GQA
-// group share KV head hk; up to 8 (G <= 8) or 16 of them form the N columns
-// of every mma.sync, so each KV page is read from HBM once for the group.  A
-// unit owns the KV tiles (128 positions) its query row can see.
+// Columns and units: the query side of KV head hk of a sequence is its
+// (query row i, query head h of the GQA group) pairs, column c = i*G + h%G,
+// S_max*G of them.  A work unit (batch b, KV head hk, column group hg) holds up
+// to GH = 8 or 16 consecutive columns: they form the N columns of every
+// mma.sync, so each KV page is read from HBM once for all of them (the GQA
+// heads and, for multi-token decode, the query rows too).  Only the groups
+// holding columns of the sequence's own rows are scheduled ("active").  A
+// unit owns the KV tiles (128 positions) its rows see together; every column
+// is masked with its own row's bounds.
 //
 // Scheduler (decode_schedule_kernel): cost(u) = visible tiles (>= 1; 0 when
-// the batch has no query row).  With T the total cost and n persistent CTAs,
-// the chunk size is C = ceil(T / (n * W)) tiles (W chunks per CTA, at least
-// one tile), and a unit of cost c is cut into n1 = max(0, floor(c/C) - 1) big
-// chunks of C tiles followed by the remaining r = c - n1*C tiles (C <= r < 2C
-// unless c < C) in small chunks of c2 = ceil(C/3) tiles.  The claim queue
-// lists every big chunk (batch-major, then chunk, then unit of the batch)
-// before every small chunk (same order), so the work left at the end is
-// always small pieces.  CTAs claim chunks from the queue with one atomic each:
-// an SM that streams faster simply takes more chunks.  A unit cut into several
-// chunks is split-KV: each chunk writes its (m, l, acc) partial to the slot
-// of its (unit, chunk index), and a combine kernel chained behind the decode
-// kernel folds them in chunk order (deterministic, whichever CTAs ran them).
+// the batch has no query row).  With T the total cost of the active units and
+// n persistent CTAs, the chunk size is C = ceil(T / (n * W)) tiles (W chunks
+// per CTA, at least one tile), and a unit of cost c is cut into
+// n1 = max(0, floor(c/C) - 1) big chunks of C tiles followed by the remaining
+// r = c - n1*C tiles (C <= r < 2C unless c < C) in small chunks of
+// c2 = ceil(C/3) tiles.  The claim queue lists every big chunk (batch-major,
+// then chunk, then active unit of the batch) before every small chunk (same
+// order), so the work left at the end is always small pieces.  CTAs claim
+// chunks from the queue with one atomic each: an SM that streams faster
+// simply takes more chunks.  A unit cut into several chunks is split-KV: each
+// chunk writes its (m, l, acc) partial to the slot of its (unit, chunk
+// index), and a combine kernel chained behind the decode kernel folds them in
+// chunk order (deterministic, whichever CTAs ran them).
 //
 // Decode kernel: one producer warp streams K and V pages with TMA (page rows
-// from block_table) into a ring of shared-memory stages; eight consumer warps
-// each take 16 rows of every tile.  The products are computed transposed
-// ("swap AB"): S^T = K Q^T with the KV rows as the mma M dimension and the
-// query heads as N, then O^T += V^T P^T, where P^T comes out of the S^T
-// accumulators with movmatrix.  Softmax is online, in the exp2 domain, per
-// head (column).  FP8 E4M3 pages are widened to fp16 in registers (exact);
-// K tile scales multiply the per-64-column partial scores and V tile scales
-// are folded into P^T, so the dequantised cache is never materialised.
+// from block_table) into a ring of shared-memory stages, with the rows of an
+// explicit mask when there is one; eight consumer warps each take 16 rows of
+// every tile.  The products are computed transposed ("swap AB"):
+// S^T = K Q^T with the KV rows as the mma M dimension and the query columns
+// as N, then O^T += V^T P^T, where P^T comes out of the S^T accumulators with
+// movmatrix.  Softmax is online, in the exp2 domain, per column.  FP8 E4M3
+// pages are widened to fp16 in registers (exact); K tile scales multiply the
+// per-64-column partial scores and V tile scales are folded into P^T, so the
+// dequantised cache is never materialised.
 #include <algorithm>
 #include <atomic>
 
@@ -59,7 +67,10 @@ struct DecodeCfg {
   static constexpr int kNsub = FP8 ? 1 : D / 64;            // 128-byte slices per row
   static constexpr int kTileBytes = kNsub * kKvTile * 128;  // one of K or V
   static constexpr int kScaleBytes = FP8 ? kKvTile * (D / 64) * 4 : 0;
-  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleBytes;
+  // explicit mask: one 128-byte row slice per query row of the unit
+  static constexpr int kMaskBytes = kDecodeMaxRows * kKvTile;
+  static constexpr int kOffMask = 2 * kTileBytes + 2 * kScaleBytes;  // inside a stage
+  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleBytes + kMaskBytes;
   static constexpr int kStages = FP8 ? 5 : (D == 128 ? 3 : 6);
   static constexpr int kQBytes = kMaxGH * D * 2;
   static constexpr int kRedBytes = 4 * 8 * D * 4;           // 4 warps x 8 heads x D
@@ -76,45 +87,72 @@ struct DecodeCfg {
 };
 
 struct UnitInfo {
-  int b, hk, hg, h0, nrows;
-  int64_t qrow;  // token row of q/out
-  int64_t kv_len, lo, hi;
+  int b, hk, hg, c0, ncols;  // columns c0 .. c0 + ncols - 1 of KV head hk
+  int qrow0, q_len, kv_len;  // the batch's first token row; lengths (q_len <= S_max)
+  int lo, hi;                // keys the batch's rows see together
+  int lo_last, hi_first;     // the last row's lower bound, the first row's upper
   int tile0, ntiles;
 };
 
-// Unit u of batch b (unit w of the batch) with the batch's query row, query
-// length and KV length already known.
-__device__ __forceinline__ UnitInfo unit_from(const DecodeArgs& a, int b, int w, int64_t qrow,
-                                              int64_t ql, int64_t kv_len) {
+// Keys [lo, hi] that query row i of a sequence sees, per the mask mode: modes
+// 0 and 1 every key (an explicit mask then hides single keys), 2 the causal
+// mask from the top-left corner (p = i), 3 from the bottom-right corner
+// (p = kv_len - q_len + i), 4 the band p - pre .. p + next.  Clipped to
+// [0, kv_len); hi < lo when the row sees nothing.
+__device__ __forceinline__ void row_bounds(const DecodeArgs& a, int q_len, int kv_len, int i,
+                                           int* lo, int* hi) {
+  const int64_t p = (int64_t)(a.mask_mode == 2 ? 0 : kv_len - q_len) + i;
+  int64_t l = 0, h = (int64_t)kv_len - 1;
+  if (a.mask_mode == 2 || a.mask_mode == 3) {
+    h = min(h, p);
+  } else if (a.mask_mode == 4) {
+    l = max(l, p - a.pre_tokens);
+    h = min(h, p + a.next_tokens);
+  }
+  *lo = (int)min(l, (int64_t)kv_len);
+  *hi = (int)max(h, (int64_t)-1);
+}
+
+// Rows of batch b the decode units cover: its query length, at most S_max.
+__device__ __forceinline__ int clamp_rows(const DecodeArgs& a, int64_t ql) {
+  return (int)min(max(ql, (int64_t)0), (int64_t)a.S_max);
+}
+
+// Active column groups of a KV head of a batch with q_len rows.
+__device__ __forceinline__ int active_groups(const DecodeArgs& a, int q_len) {
+  return q_len > 0 ? (q_len * a.G + a.GH - 1) / a.GH : 0;
+}
+
+// Unit w of batch b with the batch's first token row and lengths known.
+__device__ __forceinline__ UnitInfo unit_from(const DecodeArgs& a, int b, int w, int qrow0,
+                                              int64_t ql, int kv_len) {
   UnitInfo r;
   r.b = b;
   r.hk = w / a.HG;
   r.hg = w % a.HG;
-  r.h0 = r.hk * a.G + r.hg * a.GH;
-  r.nrows = min(a.GH, a.G - r.hg * a.GH);
-  r.qrow = qrow;
+  r.c0 = r.hg * a.GH;
+  r.q_len = clamp_rows(a, ql);
+  r.ncols = max(0, min(a.GH, r.q_len * a.G - r.c0));
+  r.qrow0 = qrow0;
   r.kv_len = kv_len;
-  const int64_t p = r.kv_len - 1;  // the single query row sits at the last key
-  int64_t lo = 0, hi = r.kv_len - 1;
-  if (a.mask_mode == 3) {
-    hi = min(hi, p);
-  } else if (a.mask_mode == 4) {
-    lo = max(lo, p - a.pre_tokens);
-    hi = min(hi, p + a.next_tokens);
-  }
-  r.lo = lo;
-  r.hi = hi;
-  if (ql <= 0 || r.kv_len <= 0 || hi < lo) {
-    r.tile0 = 0;
-    r.ntiles = 0;
-  } else {
-    r.tile0 = (int)(lo / kKvTile);
-    r.ntiles = (int)(hi / kKvTile - lo / kKvTile + 1);
+  r.lo = r.lo_last = 0;
+  r.hi = r.hi_first = -1;
+  r.tile0 = r.ntiles = 0;
+  if (r.q_len > 0 && kv_len > 0) {
+    int lo1, hi0;
+    row_bounds(a, r.q_len, kv_len, 0, &r.lo, &hi0);
+    row_bounds(a, r.q_len, kv_len, r.q_len - 1, &lo1, &r.hi);
+    r.lo_last = lo1;
+    r.hi_first = hi0;
+    if (r.hi >= r.lo) {
+      r.tile0 = r.lo / kKvTile;
+      r.ntiles = r.hi / kKvTile - r.lo / kKvTile + 1;
+    }
   }
   return r;
 }
 
-// Query row, query length and KV length of batch b.
+// First token row, query length and KV length of batch b.
 __device__ __forceinline__ void batch_lengths(const DecodeArgs& a, int b, int64_t* qrow,
                                               int64_t* ql, int64_t* kv_len) {
   if (a.layout == 1) {
@@ -127,19 +165,11 @@ __device__ __forceinline__ void batch_lengths(const DecodeArgs& a, int b, int64_
   *kv_len = a.seqused_kv ? a.seqused_kv[b] : a.S_kv;
 }
 
-__device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int64_t u) {
-  const int per_b = a.KVN * a.HG;
-  const int b = (int)(u / per_b);
-  int64_t qrow, ql, kv_len;
-  batch_lengths(a, b, &qrow, &ql, &kv_len);
-  return unit_from(a, b, (int)(u % per_b), qrow, ql, kv_len);
-}
-
 // What the producer hands the consumers with each chunk's query rows (one per
 // query buffer), so that consumers never wait on global loads between chunks.
 struct UnitMsg {
   UnitInfo r;
-  int64_t u;      // unit; its chunk i owns partial slot Q[b] + i * UPB + (u - b * UPB)
+  int64_t slot;   // partial slot of this chunk: Q[b] + ci * A(b) + active index
   int ci, nch;    // chunk index within the unit, chunks of the unit
   int t_begin, t_end, done;
 };
@@ -166,13 +196,14 @@ __device__ __forceinline__ ChunkGeom chunk_geom(int64_t cost, int64_t C, int64_t
   return g;
 }
 
-// Cost of every unit of batch b (all units of a batch see the same tiles).
-__device__ __forceinline__ int64_t batch_cost(const DecodeArgs& a, int b) {
-  const UnitInfo r = unit_info(a, (int64_t)b * a.KVN * a.HG);
-  int64_t ql;
-  if (a.layout == 1) ql = (int64_t)a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b];
-  else ql = a.S_q;
-  return ql > 0 ? max(1, r.ntiles) : 0;
+// Cost of every active unit of batch b and its active groups per KV head
+// (all active units of a batch see the same tiles).
+__device__ __forceinline__ int64_t batch_cost(const DecodeArgs& a, int b, int* ha) {
+  int64_t qrow, ql, kv_len;
+  batch_lengths(a, b, &qrow, &ql, &kv_len);
+  const UnitInfo r = unit_from(a, b, 0, (int)qrow, ql, (int)kv_len);
+  *ha = active_groups(a, r.q_len);
+  return r.q_len > 0 ? max(1, r.ntiles) : 0;
 }
 
 // largest b with prefix[b] <= g (prefix[0] = 0 <= g < prefix[B])
@@ -195,12 +226,17 @@ __device__ __forceinline__ int64_t page_index(const DecodeArgs& a, int64_t j) {
 }
 // Pool row and FP8 scale row of logical KV row j of batch b, KV head hk, in
 // page blk, with jp = j - block_size * page_index(j) (j's row in its page).
-// FP8 scales are stored head-major inside each page, [pages, KV_N, page rows,
-// D/64] (the paged per-token, per-head scale shape (blockNum, N, blockSize) of
-// the FIA dequantisation parameters, with the 64-element tiles last).
-__device__ __forceinline__ int64_t pool_row(const DecodeArgs& a, int b, int64_t blk, int64_t j,
-                                            int64_t jp) {
-  return a.block_table ? blk * a.block_size + jp : (int64_t)b * a.S_kv + j;
+// Token-major pages [pages, page rows, KV_N, D] are a matrix of KV_N * D
+// columns whose rows are tokens; head-major pages [pages, KV_N, page rows, D]
+// one of D columns whose rows are (page, head, token) ("...V5" Paged
+// Attention group: BnBsH and BnNBsD).  FP8 scales are stored head-major inside
+// each page, [pages, KV_N, page rows, D/64] (the paged per-token, per-head
+// scale shape (blockNum, N, blockSize) of the FIA dequantisation parameters,
+// with the 64-element tiles last).
+__device__ __forceinline__ int64_t pool_row(const DecodeArgs& a, int b, int hk, int64_t blk,
+                                            int64_t j, int64_t jp) {
+  if (!a.block_table) return (int64_t)b * a.S_kv + j;
+  return a.kv_layout == 1 ? (blk * a.KVN + hk) * a.block_size + jp : blk * a.block_size + jp;
 }
 __device__ __forceinline__ int64_t scale_row_in(const DecodeArgs& a, int b, int hk, int64_t blk,
                                                 int64_t j, int64_t jp) {
@@ -273,38 +309,49 @@ __device__ __forceinline__ void scan3(uint32_t (&x)[3], uint32_t (&tot)[3], uint
 
 constexpr int kSchedSmemBatches = 2048;  // per-batch values kept in shared memory up to this B
 
+// Per-batch cost and active groups in one shared-memory word: the cost is at
+// most 20M / 128 tiles (< 2^24), the active groups at most 64.
+__device__ __forceinline__ uint32_t pack_cost(int64_t cost, int ha) {
+  return (uint32_t)cost | ((uint32_t)ha << 24);
+}
+
 __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs a) {
   __shared__ uint32_t ws[32][3];
   __shared__ int64_t ws_total[32];
   // up to kSchedSmemBatches batches: lengths, costs and queue prefixes stay in
   // shared memory, so the batch arrays are read from global memory once
-  __shared__ int s_cost[kSchedSmemBatches], s_kv[kSchedSmemBatches], s_qrow[kSchedSmemBatches];
+  __shared__ uint32_t s_cost[kSchedSmemBatches];
+  __shared__ int s_kv[kSchedSmemBatches], s_qrow[kSchedSmemBatches + 1];
   __shared__ int sR[2][kSchedSmemBatches + 1];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   pdl_trigger();  // the decode kernel may set up while the plan is built
   const int B = a.B;
   const bool small = B <= kSchedSmemBatches;
-  const int UPB = a.KVN * a.HG;
+  const int HG = a.HG;
   int64_t* sched = a.sched;
   int64_t* Q = sched + kSchedHeader;  // [B+1] partial slots before batch b
   int64_t* R1 = Q + (B + 1);          // [B+1] big-chunk queue positions
   int64_t* R2 = R1 + (B + 1);         // [B+1] small-chunk queue positions
   int64_t* SB = R2 + (B + 1);         // [B] batches cut into several chunks, then -1
 
-  // total cost (and, for small B, each batch's lengths and cost)
+  // total cost of the active units (and, for small B, each batch's lengths,
+  // cost and active groups)
   int64_t part = 0;
   for (int b = tid; b < B; b += blockDim.x) {
     int64_t qrow, ql, kv_len;
     batch_lengths(a, b, &qrow, &ql, &kv_len);
-    const UnitInfo r = unit_from(a, b, 0, qrow, ql, kv_len);
-    const int64_t cost = ql > 0 ? max(1, r.ntiles) : 0;
-    part += cost;
+    const UnitInfo r = unit_from(a, b, 0, (int)qrow, ql, (int)kv_len);
+    const int64_t cost = r.q_len > 0 ? max(1, r.ntiles) : 0;
+    const int ha = active_groups(a, r.q_len);
+    part += cost * a.KVN * ha;
     if (small) {
-      s_cost[b] = (int)cost;
+      s_cost[b] = pack_cost(cost, ha);
       s_kv[b] = (int)kv_len;
       s_qrow[b] = (int)qrow;
     }
   }
+  if (small && tid == 0)  // the end of the last batch's rows: query lengths are differences
+    s_qrow[B] = a.layout == 1 ? a.cu_seqlens_q[B] : B * a.S_q;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
   if (lane == 0) ws_total[wid] = part;
@@ -312,7 +359,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
   int64_t total = lane < (int)(blockDim.x >> 5) ? ws_total[lane] : 0;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-  const int64_t T = total * UPB;
+  const int64_t T = total;
   const int64_t per = (int64_t)a.num_ctas * a.chunks_per_cta;
   // C = max(1, ceil(T / per)), with a 32-bit division whenever T allows
   int64_t C = 1;
@@ -322,18 +369,26 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
             : (T - 1) / per + 1;
   const int64_t c2 = (C + 2) / 3;
 
-  // per batch: big and small chunks of its units and whether it is split ->
-  // three exclusive scans (all chunks before b = big + small before b)
+  // per batch: big and small chunks of its active units and whether it is
+  // split -> three exclusive scans (all chunks before b = big + small before b)
   int64_t carry[3] = {0, 0, 0};
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + tid;
     uint32_t x[3] = {0u, 0u, 0u};
     if (b < B) {
-      const int64_t cost = small ? s_cost[b] : batch_cost(a, b);
-      if (cost > 0) {
+      int64_t cost;
+      int ha;
+      if (small) {
+        cost = s_cost[b] & 0xffffffu;
+        ha = (int)(s_cost[b] >> 24);
+      } else {
+        cost = batch_cost(a, b, &ha);
+      }
+      const uint32_t A = (uint32_t)(a.KVN * ha);
+      if (cost > 0 && A > 0) {
         const ChunkGeom gm = chunk_geom(cost, C, c2);
-        x[0] = (uint32_t)gm.n1 * (uint32_t)UPB;
-        x[1] = (uint32_t)(gm.nch - gm.n1) * (uint32_t)UPB;
+        x[0] = (uint32_t)gm.n1 * A;
+        x[1] = (uint32_t)(gm.nch - gm.n1) * A;
         x[2] = gm.nch > 1;
       }
     }
@@ -384,7 +439,6 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
   __syncthreads();
   // the claim queue: big chunks, then small chunks (queue positions below
   // 2^31, as the workspace bound implies, take 32-bit arithmetic)
-  const uint32_t upb = (uint32_t)UPB;
   for (int64_t g = tid; g < N; g += blockDim.x) {
     int b;
     int64_t local, r1 = 0;
@@ -396,26 +450,28 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
       local = g - F - (small ? sR[1][b] : R2[b]);
       r1 = small ? sR[0][b + 1] - sR[0][b] : R1[b + 1] - R1[b];
     }
-    int ci, w;
-    if (N <= 0x7fffffffLL) {
-      const uint32_t qd = (uint32_t)local / upb;
-      w = (int)((uint32_t)local - qd * upb);
-      ci = (int)((uint32_t)r1 / upb + qd);
-    } else {
-      w = (int)(local % UPB);
-      ci = (int)(r1 / UPB + local / UPB);
-    }
-    int kv_len, qrow;
+    int ha, kv_len, qrow, qlen;
     if (small) {
+      ha = (int)(s_cost[b] >> 24);
       kv_len = s_kv[b];
       qrow = s_qrow[b];
+      qlen = clamp_rows(a, (int64_t)s_qrow[b + 1] - s_qrow[b]);
     } else {
       int64_t q64, ql, kv64;
       batch_lengths(a, b, &q64, &ql, &kv64);
+      qlen = clamp_rows(a, ql);
+      ha = active_groups(a, qlen);
       kv_len = (int)kv64;
       qrow = (int)q64;
     }
-    a.queue[g] = make_int4(b, (ci << 10) | w, kv_len, qrow);
+    // a batch with queue entries has active units, so A >= 1
+    const uint32_t A = (uint32_t)max(1, a.KVN * ha);
+    const uint32_t qd = (uint32_t)local / A;
+    const int act = (int)((uint32_t)local - qd * A);  // active unit index
+    const int ci = (int)((uint32_t)r1 / A + qd);
+    const int hac = max(ha, 1);
+    const int w = (act / hac) * HG + act % hac;      // unit of the batch
+    a.queue[g] = make_int4(b | (qlen << 16), (ci << 16) | w, kv_len, qrow);
   }
 }
 
@@ -458,16 +514,17 @@ __device__ __forceinline__ void fold_chunks(const float* base, int64_t kstride, 
   }
 }
 
-__device__ __forceinline__ void combine_store(const DecodeArgs& a, const UnitInfo& r, int head,
-                                              int D, int d, float M, float L, float o0,
+// Final O and lse of one column (query row i of the sequence, head h) whose
+// chunk partials have been folded into (M, L, o0, o1) for the d-pair at d.
+__device__ __forceinline__ void combine_store(const DecodeArgs& a, int b, int64_t tok, int i,
+                                              int h, int D, int d, float M, float L, float o0,
                                               float o1) {
-  const int h = r.h0 + head;
   float scl, lse;
   finish_head(a, h, M, L, &scl, &lse);
-  uint16_t* o = a.out + r.qrow * a.out_stride + (int64_t)h * D + d;
+  uint16_t* o = a.out + tok * a.out_stride + (int64_t)h * D + d;
   *reinterpret_cast<uint32_t*>(o) = pack_bf16(o0 * scl, o1 * scl);
   if (a.lse && d == 0) {
-    const int64_t li = a.layout == 1 ? r.qrow * a.QN + h : ((int64_t)r.b * a.QN + h) * a.S_q;
+    const int64_t li = a.layout == 1 ? tok * a.QN + h : ((int64_t)b * a.QN + h) * a.S_q + i;
     a.lse[li] = lse;
   }
 }
@@ -475,7 +532,11 @@ __device__ __forceinline__ void combine_store(const DecodeArgs& a, const UnitInf
 // ---------------------------------------------------------------------------
 // decode kernel
 // ---------------------------------------------------------------------------
-template <int D, bool FP8, int NG>  // NG: groups of 8 query heads per unit (1 or 2)
+// NG: groups of 8 query columns per unit (1 or 2).  MR: the general form --
+// several query rows per sequence (each column masked with its own row's
+// bounds) or an explicit mask; without it every column of a unit is row 0 of
+// its sequence, shares that row's bounds, and the per-column work drops out.
+template <int D, bool FP8, int NG, bool MR>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv) {
@@ -530,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t C = plan_ok ? a.sched[0] : 1, c2 = plan_ok ? a.sched[1] : 1;
     const int64_t N = plan_ok ? a.sched[2] : 0;
     const int UPB = a.KVN * a.HG;
-    int it = 0, ucount = 0;
+    int it = 0, ucount = 0;  // tiles and chunks issued
     // CTA c starts with queue entry c (no claim on the way to the first
     // loads); the entries after the first gridDim.x are claimed with the
     // counter, each claim issued one chunk ahead and read only after the
@@ -546,12 +607,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t gn = N;
       int4 ent_n = make_int4(0, 0, 0, 0);
       bool fetched = false;
-      const int b = ent.x, ci = ent.y >> 10, w = ent.y & 1023;
-      const bool ent_ok = b >= 0 && b < a.B && ci >= 0 && w < UPB && ent.z >= 0 &&
-                          ent.z <= a.S_kv && ent.w >= 0 && ent.w < a.q_rows;
+      // entry: (b | q_len << 16, chunk << 16 | unit of b, kv_len, first token row)
+      const int b = ent.x & 0xffff, ql = (int)((uint32_t)ent.x >> 16);
+      const int ci = (int)((uint32_t)ent.y >> 16), w = ent.y & 0xffff;
+      bool ent_ok = b < a.B && ql >= 1 && ql <= a.S_max && w < UPB && ent.z >= 0 &&
+                    ent.z <= a.S_kv && ent.w >= 0 && (int64_t)ent.w + ql <= a.q_rows;
+      const UnitInfo r = unit_from(a, b, w, ent.w, ql, ent.z);
+      const int ha = active_groups(a, r.q_len);
+      ent_ok = ent_ok && r.hg < ha && r.ncols > 0;  // an active unit of the batch
       if (!ent_ok && lane == 0) atomicExch(a.err, 2);
-      const int64_t u = (int64_t)b * UPB + w;
-      const UnitInfo r = unit_from(a, b, w, ent.w, 1, ent.z);
       const int64_t cost = max(1, r.ntiles);
       const ChunkGeom gm = chunk_geom(cost, C, c2);
       int t_begin, t_end;
@@ -563,22 +627,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         t_end = (int)min(cost, t_begin + c2);
       }
       if (!ent_ok || ci >= gm.nch) t_begin = t_end = 0;  // nothing of a bad entry runs
-      if (ent_ok && ci < gm.nch) {  // chunk description + query rows of the group (one bulk copy)
+      // query rows of the unit's columns: one row of the sequence per range
+      // (without MR every column is row 0)
+      const int i_first = MR ? r.c0 / a.G : 0;
+      const int i_last = MR ? (r.c0 + max(r.ncols, 1) - 1) / a.G : 0;
+      if (ent_ok && ci < gm.nch) {  // chunk description + the columns' query vectors
         const int qs = ucount & 1;
         wait_or_abort(&qempty[qs], ((ucount >> 1) & 1) ^ 1, a.err, misc);
         if (lane == 0) {
           UnitMsg& m = msg[qs];
           m.r = r;
-          m.u = u;
+          // partial slot: Q[b] + ci * A(b) + active index (clamped by the consumers)
+          m.slot = (int64_t)ci * (a.KVN * ha) + r.hk * ha + r.hg;
           m.ci = ci;
           m.nch = gm.nch;
           m.t_begin = t_begin;
           m.t_end = t_end;
           m.done = 0;
-          const uint32_t bytes = (uint32_t)(r.nrows * D * 2);
-          mbar_arrive_expect_tx(&qfull[qs], bytes);
-          bulk_load(smem + Cfg::kOffQ + qs * Cfg::kQBytes,
-                    a.q + r.qrow * a.q_stride + (int64_t)r.h0 * D, bytes, &qfull[qs]);
+          mbar_arrive_expect_tx(&qfull[qs], (uint32_t)(r.ncols * D * 2));
+        }
+        __syncwarp();
+        // the columns of query row i are heads cb - i*G .. ce - 1 - i*G of the
+        // group, contiguous in q: one bulk copy per row, row i from lane i - i_first
+        for (int i = i_first + lane; i <= i_last; i += 32) {
+          const int cb = max(r.c0, i * a.G), ce = min(r.c0 + r.ncols, (i + 1) * a.G);
+          bulk_load(smem + Cfg::kOffQ + qs * Cfg::kQBytes + (cb - r.c0) * D * 2,
+                    a.q + ((int64_t)r.qrow0 + i) * a.q_stride +
+                        ((int64_t)r.hk * a.G + cb - i * a.G) * D,
+                    (uint32_t)((ce - cb) * D * 2), &qfull[qs]);
         }
         ++ucount;
       }
@@ -596,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int npg = 0, mypage = 0;
       if (a.block_table && r.ntiles > 0 && t_begin < t_end) {
         const int64_t jlo = (int64_t)(r.tile0 + t_begin) * kKvTile;
-        const int64_t jhi = min((int64_t)(r.tile0 + t_end) * kKvTile, r.kv_len);
+        const int64_t jhi = min((int64_t)(r.tile0 + t_end) * kKvTile, (int64_t)r.kv_len);
         pg0 = page_index(a, jlo);
         npg = (int)(page_index(a, jhi - 1) - pg0 + 1);
         if (npg <= 32 && lane < npg)
@@ -621,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           blk = 0;
         }
-        const int64_t prow = mine ? pool_row(a, r.b, blk, jb, jp) : 0;
+        const int64_t prow = mine ? pool_row(a, r.b, r.hk, blk, jb, jp) : 0;
         constexpr int NT = D / 64;
         // FP8: the scales of one head inside a page are contiguous rows of NT
         // floats, so each (K or V, page piece) is one bulk copy next to its
@@ -644,18 +720,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t scale_bytes = 0;
         if constexpr (FP8)
           scale_bytes = __reduce_add_sync(0xffffffffu, scale_ok ? (uint32_t)(srows * NT * 4) : 0u);
+        // explicit mask: the tile's slice of each of the unit's query rows,
+        // 16-byte pieces up to kv_len (row strides are multiples of 16 that
+        // cover the KV capacity, so the copy stays inside the row)
+        const int mrow_bytes = (MR && a.mask)
+                                   ? (int)min((int64_t)kKvTile, ((int64_t)r.kv_len - j0 + 15) & ~(int64_t)15)
+                                   : 0;
+        const int nmrows = (MR && a.mask) ? i_last - i_first + 1 : 0;
         wait_or_abort(&empty[s], par, a.err, misc);
         if (*reinterpret_cast<volatile int*>(misc)) break;  // issue nothing after a time-out
         uint8_t* st = smem + s * Cfg::kStageBytes;
         if (lane == 0) {
           uint32_t bytes = (uint32_t)(2 * nvalid * Cfg::kNsub * a.box_rows * 128);
           if constexpr (FP8) bytes += scale_bytes;
+          bytes += (uint32_t)(nmrows * mrow_bytes);
           mbar_arrive_expect_tx(&full[s], bytes);
         }
         __syncwarp();
+        if (MR && lane < nmrows)
+          bulk_load(st + Cfg::kOffMask + lane * kKvTile,
+                    a.mask + (int64_t)r.b * a.mask_bstride +
+                        (int64_t)(i_first + lane) * a.mask_rstride + j0,
+                    (uint32_t)mrow_bytes, &full[s]);
         if (mine) {
           uint8_t* dst = st + isv * Cfg::kTileBytes + sub * (kKvTile * 128) + rb * a.box_rows * 128;
-          const int col = FP8 ? r.hk * D : r.hk * D + sub * 64;
+          const int col = (a.kv_layout == 1 ? 0 : r.hk * D) + (FP8 ? 0 : sub * 64);
           tma_load_2d(dst, isv ? &tv : &tk, &full[s], col, (int)prow);
           if constexpr (FP8) {
             float* sdst = reinterpret_cast<float*>(st + 2 * Cfg::kTileBytes) +
@@ -728,14 +817,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier), so the stop decision is one barrier OR over the consumers
     if (named_bar_or(1, nthr, msg[qs].done || *reinterpret_cast<volatile int*>(misc))) break;
     const UnitInfo r = msg[qs].r;
-    const int kvl = (int)r.kv_len, lo32 = (int)r.lo, hi32 = (int)r.hi;
-    const int64_t u = msg[qs].u;
-    const int64_t slot0 = a.sched[kSchedHeader + r.b] + (u - (int64_t)r.b * a.KVN * a.HG);
+    const int kvl = r.kv_len;
+    // this chunk's partial slot: Q[b] + chunk * A(b) + active index
+    const int64_t slot0 = a.sched[kSchedHeader + r.b] + msg[qs].slot;
     const int t_begin = msg[qs].t_begin, t_end = msg[qs].t_end;
-    const int ci = msg[qs].ci, nch = msg[qs].nch;
+    const int nch = msg[qs].nch;
     const bool split = nch > 1;
-    const int64_t UPB = (int64_t)a.KVN * a.HG;
     const int64_t pstride = (int64_t)a.GH * (D + 2);  // floats per partial slot
+    // keys seen by the query rows of accumulator columns 2*q4 + e of each
+    // group of 8 (every column its own row; columns past the unit's count
+    // take its last one), and their rows among the unit's mask rows
+    int loc[NG][2], hic[NG][2], mrow[NG][2];
+    if constexpr (MR) {
+      const int i_first = r.c0 / a.G;
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = (r.c0 + min(ng * 8 + 2 * q4 + e, max(r.ncols, 1) - 1)) / a.G;
+          row_bounds(a, r.q_len, kvl, i, &loc[ng][e], &hic[ng][e]);
+          mrow[ng][e] = (i - i_first) * kKvTile;
+        }
+    } else {
+      // one row: the unit's bounds are every column's
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          loc[ng][e] = r.lo;
+          hic[ng][e] = r.hi;
+          mrow[ng][e] = 0;
+        }
+    }
 
     // ---- Q^T fragments (mma B operand: k = d, n = head) ----
     uint32_t qb[NG][KS][2];
@@ -746,8 +859,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t* qsm = reinterpret_cast<const uint16_t*>(smem + Cfg::kOffQ + qs * Cfg::kQBytes);
 #pragma unroll
       for (int ng = 0; ng < NG; ++ng) {
-        const int head = ng * 8 + g;
-        const bool ok = head < r.nrows;
+        const int head = ng * 8 + g;  // the unit's column in this lane's B fragments
+        const bool ok = head < r.ncols;
         slc[ng][0] = slc[ng][1] = a.scale_log2;
         if constexpr (!FP8) {
 #pragma unroll
@@ -901,7 +1014,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // KV positions in 32 bits: lengths are int32, so every position and
       // bound here is below 2^31
       const int jw = (r.tile0 + t) * kKvTile + R0;  // first KV row of this warp
-      const bool edge = (jw < lo32) || (jw + kRowsPerWarp - 1 > hi32);
+      // rows of this warp some column may not see (every column sees keys
+      // lo_last .. hi_first, and hi_first < kv_len, so a tail is an edge)
+      const bool edge =
+          (jw < r.lo_last) || (jw + kRowsPerWarp - 1 > r.hi_first) || (MR && a.mask != nullptr);
       const bool tail = (jw + kRowsPerWarp > kvl);
       // KV positions of fragment rows g and g+8
       const int jg0 = jw + rho16(g), jg1 = jw + rho16(g + 8);
@@ -964,24 +1080,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      // ---------------- mask + online softmax per head ----------------
-      const bool ok0 = !(edge || tail) || (jg0 >= lo32 && jg0 <= hi32);
-      const bool ok1 = !(edge || tail) || (jg1 >= lo32 && jg1 <= hi32);
+      // ---------------- mask + online softmax per column ----------------
       float corr[NG][2];
       // the reference moves only when a score passes it by more than 8 (log2
       // units): p <= 2^8 stays exact enough in 16-bit P, and the
       // accumulators are rarely rescaled.  One warp vote finds out whether
-      // any head needs that; only then are the row maxima reduced.
+      // any column needs that; only then are the row maxima reduced.
       float xs[NG][4];
       bool over = false;
+      if (!edge) {
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            xs[ng][e] = sc[ng][e] * slc[ng][e];
+            xs[ng][2 + e] = sc[ng][2 + e] * slc[ng][e];
+          }
+      } else {
+        // each column against its own row's bounds, and the explicit mask's
+        // bytes of that row (staged with the tile) where there is one
+        const uint8_t* mk = stp + Cfg::kOffMask;
+        const int ta = R0 + rho16(g), tb = R0 + rho16(g + 8);  // rows within the tile
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            bool okA = jg0 >= loc[ng][e] && jg0 <= hic[ng][e];
+            bool okB = jg1 >= loc[ng][e] && jg1 <= hic[ng][e];
+            if (MR && a.mask) {
+              okA = okA && mk[mrow[ng][e] + ta] == 0;
+              okB = okB && mk[mrow[ng][e] + tb] == 0;
+            }
+            xs[ng][e] = okA ? sc[ng][e] * slc[ng][e] : -INFINITY;
+            xs[ng][2 + e] = okB ? sc[ng][2 + e] * slc[ng][e] : -INFINITY;
+          }
+      }
 #pragma unroll
       for (int ng = 0; ng < NG; ++ng)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          xs[ng][e] = ok0 ? sc[ng][e] * slc[ng][e] : -INFINITY;
-          xs[ng][2 + e] = ok1 ? sc[ng][2 + e] * slc[ng][e] : -INFINITY;
-          over |= fmaxf(xs[ng][e], xs[ng][2 + e]) > m_r[ng][e] + 8.f;
-        }
+        for (int e = 0; e < 2; ++e) over |= fmaxf(xs[ng][e], xs[ng][2 + e]) > m_r[ng][e] + 8.f;
       const bool any_over = __any_sync(0xffffffffu, over);
 #pragma unroll
       for (int ng = 0; ng < NG; ++ng) {
@@ -1232,25 +1369,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       named_bar_sync(1, nthr);
-      // all consumer threads: write this head group (final O or a partial)
-      const int nh = min(8, r.nrows - ng * 8);
+      // all consumer threads: write this group of 8 columns (final O or a partial)
+      const int nh = min(8, r.ncols - ng * 8);
       if (!split) {
         for (int idx = ctid; idx < nh * (D / 2); idx += nthr) {
           const int hh = idx / (D / 2), d = (idx % (D / 2)) * 2;
-          const int h = r.h0 + ng * 8 + hh;
+          const int c = r.c0 + ng * 8 + hh;                 // column: query row i, head h
+          const int i = c / a.G, h = r.hk * a.G + (c - i * a.G);
+          const int64_t tok = (int64_t)r.qrow0 + i;
           float scl, lse;
           finish_head(a, h, red_ml[hh * 2], red_ml[hh * 2 + 1], &scl, &lse);
-          uint16_t* o = a.out + r.qrow * a.out_stride + (int64_t)h * D + d;
+          uint16_t* o = a.out + tok * a.out_stride + (int64_t)h * D + d;
           *reinterpret_cast<uint32_t*>(o) = pack_bf16(red[d * 8 + hh] * scl, red[(d + 1) * 8 + hh] * scl);
           if (a.lse && d == 0) {
-            const int64_t li = a.layout == 1 ? r.qrow * a.QN + h : ((int64_t)r.b * a.QN + h) * a.S_q;
+            const int64_t li = a.layout == 1 ? tok * a.QN + h : ((int64_t)r.b * a.QN + h) * a.S_q + i;
             a.lse[li] = lse;
           }
         }
       } else {
         // (clamped: a plan of other lengths cannot move the write out of the
         // partial slots; the combine rejects such a plan's prefixes)
-        const int64_t slot = min(max(slot0 + ci * UPB, (int64_t)0), a.max_chunks - 1);
+        const int64_t slot = min(max(slot0, (int64_t)0), a.max_chunks - 1);
         float* pp = a.partials + slot * pstride;
         for (int idx = ctid; idx < nh * (D + 2); idx += nthr) {
           const int hh = idx / (D + 2), d = idx % (D + 2);
@@ -1269,22 +1408,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 // list of such batches; the partials are folded in chunk order.
 // ---------------------------------------------------------------------------
 struct CombineItem {
-  UnitInfo r;  // h0, b, qrow are used
-  int head, nch;
-  const float* base;
+  int b, i, h;         // batch, query row of the sequence, query head
+  int64_t tok;         // token row of q/out
+  int nch;             // chunks of the unit
+  int64_t kstride;     // floats between the unit's consecutive chunk partials
+  const float* base;   // the column's partial in the unit's first chunk
 };
 
+// Item pr of the combine: (split batch m, active unit index act of it, column
+// col of the unit), pr = (m * UPB + act) * GH + col; false for indices past
+// the batch's active units or the unit's columns.
 __device__ __forceinline__ bool combine_item(const DecodeArgs& a, int64_t pr, int D,
                                              CombineItem* it) {
   const int64_t UPB = (int64_t)a.KVN * a.HG;
   const int64_t* Q = a.sched + kSchedHeader;
   const int64_t* SB = Q + 3 * ((int64_t)a.B + 1);
-  it->head = (int)(pr % a.GH);
-  const int64_t bw = pr / a.GH;
-  const int w = (int)(bw % UPB);
-  const int hg = w % a.HG;
-  if (it->head >= min(a.GH, a.G - hg * a.GH)) return false;  // past the group's heads
-  const int64_t b64 = SB[bw / UPB];
+  const int col = (int)(pr % a.GH);
+  const int64_t ma = pr / a.GH;
+  const int act = (int)(ma % UPB);
+  const int64_t b64 = SB[ma / UPB];
   // an entry outside the batches or the partial slots (a plan of other
   // lengths) is skipped: the decode kernel has reported the plan
   if (b64 < 0 || b64 >= a.B) {
@@ -1292,15 +1434,26 @@ __device__ __forceinline__ bool combine_item(const DecodeArgs& a, int64_t pr, in
     return false;
   }
   const int b = (int)b64;
-  if (Q[b] < 0 || Q[b + 1] < Q[b] + UPB || Q[b + 1] > a.max_chunks) {
+  int64_t qrow, ql, kv_len;
+  batch_lengths(a, b, &qrow, &ql, &kv_len);
+  const int qlen = clamp_rows(a, ql);
+  const int ha = active_groups(a, qlen);
+  const int A = a.KVN * ha;
+  if (act >= A) return false;  // past the batch's active units
+  const int hk = act / ha, hg = act % ha;
+  const int c = hg * a.GH + col;
+  if (c >= qlen * a.G || col >= a.GH) return false;  // past the unit's columns
+  if (Q[b] < 0 || Q[b + 1] < Q[b] + A || Q[b + 1] > a.max_chunks || (Q[b + 1] - Q[b]) % A) {
     atomicExch(a.err, 2);
     return false;
   }
-  it->nch = (int)((Q[b + 1] - Q[b]) / UPB);
-  it->r.b = b;
-  it->r.h0 = (w / a.HG) * a.G + hg * a.GH;
-  it->r.qrow = a.layout == 1 ? (int64_t)a.cu_seqlens_q[b] : (int64_t)b * a.S_q;
-  it->base = a.partials + (Q[b] + w) * (int64_t)a.GH * (D + 2) + it->head * (D + 2);
+  it->b = b;
+  it->i = c / a.G;
+  it->h = hk * a.G + (c - it->i * a.G);
+  it->tok = qrow + it->i;
+  it->nch = (int)((Q[b + 1] - Q[b]) / A);
+  it->kstride = (int64_t)A * a.GH * (D + 2);
+  it->base = a.partials + (Q[b] + act) * (int64_t)a.GH * (D + 2) + col * (D + 2);
   return true;
 }
 
@@ -1315,7 +1468,6 @@ __global__ void __launch_bounds__(256, 4) decode_combine_flat(const DecodeArgs a
   // the first item is located while the decode kernel still runs; only the
   // partials need its completion.
   const int64_t items = a.sched[4] * a.KVN * a.HG * a.GH;
-  const int64_t kstride = (int64_t)a.KVN * a.HG * a.GH * (D + 2);
   const int d = 2 * (threadIdx.x % TPP);
   int64_t pr = (int64_t)blockIdx.x * PPB + threadIdx.x / TPP;
   CombineItem it;
@@ -1324,8 +1476,8 @@ __global__ void __launch_bounds__(256, 4) decode_combine_flat(const DecodeArgs a
   while (pr < items) {
     if (have) {
       float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f;
-      fold_chunks<D>(it.base, kstride, d, 0, 1, it.nch, M, L, o0, o1);
-      combine_store(a, it.r, it.head, D, d, M, L, o0, o1);
+      fold_chunks<D>(it.base, it.kstride, d, 0, 1, it.nch, M, L, o0, o1);
+      combine_store(a, it.b, it.tok, it.i, it.h, D, d, M, L, o0, o1);
     }
     pr += (int64_t)gridDim.x * PPB;
     have = pr < items && combine_item(a, pr, D, &it);
@@ -1342,7 +1494,6 @@ __global__ void __launch_bounds__(256, 4) decode_combine_grouped(const DecodeArg
   constexpr int TPP = D / 2, NGRP = 256 / TPP;
   __shared__ float4 st[NGRP][TPP];
   const int64_t items = a.sched[4] * a.KVN * a.HG * a.GH;
-  const int64_t kstride = (int64_t)a.KVN * a.HG * a.GH * (D + 2);
   const int grp = threadIdx.x / TPP, t = threadIdx.x % TPP, d = 2 * t;
   int64_t pr = blockIdx.x;
   CombineItem it;
@@ -1351,7 +1502,7 @@ __global__ void __launch_bounds__(256, 4) decode_combine_grouped(const DecodeArg
   for (; pr < items; pr += gridDim.x, have = pr < items && combine_item(a, pr, D, &it)) {
     if (!have) continue;  // uniform over the CTA
     float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f;
-    fold_chunks<D>(it.base, kstride, d, grp, NGRP, it.nch, M, L, o0, o1);
+    fold_chunks<D>(it.base, it.kstride, d, grp, NGRP, it.nch, M, L, o0, o1);
     st[grp][t] = make_float4(M, L, o0, o1);
     __syncthreads();
     if (grp == 0) {
@@ -1366,7 +1517,7 @@ __global__ void __launch_bounds__(256, 4) decode_combine_grouped(const DecodeArg
         o1 = o1 * fo + x.w * fn;
         M = Mn;
       }
-      combine_store(a, it.r, it.head, D, d, M, L, o0, o1);
+      combine_store(a, it.b, it.tok, it.i, it.h, D, d, M, L, o0, o1);
     }
     __syncthreads();
   }
@@ -1385,11 +1536,11 @@ cudaError_t launch_decode_schedule(const DecodeArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int D, bool FP8, int NG>
+template <int D, bool FP8, int NG, bool MR>
 static cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& tk,
                                    const CUtensorMap& tv, cudaStream_t s) {
   using Cfg = DecodeCfg<D, FP8>;
-  auto kern = decode_kernel<D, FP8, NG>;
+  auto kern = decode_kernel<D, FP8, NG, MR>;
   // the shared-memory opt-in is per device and function: set it once for each
   static std::atomic<uint64_t> done_mask[4];
   int dev = 0;
@@ -1404,15 +1555,23 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& tk,
   return launch_pdl(kern, dim3(a.num_ctas), dim3(kThreads), Cfg::kSmem, s, a, tk, tv);
 }
 
+template <int D, bool FP8, int NG>
+static cudaError_t launch_decode_mr(const DecodeArgs& a, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, cudaStream_t s) {
+  const bool mr = a.S_max > 1 || a.mask != nullptr;
+  return mr ? launch_decode_t<D, FP8, NG, true>(a, tk, tv, s)
+            : launch_decode_t<D, FP8, NG, false>(a, tk, tv, s);
+}
+
 static cudaError_t launch_decode_main(const DecodeArgs& a, const CUtensorMap& tk,
                                       const CUtensorMap& tv, int fp8, cudaStream_t s) {
   const bool two = a.GH > 8;
-  if (fp8) return two ? launch_decode_t<128, true, 2>(a, tk, tv, s)
-                      : launch_decode_t<128, true, 1>(a, tk, tv, s);
-  if (a.D == 64) return two ? launch_decode_t<64, false, 2>(a, tk, tv, s)
-                            : launch_decode_t<64, false, 1>(a, tk, tv, s);
-  return two ? launch_decode_t<128, false, 2>(a, tk, tv, s)
-             : launch_decode_t<128, false, 1>(a, tk, tv, s);
+  if (fp8) return two ? launch_decode_mr<128, true, 2>(a, tk, tv, s)
+                      : launch_decode_mr<128, true, 1>(a, tk, tv, s);
+  if (a.D == 64) return two ? launch_decode_mr<64, false, 2>(a, tk, tv, s)
+                            : launch_decode_mr<64, false, 1>(a, tk, tv, s);
+  return two ? launch_decode_mr<128, false, 2>(a, tk, tv, s)
+             : launch_decode_mr<128, false, 1>(a, tk, tv, s);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -94,7 +94,11 @@ fia_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, in
 // ---------------------------------------------------------------------------
 // FIA validation ("...V5" constraint catalogue, the parts this library builds)
 // ---------------------------------------------------------------------------
-bool is_decode(const fia_params* p) { return p->max_seqlen_q == 1; }
+// The decode kernel takes sequences of up to kDecodeMaxRows query rows (the
+// incremental branch; multi-token decode); longer ones run on the prefill kernel.
+bool is_decode(const fia_params* p) {
+  return p->max_seqlen_q >= 1 && p->max_seqlen_q <= kDecodeMaxRows;
+}
 
 int64_t kv_capacity_of(const fia_params* p) {
   return p->block_table ? (int64_t)p->max_blocks_per_seq * p->block_size : p->max_seqlen_kv;
@@ -124,7 +128,7 @@ fia_status validate(const fia_params* p) {
     return FIA_ERR_BAD_SHAPE;
   if (p->atten_mask) {
     if (!aligned16(p->atten_mask) || p->mask_row_stride <= 0 || p->mask_row_stride % 16 ||
-        p->mask_batch_stride < 0)
+        p->mask_batch_stride < 0 || p->mask_batch_stride % 16)
       return FIA_ERR_BAD_SHAPE;
   }
   if (p->kv_layout != FIA_KV_LAYOUT_BNBSH && p->kv_layout != FIA_KV_LAYOUT_BNNBSD)
@@ -157,7 +161,9 @@ fia_status validate(const fia_params* p) {
     if (p->kv_dtype == FIA_KV_FP8_E4M3 && (p->block_size % 32 || p->block_size > 512))
       return FIA_ERR_BAD_SHAPE;
     if (p->num_blocks <= 0 || p->max_blocks_per_seq <= 0) return FIA_ERR_BAD_SHAPE;
-    if ((int64_t)p->num_blocks * p->block_size > INT32_MAX) return FIA_ERR_BAD_SHAPE;
+    if ((int64_t)p->num_blocks * p->block_size *
+            (p->kv_layout == FIA_KV_LAYOUT_BNNBSD ? p->num_kv_heads : 1) > INT32_MAX)
+      return FIA_ERR_BAD_SHAPE;
     if ((int64_t)p->max_blocks_per_seq * p->block_size > 20971520) return FIA_ERR_BAD_SHAPE;
   } else {
     if (p->max_seqlen_kv < 0 || p->max_seqlen_kv > 20971520) return FIA_ERR_BAD_SHAPE;
@@ -170,8 +176,9 @@ fia_status validate(const fia_params* p) {
   }
   // what is built
   if (p->head_dim != 64 && p->head_dim != 128) return FIA_ERR_UNSUPPORTED;
-  if (p->atten_mask || p->mask_mode == FIA_MASK_ALL || p->mask_mode == FIA_MASK_LEFT_UP_CAUSAL ||
-      p->kv_layout != FIA_KV_LAYOUT_BNBSH)
+  if (!is_decode(p) && (p->atten_mask || p->mask_mode == FIA_MASK_ALL ||
+                        p->mask_mode == FIA_MASK_LEFT_UP_CAUSAL ||
+                        p->kv_layout != FIA_KV_LAYOUT_BNBSH))
     return FIA_ERR_UNSUPPORTED;
   if (p->kv_dtype == FIA_KV_FP8_E4M3 && (p->head_dim != 128 || !is_decode(p)))
     return FIA_ERR_UNSUPPORTED;
@@ -194,11 +201,14 @@ fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
   fia_status st = sm_count(p->num_sms, &n);
   if (st != FIA_OK) return st;
   const int G = p->num_q_heads / p->num_kv_heads;
-  const int GH = decode_group_heads(G);
-  const int HG = (int)ceil_div(G, GH);
+  const int cols = p->max_seqlen_q * G;  // (query row, head) columns of a KV head
+  const int GH = decode_group_heads(cols);
+  const int HG = (int)ceil_div(cols, GH);
   pl->n = n;
   pl->U = (int64_t)p->batch * p->num_kv_heads * HG;
   pl->max_chunks = (int64_t)n * kDecodeChunksPerCta + 6 * pl->U;
+  // queue positions and slots are 32-bit in the kernels
+  if (pl->max_chunks >= INT32_MAX) return FIA_ERR_BAD_SHAPE;
   int64_t off = kAlign;
   pl->off_sched = off;
   off = align_up(off + 8 * (kSchedHeader + 3 * ((int64_t)p->batch + 1) + p->batch));
@@ -219,10 +229,15 @@ DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
   a.KVN = p->num_kv_heads;
   a.D = p->head_dim;
   a.G = G;
-  a.GH = decode_group_heads(G);
-  a.HG = (int)ceil_div(G, a.GH);
+  a.GH = decode_group_heads(p->max_seqlen_q * G);
+  a.HG = (int)ceil_div(p->max_seqlen_q * G, a.GH);
   a.layout = p->layout;
   a.S_q = p->layout == FIA_LAYOUT_BSND ? p->max_seqlen_q : 1;
+  a.S_max = p->max_seqlen_q;
+  a.kv_layout = p->block_table ? p->kv_layout : 0;
+  a.mask = p->atten_mask;
+  a.mask_bstride = p->mask_batch_stride;
+  a.mask_rstride = p->mask_row_stride;
   a.q = static_cast<const uint16_t*>(p->q);
   a.q_stride = p->q_token_stride ? p->q_token_stride : (int64_t)p->num_q_heads * p->head_dim;
   a.out = static_cast<uint16_t*>(p->out);
@@ -260,11 +275,18 @@ DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
   return a;
 }
 
+// Tensor maps of the K and V caches: token-major pools (and contiguous
+// caches) as a matrix of KV_N * D columns with one row per token, head-major
+// pools [num_blocks, KV_N, block_size, D] as one of D columns with one row per
+// (block, head, token).
 fia_status kv_maps(const fia_params* p, int box_rows, CUtensorMap* tk, CUtensorMap* tv) {
   const bool fp8 = p->kv_dtype == FIA_KV_FP8_E4M3;
-  const uint64_t cols = (uint64_t)p->num_kv_heads * p->head_dim;
-  const uint64_t rows = p->block_table ? (uint64_t)p->num_blocks * p->block_size
-                                       : (uint64_t)p->batch * p->max_seqlen_kv;
+  const bool head_major = p->block_table && p->kv_layout == FIA_KV_LAYOUT_BNNBSD;
+  const uint64_t cols = head_major ? (uint64_t)p->head_dim
+                                   : (uint64_t)p->num_kv_heads * p->head_dim;
+  const uint64_t rows = p->block_table
+                            ? (uint64_t)p->num_blocks * p->block_size * (head_major ? p->num_kv_heads : 1)
+                            : (uint64_t)p->batch * p->max_seqlen_kv;
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int es = fp8 ? 1 : 2;
   const uint32_t bc = fp8 ? 128 : 64;

@@ -10,16 +10,22 @@ namespace fia {
 
 constexpr int kKvTile = 128;   // KV positions per tile (one split granule)
 constexpr int kQTile = 128;    // query rows per prefill tile
-constexpr int kMaxHeadGroup = 16;  // query heads packed per decode unit, at most
+constexpr int kMaxHeadGroup = 16;  // query columns packed per decode unit, at most
+constexpr int kDecodeMaxRows = 16; // query rows per sequence the decode kernel takes
 
-// Query heads per decode unit: the GQA group in mma N columns of 8.
-inline int decode_group_heads(int G) { return G <= 8 ? 8 : 16; }
+// Columns per decode unit: the (query row, query head) pairs of a KV head,
+// S rows x G heads of them, in mma N columns of 8 (up to 16 per unit).
+inline int decode_group_heads(int cols) { return cols <= 8 ? 8 : 16; }
 
 // Everything the decode schedule and the decode kernel read.
 struct DecodeArgs {
-  int B, QN, KVN, D, G, GH, HG;  // GH heads per unit, HG units per GQA group
+  int B, QN, KVN, D, G, GH, HG;  // GH columns per unit, HG units per KV head
   int layout;            // 0 BSND, 1 TND
-  int S_q;               // BSND query length (1)
+  int S_q;               // BSND query length
+  int S_max;             // query rows per sequence the units cover (1..16)
+  int kv_layout;         // 0 [nb, bs, KVN, D], 1 [nb, KVN, bs, D]
+  const uint8_t* mask;   // explicit mask (modes 0/1) or null
+  int64_t mask_bstride, mask_rstride;
   const uint16_t* q;     // bf16
   int64_t q_stride;      // elements between tokens
   uint16_t* out;
@@ -45,9 +51,9 @@ struct DecodeArgs {
   int64_t num_units;           // B * KVN * HG
   int64_t max_chunks;          // partial slots: a bound on the number of chunks
   int64_t* sched;              // [8 + 3(B+1) + B]: C, c2, chunks, big chunks, split
-                               // batches, 3 zeros; the partial-slot prefix Q, the queue
-                               // prefixes R1, R2; the split batches (then -1)
-  int4* queue;                 // [max_chunks] (b, chunk << 10 | unit of b, kv_len, qrow)
+                               // batches, mark, B, CTAs; the partial-slot prefix Q, the
+                               // queue prefixes R1, R2; the split batches (then -1)
+  int4* queue;                 // [max_chunks] (b, chunk << 16 | unit of b, kv_len, qrow)
   int* claim;                  // [2]: next queue entry, CTAs done with the queue
   int64_t* prefill_mark;       // header word of a prefill plan: a decode plan clears it
   float* partials;             // [max_chunks][GH][D + 2]: acc, then m and l

@@ -241,8 +241,12 @@ fia_status fia_decode_run_noalloc(const fia_params *p, int32_t *status, void *st
  * of the keys, it writes the result against their union:
  *   lse = log sum_k exp(lse_k),   O = sum_k exp(lse_k - lse) * O_k.
  * Parts with lse_k = +inf saw no key and are skipped; when every part is
- * skipped, O = 0 and lse = +inf (the empty-row rule).  A sink belongs to one
- * part only: run the other parts without sinks.
+ * skipped, O = 0 and lse = +inf (the empty-row rule).  Sinks: run every part
+ * without them and pass them here (fp32 [N], nullable); each enters the sum
+ * once as one more logit that carries no value,
+ *   lse = log(sum_k exp(lse_k) + exp(sink_h)),
+ * which gives the result of one call over all keys with the sinks (a part
+ * that kept the sink would lose it whenever that part sees no key).
  * Layouts are those of fia_params' out and lse: O bf16 [tokens, N, D] (BSND
  * tokens = B * S_q, TND tokens = T) and lse fp32 BSND [B, N, S_q] or TND
  * [T, N].  o_parts and lse_parts are HOST arrays of n_parts DEVICE pointers
@@ -265,6 +269,7 @@ typedef struct fia_combine_params {
     const float *const *lse_parts;  /* host array [n_parts] of device pointers */
     void *out;                /* bf16 [tokens, N, D]                           */
     float *lse;               /* fp32, nullable                                */
+    const float *sinks;       /* fp32 [N], nullable                            */
     int32_t reserved[8];      /* must be 0                                     */
 } fia_combine_params;
 fia_status fia_lse_combine(const fia_combine_params *p, void *stream);

@@ -296,13 +296,15 @@ def e8m0_to_double(code: int) -> float:
     return lib().oracle_e8m0_to_double(code)
 
 
-def lse_combine(outs, lses):
+def lse_combine(outs, lses, sinks=None, head_axis=None):
     """Attention over the union of disjoint key sets from the results over
     each set ("aclnnFusedInferAttentionScoreV2", softmax_lse restriction: the
     lse exists for ring attention, which joins partial results this way):
-        lse = log sum_k exp(lse_k),   O = sum_k exp(lse_k - lse) * O_k,
+        lse = log(sum_k exp(lse_k) + exp(sink)),   O = sum_k exp(lse_k - lse) * O_k,
     leaving out parts with lse_k = +inf (they saw no key); when every part is
-    left out, O = 0 and lse = +inf.  `outs[k]` is [..., D], `lses[k]` the
+    left out, O = 0 and lse = +inf.  The parts are computed without sinks;
+    `sinks[h]` (optional) is the sink of head h, the index along `head_axis`
+    of the lse arrays, added once.  `outs[k]` is [..., D], `lses[k]` the
     matching [...]; fp64 throughout, parts in the order given."""
     outs = [np.asarray(o, dtype=np.float64) for o in outs]
     lses = [np.asarray(l, dtype=np.float64) for l in lses]
@@ -313,6 +315,8 @@ def lse_combine(outs, lses):
         vals = [l[idx] for l in lses if not np.isinf(l[idx])]
         if not vals:
             continue
+        if sinks is not None:
+            vals.append(float(sinks[idx[head_axis]]))
         m = max(vals)
         tot = m + math.log(sum(math.exp(v - m) for v in vals))
         lse[idx] = tot

@@ -606,8 +606,9 @@ static int64_t or_tiles(int64_t lo, int64_t hi)
  * followed by -1 up to B entries.  Chunk i of active unit a of batch b owns
  * partial slot Q[b] + i*A(b) + a.
  * The queue (N entries of four int32) lists for b = 0..B-1, chunk i =
- * 0..n1-1, active unit a = 0..A(b)-1 the entry (b, i << 16 | u - b*UPB,
- * kv_len(b), first query row of b), then the small chunks in the same
+ * 0..n1-1, active unit a = 0..A(b)-1 the entry (b | q_len(b) << 16,
+ * i << 16 | u - b*UPB, kv_len(b), first query row of b), then the small
+ * chunks in the same
  * nesting with i = n1..n1+n2-1.  Query lengths above S count as S.  Returns
  * N, or -1 if N > cap. */
 int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32_t per_cta,
@@ -687,6 +688,7 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
                 int64_t A = a->KVN * ha[b], i, k, ql, qs, kl, i0, i1;
                 if (A == 0) continue;
                 fia_lengths(a, b, &ql, &qs, &kl);
+                if (ql > S) ql = S;
                 if (pass == 0) {
                     i0 = 0;
                     i1 = (R1[b + 1] - R1[b]) / A;
@@ -697,7 +699,7 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
                 for (i = i0; i < i1; ++i)
                     for (k = 0; k < A; ++k) {
                         int64_t w = (k / ha[b]) * HG + k % ha[b];
-                        queue[4 * n] = b;
+                        queue[4 * n] = (int32_t)(b | (ql << 16));
                         queue[4 * n + 1] = (int32_t)((i << 16) | w);
                         queue[4 * n + 2] = (int32_t)kl;
                         queue[4 * n + 3] = (int32_t)qs;

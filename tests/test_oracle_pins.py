@@ -448,7 +448,8 @@ def test_sparse_csa_equals_dense_over_gathered_rows():
 def _unit_chunks(sched, queue, B, UPB):
     """{unit: [(queue position, chunk index)]} from the queue entries."""
     out = {}
-    for pos, (b, y, _, _) in enumerate(queue.tolist()):
+    for pos, (x, y, _, _) in enumerate(queue.tolist()):
+        b = x & 0xFFFF
         w, i = y & 0xFFFF, y >> 16
         assert 0 <= b < B and w < UPB
         out.setdefault(b * UPB + w, []).append((pos, i))
@@ -491,10 +492,13 @@ def test_decode_schedule_chunks_cover_each_unit_once(ctas, per_cta):
             if n1 > 0:
                 assert C <= rest < 2 * C                 # one big chunk left for the small ones
     # claim order: big chunks, then small, each batch-major, chunk, then unit
-    keys = [(b, y >> 16, y & 0xFFFF) for b, y, _, _ in queue.tolist()]
+    keys = [(x & 0xFFFF, y >> 16, y & 0xFFFF) for x, y, _, _ in queue.tolist()]
     assert keys[:F] == sorted(keys[:F]) and keys[F:] == sorted(keys[F:])
-    # every entry carries its batch's KV length and query row (BSND: b * S_q)
-    assert [(kl, qr) for b, _, kl, qr in queue.tolist()] == [(kv[b], b) for b, _, _, _ in queue.tolist()]
+    # every entry carries its batch, query length (one row here), KV length
+    # and first query row (BSND: b * S_q)
+    assert all(x >> 16 == 1 for x, _, _, _ in queue.tolist())
+    assert [(kl, qr) for x, _, kl, qr in queue.tolist()] == \
+        [(kv[x & 0xFFFF], x & 0xFFFF) for x, _, _, _ in queue.tolist()]
 
 
 def test_decode_schedule_band_counts_window_tiles_only():
@@ -538,7 +542,9 @@ def test_decode_schedule_multi_row_units(S, G, layout):
         C = max(1, -(-T // (ctas * per)))
         assert sched[0] == C
         chunks = {}
-        for pos, (b, y, klen, qrow) in enumerate(queue.tolist()):
+        for pos, (x, y, klen, qrow) in enumerate(queue.tolist()):
+            b, qlen = x & 0xFFFF, x >> 16
+            assert qlen == min(ql[b], S)
             w, i = y & 0xFFFF, y >> 16
             hk, hg = divmod(w, HG)
             assert hg < HA[b] and hk < KVN          # only units with columns

@@ -214,33 +214,42 @@ def test_oracle_matches_naive_with_masks(case):
 # log-sum-exp combine ("...V2" softmax_lse: the ring-attention use)
 # --------------------------------------------------------------------------
 
-def _kv_part(p, first_block, n_blocks, sinks=True):
+def _kv_part(p, first_block, n_blocks):
     """The same decode problem restricted to keys [first_block*bs,
     (first_block+n_blocks)*bs) of each sequence (clipped to its length),
-    built by slicing the block table and the lengths."""
+    built by slicing the block table and the lengths; without sinks."""
     bs = p.block_size
     lens = [max(0, min(k, (first_block + n_blocks) * bs) - first_block * bs) for k in p.kv_lens]
     bt = p.block_table[:, first_block:first_block + n_blocks].contiguous()
     return dataclasses.replace(p, block_table=bt, kv_lens=lens,
-                               seqused_kv=torch.tensor(lens, dtype=torch.int32),
-                               sinks=p.sinks if sinks else None)
+                               seqused_kv=torch.tensor(lens, dtype=torch.int32), sinks=None)
 
 
-@pytest.mark.parametrize("cuts", [[2], [1, 3], [1, 2, 3]])
+@pytest.mark.parametrize("cuts", [[2], [1, 3], [1, 2, 3], [5, 8]])
 def test_combine_of_disjoint_key_parts_equals_the_whole(cuts):
+    # the cut at block 5 leaves the second and third sequences without keys
+    # in the later parts; the sink enters through the combine
     p = fi.make_fia(B=3, QN=8, KVN=2, D=32, q_lens=[1] * 3, kv_lens=[70, 17, 33],
                     block_size=8, with_sinks=True, seed=21)
     bounds = [0] + cuts + [p.max_blocks]
     parts = []
     for k in range(len(bounds) - 1):
-        part = _kv_part(p, bounds[k], bounds[k + 1] - bounds[k], sinks=(k == 0))
-        parts.append(oracle.fia(part))
+        parts.append(oracle.fia(_kv_part(p, bounds[k], bounds[k + 1] - bounds[k])))
     # one query row per sequence: out [B, QN, D] goes with lse [B, QN]
     out, lse = oracle.lse_combine([o for o, _ in parts],
-                                  [l.reshape(p.B, p.QN) for _, l in parts])
+                                  [l.reshape(p.B, p.QN) for _, l in parts],
+                                  sinks=p.sinks.numpy(), head_axis=1)
     ow, lw = oracle.fia(p)
     np.testing.assert_allclose(out, ow, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lse, lw.reshape(p.B, p.QN), rtol=0, atol=1e-12)
+
+
+def test_combine_sink_alone_does_not_make_a_row_visible():
+    # every part empty: 0 / +inf even with a sink (the empty-row rule)
+    o = np.ones((2, 3, 4))
+    l = np.full((2, 3), np.inf)
+    out, lse = oracle.lse_combine([o, o], [l, l], sinks=np.array([0.5, 1.0, 2.0]), head_axis=1)
+    assert np.all(out == 0.0) and np.all(np.isinf(lse))
 
 
 def test_combine_skips_empty_parts_and_keeps_the_empty_rule():

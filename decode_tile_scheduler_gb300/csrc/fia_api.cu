@@ -100,6 +100,11 @@ bool is_decode(const fia_params* p) {
   return p->max_seqlen_q >= 1 && p->max_seqlen_q <= kDecodeMaxRows;
 }
 
+int64_t q_rows_of(const fia_params* p) {
+  return p->layout == FIA_LAYOUT_TND ? (int64_t)p->total_q
+                                     : (int64_t)p->batch * p->max_seqlen_q;
+}
+
 int64_t kv_capacity_of(const fia_params* p) {
   return p->block_table ? (int64_t)p->max_blocks_per_seq * p->block_size : p->max_seqlen_kv;
 }
@@ -176,12 +181,7 @@ fia_status validate(const fia_params* p) {
   }
   // what is built
   if (p->head_dim != 64 && p->head_dim != 128) return FIA_ERR_UNSUPPORTED;
-  if (!is_decode(p) && (p->atten_mask || p->mask_mode == FIA_MASK_ALL ||
-                        p->mask_mode == FIA_MASK_LEFT_UP_CAUSAL ||
-                        p->kv_layout != FIA_KV_LAYOUT_BNBSH))
-    return FIA_ERR_UNSUPPORTED;
-  if (p->kv_dtype == FIA_KV_FP8_E4M3 && (p->head_dim != 128 || !is_decode(p)))
-    return FIA_ERR_UNSUPPORTED;
+  if (p->kv_dtype == FIA_KV_FP8_E4M3 && p->head_dim != 128) return FIA_ERR_UNSUPPORTED;
   return FIA_OK;
 }
 
@@ -307,6 +307,10 @@ struct PrefillPlan {
   int n, per_pair, npairs, max_cost;
   int64_t U_max;
   int64_t off_seq, off_hist, off_list, total;
+  // FP8 caches: their fp16 copies [B, cap, KVN, D], the fp16 queries
+  // [rows, QN, D] with their factors [rows * QN], the largest scales and the
+  // K/V factors [B * KVN * 2] (all 0 for bf16 caches)
+  int64_t off_kbf, off_vbf, off_q, off_qfac, off_smax, off_kvfac;
 };
 
 fia_status prefill_plan(const fia_params* p, PrefillPlan* pl) {
@@ -329,8 +333,79 @@ fia_status prefill_plan(const fia_params* p, PrefillPlan* pl) {
   off = align_up(off + 4 * ((int64_t)pl->max_cost + 2));
   pl->off_list = off;
   off = align_up(off + 8 * pl->U_max);
+  pl->off_kbf = pl->off_vbf = pl->off_q = pl->off_qfac = pl->off_smax = pl->off_kvfac = 0;
+  if (p->kv_dtype == FIA_KV_FP8_E4M3) {
+    const int64_t bytes = 2 * (int64_t)p->batch * kv_capacity_of(p) * p->num_kv_heads * p->head_dim;
+    const int64_t rows = q_rows_of(p);
+    pl->off_kbf = off;
+    off = align_up(off + bytes);
+    pl->off_vbf = off;
+    off = align_up(off + bytes);
+    pl->off_q = off;
+    off = align_up(off + 2 * rows * p->num_q_heads * p->head_dim);
+    pl->off_qfac = off;
+    off = align_up(off + 4 * rows * p->num_q_heads);
+    pl->off_smax = off;
+    off = align_up(off + 8 * (int64_t)p->batch * p->num_kv_heads);
+    pl->off_kvfac = off;
+    off = align_up(off + 8 * (int64_t)p->batch * p->num_kv_heads);
+  }
   pl->total = off;
   return FIA_OK;
+}
+
+// The parameters the tcgen05 prefill kernel runs on: for FP8 caches, their
+// fp16 copies in the workspace as contiguous caches [B, cap, KVN, D] and the
+// fp16 queries (16-bit elements move through the same tensor maps).
+fia_params prefill_view(const fia_params* p, const PrefillPlan& pl, void* ws) {
+  fia_params v = *p;
+  if (p->kv_dtype != FIA_KV_FP8_E4M3) return v;
+  char* w = static_cast<char*>(ws);
+  v.k_cache = w + pl.off_kbf;
+  v.v_cache = w + pl.off_vbf;
+  v.q = w + pl.off_q;
+  v.q_token_stride = (int64_t)p->num_q_heads * p->head_dim;
+  v.max_seqlen_kv = (int32_t)kv_capacity_of(p);
+  v.kv_dtype = FIA_KV_BF16;
+  v.k_scale = v.v_scale = nullptr;
+  v.quant_tile = 0;
+  v.block_table = nullptr;
+  v.max_blocks_per_seq = v.block_size = v.num_blocks = 0;
+  v.kv_layout = FIA_KV_LAYOUT_BNBSH;
+  return v;
+}
+
+DequantArgs dequant_args(const fia_params* p, const PrefillPlan& pl, void* ws) {
+  DequantArgs d;
+  memset(&d, 0, sizeof d);
+  d.B = p->batch;
+  d.KVN = p->num_kv_heads;
+  d.D = p->head_dim;
+  d.cap = (int)kv_capacity_of(p);
+  d.kv_layout = p->block_table ? p->kv_layout : 0;
+  d.k = static_cast<const uint8_t*>(p->k_cache);
+  d.v = static_cast<const uint8_t*>(p->v_cache);
+  d.k_scale = p->k_scale;
+  d.v_scale = p->v_scale;
+  d.block_table = p->block_table;
+  d.max_blocks = p->max_blocks_per_seq;
+  d.block_size = p->block_table ? p->block_size : 1;
+  d.num_blocks = p->num_blocks;
+  d.seqused_kv = p->seqused_kv;
+  char* w = static_cast<char*>(ws);
+  d.k_out = reinterpret_cast<uint16_t*>(w + pl.off_kbf);
+  d.v_out = reinterpret_cast<uint16_t*>(w + pl.off_vbf);
+  d.smax = reinterpret_cast<uint32_t*>(w + pl.off_smax);
+  d.kvfac = reinterpret_cast<float*>(w + pl.off_kvfac);
+  d.QN = p->num_q_heads;
+  d.layout = p->layout;
+  d.S_q = p->max_seqlen_q;
+  d.q_rows = q_rows_of(p);
+  d.q_stride = p->q_token_stride ? p->q_token_stride : (int64_t)p->num_q_heads * p->head_dim;
+  d.q = static_cast<const uint16_t*>(p->q);
+  d.q_out = reinterpret_cast<uint16_t*>(w + pl.off_q);
+  d.qfac = reinterpret_cast<float*>(w + pl.off_qfac);
+  return d;
 }
 
 PrefillArgs prefill_args(const fia_params* p, const PrefillPlan& pl, void* ws) {
@@ -345,6 +420,10 @@ PrefillArgs prefill_args(const fia_params* p, const PrefillPlan& pl, void* ws) {
   a.per_pair = pl.per_pair;
   a.layout = p->layout;
   a.S_q = p->max_seqlen_q;
+  a.kv_layout = p->block_table ? p->kv_layout : 0;
+  a.mask = p->atten_mask;
+  a.mask_bstride = p->mask_batch_stride;
+  a.mask_rstride = p->mask_row_stride;
   a.out = static_cast<uint16_t*>(p->out);
   a.out_stride = p->out_token_stride ? p->out_token_stride : (int64_t)p->num_q_heads * p->head_dim;
   a.lse = p->lse;
@@ -581,7 +660,8 @@ fia_status fia_plan(const fia_params* p, void* ws, size_t ws_bytes, void* stream
     PrefillPlan pp;
     st = prefill_plan(p, &pp);
     if (st != FIA_OK) return st;
-    PrefillArgs a = prefill_args(p, pp, ws);
+    const fia_params v = prefill_view(p, pp, ws);
+    PrefillArgs a = prefill_args(&v, pp, ws);
     return launch_prefill_schedule(a, s) == cudaSuccess ? FIA_OK : FIA_ERR_CUDA;
   }
   DecodePlan pl;
@@ -602,12 +682,24 @@ fia_status fia_execute(const fia_params* p, void* ws, size_t ws_bytes, void* str
     PrefillPlan pp;
     st = prefill_plan(p, &pp);
     if (st != FIA_OK) return st;
-    PrefillArgs a = prefill_args(p, pp, ws);
+    const fia_params v = prefill_view(p, pp, ws);
+    PrefillArgs a = prefill_args(&v, pp, ws);
+    if (p->kv_dtype == FIA_KV_FP8_E4M3) {
+      char* w = static_cast<char*>(ws);
+      a.qfac = reinterpret_cast<const float*>(w + pp.off_qfac);
+      a.kvfac = reinterpret_cast<const float*>(w + pp.off_kvfac);
+    }
     CUtensorMap tq, tk, tv;
-    st = q_map(p, &tq);
+    st = q_map(&v, &tq);
     if (st != FIA_OK) return st;
-    st = kv_maps(p, a.box_rows, &tk, &tv);
+    st = kv_maps(&v, a.box_rows, &tk, &tv);
     if (st != FIA_OK) return st;
+    if (p->kv_dtype == FIA_KV_FP8_E4M3) {
+      int n;
+      st = sm_count(p->num_sms, &n);
+      if (st != FIA_OK) return st;
+      if (launch_kv_dequant(dequant_args(p, pp, ws), n, s) != cudaSuccess) return FIA_ERR_CUDA;
+    }
     return launch_prefill(a, tq, tk, tv, s) == cudaSuccess ? FIA_OK : FIA_ERR_CUDA;
   }
   DecodePlan pl;

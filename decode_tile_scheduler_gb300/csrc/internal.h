@@ -80,6 +80,13 @@ struct PrefillArgs {
   int B, QN, KVN, D, G, npairs, per_pair;  // per_pair query heads per unit (2, or 1 if G odd)
   int layout;
   int S_q;
+  int kv_layout;             // 0 [nb, bs, KVN, D], 1 [nb, KVN, bs, D]
+  const uint8_t* mask;       // explicit mask (modes 0/1) or null
+  int64_t mask_bstride, mask_rstride;
+  // fp16 operands (FP8 caches): the scores of row (token t, head h) are
+  // S' * qfac[t*QN + h] * kvfac[(b*KVN + hk)*2], the output O' * kvfac[.. + 1]
+  const float* qfac;
+  const float* kvfac;
   int64_t out_stride;
   uint16_t* out;
   float* lse;
@@ -139,6 +146,34 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUte
 size_t decode_smem_bytes(int D, int fp8);
 
 cudaError_t launch_prefill_schedule(const PrefillArgs& a, cudaStream_t s);
+
+// FP8 K/V for the prefill kernel: every visible row of the paged (or
+// contiguous) E4M3 caches dequantised once into contiguous fp16 caches
+// [B, cap, KVN, D] in the workspace, each (batch, KV head) scaled by a power
+// of two that keeps it inside fp16, and the queries converted to fp16 with a
+// power-of-two shift per (token, head).
+struct DequantArgs {
+  int B, KVN, D, cap, kv_layout;
+  const uint8_t* k;
+  const uint8_t* v;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* block_table;  // null: contiguous [B, cap, KVN, D]
+  int max_blocks, block_size;
+  int64_t num_blocks;
+  const int32_t* seqused_kv;   // null: cap for every batch
+  uint16_t* k_out;
+  uint16_t* v_out;
+  uint32_t* smax;              // [B * KVN * 2] largest K and V scale (bits), zeroed first
+  float* kvfac;                // [B * KVN * 2] the power of two taken out of K and V
+  // queries
+  int QN, layout, S_q;
+  int64_t q_rows, q_stride;
+  const uint16_t* q;           // bf16
+  uint16_t* q_out;             // fp16 [q_rows, QN, D]
+  float* qfac;                 // [q_rows * QN]
+};
+cudaError_t launch_kv_dequant(const DequantArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t s);
 

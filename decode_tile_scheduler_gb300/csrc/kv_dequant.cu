@@ -1,0 +1,174 @@
+// kv_dequant.cu -- FP8 E4M3 K/V for the prefill branch.
+//
+// The FIA pages allow FP8 K/V with per-64-element fp32 scales in the prefill
+// layouts as well ("aclnnFusedInferAttentionScoreV5", FLOAT8_E4M3FN key/value
+// rules and the DequantChecker group).  Prefill is bound by the tensor cores,
+// and each K/V tile is read by every 128-row query tile and head pair of its
+// sequence, so the visible rows are dequantised once, here, into contiguous
+// caches in the workspace, and the tcgen05 prefill kernel runs on those with
+// fp16 operands (11 significant bits: a code times its fp32 scale keeps its
+// value to 2^-12, where bf16 would lose it at 2^-9 -- too coarse for the
+// 1e-3 lse bound).  fp16's range is kept by powers of two that the prefill
+// kernel takes back exactly:
+//   K', V': every (batch, KV head) divided by 2^E, E the exponent of its
+//           largest K (V) scale, so |K'| < 2 * 448;
+//   Q':     every (token, head) times 2^sh, sh = 15 - (the exponent of its
+//           largest element), kept in [-100, 100] -- the same exact move the
+//           FP8 decode kernel makes.
+// The scores of row (t, h) are then S' * 2^-sh * 2^EK, and the output O' * 2^EV.
+//
+// Three passes, all HBM-bound and short next to the prefill: the largest
+// scale of each (batch, KV head) (an atomic maximum over the float bits,
+// positive floats ordering like their bit patterns), the K/V conversion (one
+// thread per 16 elements of a (batch, row, head) vector), the Q conversion
+// (one warp per (token, head)).  Rows at or past a batch's KV length are not
+// touched (the prefill kernel masks their scores and zeroes their V rows).
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fia {
+
+namespace {
+
+// Code offset and scale row of element d0 of (batch b, row j, head hk); false
+// when the row's page lies outside the pool.
+__device__ __forceinline__ bool locate(const DequantArgs& a, int b, int j, int hk, int d0,
+                                       int64_t* code_off, int64_t* scale_row) {
+  if (a.block_table) {
+    const int64_t blk = a.block_table[(int64_t)b * a.max_blocks + j / a.block_size];
+    if (blk < 0 || blk >= a.num_blocks) return false;
+    const int jp = j % a.block_size;
+    *code_off = a.kv_layout == 1 ? ((blk * a.KVN + hk) * a.block_size + jp) * a.D + d0
+                                 : ((blk * a.block_size + jp) * a.KVN + hk) * a.D + d0;
+    *scale_row = (blk * a.KVN + hk) * a.block_size + jp;
+  } else {
+    *code_off = (((int64_t)b * a.cap + j) * a.KVN + hk) * a.D + d0;
+    *scale_row = ((int64_t)b * a.KVN + hk) * a.cap + j;
+  }
+  return true;
+}
+
+// Largest K and V scale of every (batch, KV head) over its visible rows.
+__global__ void __launch_bounds__(256) scale_max_kernel(const DequantArgs a) {
+  const int NT = a.D / 64;
+  const int64_t total = (int64_t)a.B * a.cap * a.KVN;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t bj = t / a.KVN;
+    const int hk = (int)(t - bj * a.KVN);
+    const int b = (int)(bj / a.cap), j = (int)(bj - (int64_t)b * a.cap);
+    const int kv_len = a.seqused_kv ? a.seqused_kv[b] : a.cap;
+    int64_t off, srow;
+    if (j >= kv_len || !locate(a, b, j, hk, 0, &off, &srow)) continue;
+    uint32_t mk = 0, mv = 0;
+    for (int k = 0; k < NT; ++k) {
+      mk = max(mk, __float_as_uint(fabsf(__ldg(a.k_scale + srow * NT + k))));
+      mv = max(mv, __float_as_uint(fabsf(__ldg(a.v_scale + srow * NT + k))));
+    }
+    atomicMax(a.smax + ((int64_t)b * a.KVN + hk) * 2, mk);
+    atomicMax(a.smax + ((int64_t)b * a.KVN + hk) * 2 + 1, mv);
+  }
+}
+
+// 2^-E for the largest scale bits m (E its exponent, kept in [-100, 100]);
+// a zero or non-finite maximum takes 1.
+__device__ __forceinline__ float inv_pow2_of(uint32_t m) {
+  const int e = (int)((m >> 23) & 0xffu);
+  if (e == 0 || e == 0xff) return 1.f;
+  const int E = min(max(e - 127, -100), 100);
+  return __int_as_float((127 - E) << 23);
+}
+
+__global__ void __launch_bounds__(256) kv_dequant_kernel(const DequantArgs a) {
+  const int per_row = a.KVN * (a.D / 16);  // threads per (batch, row)
+  const int64_t total = (int64_t)a.B * a.cap * per_row;
+  const int NT = a.D / 64;
+  // the factors the prefill kernel multiplies back (thread 0 of the grid)
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < a.B * a.KVN * 2; i += blockDim.x)
+      a.kvfac[i] = 1.f / inv_pow2_of(a.smax[i]);
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t bj = t / per_row;
+    const int rest = (int)(t - bj * per_row);
+    const int b = (int)(bj / a.cap);
+    const int j = (int)(bj - (int64_t)b * a.cap);
+    const int kv_len = a.seqused_kv ? a.seqused_kv[b] : a.cap;
+    if (j >= kv_len) continue;
+    const int hk = rest / (a.D / 16), d0 = (rest % (a.D / 16)) * 16;
+    int64_t code_off, scale_row;
+    if (!locate(a, b, j, hk, d0, &code_off, &scale_row)) continue;
+    const int64_t out_off = (((int64_t)b * a.cap + j) * a.KVN + hk) * a.D + d0;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint8_t* src = kv ? a.v : a.k;
+      const float f = inv_pow2_of(__ldg(a.smax + ((int64_t)b * a.KVN + hk) * 2 + kv));
+      const float sc = __ldg((kv ? a.v_scale : a.k_scale) + scale_row * NT + d0 / 64) * f;
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(src + code_off));
+      const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t lo, hi;
+        e4m3x4_to_f16x2x2(cw[w], lo, hi);  // exact: E4M3 values are fp16 values
+        const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+        const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+        o[2 * w] = pack_f16(fl.x * sc, fl.y * sc);
+        o[2 * w + 1] = pack_f16(fh.x * sc, fh.y * sc);
+      }
+      uint16_t* dst = (kv ? a.v_out : a.k_out) + out_off;
+      reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
+// Q to fp16: one warp per (token, head), D/32 elements per lane (D = 128).
+__global__ void __launch_bounds__(256) q_convert_kernel(const DequantArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t total = a.q_rows * a.QN;
+  const int per = a.D / 32;  // 4
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < total;
+       r += (int64_t)gridDim.x * (blockDim.x >> 5)) {
+    const int64_t tok = r / a.QN;
+    const int h = (int)(r - tok * a.QN);
+    const uint16_t* src = a.q + tok * a.q_stride + (int64_t)h * a.D + lane * per;
+    const uint2 v = *reinterpret_cast<const uint2*>(src);  // 4 bf16
+    uint32_t e = max(max((v.x >> 7) & 0xffu, (v.x >> 23) & 0xffu),
+                     max((v.y >> 7) & 0xffu, (v.y >> 23) & 0xffu));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) e = max(e, __shfl_xor_sync(0xffffffffu, e, o));
+    const int sh = min(max(142 - (int)e, -100), 100);  // 15 - (e - 127)
+    const float up = __int_as_float((127 + sh) << 23);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    *reinterpret_cast<uint2*>(a.q_out + r * a.D + lane * per) =
+        make_uint2(pack_f16(lo.x * up, lo.y * up), pack_f16(hi.x * up, hi.y * up));
+    if (lane == 0) a.qfac[r] = __int_as_float((127 - sh) << 23);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_dequant(const DequantArgs& a, int num_sms, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(a.smax, 0, sizeof(uint32_t) * 2 * (size_t)a.B * a.KVN, s);
+  if (e != cudaSuccess) return e;
+  const int64_t rows = (int64_t)a.B * a.cap * a.KVN;
+  if (rows > 0) {
+    const int g1 = (int)std::min<int64_t>((rows + 255) / 256, (int64_t)num_sms * 8);
+    scale_max_kernel<<<g1, 256, 0, s>>>(a);
+    const int64_t total = rows * (a.D / 16);
+    const int g2 = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms * 8);
+    kv_dequant_kernel<<<g2, 256, 0, s>>>(a);
+  }
+  const int64_t qr = a.q_rows * a.QN;
+  if (qr > 0) {
+    const int g3 = (int)std::min<int64_t>((qr + 7) / 8, (int64_t)num_sms * 16);
+    q_convert_kernel<<<g3, 256, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fia

@@ -119,13 +119,24 @@ __device__ __forceinline__ void seq_lengths(const PrefillArgs& a, int b, int64_t
   *kv_len = a.seqused_kv ? a.seqused_kv[b] : a.S_kv;
 }
 
+// Position of query row i of a sequence: right-down alignment
+// (kv_len - q_len + i) for modes 3 and 4, the row itself for the left-up
+// causal mode 2 (modes 0 and 1 do not use it).
+__device__ __forceinline__ int64_t row_pos(const PrefillArgs& a, int64_t q_len, int64_t kv_len,
+                                           int64_t i) {
+  return (a.mask_mode == 2 ? 0 : kv_len - q_len) + i;
+}
+
 // KV interval [lo, hi] (clipped) seen by query rows i0..i1 of a sequence, as a
-// tile range; returns the number of 128-wide KV tiles (0 if none).
+// tile range; returns the number of 128-wide KV tiles (0 if none).  An
+// explicit mask narrows nothing here: its bytes are read per row.
 __device__ __forceinline__ int tile_span(const PrefillArgs& a, int64_t q_len, int64_t kv_len,
                                          int64_t i0, int64_t i1, int* tile0) {
-  const int64_t p0 = kv_len - q_len + i0, p1 = kv_len - q_len + i1;
+  const int64_t p0 = row_pos(a, q_len, kv_len, i0), p1 = row_pos(a, q_len, kv_len, i1);
   int64_t lo = a.mask_mode == 4 ? p0 - a.pre_tokens : 0;
-  int64_t hi = a.mask_mode == 3 ? p1 : (a.mask_mode == 4 ? p1 + a.next_tokens : kv_len - 1);
+  int64_t hi = (a.mask_mode == 2 || a.mask_mode == 3)
+                   ? p1
+                   : (a.mask_mode == 4 ? p1 + a.next_tokens : kv_len - 1);
   lo = max(lo, (int64_t)0);
   hi = min(hi, kv_len - 1);
   *tile0 = 0;
@@ -134,9 +145,13 @@ __device__ __forceinline__ int tile_span(const PrefillArgs& a, int64_t q_len, in
   return (int)(hi / kKvTile - lo / kKvTile + 1);
 }
 
-__device__ __forceinline__ int64_t kv_phys_row(const PrefillArgs& a, int b, int64_t j) {
+// Tensor-map row of logical KV row j of batch b, KV head hk: token-major
+// pools have one row per token (the head is a column offset), head-major
+// pools [nb, KVN, bs, D] one per (page, head, token).
+__device__ __forceinline__ int64_t kv_phys_row(const PrefillArgs& a, int b, int hk, int64_t j) {
   if (a.block_table) {
     const int64_t blk = a.block_table[(int64_t)b * a.max_blocks + j / a.block_size];
+    if (a.kv_layout == 1) return (blk * a.KVN + hk) * a.block_size + j % a.block_size;
     return blk * a.block_size + j % a.block_size;
   }
   return (int64_t)b * a.S_kv + j;
@@ -261,7 +276,11 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(const PrefillArg
 // ---------------------------------------------------------------------------
 // attention kernel
 // ---------------------------------------------------------------------------
-template <int D, bool NEG>  // NEG: the softmax scale is negative
+// NEG: the softmax scale is negative.  F16: fp16 operands (FP8 caches after
+// their conversion): Q' = Q * 2^sh per (token, head), K' and V' divided by a
+// power of two per (batch, KV head); every row takes the factors back in its
+// score scale and its output.
+template <int D, bool NEG, bool F16>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tq,
                    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
@@ -425,7 +444,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int rb = lane / NSUB, sub = lane % NSUB;
         const int64_t jb = j0 + (int64_t)rb * a.box_rows;
         const bool mine = lane < nrb * NSUB && jb < kl;
-        const int64_t prow = mine ? kv_phys_row(a, m.b, jb) : 0;
+        const int64_t prow = mine ? kv_phys_row(a, m.b, m.hk, jb) : 0;
+        const int kcol = (a.kv_layout == 1 ? 0 : m.hk * D) + sub * 64;
         int nvalid = 0;
         for (int q = 0; q < nrb; ++q)
           if (j0 + (int64_t)q * a.box_rows < kl) ++nvalid;
@@ -436,13 +456,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
         __syncwarp();
         if (mine)
           tma_load_2d(smem + Cfg::kOffK + ks * Cfg::kTileBytes + sub * 16384 + rb * a.box_rows * 128,
-                      &tk, &kfull[ks], m.hk * D + sub * 64, (int)prow);
+                      &tk, &kfull[ks], kcol, (int)prow);
         pwait(&vempty[vs], ((kv_it / VS) & 1) ^ 1, a.err, misc);
         if (lane == 0) mbar_arrive_expect_tx(&vfull[vs], bytes);
         __syncwarp();
         if (mine)
           tma_load_2d(smem + Cfg::kOffV + vs * Cfg::kTileBytes + sub * 16384 + rb * a.box_rows * 128,
-                      &tv, &vfull[vs], m.hk * D + sub * 64, (int)prow);
+                      &tv, &vfull[vs], kcol, (int)prow);
       }
     }
   } else if (warp == 1 || warp == 3) {
@@ -456,8 +476,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
     const int s = warp == 3 ? 1 : 0;
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false);
-      constexpr uint32_t kIdO = idesc_bf16(128, D, true);
+      constexpr uint32_t kIdS = F16 ? idesc_f16(128, 128, false) : idesc_bf16(128, 128, false);
+      constexpr uint32_t kIdO = F16 ? idesc_f16(128, D, true) : idesc_bf16(128, D, true);
       const uint32_t sq = smem_u32(smem + Cfg::kOffQ);
       const uint32_t sk = smem_u32(smem + Cfg::kOffK);
       const uint32_t sv = smem_u32(smem + Cfg::kOffV);
@@ -633,22 +653,58 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int h = s ? m.h1 : m.h0;
       const int64_t i = (int64_t)m.t * kQTile + row;
       const bool valid = i < m.q_len;
-      const int64_t p = (int64_t)m.kv_len - m.q_len + i;
+      const int64_t p = row_pos(a, m.q_len, m.kv_len, i);
       int64_t lo = a.mask_mode == 4 ? p - a.pre_tokens : 0;
-      int64_t hi = a.mask_mode == 3 ? p : (a.mask_mode == 4 ? p + a.next_tokens : m.kv_len - 1);
+      int64_t hi = (a.mask_mode == 2 || a.mask_mode == 3)
+                       ? p
+                       : (a.mask_mode == 4 ? p + a.next_tokens : m.kv_len - 1);
       lo = max(lo, (int64_t)0);
       hi = min(hi, (int64_t)m.kv_len - 1);
+      // explicit mask: this row's bytes (1 = hidden) of sequence m.b
+      const uint8_t* mrow_ptr =
+          (a.mask && valid) ? a.mask + (int64_t)m.b * a.mask_bstride + i * a.mask_rstride : nullptr;
+      // score scale of this row (log2 units); fp16 operands take back their
+      // powers of two here and in the output
+      float sl = a.scale_log2, vfac = 1.f;
+      if constexpr (F16) {
+        const int64_t hkv = ((int64_t)m.b * a.KVN + m.hk) * 2;
+        if (valid) sl *= __ldg(a.qfac + (m.q_row0 + row) * a.QN + h);
+        sl *= __ldg(a.kvfac + hkv);
+        vfac = __ldg(a.kvfac + hkv + 1);
+      }
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < m.ntiles; ++j) {
-        pwait(&sfull[s], s_it & 1, a.err, misc);
-        ++s_it;
-        tc_fence_after();
         // visible columns of this row in the tile: [c0, c1) (tile-local)
         const int64_t j0 = (int64_t)(m.tile0 + j) * kKvTile;
         const int c0 = (int)min(max(lo - j0, (int64_t)0), (int64_t)kKvTile);
         const int c1 = (int)min(max(hi - j0 + 1, (int64_t)0), (int64_t)kKvTile);
-        const bool all_full = __all_sync(0xffffffffu, c0 == 0 && c1 == kKvTile);
-        const float sl = a.scale_log2;
+        // explicit mask: the tile's bytes of this row, 16 at a time up to the
+        // row's visible end (rows are 16-byte multiples covering the KV
+        // capacity), as four 32-bit hidden-key bit sets; the loads are issued
+        // before the wait for the scores
+        uint32_t hidden[4] = {0u, 0u, 0u, 0u};
+        if (a.mask) {
+          if (mrow_ptr) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              uint4 w = make_uint4(0u, 0u, 0u, 0u);
+              if (16 * k < c1) w = __ldg(reinterpret_cast<const uint4*>(mrow_ptr + j0) + k);
+              const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                // nonzero bytes -> 0x80 in their top bit, gathered into 4 bits
+                const uint32_t nz = (((wv[q] & 0x7f7f7f7fu) + 0x7f7f7f7fu) | wv[q]) & 0x80808080u;
+                hidden[k >> 1] |= ((nz * 0x00204081u) >> 28) << (16 * (k & 1) + 4 * q);
+              }
+            }
+          }
+        }
+        pwait(&sfull[s], s_it & 1, a.err, misc);
+        ++s_it;
+        tc_fence_after();
+        const bool all_full =
+            __all_sync(0xffffffffu, c0 == 0 && c1 == kKvTile &&
+                                        (hidden[0] | hidden[1] | hidden[2] | hidden[3]) == 0u);
         // masked score: -inf after the scaling for either sign of the scale
         const uint32_t hole = __float_as_uint(NEG ? INFINITY : -INFINITY);
         // the row's 128 scores: four TMEM loads, one wait; they stay in
@@ -661,7 +717,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (!all_full) {
 #pragma unroll
           for (int e = 0; e < kKvTile; ++e)
-            if (e < c0 || e >= c1) v[e] = hole;
+            if (e < c0 || e >= c1 || ((hidden[e >> 5] >> (e & 31)) & 1u)) v[e] = hole;
         }
         // row maximum of the raw scores (minimum for a negative scale), four
         // three-input chains
@@ -722,7 +778,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                    sl2, nb2);
             const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             ps[e & 3] = fadd2(ps[e & 3], pp);
-            pv[e] = pack_bf16(pp.x, pp.y);
+            pv[e] = F16 ? pack_f16(pp.x, pp.y) : pack_bf16(pp.x, pp.y);
           }
           tmem_st32(tS + 32 * c, pv);
         }
@@ -743,7 +799,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           Mp = fmaxf(m_used, sk);
           L = l * exp2f(m_used - Mp) + exp2f(sk - Mp);
         }
-        scl = exp2f(m_used - Mp) / L;
+        scl = exp2f(m_used - Mp) / L * vfac;
         lse = (Mp + log2f(L)) * 0.6931471805599453f;
       }
       uint16_t* orow = a.out + (m.q_row0 + row) * a.out_stride + (int64_t)h * D;
@@ -798,12 +854,12 @@ cudaError_t launch_prefill_schedule(const PrefillArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int D, bool NEG>
+template <int D, bool NEG, bool F16>
 static cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& tq,
                                     const CUtensorMap& tk, const CUtensorMap& tv,
                                     cudaStream_t s) {
   using Cfg = PrefillCfg<D>;
-  auto kern = prefill_kernel<D, NEG>;
+  auto kern = prefill_kernel<D, NEG, F16>;
   static std::atomic<uint64_t> done_mask[4];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -820,10 +876,13 @@ static cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& tq,
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t s) {
   const bool neg = a.scale_log2 < 0.f;
-  if (a.D == 64) return neg ? launch_prefill_t<64, true>(a, tq, tk, tv, s)
-                            : launch_prefill_t<64, false>(a, tq, tk, tv, s);
-  return neg ? launch_prefill_t<128, true>(a, tq, tk, tv, s)
-             : launch_prefill_t<128, false>(a, tq, tk, tv, s);
+  if (a.qfac)  // fp16 operands: FP8 caches, D = 128
+    return neg ? launch_prefill_t<128, true, true>(a, tq, tk, tv, s)
+               : launch_prefill_t<128, false, true>(a, tq, tk, tv, s);
+  if (a.D == 64) return neg ? launch_prefill_t<64, true, false>(a, tq, tk, tv, s)
+                            : launch_prefill_t<64, false, false>(a, tq, tk, tv, s);
+  return neg ? launch_prefill_t<128, true, false>(a, tq, tk, tv, s)
+             : launch_prefill_t<128, false, false>(a, tq, tk, tv, s);
 }
 
 }  // namespace fia

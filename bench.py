@@ -364,6 +364,44 @@ def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds):
     except Exception as e:
         res["varlen_causal_prefill"] = {"unavailable": str(e)[:200]}
     torch.cuda.empty_cache()
+    # forms beyond the headline workloads: multi-token decode (4 query rows
+    # per sequence), head-major pages, FP8 prefill
+    for key, mk, what in (
+            ("mtp_decode_s4", lambda: fi.workload_paged_decode(device="cuda", S_q=4),
+             "paged GQA decode sequences with 4 query rows each (right-down causal)"),
+            ("paged_decode_bnnbsd",
+             lambda: fi.workload_paged_decode(device="cuda", kv_layout=fi.KV_LAYOUT_BNNBSD),
+             "paged GQA decode with head-major pages [nb, KV_N, bs, D]")):
+        try:
+            p = mk()
+            call = fia.FiaCall(p, with_lse=True)
+            st, ex = _bench_call(call, steps, warmup, flush)
+            (ms, ms_med), (kms, kms_med) = _stats(st), _stats(ex)
+            by = p.kv_bytes_visible()
+            res[key] = {"workload": what, "ms_per_step": ms, "ms_median": ms_med,
+                        "kernel_ms": kms, "kernel_ms_median": kms_med, "GB/s": by / ms / 1e6,
+                        "kernel_GB/s": by / kms / 1e6,
+                        "frac_of_hbm": by / kms / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": by}
+            del call, p
+        except Exception as e:
+            res[key] = {"unavailable": str(e)[:200]}
+        torch.cuda.empty_cache()
+    try:
+        p = fi.workload_varlen_prefill(device="cuda", kv_dtype=fi.KV_FP8_E4M3)
+        call = fia.FiaCall(p, with_lse=True)
+        st, ex = _bench_call(call, steps, warmup, flush)
+        (ms, ms_med), (kms, kms_med) = _stats(st), _stats(ex)
+        fl = 4 * p.D * p.QN * sum(L * (L + 1) // 2 for L in p.q_lens)
+        res["fp8_varlen_causal_prefill"] = {
+            "workload": "the varlen causal prefill with an FP8 E4M3 cache (converted to fp16 "
+                        "once per call, then the tcgen05 kernel on fp16 operands)",
+            "ms_per_step": ms, "ms_median": ms_med, "kernel_ms": kms, "kernel_ms_median": kms_med,
+            "TFLOP/s": fl / ms / 1e9, "kernel_TFLOP/s": fl / kms / 1e9,
+            "frac_of_bf16": fl / kms / 1e9 / peaks["bf16_tflops"], "flops": fl}
+        del call, p
+    except Exception as e:
+        res["fp8_varlen_causal_prefill"] = {"unavailable": str(e)[:200]}
+    torch.cuda.empty_cache()
     try:
         sp = fi.workload_sparse_csa(device="cuda")
         call = fia.SparseCall(sp, with_lse=True)
@@ -383,8 +421,27 @@ def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds):
             spc = sp.to("cpu")
             res["sparse_csa_decode"]["cpu_baseline"] = cpu_sparse(spc, by, _cores(), cpu_seconds)
             res["sparse_csa_decode"]["cpu_single_thread"] = cpu_sparse(spc, by, 1, 0.0)
+        del call, sp
     except Exception as e:
         res["sparse_csa_decode"] = {"unavailable": str(e)[:200]}
+    try:
+        sp = fi.workload_sparse_csa(device="cuda", kv_dtype=fi.SPARSE_KV_FP8_PACKED)
+        call = fia.SparseCall(sp, with_lse=True)
+        call.plan()
+        for _ in range(warmup):
+            call.run()
+        torch.cuda.synchronize()
+        st, ex = _time_steps(call.plan, call.run, steps, flush)
+        (ms, ms_med), (kms, kms_med) = _stats(st), _stats(ex)
+        by = sp.B * (sp.win_left + 1 + sp.K2) * 640  # packed rows, once each
+        res["sparse_csa_decode_fp8_packed"] = {
+            "workload": "the sparse CSA decode with packed FP8 K~ rows (640 bytes: bf16 rope "
+                        "64, E4M3 nope 448, E8M0 scales)",
+            "ms_per_step": ms, "ms_median": ms_med, "kernel_ms": kms, "kernel_ms_median": kms_med,
+            "GB/s": by / ms / 1e6, "kernel_GB/s": by / kms / 1e6,
+            "frac_of_hbm": by / kms / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": by}
+    except Exception as e:
+        res["sparse_csa_decode_fp8_packed"] = {"unavailable": str(e)[:200]}
     if with_cpu:
         try:
             import oracle

@@ -850,50 +850,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // ---- Q^T fragments (mma B operand: k = d, n = head) ----
+    // ---- Q^T fragments (mma B operand: k = d, n = column) ----
     uint32_t qb[NG][KS][2];
-    // score factor of accumulator column 2*q4 + e of head group ng: scale *
-    // log2(e), times 2^-sh of that head on the FP8 path (below)
-    float slc[NG][2];
+    // score factor: scale * log2(e), times 2^-sh on the FP8 path (below)
+    float slc = a.scale_log2;
     {
       const uint16_t* qsm = reinterpret_cast<const uint16_t*>(smem + Cfg::kOffQ + qs * Cfg::kQBytes);
+      if constexpr (!FP8) {
 #pragma unroll
-      for (int ng = 0; ng < NG; ++ng) {
-        const int head = ng * 8 + g;  // the unit's column in this lane's B fragments
-        const bool ok = head < r.ncols;
-        slc[ng][0] = slc[ng][1] = a.scale_log2;
-        if constexpr (!FP8) {
+        for (int ng = 0; ng < NG; ++ng) {
+          const int head = ng * 8 + g;  // the unit's column in this lane's B fragments
+          const bool ok = head < r.ncols;
 #pragma unroll
           for (int kk = 0; kk < KS; ++kk) {
             const int d0 = kk * 16 + 2 * q4;
             qb[ng][kk][0] = ok ? *reinterpret_cast<const uint32_t*>(qsm + head * D + d0) : 0u;
             qb[ng][kk][1] = ok ? *reinterpret_cast<const uint32_t*>(qsm + head * D + d0 + 8) : 0u;
           }
-        } else {
-          // The FP8 products run in fp16, whose range is far narrower than
-          // bf16's.  Each head's query is multiplied by 2^sh, a power of two
-          // chosen from the head's largest exponent E so that the largest
-          // element lands at exponent 15 (sh = 15 - E, kept in [-100, 100]):
-          // nothing overflows, every element within 2^-32 of the head's
-          // largest converts exactly, and the scores take 2^-sh back in
-          // their scale factor.  Powers of two scale exactly.
-          // k-step kk = 4*tile + j covers d = 64*tile + 16*q + 4*j + {0..3}:
-          // slots 2q,2q+1 <- the first two, slots 2q+8,2q+9 <- the last two
-          uint32_t emax = 0;
+        }
+      } else {
+        // The FP8 products run in fp16, whose range is far narrower than
+        // bf16's.  The unit's queries are multiplied by 2^sh, a power of two
+        // chosen from the largest exponent E among them so that the largest
+        // element lands at exponent 15 (sh = 15 - E, kept in [-100, 100]):
+        // nothing overflows, every element within 2^-29 of the largest
+        // converts exactly (smaller ones round to multiples of 2^(E-39),
+        // far below the scores' tolerance), and the scores take 2^-sh back
+        // in their scale factor.  Powers of two scale exactly.
+        // k-step kk = 4*tile + j covers d = 64*tile + 16*q + 4*j + {0..3}:
+        // slots 2q,2q+1 <- the first two, slots 2q+8,2q+9 <- the last two
+        uint32_t emax = 0;
 #pragma unroll
-          for (int kk = 0; kk < KS; ++kk) {
-            const int d0 = (kk >> 2) * 64 + 16 * q4 + 4 * (kk & 3);
-            if (ok) {
+        for (int ng = 0; ng < NG; ++ng) {
+          const int head = ng * 8 + g;
+          if (head < r.ncols) {
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+              const int d0 = (kk >> 2) * 64 + 16 * q4 + 4 * (kk & 3);
               const uint2 v = *reinterpret_cast<const uint2*>(qsm + head * D + d0);
               emax = max(emax, max(max((v.x >> 7) & 0xffu, (v.x >> 23) & 0xffu),
                                    max((v.y >> 7) & 0xffu, (v.y >> 23) & 0xffu)));
             }
           }
-          emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, 1));  // the quad holds the head
-          emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, 2));
-          const int sh = min(max(142 - (int)emax, -100), 100);  // 15 - (emax - 127)
-          const float up = __int_as_float((127 + sh) << 23);
-          const float sl_mine = a.scale_log2 * __int_as_float((127 - sh) << 23);
+        }
+        emax = __reduce_max_sync(0xffffffffu, emax);  // over the unit's columns
+        const int sh = min(max(142 - (int)emax, -100), 100);  // 15 - (emax - 127)
+        const float up = __int_as_float((127 + sh) << 23);
+        slc = a.scale_log2 * __int_as_float((127 - sh) << 23);
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) {
+          const int head = ng * 8 + g;
+          const bool ok = head < r.ncols;
 #pragma unroll
           for (int kk = 0; kk < KS; ++kk) {
             const int d0 = (kk >> 2) * 64 + 16 * q4 + 4 * (kk & 3);
@@ -907,9 +914,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               qb[ng][kk][0] = qb[ng][kk][1] = 0u;
             }
           }
-          // accumulator columns 2*q4 + e belong to the heads of lanes 4*(2*q4 + e)
-          slc[ng][0] = __shfl_sync(0xffffffffu, sl_mine, 8 * q4);
-          slc[ng][1] = __shfl_sync(0xffffffffu, sl_mine, 8 * q4 + 4);
         }
       }
       __syncwarp();
@@ -1093,8 +1097,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ng = 0; ng < NG; ++ng)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            xs[ng][e] = sc[ng][e] * slc[ng][e];
-            xs[ng][2 + e] = sc[ng][2 + e] * slc[ng][e];
+            xs[ng][e] = sc[ng][e] * slc;
+            xs[ng][2 + e] = sc[ng][2 + e] * slc;
           }
       } else {
         // each column against its own row's bounds, and the explicit mask's
@@ -1111,8 +1115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               okA = okA && mk[mrow[ng][e] + ta] == 0;
               okB = okB && mk[mrow[ng][e] + tb] == 0;
             }
-            xs[ng][e] = okA ? sc[ng][e] * slc[ng][e] : -INFINITY;
-            xs[ng][2 + e] = okB ? sc[ng][2 + e] * slc[ng][e] : -INFINITY;
+            xs[ng][e] = okA ? sc[ng][e] * slc : -INFINITY;
+            xs[ng][2 + e] = okB ? sc[ng][2 + e] * slc : -INFINITY;
           }
       }
 #pragma unroll

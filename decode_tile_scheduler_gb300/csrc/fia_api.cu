@@ -463,7 +463,7 @@ fia_status q_map(const fia_params* p, CUtensorMap* tq) {
 // ---------------------------------------------------------------------------
 // shared-KV sparse attention ("kv_quant_sparse_attn_sharedkv" constraints)
 // ---------------------------------------------------------------------------
-constexpr int kSparseHeads = 8;     // query heads per work item
+constexpr int kSparseHeads = 8;       // query heads per work item
 constexpr int kSparseMaxCtas = 1007;  // 1024 - 16 - 1 begins fit the metadata
 
 struct SparsePlan {
@@ -512,7 +512,6 @@ fia_status sparse_validate(const sparse_attn_params* p) {
     return FIA_ERR_BAD_SHAPE;  // indices without a compressed cache
   }
   if (p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512) return FIA_ERR_UNSUPPORTED;
-  if (p->kv_dtype == FIA_SPARSE_KV_FP8_PACKED) return FIA_ERR_UNSUPPORTED;
   return FIA_OK;
 }
 
@@ -527,6 +526,8 @@ fia_status sparse_plan(const sparse_attn_params* p, SparsePlan* pl) {
   pl->rows = p->layout == FIA_LAYOUT_TND ? (int64_t)p->total_q
                                          : (int64_t)p->batch * p->max_seqlen_q;
   // the metadata holds the item count and the total item weight as int32
+  // (a row's weight is its chunk count: the window's, then the compressed
+  // rows' -- for CSA at most topk, for HCA at most the compressed capacity)
   const int64_t W = (int64_t)p->ori_win_left + p->ori_win_right + 1;
   int64_t kc = 0;
   if (pl->mode == 1) kc = p->topk;
@@ -549,13 +550,13 @@ SparseArgs sparse_args(const sparse_attn_params* p, const SparsePlan& pl, void* 
   a.q = static_cast<const uint16_t*>(p->q);
   a.out = static_cast<uint16_t*>(p->out);
   a.lse = p->lse;
-  a.ori_kv = static_cast<const uint16_t*>(p->ori_kv);
+  a.ori_kv = p->ori_kv;
   a.ori_block_table = p->ori_block_table;
   a.ori_max_blocks = p->ori_max_blocks;
   a.ori_block_size = p->ori_block_size;
   a.ori_num_blocks = p->ori_num_blocks;
   a.cmp_num_blocks = p->cmp_kv ? p->cmp_num_blocks : 0;
-  a.cmp_kv = static_cast<const uint16_t*>(p->cmp_kv);
+  a.cmp_kv = p->cmp_kv;
   a.cmp_block_table = p->cmp_block_table;
   a.cmp_max_blocks = p->cmp_max_blocks;
   a.cmp_block_size = p->cmp_kv ? p->cmp_block_size : 1;
@@ -569,6 +570,7 @@ SparseArgs sparse_args(const sparse_attn_params* p, const SparsePlan& pl, void* 
   a.win_left = p->ori_win_left;
   a.win_right = p->ori_win_right;
   a.mode = pl.mode;
+  a.kv_dtype = p->kv_dtype;
   a.rows = pl.rows;
   a.hgs = (p->num_q_heads + kSparseHeads - 1) / kSparseHeads;
   fast_divisor(p->ori_block_size, &a.ori_magic, &a.ori_shift);
@@ -722,6 +724,7 @@ fia_status fia_run(const fia_params* p, void* ws, size_t ws_bytes, void* stream)
 fia_status sparse_attn_metadata(const sparse_attn_params* p, int32_t* metadata,
                                 size_t* workspace_bytes, void* stream) {
   if (!p || !metadata || !workspace_bytes) return FIA_ERR_NULL_ARG;
+  if (!aligned16(metadata)) return FIA_ERR_BAD_SHAPE;  // the documented alignment
   SparsePlan pl;
   fia_status st = sparse_plan(p, &pl);
   if (st != FIA_OK) return st;
@@ -736,6 +739,7 @@ fia_status sparse_attn_metadata(const sparse_attn_params* p, int32_t* metadata,
 fia_status sparse_attn_run(const sparse_attn_params* p, const int32_t* metadata, void* ws,
                            size_t ws_bytes, void* stream) {
   if (!p || !metadata) return FIA_ERR_NULL_ARG;
+  if (!aligned16(metadata)) return FIA_ERR_BAD_SHAPE;
   SparsePlan pl;
   fia_status st = sparse_plan(p, &pl);
   if (st != FIA_OK) return st;

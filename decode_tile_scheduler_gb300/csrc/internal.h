@@ -115,11 +115,11 @@ struct SparseArgs {
   const uint16_t* q;
   uint16_t* out;
   float* lse;
-  const uint16_t* ori_kv;
+  const void* ori_kv;    // bf16 rows of D, or packed FP8 rows of 640 bytes
   const int32_t* ori_block_table;
   int ori_max_blocks, ori_block_size;
   int64_t ori_num_blocks;
-  const uint16_t* cmp_kv;
+  const void* cmp_kv;
   const int32_t* cmp_block_table;
   int cmp_max_blocks, cmp_block_size;
   int64_t cmp_num_blocks;
@@ -131,6 +131,7 @@ struct SparseArgs {
   float scale_log2;
   int cmp_ratio, win_left, win_right;
   int mode;              // 0 SWA, 1 CSA, 2 HCA
+  int kv_dtype;          // 0 bf16 rows, 1 packed FP8 rows (640 bytes, D = 512)
   int64_t rows;
   int64_t hgs;           // groups of 8 query heads per row (work items per row)
   uint32_t ori_magic, cmp_magic;  // j / block_size == (j * magic) >> shift, 0 <= j < 2^31

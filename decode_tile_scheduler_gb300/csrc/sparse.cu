@@ -1,13 +1,16 @@
 // sparse.cu -- shared-KV sparse attention ("kv_quant_sparse_attn_sharedkv":
 // O = softmax(Q K~^T * softmax_scale) V~ with K~ = V~; "sparse_flash_mla":
-// SWA, CSA and HCA modes and the metadata pre-step), bf16 KV.
+// SWA, CSA and HCA modes and the metadata pre-step), with bf16 K~ rows or the
+// packed FP8 rows of the kv_quant page (bf16 rope 64, E4M3 nope 448, E8M0
+// tile scales; widened to bf16 in shared memory, exactly: an E4M3 value times
+// a power of two is a bf16 value).
 //
 // K~ of a query row is the band window of the original KV followed by the
 // compressed rows (the listed top-k indices for CSA, scanned up to the first
 // -1 and kept when causally visible; every visible compressed row for HCA).
 // A work item is (query row, group of 8 query heads); the metadata kernel
-// hands each CTA a contiguous run of items of balanced weight.  In a CTA one
-// producer warp gathers K~ in 64-row chunks (index -> block table -> pool
+// hands each CTA a contiguous run of items of balanced weight.  In a CTA four
+// producer warps gather K~ in 64-row chunks (index -> block table -> pool
 // row, one bulk copy per row) into a ring of shared-memory stages, and eight
 // consumer warps run the whole item: S^T = K~ Q^T and O^T += V~^T P^T with
 // mma.sync (the K~ rows are the M dimension, the 8 heads N), the online
@@ -32,6 +35,7 @@ constexpr int kSThreads = 32 * (kSProd + kSCons);
 constexpr int kMdBase = 16;               // metadata: CTA begins from this entry
 constexpr int32_t kMdMagic = 0x46534D32;
 constexpr int kMaxK2 = 2048;              // longest index list (validated on the host)
+constexpr int kPackedRow = 640;           // bytes of a packed FP8 row (D = 512)
 
 struct SparseRow {
   int b;
@@ -70,6 +74,13 @@ __device__ __forceinline__ SparseRow sparse_row(const SparseArgs& a, int64_t u) 
 // j / d for 0 <= j < 2^31 with the host's multiplier and shift
 __device__ __forceinline__ int64_t fast_div(int64_t j, uint32_t magic, int shift) {
   return (int64_t)(((uint64_t)(uint32_t)j * magic) >> shift);
+}
+
+// 2^(e - 127) of an E8M0 scale byte (255 is NaN)
+__device__ __forceinline__ float e8m0_value(uint32_t e) {
+  if (e == 0xffu) return __int_as_float(0x7fc00000);
+  if (e == 0u) return __int_as_float(0x00400000);  // 2^-127, subnormal
+  return __int_as_float((int)(e << 23));
 }
 
 }  // namespace
@@ -154,6 +165,7 @@ __global__ void __launch_bounds__(1024) sparse_metadata_kernel(const SparseArgs 
     md[11] = a.mode;
     md[12] = kHeads;
     md[13] = (int32_t)(a.rows * G);
+    md[14] = a.kv_dtype;
   }
 }
 
@@ -177,6 +189,7 @@ struct SparseCfg {
   static constexpr int kOffMisc = kOffBar + 8 * (2 * kStages + 2);
   static constexpr int kSmem = kOffMisc + 16;  // misc: abort flag, -, CSA list length
   static_assert(kStageBytes % 16 == 0 && kOffQ % 16 == 0, "bulk-copy alignment");
+  static_assert(D != 512 || kRowBytes >= kPackedRow, "a packed row fits its slot");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
   static_assert(kSmem <= 232448, "shared memory");
 };
@@ -201,6 +214,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   int* misc = reinterpret_cast<int*>(sm + Cfg::kOffMisc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
+  const bool packed = a.kv_dtype == 1;
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -218,7 +232,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
   // __restrict__ its loads could be hoisted above this wait.
   pdl_wait();
   if (md[0] != kMdMagic || md[1] != a.num_ctas || md[2] != (int32_t)a.rows || md[5] != a.B ||
-      md[6] != a.N1 || md[7] != a.K2 || md[12] != kHeads || md[13] != (int32_t)(a.rows * a.hgs)) {
+      md[6] != a.N1 || md[7] != a.K2 || md[12] != kHeads || md[13] != (int32_t)(a.rows * a.hgs) ||
+      md[14] != a.kv_dtype) {
     if (tid == 0) atomicExch(a.err, 2);
     return;
   }
@@ -227,6 +242,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (c == 0 && tid == 0) *reinterpret_cast<volatile int*>(a.err) = 0;
   const int64_t k_begin = md[kMdBase + c], k_end = md[kMdBase + c + 1];
   if (k_begin >= k_end) return;
+  const int row_src_bytes = packed ? kPackedRow : D * 2;
 
   if (warp < kSProd) {
     // ======================= producers =======================
@@ -268,14 +284,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
             const int64_t blk = pg < a.ori_max_blocks
                                     ? a.ori_block_table[(int64_t)r.b * a.ori_max_blocks + pg] : -1;
             ok[h2] = blk >= 0 && blk < a.ori_num_blocks;
-            off[h2] = (blk * a.ori_block_size + (j - pg * a.ori_block_size)) * D;
+            off[h2] = (blk * a.ori_block_size + (j - pg * a.ori_block_size)) * row_src_bytes;
           } else {
             const int64_t cr = a.mode == 1 ? (int64_t)list[pos] : (int64_t)pos;
             const int64_t pg = fast_div(cr, a.cmp_magic, a.cmp_shift);
             const int64_t blk = pg < a.cmp_max_blocks
                                     ? a.cmp_block_table[(int64_t)r.b * a.cmp_max_blocks + pg] : -1;
             ok[h2] = blk >= 0 && blk < a.cmp_num_blocks;
-            off[h2] = (blk * a.cmp_block_size + (cr - pg * a.cmp_block_size)) * D;
+            off[h2] = (blk * a.cmp_block_size + (cr - pg * a.cmp_block_size)) * row_src_bytes;
           }
         }
       }
@@ -296,13 +312,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
       // the zero rows (generic proxy) precede later bulk copies into them
       fence_proxy_async_smem();
       __syncwarp();
-      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(__popcll(valid) * D * 2));
+      uint64_t* txb = &full[s];
+      if (pw == 0 && lane == 0)
+        mbar_arrive_expect_tx(txb, (uint32_t)(__popcll(valid) * row_src_bytes));
       __syncwarp();
-      const uint16_t* src = cmp ? a.cmp_kv : a.ori_kv;
+      const uint8_t* src =
+          reinterpret_cast<const uint8_t*>(cmp ? a.cmp_kv : a.ori_kv);
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2)
         if (ok[h2] && (lane + 32 * h2) % kSProd == pw)
-          bulk_load(st + (lane + 32 * h2) * Cfg::kRowBytes, src + off[h2], D * 2, &full[s]);
+          bulk_load(st + (lane + 32 * h2) * Cfg::kRowBytes, src + off[h2], row_src_bytes, txb);
       ++it;
     };
 
@@ -358,15 +377,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // in order (warp compaction into shared memory)
         const int32_t* ix = a.cmp_sparse_indices + u * (int64_t)a.K2;
         bool stop = false;
-        for (int t0 = 0; t0 < a.K2 && !stop; t0 += 32 * 8) {
-          int v[8];
+        // 16 entries per lane per round: a list of up to 512 in one round trip
+        for (int t0 = 0; t0 < a.K2 && !stop; t0 += 32 * 16) {
+          int v[16];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < 16; ++j) {
             const int t = t0 + 32 * j + lane;
-            v[j] = t < a.K2 ? ix[t] : -1;
+            v[j] = t < a.K2 ? __ldg(ix + t) : -1;
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < 16; ++j) {
             if (!stop) {
               const uint32_t neg = __ballot_sync(0xffffffffu, v[j] < 0);
               const int first = neg ? __ffs(neg) - 1 : 32;
@@ -446,6 +466,58 @@ __global__ void __launch_bounds__(kSThreads, 1)
       const uint64_t valid = hdr[s].valid;
       const bool last = hdr[s].last != 0;
       const uint32_t st = sm_base + s * Cfg::kStageBytes;
+      // packed FP8 rows -> bf16 rows in place, this warp's 8 rows in two
+      // batches of 4: the rope values are bf16 already; lane l < 28 widens
+      // nope codes 16 l .. 16 l + 15 (tile l / 4).  A batch's reads precede
+      // its writes (__syncwarp), and the named barrier orders every warp's
+      // rows before any warp's reads.
+      if constexpr (D == 512) {
+        if (packed) {
+#pragma unroll
+          for (int bt = 0; bt < 2; ++bt) {
+            uint4 c16[4];
+            uint32_t ex[4];
+            bool vr[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int rr = cw * 8 + bt * 4 + j;
+              vr[j] = ((valid >> rr) & 1) && lane < 28;
+              c16[j] = make_uint4(0, 0, 0, 0);
+              ex[j] = 127;
+              if (vr[j]) {
+                const uint8_t* row = sm + s * Cfg::kStageBytes + rr * Cfg::kRowBytes;
+                c16[j] = *reinterpret_cast<const uint4*>(row + 128 + 16 * lane);
+                ex[j] = row[128 + 448 + (lane >> 2)];
+              }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (vr[j]) {
+                const float f = e8m0_value(ex[j]);
+                const uint32_t w4[4] = {c16[j].x, c16[j].y, c16[j].z, c16[j].w};
+                uint32_t o[8];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                  uint32_t lo2, hi2;
+                  e4m3x4_to_f16x2x2(w4[w], lo2, hi2);
+                  const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&lo2));
+                  const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hi2));
+                  o[2 * w] = pack_bf16(fl.x * f, fl.y * f);
+                  o[2 * w + 1] = pack_bf16(fh.x * f, fh.y * f);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(sm + s * Cfg::kStageBytes +
+                                                      (cw * 8 + bt * 4 + j) * Cfg::kRowBytes +
+                                                      128 + 32 * lane);
+                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+              }
+            }
+            __syncwarp();
+          }
+          named_bar_sync(1, nthr);
+        }
+      }
       // ---- partial S^T = K~ Q^T: rows of this row group, half hf of D ----
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll

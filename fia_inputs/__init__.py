@@ -466,23 +466,28 @@ def workload_tiny_prefill(device="cpu") -> FiaProblem:
                     device=device)
 
 
-def workload_paged_decode(device="cpu", B=32) -> FiaProblem:
+def workload_paged_decode(device="cpu", B=32, S_q=1, kv_layout=KV_LAYOUT_BNBSH) -> FiaProblem:
     """B=32, S_q=1, Q_N=32, KV_N=8, D=128, kv len ~ U[512,4096], block 128,
-    permuted pages, scale 1/sqrt(128)."""
+    permuted pages, scale 1/sqrt(128).  S_q > 1 gives the same sequences with
+    S_q query rows each (multi-token decode, right-down causal);
+    kv_layout=KV_LAYOUT_BNNBSD stores the pages head-major."""
     g = torch.Generator().manual_seed(1002)
     kv = _lens(g, B, 512, 4096)
-    return make_fia(B=B, QN=32, KVN=8, D=128, q_lens=[1] * B, kv_lens=kv, layout=LAYOUT_BSND,
-                    paged=True, block_size=128, seed=1002, device=device)
+    return make_fia(B=B, QN=32, KVN=8, D=128, q_lens=[S_q] * B, kv_lens=kv, layout=LAYOUT_BSND,
+                    paged=True, block_size=128, seed=1002, device=device,
+                    mask_mode=MASK_RIGHT_DOWN_CAUSAL if S_q > 1 else MASK_NONE,
+                    kv_layout=kv_layout)
 
 
-def workload_varlen_prefill(device="cpu", B=8) -> FiaProblem:
+def workload_varlen_prefill(device="cpu", B=8, kv_dtype=KV_BF16) -> FiaProblem:
     """TND, B=8, lengths ~ U[256,4096], Q_N=32, KV_N=8, D=128, paged block 128,
-    kv_len = q_len, right-down causal, per-head fp32 sinks."""
+    kv_len = q_len, right-down causal, per-head fp32 sinks (kv_dtype
+    KV_FP8_E4M3: the same sequences with an FP8 cache)."""
     g = torch.Generator().manual_seed(1003)
     L = _lens(g, B, 256, 4096)
     return make_fia(B=B, QN=32, KVN=8, D=128, q_lens=L, kv_lens=L, layout=LAYOUT_TND, paged=True,
                     block_size=128, mask_mode=MASK_RIGHT_DOWN_CAUSAL, with_sinks=True, seed=1003,
-                    device=device)
+                    device=device, kv_dtype=kv_dtype)
 
 
 def workload_fp8_long_decode(device="cpu", B=4, lo=32768, hi=131072) -> FiaProblem:
@@ -494,9 +499,10 @@ def workload_fp8_long_decode(device="cpu", B=4, lo=32768, hi=131072) -> FiaProbl
                     paged=True, block_size=128, kv_dtype=KV_FP8_E4M3, seed=1004, device=device)
 
 
-def workload_sparse_csa(device="cpu", B=16) -> SparseProblem:
+def workload_sparse_csa(device="cpu", B=16, kv_dtype=SPARSE_KV_BF16) -> SparseProblem:
     """B=16, S_q=1, N1=64, KV_N=1, D=512; ori len 8192, band 127/0; cmp 2048
-    rows (ratio 4); top-512 distinct visible indices; fp32 sinks; block 128."""
+    rows (ratio 4); top-512 distinct visible indices; fp32 sinks; block 128
+    (kv_dtype SPARSE_KV_FP8_PACKED: the same rows in the packed FP8 format)."""
     return make_sparse(B=B, N1=64, D=512, q_lens=[1] * B, kv_lens=[8192] * B,
                        layout=LAYOUT_BSND, mode="csa", K2=512, cmp_ratio=4, seed=1005,
-                       device=device)
+                       device=device, kv_dtype=kv_dtype)

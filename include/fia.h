@@ -348,7 +348,9 @@ fia_status fia_get_plan_layout(const fia_params *p, fia_plan_layout *layout);
  *    visible iff (c+1)*cmp_ratio <= p+1.
  *  - sinks fp32 [N1] or NULL; lse fp32 [B, 1, S1, N1] / [1, T1, N1] or NULL.
  * Built here: D = 512 (the pages' only value) and D in {128, 256}; N1 a power
- * of two <= 128; block sizes multiples of 16, <= 1024; topk <= 2048. */
+ * of two <= 128; block sizes multiples of 16, <= 1024; topk <= 2048; K~ rows
+ * in bf16, or packed FP8 (kv_dtype FIA_SPARSE_KV_FP8_PACKED, D = 512,
+ * tile_size = rope_head_dim = 64, ori_kv and cmp_kv bytes [nb, bs, 1, 640]). */
 typedef struct sparse_attn_params {
     int32_t batch;            /* B                                             */
     int32_t num_q_heads;      /* N1                                            */
@@ -389,18 +391,19 @@ typedef struct sparse_attn_params {
 /* Metadata step ("sparse_flash_mla_metadata": generates, before the main call,
  * the task list of every core; "kv_quant_sparse_attn_sharedkv": metadata
  * int32 [1024]).  Validates p, launches the scheduler kernel on `stream`,
- * which writes `metadata` (device int32 [1024]), and stores the workspace
- * size that sparse_attn_run needs in *workspace_bytes (host; the status word
- * only).  A work item is (query row u, group g of 8 query heads), numbered
- * k = u * G + g with G = ceil(N1 / 8); it weighs its row's chunk count
- * ceil(W/64) + ceil(kc/64) (W = win_left + win_right + 1, kc = visible
+ * which writes `metadata` (device int32 [1024], 16-byte aligned, else
+ * FIA_ERR_BAD_SHAPE -- in this call and in sparse_attn_run), and stores the
+ * workspace size that sparse_attn_run needs in *workspace_bytes (host; the
+ * status word only).  A work item is (query row u, group g of 8 query heads),
+ * numbered k = u * G + g with G = ceil(N1 / 8); it weighs its row's chunk
+ * count ceil(W/64) + ceil(kc/64) (W = win_left + win_right + 1, kc = visible
  * compressed rows, capped at topk for CSA, 0 for SWA).  With P_k the weight
  * before item k and T the total, CTA c takes the items with
  * floor(c*T/n) <= P_k < floor((c+1)*T/n).  Layout of metadata:
  *   [0] 0x46534D32  [1] n = CTAs  [2] query rows  [3] chunk rows (64)
  *   [4] T  [5] B  [6] N1  [7] topk  [8] cmp_ratio (1 without cmp_kv)
  *   [9] win_left  [10] win_right  [11] mode (0 SWA, 1 CSA, 2 HCA)
- *   [12] heads per item (8)  [13] items  [14..15] 0
+ *   [12] heads per item (8)  [13] items  [14] kv_dtype  [15] 0
  *   [16 + c]: first item of CTA c, c = 0..n;  remaining entries 0.
  * A query row's K~ is processed whole by one CTA, in order, so results do
  * not depend on the other rows of the batch ("sparse_flash_mla":
@@ -413,7 +416,7 @@ fia_status sparse_attn_metadata(const sparse_attn_params *p, int32_t *metadata,
  * needs the size sparse_attn_metadata reported.
  * `metadata` must come from sparse_attn_metadata with the same shapes.  The
  * kernel checks its header (magic, CTA count, rows, B, N1, topk, heads per
- * item, items) on the device; on a mismatch it writes nothing to out/lse and set the int32
+ * item, items, kv_dtype) on the device; on a mismatch it writes nothing to out/lse and sets the int32
  * status word at workspace offset 0 to FIA_ERR_BAD_SHAPE (0 otherwise; read
  * it with any device-to-host copy after the call). */
 fia_status sparse_attn_run(const sparse_attn_params *p, const int32_t *metadata,

@@ -776,7 +776,7 @@ int64_t oracle_prefill_units(const oracle_fia_args *a, int32_t *units, int64_t *
  *   [0] 0x46534D32  [1] n  [2] rows  [3] chunk  [4] T  [5] B  [6] N1  [7] K2
  *   [8] cmp_ratio (1 without a compressed cache)  [9] win_left
  *   [10] win_right  [11] mode (0 SWA, 1 CSA, 2 HCA)  [12] heads  [13] items
- *   [14..15] 0
+ *   [14] K~ row format (0 bf16, 1 packed FP8)  [15] 0
  *   [16 + c]: first item of CTA c, c = 0..n;  the rest 0.
  * Returns 0, or -1 if n does not fit. */
 int oracle_sparse_metadata(const oracle_sparse_args *a, int32_t num_ctas, int32_t chunk,
@@ -829,6 +829,7 @@ int oracle_sparse_metadata(const oracle_sparse_args *a, int32_t num_ctas, int32_
     md[11] = mode;
     md[12] = heads;
     md[13] = (int32_t)items;
+    md[14] = a->kv_dtype;
     for (c = 0; c <= num_ctas; ++c) {
         int64_t theta = c * total / num_ctas, cnt = 0;
         for (k = 0; k < items; ++k) cnt += P[k] < theta;

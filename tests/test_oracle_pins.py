@@ -583,6 +583,11 @@ def test_sparse_metadata_worked_example():
     assert list(md[:14]) == [0x46534D32, 4, 3, 64, 12, 3, 16, 0, 1, 127, 0, 0, 8, 6]
     assert list(md[16:21]) == [0, 2, 3, 5, 6]
     assert np.all(md[21:] == 0) and md[14] == 0 and md[15] == 0
+    # the packed FP8 row format is recorded in [14]; nothing else changes
+    spp = fi.make_sparse(B=3, N1=16, D=512, q_lens=[1, 1, 1], kv_lens=[500, 7, 130], mode="swa",
+                         ori_block_size=16, seed=62, kv_dtype=fi.SPARSE_KV_FP8_PACKED)
+    mdp = oracle.sparse_metadata(spp, 4, 64, 8)
+    assert mdp[14] == 1 and list(mdp[:14]) == list(md[:14]) and list(mdp[16:21]) == [0, 2, 3, 5, 6]
 
 
 def test_sparse_metadata_covers_every_item_in_order():

@@ -106,6 +106,36 @@ def test_sparse_metadata_bit_exact_other_modes(mode):
         assert np.array_equal(c.metadata.cpu().numpy(), ref)
 
 
+# packed FP8 K~ rows ("kv_quant_sparse_attn_sharedkv": bf16 rope 64, E4M3
+# nope 448, E8M0 scales; D = 512)
+PACKED = {
+    "csa": dict(B=3, N1=64, q_lens=[1, 1, 1], kv_lens=[5000, 70, 1200], mode="csa", K2=512),
+    "swa_tnd": dict(B=2, N1=8, q_lens=[3, 2], kv_lens=[400, 90], mode="swa",
+                    layout=fi.LAYOUT_TND, ori_block_size=32),
+    "hca_128_heads": dict(B=2, N1=128, q_lens=[1, 1], kv_lens=[9000, 300], mode="hca",
+                          cmp_ratio=128, cmp_block_size=16),
+    "csa_odd_pages": dict(B=2, N1=16, q_lens=[2, 2], kv_lens=[3000, 64], mode="csa", K2=300,
+                          ori_block_size=80, cmp_block_size=48),
+}
+
+
+@pytest.mark.parametrize("num_sms", [0, 7])
+@pytest.mark.parametrize("name", sorted(PACKED))
+def test_sparse_packed_fp8_rows(name, num_sms):
+    sp = fi.make_sparse(D=512, kv_dtype=fi.SPARSE_KV_FP8_PACKED, seed=70 + len(name), device=dev,
+                        **PACKED[name])
+    _, out, lse = _run(sp, num_sms)
+    ro, rl = oracle.sparse(sp.to("cpu"))
+    check_close(out, lse, ro, rl, name)
+
+
+def test_sparse_packed_csa_workload_full_size():
+    sp = fi.workload_sparse_csa(device=dev, kv_dtype=fi.SPARSE_KV_FP8_PACKED)
+    _, out, lse = _run(sp)
+    ro, rl = oracle.sparse(sp.to("cpu"))
+    check_close(out, lse, ro, rl, "packed CSA workload")
+
+
 def test_sparse_batch_invariance():
     full = fi.make_sparse(B=4, N1=8, D=128, q_lens=[2] * 4, kv_lens=[900, 300, 2500, 64],
                           mode="csa", K2=128, seed=7, device=dev)

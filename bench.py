@@ -30,6 +30,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "paged-decode KV GB/s and prefill TFLOP/s on 1 GB300, % of roofline"
@@ -253,7 +254,6 @@ def cpu_single_thread(prob_cpu, bytes_per_run):
 
 
 def _sample_rows_heads(p, n_pairs, seed):
-    import numpy as np
     g = np.random.default_rng(seed)
     rows = g.integers(0, p.rows, n_pairs)
     heads = g.integers(0, p.QN, n_pairs)
@@ -276,29 +276,32 @@ def _row_kv(p, rows):
     return out
 
 
-def cpu_fp8_decode(p_cpu, min_seconds):
-    """Oracle on a sample of (batch, head) rows of the long FP8 decode; the
-    rate counts the KV bytes those rows stand for (a row's share of its KV
-    head's bytes: 1/G of them)."""
+def cpu_sampled(p_cpu, units_total, unit, nthreads, min_seconds, n_pairs, seed):
+    """The oracle on a sample of (query row, head) pairs of a workload.  The
+    sample does a fraction f of the whole workload's oracle work (its pairs'
+    visible keys over those of every pair), so the rate credited is
+    f * units_total per elapsed second: the whole workload's metric at the
+    oracle's speed on this sample."""
     import oracle
-    cores = _cores()
-    rows, heads = _sample_rows_heads(p_cpu, 32, 5)
-    G = p_cpu.QN // p_cpu.KVN
-    per_tok = 2 * (p_cpu.D + 4 * (p_cpu.D // 64))
-    by = sum(per_tok * k for k in _row_kv(p_cpu, rows)) / G
-    n, dt = _timed_repeats(lambda: oracle.fia_sample(p_cpu, rows, heads, cores), min_seconds)
-    return {"value": by * n / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"32 (batch, head) rows, repeated {n}x ({dt:.1f} s)"}
+    rows, heads = _sample_rows_heads(p_cpu, n_pairs, seed)
+    all_rows = np.arange(p_cpu.rows)
+    work_all = p_cpu.QN * sum(_row_kv(p_cpu, all_rows))
+    f = sum(_row_kv(p_cpu, rows)) / max(1, work_all)
+    oracle.fia_sample(p_cpu, rows, heads, nthreads)  # build + warm
+    n, dt = _timed_repeats(lambda: oracle.fia_sample(p_cpu, rows, heads, nthreads), min_seconds)
+    scale = 1e9 if unit == "GB/s" else 1e12
+    return {"value": f * units_total * n / dt / scale, "unit": unit, "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{n_pairs} (query row, head) pairs ({100 * f:.3g} % of the workload's "
+                      f"oracle work), repeated {n}x ({dt:.1f} s)"}
 
 
-def cpu_prefill(p_cpu, min_seconds):
-    import oracle
-    cores = _cores()
-    rows, heads = _sample_rows_heads(p_cpu, 256, 7)
-    fl = sum(4 * p_cpu.D * k for k in _row_kv(p_cpu, rows))
-    n, dt = _timed_repeats(lambda: oracle.fia_sample(p_cpu, rows, heads, cores), min_seconds)
-    return {"value": fl * n / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"256 (query row, head) pairs, repeated {n}x ({dt:.1f} s)"}
+def cpu_both(p_cpu, units_total, unit, min_seconds, n_pairs, seed):
+    """All host cores, and one thread, on the same sample."""
+    allc = cpu_sampled(p_cpu, units_total, unit, _cores(), min_seconds, n_pairs, seed)
+    one = cpu_sampled(p_cpu, units_total, unit, 1, min(1.0, min_seconds), max(1, n_pairs // 8),
+                      seed)
+    return allc, one
 
 
 def cpu_sparse(sp_cpu, by, nthreads, min_seconds):
@@ -312,6 +315,10 @@ def cpu_sparse(sp_cpu, by, nthreads, min_seconds):
 # extra workloads (evidence only)
 # ---------------------------------------------------------------------------
 
+class _Skip(Exception):
+    """A workload left out by --only."""
+
+
 def _bench_call(call, steps, warmup, flush):
     for _ in range(warmup):
         call.run()
@@ -323,12 +330,18 @@ def _stats(xs):
     return statistics.mean(xs), statistics.median(xs)
 
 
-def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds):
+def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds, only=None):
     import decode_tile_scheduler_gb300 as fia
     import fia_inputs as fi
     res = {}
+
+    def want(key):
+        return only is None or key in only.split(",")
+
     # long-context FP8 decode
     try:
+        if not want("fp8_long_decode"):
+            raise _Skip
         p = fi.workload_fp8_long_decode(device="cuda")
         call = fia.FiaCall(p, with_lse=True)
         st, ex = _bench_call(call, steps, warmup, flush)
@@ -341,12 +354,18 @@ def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds):
             "GB/s": by / ms / 1e6, "kernel_GB/s": by / kms / 1e6,
             "frac_of_hbm": by / kms / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": by}
         if with_cpu:
-            res["fp8_long_decode"]["cpu_baseline"] = cpu_fp8_decode(p.to("cpu"), cpu_seconds)
+            r = res["fp8_long_decode"]
+            r["cpu_baseline"], r["cpu_single_thread"] = cpu_both(p.to("cpu"), by, "GB/s",
+                                                                 cpu_seconds, 32, 5)
         del call, p
+    except _Skip:
+        pass
     except Exception as e:  # not built yet
         res["fp8_long_decode"] = {"unavailable": str(e)[:200]}
     torch.cuda.empty_cache()
     try:
+        if not want("varlen_causal_prefill"):
+            raise _Skip
         p = fi.workload_varlen_prefill(device="cuda")
         call = fia.FiaCall(p, with_lse=True)
         st, ex = _bench_call(call, steps, warmup, flush)
@@ -359,8 +378,12 @@ def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds):
             "TFLOP/s": fl / ms / 1e9, "kernel_TFLOP/s": fl / kms / 1e9,
             "frac_of_bf16": fl / kms / 1e9 / peaks["bf16_tflops"], "flops": fl}
         if with_cpu:
-            res["varlen_causal_prefill"]["cpu_baseline"] = cpu_prefill(p.to("cpu"), cpu_seconds)
+            r = res["varlen_causal_prefill"]
+            r["cpu_baseline"], r["cpu_single_thread"] = cpu_both(p.to("cpu"), fl, "TFLOP/s",
+                                                                 cpu_seconds, 256, 7)
         del call, p
+    except _Skip:
+        pass
     except Exception as e:
         res["varlen_causal_prefill"] = {"unavailable": str(e)[:200]}
     torch.cuda.empty_cache()
@@ -373,6 +396,8 @@ def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds):
              lambda: fi.workload_paged_decode(device="cuda", kv_layout=fi.KV_LAYOUT_BNNBSD),
              "paged GQA decode with head-major pages [nb, KV_N, bs, D]")):
         try:
+            if not want(key):
+                raise _Skip
             p = mk()
             call = fia.FiaCall(p, with_lse=True)
             st, ex = _bench_call(call, steps, warmup, flush)
@@ -382,11 +407,18 @@ def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds):
                         "kernel_ms": kms, "kernel_ms_median": kms_med, "GB/s": by / ms / 1e6,
                         "kernel_GB/s": by / kms / 1e6,
                         "frac_of_hbm": by / kms / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": by}
+            if with_cpu:
+                res[key]["cpu_baseline"], res[key]["cpu_single_thread"] = cpu_both(
+                    p.to("cpu"), by, "GB/s", cpu_seconds, 64, 11)
             del call, p
+        except _Skip:
+            pass
         except Exception as e:
             res[key] = {"unavailable": str(e)[:200]}
         torch.cuda.empty_cache()
     try:
+        if not want("fp8_varlen_causal_prefill"):
+            raise _Skip
         p = fi.workload_varlen_prefill(device="cuda", kv_dtype=fi.KV_FP8_E4M3)
         call = fia.FiaCall(p, with_lse=True)
         st, ex = _bench_call(call, steps, warmup, flush)
@@ -398,11 +430,19 @@ def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds):
             "ms_per_step": ms, "ms_median": ms_med, "kernel_ms": kms, "kernel_ms_median": kms_med,
             "TFLOP/s": fl / ms / 1e9, "kernel_TFLOP/s": fl / kms / 1e9,
             "frac_of_bf16": fl / kms / 1e9 / peaks["bf16_tflops"], "flops": fl}
+        if with_cpu:
+            r = res["fp8_varlen_causal_prefill"]
+            r["cpu_baseline"], r["cpu_single_thread"] = cpu_both(p.to("cpu"), fl, "TFLOP/s",
+                                                                 cpu_seconds, 256, 7)
         del call, p
+    except _Skip:
+        pass
     except Exception as e:
         res["fp8_varlen_causal_prefill"] = {"unavailable": str(e)[:200]}
     torch.cuda.empty_cache()
     try:
+        if not want("sparse_csa_decode"):
+            raise _Skip
         sp = fi.workload_sparse_csa(device="cuda")
         call = fia.SparseCall(sp, with_lse=True)
         call.plan()
@@ -422,9 +462,13 @@ def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds):
             res["sparse_csa_decode"]["cpu_baseline"] = cpu_sparse(spc, by, _cores(), cpu_seconds)
             res["sparse_csa_decode"]["cpu_single_thread"] = cpu_sparse(spc, by, 1, 0.0)
         del call, sp
+    except _Skip:
+        pass
     except Exception as e:
         res["sparse_csa_decode"] = {"unavailable": str(e)[:200]}
     try:
+        if not want("sparse_csa_decode_fp8_packed"):
+            raise _Skip
         sp = fi.workload_sparse_csa(device="cuda", kv_dtype=fi.SPARSE_KV_FP8_PACKED)
         call = fia.SparseCall(sp, with_lse=True)
         call.plan()
@@ -440,9 +484,17 @@ def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds):
             "ms_per_step": ms, "ms_median": ms_med, "kernel_ms": kms, "kernel_ms_median": kms_med,
             "GB/s": by / ms / 1e6, "kernel_GB/s": by / kms / 1e6,
             "frac_of_hbm": by / kms / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": by}
+        if with_cpu:
+            spc = sp.to("cpu")
+            r = res["sparse_csa_decode_fp8_packed"]
+            r["cpu_baseline"] = cpu_sparse(spc, by, _cores(), cpu_seconds)
+            r["cpu_single_thread"] = cpu_sparse(spc, by, 1, 0.0)
+        del call, sp
+    except _Skip:
+        pass
     except Exception as e:
         res["sparse_csa_decode_fp8_packed"] = {"unavailable": str(e)[:200]}
-    if with_cpu:
+    if with_cpu and only is None:
         try:
             import oracle
             t = fi.workload_tiny_prefill(device="cpu")
@@ -614,6 +666,18 @@ def run_fia(args):
         dist.destroy_process_group()
 
 
+def run_only(args):
+    """One extra workload alone: its JSON object on one line (not the
+    contract's line).  Launches: W warm-up steps, then K timed steps."""
+    peaks = _peaks()
+    flush = _flush_buf()
+    res = extra_workloads(max(1, args.steps), args.warmup, flush, peaks, not args.no_cpu,
+                          min(3.0, args.cpu_seconds), only=args.only)
+    if not res:
+        raise SystemExit(f"no extra workload named {args.only!r}")
+    print(json.dumps(res))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -623,11 +687,16 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", default=None,
+                    help="time one extra workload alone (e.g. mtp_decode_s4) and print "
+                         "its figures; for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_fia(args)
 

@@ -73,7 +73,7 @@ struct DecodeCfg {
   static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleBytes + kMaskBytes;
   static constexpr int kStages = FP8 ? 5 : (D == 128 ? 3 : 6);
   static constexpr int kQBytes = kMaxGH * D * 2;
-  static constexpr int kRedBytes = 4 * 8 * D * 4;           // 4 warps x 8 heads x D
+  static constexpr int kRedBytes = 4 * kConsumers * 32 * 16;  // merge rounds: [4][8 warps][32] float4
   static constexpr int kRedMlBytes = kConsumers * kMaxGH * 2 * 4;
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffRed = kOffQ + 2 * kQBytes;
@@ -1304,7 +1304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     named_bar_sync(1, nthr);
-    // every thread: combined (M, L) of its heads, and its own scale factor
+    // every thread: combined (M, L) of its columns, and its own scale factor
     float Mh[NG][2], Lh[NG][2];
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng) {
@@ -1331,77 +1331,85 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    named_bar_sync(1, nthr);  // red_ml is rewritten below
-    // tree sum of the scaled accumulators (8 -> 4 -> 2 -> 1 warps), one head
-    // group at a time through a [4][D][8] buffer; slot 0 ends as the result
+    // Reduce-scatter of the scaled accumulators: warp w ends with m-tile w
+    // (its 16 d rows) summed over the eight warps.  The m-tiles go through
+    // shared memory in rounds of four ([4 slots][8 warps][32 lanes] float4,
+    // 16 KB): round r carries m-tiles i = r, r + R, ... (R = MT / 4 rounds),
+    // every warp stores those it does not own, then each owner adds the
+    // other seven warps' copies of its m-tile to its own.  Lanes keep their
+    // fragment layout throughout, so every access is a conflict-free 16-byte
+    // one.  red_ml (read above) is rewritten only by the next chunk's merge.
+    constexpr int R = MT / 4;
+    float4* red4 = reinterpret_cast<float4*>(red);
+    const int d0 = drow(cw, g), d1 = drow(cw, g + 8);
+    const int64_t slot = min(max(slot0, (int64_t)0), a.max_chunks - 1);
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng) {
+      float own[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int half = 4; half >= 1; half >>= 1) {
-        if (cw >= half && cw < 2 * half) {
-          float* bp = red + (size_t)(cw - half) * D * 8;
+      for (int rnd = 0; rnd < R; ++rnd) {
+        if (ng > 0 || rnd > 0) named_bar_sync(1, nthr);  // the previous round's reads are done
 #pragma unroll
-          for (int i = 0; i < MT; ++i) {
-            *reinterpret_cast<float2*>(bp + drow(i, g) * 8 + 2 * q4) = make_float2(acc[i][ng][0], acc[i][ng][1]);
-            *reinterpret_cast<float2*>(bp + drow(i, g + 8) * 8 + 2 * q4) = make_float2(acc[i][ng][2], acc[i][ng][3]);
-          }
-        }
+        for (int i = rnd; i < MT; i += R)
+          if (i != cw)
+            red4[((i / R) * kConsumers + cw) * 32 + lane] =
+                make_float4(acc[i][ng][0], acc[i][ng][1], acc[i][ng][2], acc[i][ng][3]);
         named_bar_sync(1, nthr);
-        if (cw < half) {
-          const float* bp = red + (size_t)cw * D * 8;
+        if (cw < MT && cw % R == rnd) {
 #pragma unroll
-          for (int i = 0; i < MT; ++i) {
-            const float2 x = *reinterpret_cast<const float2*>(bp + drow(i, g) * 8 + 2 * q4);
-            const float2 y = *reinterpret_cast<const float2*>(bp + drow(i, g + 8) * 8 + 2 * q4);
-            acc[i][ng][0] += x.x; acc[i][ng][1] += x.y;
-            acc[i][ng][2] += y.x; acc[i][ng][3] += y.y;
+          for (int i = rnd; i < MT; i += R)
+            if (i == cw) {
+              own[0] = acc[i][ng][0];
+              own[1] = acc[i][ng][1];
+              own[2] = acc[i][ng][2];
+              own[3] = acc[i][ng][3];
+            }
+#pragma unroll
+          for (int w2 = 0; w2 < kConsumers; ++w2) {
+            if (w2 == cw) continue;
+            const float4 x = red4[((cw / R) * kConsumers + w2) * 32 + lane];
+            own[0] += x.x; own[1] += x.y; own[2] += x.z; own[3] += x.w;
           }
         }
-        named_bar_sync(1, nthr);
       }
-      if (cw == 0) {
+      // the owner warp writes its d rows of this group's columns: the final
+      // O (bf16, times the column's 1/L and sink factor) and lse, or the
+      // partial slot (fp32 accumulator, then m and l after the D values)
+      if (cw < MT) {
 #pragma unroll
-        for (int i = 0; i < MT; ++i) {
-          *reinterpret_cast<float2*>(red + drow(i, g) * 8 + 2 * q4) = make_float2(acc[i][ng][0], acc[i][ng][1]);
-          *reinterpret_cast<float2*>(red + drow(i, g + 8) * 8 + 2 * q4) = make_float2(acc[i][ng][2], acc[i][ng][3]);
-        }
-        if (g == 0) {  // (M, L) of this head group into red_ml[0..7]
-          red_ml[(2 * q4) * 2 + 0] = Mh[ng][0];
-          red_ml[(2 * q4) * 2 + 1] = Lh[ng][0];
-          red_ml[(2 * q4 + 1) * 2 + 0] = Mh[ng][1];
-          red_ml[(2 * q4 + 1) * 2 + 1] = Lh[ng][1];
-        }
-      }
-      named_bar_sync(1, nthr);
-      // all consumer threads: write this group of 8 columns (final O or a partial)
-      const int nh = min(8, r.ncols - ng * 8);
-      if (!split) {
-        for (int idx = ctid; idx < nh * (D / 2); idx += nthr) {
-          const int hh = idx / (D / 2), d = (idx % (D / 2)) * 2;
-          const int c = r.c0 + ng * 8 + hh;                 // column: query row i, head h
-          const int i = c / a.G, h = r.hk * a.G + (c - i * a.G);
-          const int64_t tok = (int64_t)r.qrow0 + i;
-          float scl, lse;
-          finish_head(a, h, red_ml[hh * 2], red_ml[hh * 2 + 1], &scl, &lse);
-          uint16_t* o = a.out + tok * a.out_stride + (int64_t)h * D + d;
-          *reinterpret_cast<uint32_t*>(o) = pack_bf16(red[d * 8 + hh] * scl, red[(d + 1) * 8 + hh] * scl);
-          if (a.lse && d == 0) {
-            const int64_t li = a.layout == 1 ? tok * a.QN + h : ((int64_t)r.b * a.QN + h) * a.S_q + i;
-            a.lse[li] = lse;
+        for (int e = 0; e < 2; ++e) {
+          const int hh = ng * 8 + 2 * q4 + e;  // the unit's column
+          if (hh >= r.ncols) continue;
+          if (!split) {
+            const int c = r.c0 + hh;  // column: query row i, head h
+            const int i = c / a.G, h = r.hk * a.G + (c - i * a.G);
+            const int64_t tok = (int64_t)r.qrow0 + i;
+            float scl, lse;
+            finish_head(a, h, Mh[ng][e], Lh[ng][e], &scl, &lse);
+            uint16_t* o = a.out + tok * a.out_stride + (int64_t)h * D;
+            const __nv_bfloat16 v0 = __float2bfloat16_rn(own[e] * scl);
+            const __nv_bfloat16 v1 = __float2bfloat16_rn(own[2 + e] * scl);
+            o[d0] = *reinterpret_cast<const uint16_t*>(&v0);
+            o[d1] = *reinterpret_cast<const uint16_t*>(&v1);
+            if (a.lse && cw == 0 && g == 0) {
+              const int64_t li =
+                  a.layout == 1 ? tok * a.QN + h : ((int64_t)r.b * a.QN + h) * a.S_q + i;
+              a.lse[li] = lse;
+            }
+          } else {
+            // (the slot is clamped: a plan of other lengths cannot move the
+            // write out of the partial slots; the combine rejects such a
+            // plan's prefixes)
+            float* col = a.partials + slot * pstride + (int64_t)hh * (D + 2);
+            col[d0] = own[e];
+            col[d1] = own[2 + e];
+            if (cw == 0 && g == 0) {
+              col[D] = Mh[ng][e];
+              col[D + 1] = Lh[ng][e];
+            }
           }
         }
-      } else {
-        // (clamped: a plan of other lengths cannot move the write out of the
-        // partial slots; the combine rejects such a plan's prefixes)
-        const int64_t slot = min(max(slot0, (int64_t)0), a.max_chunks - 1);
-        float* pp = a.partials + slot * pstride;
-        for (int idx = ctid; idx < nh * (D + 2); idx += nthr) {
-          const int hh = idx / (D + 2), d = idx % (D + 2);
-          const float v = d < D ? red[d * 8 + hh] : red_ml[hh * 2 + (d - D)];
-          pp[(ng * 8 + hh) * (D + 2) + d] = v;
-        }
       }
-      named_bar_sync(1, nthr);
     }
   }
 }

@@ -5,9 +5,13 @@
  * Operations
  *   FIA     O = softmax(Q K^T * scale + mask) V, per query head h against KV
  *           head floor(h / G), G = Q_N / KV_N ("aclnnFusedInferAttentionScoreV5",
- *           formula section; "...V2": the IncreFlashAttention branch runs when
- *           the query S is 1, the PromptFlashAttention branch otherwise; GQA
- *           needs Q_N divisible by KV_N with ratio <= 64).
+ *           formula section; "...V2": an incremental branch for short queries
+ *           and a prompt branch otherwise -- here a query of at most 16 rows
+ *           per sequence runs the split-KV decode kernel, a longer one the
+ *           prefill kernel; GQA needs Q_N divisible by KV_N with ratio <= 64).
+ *   COMBINE the log-sum-exp join of partial results computed over disjoint
+ *           key sets (fia_lse_combine; the softmax_lse use of "...V2" and the
+ *           context-parallel example of "sparse_flash_mla").
  *   SPARSE  O = softmax(Q K~^T * softmax_scale) V~ with K~ = V~ gathered from a
  *           band window of the original KV and from compressed KV rows
  *           ("kv_quant_sparse_attn_sharedkv", formula and parameter table;
@@ -27,7 +31,8 @@
  * Readings where the pages are silent (they are restated in the design notes):
  *  - query rows are aligned to the bottom-right corner of the score matrix:
  *    row i of a sequence sits at KV position p = kv_len - q_len + i;
- *  - mask modes: 0 none; 3 right-down causal (j <= p); 4 band
+ *  - mask modes: 0 none (or an explicit mask); 1 the explicit mask; 2
+ *    left-up causal (j <= i); 3 right-down causal (j <= p); 4 band
  *    (p - pre_tokens <= j <= p + next_tokens);
  *  - a sink is one extra logit per query head that enters the softmax
  *    denominator only (not multiplied by scale, carries no value); lse
@@ -36,7 +41,7 @@
  *    lse = +inf, with or without a sink ("...V4" empty-tensor rule; "...V2"
  *    invalid-row correction);
  *  - FP8 KV: E4M3 codes with one fp32 scale per 64 consecutive elements of D,
- *    value = code * scale.
+ *    value = code * scale; sparse packed FP8 rows carry E8M0 tile scales.
  */
 #ifndef FIA_H_
 #define FIA_H_

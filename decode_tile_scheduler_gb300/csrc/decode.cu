@@ -20,7 +20,8 @@
 // per CTA, at least one tile), and a unit of cost c is cut into
 // n1 = max(0, floor(c/C) - 1) big chunks of C tiles followed by the remaining
 // r = c - n1*C tiles (C <= r < 2C unless c < C) in small chunks of
-// c2 = ceil(C/3) tiles.  The claim queue lists every big chunk (batch-major,
+// c2 = ceil(C/k) tiles, k = 3 (6 with an FP8 cache, whose long units gain
+// from smaller last pieces).  The claim queue lists every big chunk (batch-major,
 // then chunk, then active unit of the batch) before every small chunk (same
 // order), so the work left at the end is always small pieces.  CTAs claim
 // chunks from the queue with one atomic each: an SM that streams faster
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
     C = (T - 1 <= 0xffffffffLL && per <= 0xffffffffLL)
             ? (int64_t)((uint32_t)(T - 1) / (uint32_t)per) + 1
             : (T - 1) / per + 1;
-  const int64_t c2 = (C + 2) / 3;
+  const int64_t c2 = (C + a.small_div - 1) / a.small_div;
 
   // per batch: big and small chunks of its active units and whether it is
   // split -> three exclusive scans (all chunks before b = big + small before b)
@@ -1594,7 +1595,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUte
   // with more than 16 an item gets a whole CTA.  The choice depends on shapes
   // only, so results stay deterministic.
   const int64_t items = a.num_units * a.GH;  // bound: every batch split
-  const int64_t est = (int64_t)a.num_ctas * a.chunks_per_cta / a.num_units + 6;
+  const int64_t est = (int64_t)a.num_ctas * a.chunks_per_cta / a.num_units + 2 * a.small_div;
   if (est > 16) {
     const int grid = (int)std::min<int64_t>(items, (int64_t)a.num_ctas * 8);
     if (a.D == 64) return launch_pdl(decode_combine_grouped<64>, dim3(grid), dim3(256), 0, s, a);

@@ -192,10 +192,17 @@ struct DecodePlan {
   int64_t off_sched, off_queue, off_part, total;
 };
 
+// Small chunks are ceil(C/3) tiles, ceil(C/6) with an FP8 cache: its units
+// are long, so a smaller last piece shortens the wait for the slowest CTA at
+// the end of the queue (bf16 decode units are short, and more pieces there
+// cost more partial writes than they save).
+int decode_small_div(const fia_params* p) { return p->kv_dtype == FIA_KV_FP8_E4M3 ? 6 : 3; }
+
 // Decode workspace: [0, 256) error word (offset 0) and the claim counters
-// (offset 16); the schedule; the claim queue; the partial slots.  A unit of cost c gets at most c/C big chunks
-// (so at most n*W over all units) and at most 6 small ones, hence
-// max_chunks = n*W + 6*U bounds the chunks of any lengths.
+// (offset 16); the schedule; the claim queue; the partial slots.  A unit of
+// cost c gets at most c/C big chunks (so at most n*W over all units) and at
+// most ceil((2C - 1)/c2) <= 2*small_div small ones (the rest it leaves is
+// below 2C and c2 >= C/small_div), hence max_chunks = n*W + 2*small_div*U bounds the chunks of any lengths.
 fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
   int n;
   fia_status st = sm_count(p->num_sms, &n);
@@ -206,7 +213,7 @@ fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
   const int HG = (int)ceil_div(cols, GH);
   pl->n = n;
   pl->U = (int64_t)p->batch * p->num_kv_heads * HG;
-  pl->max_chunks = (int64_t)n * kDecodeChunksPerCta + 6 * pl->U;
+  pl->max_chunks = (int64_t)n * kDecodeChunksPerCta + 2 * decode_small_div(p) * pl->U;
   // queue positions and slots are 32-bit in the kernels
   if (pl->max_chunks >= INT32_MAX) return FIA_ERR_BAD_SHAPE;
   int64_t off = kAlign;
@@ -264,6 +271,7 @@ DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
   a.num_ctas = pl.n;
   a.num_units = pl.U;
   a.chunks_per_cta = kDecodeChunksPerCta;
+  a.small_div = decode_small_div(p);
   a.max_chunks = pl.max_chunks;
   char* w = static_cast<char*>(ws);
   a.sched = reinterpret_cast<int64_t*>(w + pl.off_sched);

@@ -293,20 +293,26 @@ fia_status fia_selftest_bounded_wait(int32_t *status, uint64_t limit_ns, void *s
 
 /* Workspace layout of the plan, for inspection (host-only).
  *
- * Decode schedule (written by fia_plan): work unit u = (b, kv head, head
- * group); cost = KV tiles (128 positions) its query row sees, at least 1 (0
- * when the batch has no query row).  With T the total cost, n CTAs and W = 5
- * chunks per CTA, C = max(1, ceil(T / (n W))) and c2 = ceil(C / 3).  A unit
- * of cost c gets n1 = max(0, floor(c/C) - 1) chunks of C tiles, then chunks
- * of c2 tiles over the rest (at most 6), so n W + 6 U bounds the chunks of U
- * units.  sched holds int64 {C, c2, chunks N, big chunks F, split batches M,
- * plan mark 0x4649414445434F44, B, CTA count}, then Q[B+1] (partial slots before batch b:
- * chunk i of unit w of batch b owns slot Q[b] + i*UPB + w, UPB = units per
- * batch), then R1[B+1] and R2[B+1] (big and small chunks before batch b),
- * then the M batches whose units have several chunks (ascending; -1 after).  The claim queue lists the
- * big chunks, batch-major then chunk then unit, followed by the small chunks
- * in the same order; entry = four int32 (b, i << 10 | w, KV length of b,
- * first query row of b). */
+ * Decode schedule (written by fia_plan): the columns of a KV head are its
+ * (query row, query head) pairs, S*G of them (S = max_seqlen_q <= 16), taken
+ * in groups of GH = 8 (S*G <= 8) or 16; work unit u = (b, kv head, group),
+ * UPB = KV_N * ceil(S*G/GH) units per batch, of which the first
+ * A(b) = KV_N * ceil(q_len(b)*G/GH) hold columns of batch b ("active", active
+ * index a).  Cost of an active unit = KV tiles (128 positions) its rows see
+ * together, at least 1 (0 when the batch has no query row).  With T the total
+ * cost, n CTAs and W = 5 chunks per CTA, C = max(1, ceil(T / (n W))) and
+ * c2 = ceil(C / k), k = 3 (6 with an FP8 cache).  A unit of cost c gets
+ * n1 = max(0, floor(c/C) - 1) chunks of C tiles, then chunks of c2 tiles
+ * over the rest (at most 2k), so n W + 2k U bounds the chunks of U units.
+ * sched holds int64 {C, c2, chunks N, big chunks F, split batches M, plan
+ * mark 0x4649414445434F44, B, CTA count}, then Q[B+1] (partial slots before
+ * batch b: chunk i of active unit a of batch b owns slot Q[b] + i*A(b) + a),
+ * then R1[B+1] and R2[B+1] (big and small chunks before batch b), then the M
+ * batches whose units have several chunks (ascending; -1 after).  The claim
+ * queue lists the big chunks, batch-major then chunk then active unit,
+ * followed by the small chunks in the same order; entry = four int32
+ * (b | q_len(b) << 16, i << 16 | u - b*UPB, KV length of b, first token row
+ * of b). */
 typedef struct fia_plan_layout {
     int32_t branch;           /* 1 decode (split-KV), 2 prefill                */
     int32_t num_ctas;         /* persistent CTAs                               */

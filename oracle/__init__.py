@@ -333,7 +333,8 @@ def decode_schedule(p, num_ctas: int, per_cta: int):
     G = p.QN // p.KVN
     HG = -(-G // (8 if G <= 8 else 16))
     U = p.B * p.KVN * HG
-    cap = num_ctas * per_cta + 6 * U
+    k = 3 if p.kv_dtype == 0 else 6  # small chunks of ceil(C/k) tiles
+    cap = num_ctas * per_cta + 2 * k * U
     sched = np.zeros(8 + 3 * (p.B + 1) + p.B, dtype=np.int64)
     queue = np.zeros((max(cap, 1), 4), dtype=np.int32)
     n = lib().oracle_decode_schedule(ctypes.byref(s), num_ctas, per_cta, sched.ctypes.data,

@@ -592,7 +592,8 @@ static int64_t or_tiles(int64_t lo, int64_t hi)
  * else the number of KV tiles its rows can see together (the interval from
  * the first row's lower bound to the last row's upper bound), at least 1.
  * With T the sum of all active units' costs, n CTAs and W chunks per CTA:
- *   C  = max(1, ceil(T / (n*W))),  c2 = ceil(C/3);
+ *   C  = max(1, ceil(T / (n*W))),  c2 = ceil(C/k), k = 3 (6 with an FP8
+ *   cache);
  *   a unit of cost c has n1 = max(0, floor(c/C) - 1) big chunks of C tiles,
  *   then its remaining c - n1*C tiles in small chunks of c2 tiles (the last
  *   one shorter), n2 of them.
@@ -647,7 +648,10 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
     }
     C = or_ceil_div(T, (int64_t)num_ctas * per_cta);
     if (C < 1) C = 1;
-    c2 = (C + 2) / 3;
+    {
+        int64_t k = a->kv_dtype == OR_KV_BF16 ? 3 : 6;
+        c2 = (C + k - 1) / k;
+    }
     for (b = 0; b < B; ++b) {
         int64_t n1 = 0, n2 = 0, A = a->KVN * ha[b];
         if (cost[b] > 0) {

@@ -163,6 +163,11 @@ def test_plan_layout_describes_decode_schedule():
     assert lay.sched_off >= 256 and lay.queue_off >= lay.sched_off + 8 * (8 + 3 * 5 + 4)
     # partial slots: max_chunks x 8 heads x (D + 2) floats fit in the workspace
     assert lay.total_bytes >= lay.queue_off + 16 * lay.max_chunks + 4 * lay.max_chunks * 8 * 130
+    # an FP8 cache cuts its units' rest into chunks of ceil(C/6) tiles: at
+    # most 12 per unit
+    lay8 = fia.fia_get_plan_layout(_decode_params(kv_dtype=fia.KV_FP8_E4M3, k_scale=FAKE,
+                                                  v_scale=FAKE, quant_tile=64))
+    assert lay8.max_chunks == 152 * per_cta + 12 * lay8.num_units
 
 
 # --------------------------------------------------------------------------

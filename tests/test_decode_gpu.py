@@ -112,6 +112,27 @@ def test_schedule_metadata_bit_exact():
         assert np.array_equal(queue, rq)
 
 
+def test_schedule_fp8_bit_exact():
+    # an FP8 cache: small chunks of ceil(C/6) tiles, the bound n*W + 12*U
+    import decode_tile_scheduler_gb300 as fia
+    p = fi.make_fia(B=4, QN=32, KVN=4, D=128, q_lens=[1] * 4, kv_lens=[40000, 3, 9000, 129],
+                    block_size=128, kv_dtype=fi.KV_FP8_E4M3, seed=31, device=dev)
+    for n in (1, 7, 152):
+        c, out, lse = _run(p, n)
+        lay = c.plan_layout()
+        ws = c.ws.cpu()
+        per_cta = (lay.max_chunks - 12 * lay.num_units) // n
+        nsched = 8 + 3 * (p.B + 1) + p.B
+        sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
+        rs, rq = oracle.decode_schedule(p.to("cpu"), n, per_cta)
+        assert np.array_equal(sched, rs)
+        N = int(sched[2])
+        queue = ws[lay.queue_off: lay.queue_off + 16 * N].view(torch.int32).numpy().reshape(N, 4)
+        assert np.array_equal(queue, rq)
+    ro, rl = _ref(p)
+    check_close(out, lse, ro, rl, "FP8 schedule")
+
+
 def test_schedule_many_batches_bit_exact_and_parity():
     # more batches than the scheduler keeps in shared memory: the global path
     import decode_tile_scheduler_gb300 as fia

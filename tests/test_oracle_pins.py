@@ -501,6 +501,31 @@ def test_decode_schedule_chunks_cover_each_unit_once(ctas, per_cta):
         [(kv[x & 0xFFFF], x & 0xFFFF) for x, _, _, _ in queue.tolist()]
 
 
+def test_decode_schedule_fp8_small_chunks_are_a_sixth():
+    """With an FP8 cache the rest of a unit (between C and 2C tiles) goes in
+    chunks of ceil(C/6) tiles, at most 12 of them."""
+    kv = [30000, 70000, 128, 129 * 128]
+    p = fi.make_fia(B=len(kv), QN=16, KVN=2, D=128, q_lens=[1] * len(kv), kv_lens=kv,
+                    block_size=128, kv_dtype=fi.KV_FP8_E4M3, seed=4)
+    for ctas, per in ((2, 5), (9, 5), (152, 5)):
+        sched, queue = oracle.decode_schedule(p, ctas, per)
+        costs = [max(1, -(-k // 128)) for k in kv]
+        T = 2 * sum(costs)
+        C = max(1, -(-T // (ctas * per)))
+        c2 = -(-C // 6)
+        assert list(sched[:2]) == [C, c2]
+        assert sched[2] <= ctas * per + 12 * 2 * len(kv)
+        chunks = _unit_chunks(sched, queue, p.B, 2)
+        F = int(sched[3])
+        for b, c in enumerate(costs):
+            for w in range(2):
+                lst = chunks[b * 2 + w]
+                n1 = sum(pos < F for pos, _ in lst)
+                n2 = len(lst) - n1
+                rest = c - n1 * C
+                assert n2 <= 12 and (n2 - 1) * c2 < rest <= n2 * c2
+
+
 def test_decode_schedule_band_counts_window_tiles_only():
     p = fi.make_fia(B=2, QN=2, KVN=1, D=16, q_lens=[1, 1], kv_lens=[1000, 100], block_size=16,
                     mask_mode=4, pre_tokens=200, next_tokens=0, seed=2)

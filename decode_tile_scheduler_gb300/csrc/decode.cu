@@ -7,9 +7,11 @@
 // Columns and units: the query side of KV head hk of a sequence is its
 // (query row i, query head h of the GQA group) pairs, column c = i*G + h%G,
 // S_max*G of them.  A work unit (batch b, KV head hk, column group hg) holds up
-// to GH = 8 or 16 consecutive columns: they form the N columns of every
-// mma.sync, so each KV page is read from HBM once for all of them (the GQA
-// heads and, for multi-token decode, the query rows too).  Only the groups
+// to GH consecutive columns (16 for one query row with G > 8, else 8): they
+// form the N columns of every mma.sync, so each KV page is read once for all
+// of them (the GQA heads and, for multi-token decode, the query rows too; the
+// units of one KV head sit next to each other in the queue and share its
+// pages through L2).  Only the groups
 // holding columns of the sequence's own rows are scheduled ("active").  A
 // unit owns the KV tiles (128 positions) its rows see together; every column
 // is masked with its own row's bounds.

@@ -209,7 +209,7 @@ fia_status decode_plan(const fia_params* p, DecodePlan* pl) {
   if (st != FIA_OK) return st;
   const int G = p->num_q_heads / p->num_kv_heads;
   const int cols = p->max_seqlen_q * G;  // (query row, head) columns of a KV head
-  const int GH = decode_group_heads(cols);
+  const int GH = decode_group_heads(p->max_seqlen_q, cols);
   const int HG = (int)ceil_div(cols, GH);
   pl->n = n;
   pl->U = (int64_t)p->batch * p->num_kv_heads * HG;
@@ -236,7 +236,7 @@ DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
   a.KVN = p->num_kv_heads;
   a.D = p->head_dim;
   a.G = G;
-  a.GH = decode_group_heads(p->max_seqlen_q * G);
+  a.GH = decode_group_heads(p->max_seqlen_q, p->max_seqlen_q * G);
   a.HG = (int)ceil_div(p->max_seqlen_q * G, a.GH);
   a.layout = p->layout;
   a.S_q = p->layout == FIA_LAYOUT_BSND ? p->max_seqlen_q : 1;

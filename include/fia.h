@@ -295,7 +295,8 @@ fia_status fia_selftest_bounded_wait(int32_t *status, uint64_t limit_ns, void *s
  *
  * Decode schedule (written by fia_plan): the columns of a KV head are its
  * (query row, query head) pairs, S*G of them (S = max_seqlen_q <= 16), taken
- * in groups of GH = 8 (S*G <= 8) or 16; work unit u = (b, kv head, group),
+ * in groups of GH = 16 (S = 1 and G > 8) or 8 (otherwise); work unit
+ * u = (b, kv head, group),
  * UPB = KV_N * ceil(S*G/GH) units per batch, of which the first
  * A(b) = KV_N * ceil(q_len(b)*G/GH) hold columns of batch b ("active", active
  * index a).  Cost of an active unit = KV tiles (128 positions) its rows see

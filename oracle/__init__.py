@@ -331,7 +331,7 @@ def decode_schedule(p, num_ctas: int, per_cta: int):
     schedule for n CTAs and W = per_cta chunks per CTA."""
     s, keep = _fia_struct(p)
     G = p.QN // p.KVN
-    HG = -(-G // (8 if G <= 8 else 16))
+    HG = -(-(max(1, p.S_q) * G) // 8)  # units per KV head, at most (8-column groups)
     U = p.B * p.KVN * HG
     k = 3 if p.kv_dtype == 0 else 6  # small chunks of ceil(C/k) tiles
     cap = num_ctas * per_cta + 2 * k * U

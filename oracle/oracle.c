@@ -584,7 +584,8 @@ static int64_t or_tiles(int64_t lo, int64_t hi)
 /* Decode schedule (query rows per sequence S = max_seqlen_q, 1..16).  The
  * columns of a KV head hk of batch b are its (query row i, query head h of
  * the GQA group) pairs, numbered c = i*G + (h - hk*G); they are taken in
- * groups of GH = 8 (S*G <= 8) or 16, HG = ceil(S*G/GH) groups per KV head,
+ * groups of GH = 16 (one query row, S = 1, and G > 8) or 8 (otherwise),
+ * HG = ceil(S*G/GH) groups per KV head,
  * unit u = (b*KVN + hk)*HG + hg, UPB = KVN*HG units per batch.  Of these, the
  * HA(b) = ceil(q_len(b)*G/GH) first groups of every KV head hold columns
  * ("active"; A(b) = KVN*HA(b) of them, active index a = hk*HA(b) + hg).  All
@@ -617,7 +618,7 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
 {
     int G = a->QN / a->KVN;
     int64_t S = a->max_seqlen_q;
-    int GH = S * G <= 8 ? 8 : 16;
+    int GH = (S == 1 && G > 8) ? 16 : 8;
     int64_t HG = or_ceil_div(S * G, GH);
     int B = a->B, b;
     int64_t *Q = sched + 8, *R1 = Q + (B + 1), *R2 = R1 + (B + 1), *SB = R2 + (B + 1);

@@ -541,7 +541,8 @@ def test_decode_schedule_band_counts_window_tiles_only():
                                          (16, 2, fi.LAYOUT_TND), (3, 1, fi.LAYOUT_TND)])
 def test_decode_schedule_multi_row_units(S, G, layout):
     """Several query rows per sequence: a KV head's columns are its (row,
-    head) pairs, S*G of them in groups of GH = 8 or 16; only the groups that
+    head) pairs, S*G of them in groups of GH = 8 (16 only for one row with
+    more than 8 heads per KV head); only the groups that
     hold columns of the sequence's own rows are scheduled, every active unit
     of a sequence costs the tiles its rows see together, and each of its
     chunks owns the slot Q[b] + i * A(b) + a."""
@@ -551,7 +552,7 @@ def test_decode_schedule_multi_row_units(S, G, layout):
     p = fi.make_fia(B=5, QN=G * KVN, KVN=KVN, D=16, q_lens=ql, kv_lens=kv, layout=layout,
                     block_size=16, mask_mode=3, seed=9)
     p.S_q = S  # the rows every decode unit covers (max_seqlen_q)
-    GH = 8 if S * G <= 8 else 16
+    GH = 16 if (S == 1 and G > 8) else 8
     HG = -(-S * G // GH)
     UPB = KVN * HG
     for ctas, per in ((1, 5), (9, 5), (152, 5)):

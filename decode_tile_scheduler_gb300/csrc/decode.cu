@@ -586,6 +586,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // prefill branch last) nothing runs and the error word says 2.  Queue
     // entries and partial slots are range-checked as well, so a plan of
     // other lengths cannot send a load or store out of bounds.
+    // (the CTA's first queue entry is loaded beside the plan's header, not
+    // after it: entry blockIdx.x lies inside the queue buffer, which holds
+    // max_chunks >= gridDim.x entries, and is used only if the plan checks out)
+    const int4 ent0 = a.queue[blockIdx.x];
     const bool plan_ok = a.sched[5] == kDecodePlanMark && a.sched[6] == a.B &&
                          a.sched[7] == a.num_ctas && a.sched[0] >= 1 && a.sched[1] >= 1 &&
                          a.sched[2] >= 0 && a.sched[2] <= a.max_chunks &&
@@ -600,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // counter, each claim issued one chunk ahead and read only after the
     // chunk's tiles are queued, so its latency hides
     int64_t g = plan_ok ? (int64_t)blockIdx.x : N;
-    int4 ent = g < N ? a.queue[g] : make_int4(0, 0, 0, 0);
+    int4 ent = g < N ? ent0 : make_int4(0, 0, 0, 0);
     bool aborted = false;
     while (g < N) {
       // claim the next chunk now; its result and queue entry are read once

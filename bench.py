@@ -388,8 +388,12 @@ def extra_workloads(steps, warmup, flush, peaks, with_cpu, cpu_seconds, only=Non
         res["varlen_causal_prefill"] = {"unavailable": str(e)[:200]}
     torch.cuda.empty_cache()
     # forms beyond the headline workloads: multi-token decode (4 query rows
-    # per sequence), head-major pages, FP8 prefill
+    # per sequence), head-major pages, FP8 decode with 16 query heads per KV
+    # head, FP8 prefill
     for key, mk, what in (
+            ("fp8_gqa16_decode",
+             lambda: fi.workload_fp8_long_decode(device="cuda", KVN=4),
+             "the long FP8 decode with KV_N=4 (16 query heads per KV head)"),
             ("mtp_decode_s4", lambda: fi.workload_paged_decode(device="cuda", S_q=4),
              "paged GQA decode sequences with 4 query rows each (right-down causal)"),
             ("paged_decode_bnnbsd",

@@ -34,7 +34,8 @@
 //
 // Decode kernel: one producer warp streams K and V pages with TMA (page rows
 // from block_table) into a ring of shared-memory stages, with the rows of an
-// explicit mask when there is one; eight consumer warps each take 16 rows of
+// explicit mask when there is one; eight consumer warps (two warpgroups, with
+// the registers the producer's warpgroup gives up) each take 16 rows of
 // every tile.  The products are computed transposed ("swap AB"):
 // S^T = K Q^T with the KV rows as the mma M dimension and the query columns
 // as N, then O^T += V^T P^T, where P^T comes out of the S^T accumulators with
@@ -53,7 +54,13 @@ namespace fia {
 namespace {
 
 constexpr int kConsumers = 8;                        // consumer warps
-constexpr int kThreads = 32 * (1 + kConsumers);
+// three warpgroups: the producer's (warp 0 works, warps 1-3 leave at once)
+// gives its registers to the two consumer warpgroups (setmaxnreg):
+// 128 * kProdRegs + 256 * kConsRegs = 384 * 168, the launch's register file
+constexpr int kThreads = 32 * (4 + kConsumers);
+constexpr int kProdRegs = 88;
+constexpr int kConsRegs = 208;
+static_assert(128 * kProdRegs + 256 * kConsRegs <= kThreads * 168, "register split");
 constexpr int kRowsPerWarp = kKvTile / kConsumers;  // 16
 constexpr int kMaxGH = 16;                           // heads per unit, max
 
@@ -578,7 +585,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   pdl_wait();  // the plan (and anything else before us on the stream) is complete
 
-  if (warp == 0) {
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs) : "memory");
+    if (warp != 0) return;  // the producer warpgroup's other warps have no work
     // ======================= producer =======================
     // A plan of these arguments carries the scheduler's mark, B and CTA
     // count, and no prefill plan has been written over the workspace since;
@@ -806,12 +815,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ======================= consumers =======================
-  const int cw = warp - 1;     // 0..7
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsRegs) : "memory");
+  const int cw = warp - 4;     // 0..7
   const int g = lane >> 2;     // fragment row group
   const int q4 = lane & 3;     // thread in quad
   const int R0 = cw * kRowsPerWarp;
   const int nthr = 32 * kConsumers;
-  const int ctid = tid - 32;
   const uint32_t smem_base = smem_u32(smem);
   constexpr int KS = D / 16;   // k-steps over D (QK)
   constexpr int MT = D / 16;   // m-tiles over D (PV)

@@ -490,12 +490,13 @@ def workload_varlen_prefill(device="cpu", B=8, kv_dtype=KV_BF16) -> FiaProblem:
                     device=device, kv_dtype=kv_dtype)
 
 
-def workload_fp8_long_decode(device="cpu", B=4, lo=32768, hi=131072) -> FiaProblem:
+def workload_fp8_long_decode(device="cpu", B=4, lo=32768, hi=131072, QN=64, KVN=8) -> FiaProblem:
     """B=4, S_q=1, Q_N=64, KV_N=8, D=128, kv len ~ U[32768,131072], E4M3 KV
-    with fp32 per-64 scales, block 128."""
+    with fp32 per-64 scales, block 128 (KVN=4: the same sequences with 16
+    query heads per KV head)."""
     g = torch.Generator().manual_seed(1004)
     kv = _lens(g, B, lo, hi)
-    return make_fia(B=B, QN=64, KVN=8, D=128, q_lens=[1] * B, kv_lens=kv, layout=LAYOUT_BSND,
+    return make_fia(B=B, QN=QN, KVN=KVN, D=128, q_lens=[1] * B, kv_lens=kv, layout=LAYOUT_BSND,
                     paged=True, block_size=128, kv_dtype=KV_FP8_E4M3, seed=1004, device=device)
 
 

@@ -89,7 +89,7 @@ struct DecodeCfg {
   static constexpr int kOffRed = kOffQ + 2 * kQBytes;
   static constexpr int kOffRedMl = kOffRed + kRedBytes;
   static constexpr int kOffBar = kOffRedMl + kRedMlBytes;
-  static constexpr int kOffMsg = kOffBar + 8 * (2 * kStages + 4);
+  static constexpr int kOffMsg = kOffBar + 8 * (2 * kStages + 6);
   static constexpr int kOffMisc = kOffMsg + 2 * 128;
   static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
@@ -559,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + S;
   uint64_t* qfull = empty + S;
   uint64_t* qempty = qfull + 2;
+  uint64_t* vpost = qempty + 2;  // [2] chunk message posted, for the V warp
   int* misc = reinterpret_cast<int*>(smem + Cfg::kOffMisc);
   UnitMsg* msg = reinterpret_cast<UnitMsg*>(smem + Cfg::kOffMsg);
   float* red = reinterpret_cast<float*>(smem + Cfg::kOffRed);
@@ -568,12 +569,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);  // the K warp's and the V warp's arrivals (with their bytes)
       mbar_init(&empty[s], kConsumers);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], kConsumers);
+      mbar_init(&qempty[s], kConsumers + 1);  // the consumers and the V warp
+      mbar_init(&vpost[s], 1);
     }
     misc[0] = 0;  // abort flag
     fence_barrier_init();
@@ -587,8 +589,156 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs) : "memory");
-    if (warp != 0) return;  // the producer warpgroup's other warps have no work
-    // ======================= producer =======================
+    if (warp >= 2) return;  // the producer warpgroup's other warps have no work
+    // ======================= producers =======================
+    // Warp 0 streams the K boxes (and the explicit-mask slices) of every
+    // tile and does the chunk bookkeeping: claims, chunk messages, query
+    // vectors.  Warp 1 streams the V boxes: it follows the messages warp 0
+    // posts (vpost) and walks the same tiles, so the per-tile page lookups,
+    // address arithmetic and copy issue are split between two warps (the FP8
+    // decode's single producer was busy most of its time).  Both wait for a
+    // free stage and each arrives on the stage's full barrier with its own
+    // bytes (count 2).  FP8 scales go with their own K or V boxes.
+    const int isv = warp;
+    const int nrb = kKvTile / a.box_rows;
+    const int nbox = nrb * Cfg::kNsub;  // boxes of K (or V) per tile, one per lane
+    const int sub = lane % Cfg::kNsub;  // 128-byte column slice
+    const int rb = lane / Cfg::kNsub;   // page piece
+    int it = 0, ucount = 0;             // tiles and chunks issued
+    bool aborted = false;
+
+    // The chunk's page ids, one per lane, with one coalesced load when the
+    // chunk spans at most 32 pages: each tile then finds its pages by a
+    // shuffle instead of a dependent global load.
+    struct Pages {
+      int64_t pg0;
+      int npg, mypage;
+    };
+    auto chunk_pages = [&](const UnitInfo& r, int t_begin, int t_end) -> Pages {
+      Pages pp{0, 0, 0};
+      if (a.block_table && r.ntiles > 0 && t_begin < t_end) {
+        const int64_t jlo = (int64_t)(r.tile0 + t_begin) * kKvTile;
+        const int64_t jhi = min((int64_t)(r.tile0 + t_end) * kKvTile, (int64_t)r.kv_len);
+        pp.pg0 = page_index(a, jlo);
+        pp.npg = (int)(page_index(a, jhi - 1) - pp.pg0 + 1);
+        if (pp.npg <= 32 && lane < pp.npg)
+          pp.mypage = a.block_table[(int64_t)r.b * a.max_blocks + pp.pg0 + lane];
+      }
+      return pp;
+    };
+    // One tile's K (isv 0) or V (isv 1) boxes and their FP8 scales, and for
+    // K the explicit-mask slices of the unit's query rows; false after a
+    // time-out (nothing issued).
+    auto issue_tile = [&](const UnitInfo& r, int t, const Pages& pp, int i_first,
+                          int i_last) -> bool {
+      const int s = it % S;
+      const uint32_t par = ((it / S) & 1) ^ 1;
+      const int64_t j0 = (int64_t)(r.tile0 + t) * kKvTile;
+      const int64_t jb = j0 + (int64_t)rb * a.box_rows;
+      const bool mine = lane < nbox && jb < r.kv_len;
+      int64_t blk, jp = 0;
+      if (a.block_table) {
+        const int64_t pj = mine ? page_index(a, jb) : 0;
+        jp = jb - pj * a.block_size;
+        if (pp.npg > 0 && pp.npg <= 32) {
+          blk = __shfl_sync(0xffffffffu, pp.mypage, (int)(pj - pp.pg0));
+        } else {
+          blk = mine ? (int64_t)a.block_table[(int64_t)r.b * a.max_blocks + pj] : 0;
+        }
+      } else {
+        blk = 0;
+      }
+      const int64_t prow = mine ? pool_row(a, r.b, r.hk, blk, jb, jp) : 0;
+      constexpr int NT = D / 64;
+      // FP8: the scales of one head inside a page are contiguous rows of NT
+      // floats, so each (K or V, page piece) is one bulk copy next to its
+      // TMA box.  Pieces are even-length at even rows (block sizes are
+      // multiples of 32; contiguous caches have an even length), hence
+      // 16-byte aligned.
+      // (a page id outside the pool reads zeros through TMA; its FP8
+      // scales, which come by plain bulk copy, are not read at all)
+      int64_t srow = 0;
+      int srows = a.box_rows;
+      bool scale_ok = false;
+      if constexpr (FP8) {
+        scale_ok = mine && (!a.block_table || (blk >= 0 && blk < a.num_blocks));
+        if (scale_ok) srow = scale_row_in(a, r.b, r.hk, blk, jb, jp);
+        if (!a.block_table) srows = (int)min((int64_t)a.box_rows, (int64_t)a.S_kv - jb);
+      }
+      int nvalid = 0;
+      for (int q = 0; q < nrb; ++q)
+        if (j0 + (int64_t)q * a.box_rows < r.kv_len) ++nvalid;
+      uint32_t scale_bytes = 0;
+      if constexpr (FP8)
+        scale_bytes = __reduce_add_sync(0xffffffffu, scale_ok ? (uint32_t)(srows * NT * 4) : 0u);
+      // explicit mask (K warp): the tile's slice of each of the unit's query
+      // rows, 16-byte pieces up to kv_len (row strides are multiples of 16
+      // that cover the KV capacity, so the copy stays inside the row)
+      const bool with_mask = MR && a.mask && isv == 0;
+      const int mrow_bytes =
+          with_mask ? (int)min((int64_t)kKvTile, ((int64_t)r.kv_len - j0 + 15) & ~(int64_t)15) : 0;
+      const int nmrows = with_mask ? i_last - i_first + 1 : 0;
+      wait_or_abort(&empty[s], par, a.err, misc);
+      if (*reinterpret_cast<volatile int*>(misc)) return false;  // issue nothing after a time-out
+      uint8_t* st = smem + s * Cfg::kStageBytes;
+      if (lane == 0) {
+        uint32_t bytes = (uint32_t)(nvalid * Cfg::kNsub * a.box_rows * 128);
+        if constexpr (FP8) bytes += scale_bytes;
+        bytes += (uint32_t)(nmrows * mrow_bytes);
+        mbar_arrive_expect_tx(&full[s], bytes);
+      }
+      __syncwarp();
+      if (with_mask && lane < nmrows)
+        bulk_load(st + Cfg::kOffMask + lane * kKvTile,
+                  a.mask + (int64_t)r.b * a.mask_bstride + (int64_t)(i_first + lane) * a.mask_rstride +
+                      j0,
+                  (uint32_t)mrow_bytes, &full[s]);
+      if (mine) {
+        uint8_t* dst = st + isv * Cfg::kTileBytes + sub * (kKvTile * 128) + rb * a.box_rows * 128;
+        const int col = (a.kv_layout == 1 ? 0 : r.hk * D) + (FP8 ? 0 : sub * 64);
+        tma_load_2d(dst, isv ? &tv : &tk, &full[s], col, (int)prow);
+        if constexpr (FP8) {
+          float* sdst = reinterpret_cast<float*>(st + 2 * Cfg::kTileBytes) + isv * (kKvTile * NT) +
+                        rb * a.box_rows * NT;
+          if (scale_ok)
+            bulk_load(sdst, (isv ? a.v_scale : a.k_scale) + srow * NT, (uint32_t)(srows * NT * 4),
+                      &full[s]);
+        }
+      }
+      ++it;
+      return true;
+    };
+    auto drain = [&]() {
+      // a wait timed out: issue nothing more, give the copies already in
+      // flight a bounded time to land, and leave (the error word is set)
+      for (int k = max(0, it - S); k < it; ++k) mbar_wait(&full[k % S], (k / S) & 1, a.err);
+    };
+
+    if (isv == 1) {
+      // ---- V warp: the chunks warp 0 posts, in order, until the empty one ----
+      while (true) {
+        const int qs = ucount & 1;
+        wait_or_abort(&vpost[qs], (ucount >> 1) & 1, a.err, misc);
+        const bool done = msg[qs].done != 0;
+        const UnitInfo r = msg[qs].r;
+        const int t_begin = msg[qs].t_begin, t_end = msg[qs].t_end;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qempty[qs]);  // the message is read
+        ++ucount;
+        if (done || *reinterpret_cast<volatile int*>(misc)) break;
+        const Pages pp = chunk_pages(r, t_begin, t_end);
+        for (int t = t_begin; r.ntiles > 0 && t < t_end; ++t)
+          if (!issue_tile(r, t, pp, 0, 0)) {
+            aborted = true;
+            break;
+          }
+        if (aborted) break;
+      }
+      if (aborted || *reinterpret_cast<volatile int*>(misc)) drain();
+      return;
+    }
+
+    // ---- K warp ----
     // A plan of these arguments carries the scheduler's mark, B and CTA
     // count, and no prefill plan has been written over the workspace since;
     // without one (execute on a workspace never planned, or planned for the
@@ -607,14 +757,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t C = plan_ok ? a.sched[0] : 1, c2 = plan_ok ? a.sched[1] : 1;
     const int64_t N = plan_ok ? a.sched[2] : 0;
     const int UPB = a.KVN * a.HG;
-    int it = 0, ucount = 0;  // tiles and chunks issued
     // CTA c starts with queue entry c (no claim on the way to the first
     // loads); the entries after the first gridDim.x are claimed with the
     // counter, each claim issued one chunk ahead and read only after the
     // chunk's tiles are queued, so its latency hides
     int64_t g = plan_ok ? (int64_t)blockIdx.x : N;
     int4 ent = g < N ? ent0 : make_int4(0, 0, 0, 0);
-    bool aborted = false;
     while (g < N) {
       // claim the next chunk now; its result and queue entry are read once
       // the first tile of this chunk is queued, so neither latency is exposed
@@ -660,6 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m.t_begin = t_begin;
           m.t_end = t_end;
           m.done = 0;
+          mbar_arrive(&vpost[qs]);  // the V warp may read the message
           mbar_arrive_expect_tx(&qfull[qs], (uint32_t)(r.ncols * D * 2));
         }
         __syncwarp();
@@ -674,101 +823,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++ucount;
       }
-      // lane roles for the boxes of a tile: K or V, 128-byte column slice,
-      // page piece
-      const int nrb = kKvTile / a.box_rows;
-      const int nbox = nrb * Cfg::kNsub * 2;  // <= 32: one box per lane
-      const int isv = lane & 1;
-      const int sub = (lane >> 1) % Cfg::kNsub;
-      const int rb = (lane >> 1) / Cfg::kNsub;
-      // The chunk's page ids, one per lane, with one coalesced load when the
-      // chunk spans at most 32 pages: each tile then finds its pages by a
-      // shuffle instead of a dependent global load.
-      int64_t pg0 = 0;
-      int npg = 0, mypage = 0;
-      if (a.block_table && r.ntiles > 0 && t_begin < t_end) {
-        const int64_t jlo = (int64_t)(r.tile0 + t_begin) * kKvTile;
-        const int64_t jhi = min((int64_t)(r.tile0 + t_end) * kKvTile, (int64_t)r.kv_len);
-        pg0 = page_index(a, jlo);
-        npg = (int)(page_index(a, jhi - 1) - pg0 + 1);
-        if (npg <= 32 && lane < npg)
-          mypage = a.block_table[(int64_t)r.b * a.max_blocks + pg0 + lane];
-      }
-      const bool pages_in_regs = npg > 0 && npg <= 32;
-      for (int t = t_begin; r.ntiles > 0 && t < t_end; ++t, ++it) {
-        const int s = it % S;
-        const uint32_t par = ((it / S) & 1) ^ 1;
-        const int64_t j0 = (int64_t)(r.tile0 + t) * kKvTile;
-        const int64_t jb = j0 + (int64_t)rb * a.box_rows;
-        const bool mine = lane < nbox && jb < r.kv_len;
-        int64_t blk, jp = 0;
-        if (a.block_table) {
-          const int64_t pj = mine ? page_index(a, jb) : 0;
-          jp = jb - pj * a.block_size;
-          if (pages_in_regs) {
-            blk = __shfl_sync(0xffffffffu, mypage, (int)(pj - pg0));
-          } else {
-            blk = mine ? (int64_t)a.block_table[(int64_t)r.b * a.max_blocks + pj] : 0;
-          }
-        } else {
-          blk = 0;
-        }
-        const int64_t prow = mine ? pool_row(a, r.b, r.hk, blk, jb, jp) : 0;
-        constexpr int NT = D / 64;
-        // FP8: the scales of one head inside a page are contiguous rows of NT
-        // floats, so each (K or V, page piece) is one bulk copy next to its
-        // TMA box.  Pieces are even-length at even rows (block sizes are
-        // multiples of 32; contiguous caches have an even length), hence
-        // 16-byte aligned.
-        // (a page id outside the pool reads zeros through TMA; its FP8
-        // scales, which come by plain bulk copy, are not read at all)
-        int64_t srow = 0;
-        int srows = a.box_rows;
-        bool scale_ok = false;
-        if constexpr (FP8) {
-          scale_ok = mine && (!a.block_table || (blk >= 0 && blk < a.num_blocks));
-          if (scale_ok) srow = scale_row_in(a, r.b, r.hk, blk, jb, jp);
-          if (!a.block_table) srows = (int)min((int64_t)a.box_rows, (int64_t)a.S_kv - jb);
-        }
-        int nvalid = 0;
-        for (int q = 0; q < nrb; ++q)
-          if (j0 + (int64_t)q * a.box_rows < r.kv_len) ++nvalid;
-        uint32_t scale_bytes = 0;
-        if constexpr (FP8)
-          scale_bytes = __reduce_add_sync(0xffffffffu, scale_ok ? (uint32_t)(srows * NT * 4) : 0u);
-        // explicit mask: the tile's slice of each of the unit's query rows,
-        // 16-byte pieces up to kv_len (row strides are multiples of 16 that
-        // cover the KV capacity, so the copy stays inside the row)
-        const int mrow_bytes = (MR && a.mask)
-                                   ? (int)min((int64_t)kKvTile, ((int64_t)r.kv_len - j0 + 15) & ~(int64_t)15)
-                                   : 0;
-        const int nmrows = (MR && a.mask) ? i_last - i_first + 1 : 0;
-        wait_or_abort(&empty[s], par, a.err, misc);
-        if (*reinterpret_cast<volatile int*>(misc)) break;  // issue nothing after a time-out
-        uint8_t* st = smem + s * Cfg::kStageBytes;
-        if (lane == 0) {
-          uint32_t bytes = (uint32_t)(2 * nvalid * Cfg::kNsub * a.box_rows * 128);
-          if constexpr (FP8) bytes += scale_bytes;
-          bytes += (uint32_t)(nmrows * mrow_bytes);
-          mbar_arrive_expect_tx(&full[s], bytes);
-        }
-        __syncwarp();
-        if (MR && lane < nmrows)
-          bulk_load(st + Cfg::kOffMask + lane * kKvTile,
-                    a.mask + (int64_t)r.b * a.mask_bstride +
-                        (int64_t)(i_first + lane) * a.mask_rstride + j0,
-                    (uint32_t)mrow_bytes, &full[s]);
-        if (mine) {
-          uint8_t* dst = st + isv * Cfg::kTileBytes + sub * (kKvTile * 128) + rb * a.box_rows * 128;
-          const int col = (a.kv_layout == 1 ? 0 : r.hk * D) + (FP8 ? 0 : sub * 64);
-          tma_load_2d(dst, isv ? &tv : &tk, &full[s], col, (int)prow);
-          if constexpr (FP8) {
-            float* sdst = reinterpret_cast<float*>(st + 2 * Cfg::kTileBytes) +
-                          isv * (kKvTile * NT) + rb * a.box_rows * NT;
-            if (scale_ok)
-              bulk_load(sdst, (isv ? a.v_scale : a.k_scale) + srow * NT,
-                        (uint32_t)(srows * NT * 4), &full[s]);
-          }
+      const Pages pp = chunk_pages(r, t_begin, t_end);
+      for (int t = t_begin; r.ntiles > 0 && t < t_end; ++t) {
+        if (!issue_tile(r, t, pp, i_first, i_last)) {
+          aborted = true;
+          break;
         }
         if (!fetched) {
           gn = __shfl_sync(0xffffffffu, (int64_t)gn_l, 0);
@@ -776,7 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fetched = true;
         }
       }
-      if (*reinterpret_cast<volatile int*>(misc)) {
+      if (aborted || *reinterpret_cast<volatile int*>(misc)) {
         aborted = true;
         break;
       }
@@ -788,9 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ent = ent_n;
     }
     if (aborted) {
-      // a wait timed out: issue nothing more, give the copies already in
-      // flight a bounded time to land, and leave (the error word is set)
-      for (int k = max(0, it - S); k < it; ++k) mbar_wait(&full[k % S], (k / S) & 1, a.err);
+      drain();
       return;
     }
     pdl_trigger();  // this CTA loads nothing more: the combine kernel may launch
@@ -803,11 +860,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.claim[1] = 0;
       }
     }
-    {  // end of the CTA's work: an empty message
+    {  // end of the CTA's work: an empty message, for the consumers and the V warp
       const int qs = ucount & 1;
       wait_or_abort(&qempty[qs], ((ucount >> 1) & 1) ^ 1, a.err, misc);
       if (lane == 0) {
         msg[qs].done = 1;
+        mbar_arrive(&vpost[qs]);
         mbar_arrive(&qfull[qs]);
       }
     }

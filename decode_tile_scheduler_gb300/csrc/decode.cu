@@ -552,6 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tv) {
   using Cfg = DecodeCfg<D, FP8>;
   constexpr int S = Cfg::kStages;
+  constexpr int kProdWarps = FP8 ? 4 : 2;  // producer warps (a whole warpgroup is reserved)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -559,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + S;
   uint64_t* qfull = empty + S;
   uint64_t* qempty = qfull + 2;
-  uint64_t* vpost = qempty + 2;  // [2] chunk message posted, for the V warp
+  uint64_t* vpost = qempty + 2;  // [2] chunk message posted, for producer warps 1-3
   int* misc = reinterpret_cast<int*>(smem + Cfg::kOffMisc);
   UnitMsg* msg = reinterpret_cast<UnitMsg*>(smem + Cfg::kOffMsg);
   float* red = reinterpret_cast<float*>(smem + Cfg::kOffRed);
@@ -574,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], kConsumers + 1);  // the consumers and the V warp
+      mbar_init(&qempty[s], kConsumers + kProdWarps - 1);  // consumers and producer warps 1..
       mbar_init(&vpost[s], 1);
     }
     misc[0] = 0;  // abort flag
@@ -589,17 +590,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs) : "memory");
-    if (warp >= 2) return;  // the producer warpgroup's other warps have no work
     // ======================= producers =======================
-    // Warp 0 streams the K boxes (and the explicit-mask slices) of every
-    // tile and does the chunk bookkeeping: claims, chunk messages, query
-    // vectors.  Warp 1 streams the V boxes: it follows the messages warp 0
-    // posts (vpost) and walks the same tiles, so the per-tile page lookups,
-    // address arithmetic and copy issue are split between two warps (the FP8
-    // decode's single producer was busy most of its time).  Both wait for a
-    // free stage and each arrives on the stage's full barrier with its own
-    // bytes (count 2).  FP8 scales go with their own K or V boxes.
-    const int isv = warp;
+    // Even warps stream the K boxes (and the explicit-mask slices), odd warps
+    // the V boxes; with an FP8 cache, warps 0/1 take the even tiles and 2/3
+    // the odd ones, without it warps 0/1 take every tile.  Warp 0 also does
+    // the chunk bookkeeping (claims, chunk messages, query vectors); the
+    // others follow the messages it posts (vpost), walking the same tiles.
+    // So the per-tile page lookups, address arithmetic and copy issue are
+    // spread over several warps (the FP8 decode's single producer was busy
+    // most of its time: 155.8 -> 150.2 us with two warps, 141.8 us with four;
+    // the bf16 decodes gain nothing from more than two).  The two warps of a
+    // tile wait for its stage and each arrives on the stage's full barrier
+    // with its own bytes (count 2).  FP8 scales go with their K or V boxes.
+    if (warp >= kProdWarps) return;
+    const int isv = warp & 1;
+    const int parity_of_mine = warp >> 1;  // (four warps) the tiles (it & 1) == this one
     const int nrb = kKvTile / a.box_rows;
     const int nbox = nrb * Cfg::kNsub;  // boxes of K (or V) per tile, one per lane
     const int sub = lane % Cfg::kNsub;  // 128-byte column slice
@@ -631,6 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // time-out (nothing issued).
     auto issue_tile = [&](const UnitInfo& r, int t, const Pages& pp, int i_first,
                           int i_last) -> bool {
+      if (kProdWarps == 4 && (it & 1) != parity_of_mine) {  // the other warp of this kind has it
+        ++it;
+        return true;
+      }
       const int s = it % S;
       const uint32_t par = ((it / S) & 1) ^ 1;
       const int64_t j0 = (int64_t)(r.tile0 + t) * kKvTile;
@@ -714,8 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = max(0, it - S); k < it; ++k) mbar_wait(&full[k % S], (k / S) & 1, a.err);
     };
 
-    if (isv == 1) {
-      // ---- V warp: the chunks warp 0 posts, in order, until the empty one ----
+    if (warp != 0) {
+      // ---- warps 1..: the chunks warp 0 posts, in order, until the empty one ----
       while (true) {
         const int qs = ucount & 1;
         wait_or_abort(&vpost[qs], (ucount >> 1) & 1, a.err, misc);
@@ -727,8 +736,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++ucount;
         if (done || *reinterpret_cast<volatile int*>(misc)) break;
         const Pages pp = chunk_pages(r, t_begin, t_end);
+        // the unit's query rows (their explicit-mask slices go with K)
+        const int i_first = MR ? r.c0 / a.G : 0;
+        const int i_last = MR ? (r.c0 + max(r.ncols, 1) - 1) / a.G : 0;
         for (int t = t_begin; r.ntiles > 0 && t < t_end; ++t)
-          if (!issue_tile(r, t, pp, 0, 0)) {
+          if (!issue_tile(r, t, pp, i_first, i_last)) {
             aborted = true;
             break;
           }
@@ -808,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m.t_begin = t_begin;
           m.t_end = t_end;
           m.done = 0;
-          mbar_arrive(&vpost[qs]);  // the V warp may read the message
+          mbar_arrive(&vpost[qs]);  // producer warps 1-3 may read the message
           mbar_arrive_expect_tx(&qfull[qs], (uint32_t)(r.ncols * D * 2));
         }
         __syncwarp();
@@ -860,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.claim[1] = 0;
       }
     }
-    {  // end of the CTA's work: an empty message, for the consumers and the V warp
+    {  // end of the CTA's work: an empty message, for the consumers and warps 1-3
       const int qs = ucount & 1;
       wait_or_abort(&qempty[qs], ((ucount >> 1) & 1) ^ 1, a.err, misc);
       if (lane == 0) {

@@ -18,10 +18,10 @@
 // The scores of row (t, h) are then S' * 2^-sh * 2^EK, and the output O' * 2^EV.
 //
 // Three passes, all HBM-bound and short next to the prefill: the largest
-// scale of each (batch, KV head) (an atomic maximum over the float bits,
-// positive floats ordering like their bit patterns), the K/V conversion (one
-// thread per 16 elements of a (batch, row, head) vector), the Q conversion
-// (one warp per (token, head)).  Rows at or past a batch's KV length are not
+// scale of each (batch, KV head) (warp maxima, then atomic maxima over the
+// float bits, positive floats ordering like their bit patterns), the K/V
+// conversion (one thread per 16 elements of a (batch, row, head) vector), the
+// Q conversion (eight (token, head) rows per warp pass).  Rows at or past a batch's KV length are not
 // touched (the prefill kernel masks their scores and zeroes their V rows).
 #include <algorithm>
 
@@ -50,25 +50,37 @@ __device__ __forceinline__ bool locate(const DequantArgs& a, int b, int j, int h
   return true;
 }
 
-// Largest K and V scale of every (batch, KV head) over its visible rows.
+// Largest K and V scale of every (batch, KV head) over its visible rows: a
+// warp per (batch, KV head, run of 1024 rows), a warp maximum, then one
+// atomic per warp (an atomic per row serialised on the few addresses).
+constexpr int kScaleRun = 1024;
 __global__ void __launch_bounds__(256) scale_max_kernel(const DequantArgs a) {
   const int NT = a.D / 64;
-  const int64_t total = (int64_t)a.B * a.cap * a.KVN;
-  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
-       t += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t bj = t / a.KVN;
-    const int hk = (int)(t - bj * a.KVN);
-    const int b = (int)(bj / a.cap), j = (int)(bj - (int64_t)b * a.cap);
+  const int lane = threadIdx.x & 31;
+  const int nrun = (a.cap + kScaleRun - 1) / kScaleRun;
+  const int64_t items = (int64_t)a.B * a.KVN * nrun;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < items; w += nw) {
+    const int64_t pair = w / nrun;
+    const int run = (int)(w - pair * nrun);
+    const int b = (int)(pair / a.KVN), hk = (int)(pair - (int64_t)b * a.KVN);
     const int kv_len = a.seqused_kv ? a.seqused_kv[b] : a.cap;
-    int64_t off, srow;
-    if (j >= kv_len || !locate(a, b, j, hk, 0, &off, &srow)) continue;
+    const int j_end = min(kv_len, (run + 1) * kScaleRun);
     uint32_t mk = 0, mv = 0;
-    for (int k = 0; k < NT; ++k) {
-      mk = max(mk, __float_as_uint(fabsf(__ldg(a.k_scale + srow * NT + k))));
-      mv = max(mv, __float_as_uint(fabsf(__ldg(a.v_scale + srow * NT + k))));
+    for (int j = run * kScaleRun + lane; j < j_end; j += 32) {
+      int64_t off, srow;
+      if (!locate(a, b, j, hk, 0, &off, &srow)) continue;
+      for (int k = 0; k < NT; ++k) {
+        mk = max(mk, __float_as_uint(fabsf(__ldg(a.k_scale + srow * NT + k))));
+        mv = max(mv, __float_as_uint(fabsf(__ldg(a.v_scale + srow * NT + k))));
+      }
     }
-    atomicMax(a.smax + ((int64_t)b * a.KVN + hk) * 2, mk);
-    atomicMax(a.smax + ((int64_t)b * a.KVN + hk) * 2 + 1, mv);
+    mk = __reduce_max_sync(0xffffffffu, mk);
+    mv = __reduce_max_sync(0xffffffffu, mv);
+    if (lane == 0 && (mk | mv)) {
+      atomicMax(a.smax + pair * 2, mk);
+      atomicMax(a.smax + pair * 2 + 1, mv);
+    }
   }
 }
 
@@ -125,28 +137,51 @@ __global__ void __launch_bounds__(256) kv_dequant_kernel(const DequantArgs a) {
   }
 }
 
-// Q to fp16: one warp per (token, head), D/32 elements per lane (D = 128).
+// Q to fp16 (D = 128): a (token, head) row is 256 bytes, 16 lanes x 16
+// bytes, so a warp holds two rows per load and takes eight per pass with four
+// independent loads per lane in flight (one row per warp left each warp
+// waiting on a single load).  Row shift: sh = 15 - (the exponent of the row's
+// largest element), kept in [-100, 100], a maximum over the row's 16 lanes.
+constexpr int kQRowsPerPass = 8;
 __global__ void __launch_bounds__(256) q_convert_kernel(const DequantArgs a) {
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
   const int64_t total = a.q_rows * a.QN;
-  const int per = a.D / 32;  // 4
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < total;
-       r += (int64_t)gridDim.x * (blockDim.x >> 5)) {
-    const int64_t tok = r / a.QN;
-    const int h = (int)(r - tok * a.QN);
-    const uint16_t* src = a.q + tok * a.q_stride + (int64_t)h * a.D + lane * per;
-    const uint2 v = *reinterpret_cast<const uint2*>(src);  // 4 bf16
-    uint32_t e = max(max((v.x >> 7) & 0xffu, (v.x >> 23) & 0xffu),
-                     max((v.y >> 7) & 0xffu, (v.y >> 23) & 0xffu));
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kQRowsPerPass;
+       base < total; base += nw * kQRowsPerPass) {
+    uint4 v[kQRowsPerPass / 2];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) e = max(e, __shfl_xor_sync(0xffffffffu, e, o));
-    const int sh = min(max(142 - (int)e, -100), 100);  // 15 - (e - 127)
-    const float up = __int_as_float((127 + sh) << 23);
-    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-    *reinterpret_cast<uint2*>(a.q_out + r * a.D + lane * per) =
-        make_uint2(pack_f16(lo.x * up, lo.y * up), pack_f16(hi.x * up, hi.y * up));
-    if (lane == 0) a.qfac[r] = __int_as_float((127 - sh) << 23);
+    for (int u = 0; u < kQRowsPerPass / 2; ++u) {
+      const int64_t r = base + 2 * u + half;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < total) {
+        const int64_t tok = r / a.QN;
+        const int h = (int)(r - tok * a.QN);
+        v[u] = __ldg(reinterpret_cast<const uint4*>(a.q + tok * a.q_stride + (int64_t)h * a.D) + l16);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kQRowsPerPass / 2; ++u) {
+      const int64_t r = base + 2 * u + half;
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t e = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) e = max(e, max((w[k] >> 7) & 0xffu, (w[k] >> 23) & 0xffu));
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) e = max(e, __shfl_xor_sync(0xffffffffu, e, o));
+      const int sh = min(max(142 - (int)e, -100), 100);  // 15 - (e - 127)
+      const float up = __int_as_float((127 + sh) << 23);
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        o[k] = pack_f16(f.x * up, f.y * up);
+      }
+      if (r < total) {
+        reinterpret_cast<uint4*>(a.q_out + r * a.D)[l16] = make_uint4(o[0], o[1], o[2], o[3]);
+        if (l16 == 0) a.qfac[r] = __int_as_float((127 - sh) << 23);
+      }
+    }
   }
 }
 
@@ -157,7 +192,8 @@ cudaError_t launch_kv_dequant(const DequantArgs& a, int num_sms, cudaStream_t s)
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)a.B * a.cap * a.KVN;
   if (rows > 0) {
-    const int g1 = (int)std::min<int64_t>((rows + 255) / 256, (int64_t)num_sms * 8);
+    const int64_t warps = (int64_t)a.B * a.KVN * ((a.cap + kScaleRun - 1) / kScaleRun);
+    const int g1 = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)num_sms * 8);
     scale_max_kernel<<<g1, 256, 0, s>>>(a);
     const int64_t total = rows * (a.D / 16);
     const int g2 = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms * 8);
@@ -165,7 +201,8 @@ cudaError_t launch_kv_dequant(const DequantArgs& a, int num_sms, cudaStream_t s)
   }
   const int64_t qr = a.q_rows * a.QN;
   if (qr > 0) {
-    const int g3 = (int)std::min<int64_t>((qr + 7) / 8, (int64_t)num_sms * 16);
+    const int64_t warps = (qr + kQRowsPerPass - 1) / kQRowsPerPass;
+    const int g3 = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)num_sms * 8);
     q_convert_kernel<<<g3, 256, 0, s>>>(a);
   }
   return cudaGetLastError();

@@ -15,11 +15,12 @@ constexpr int kDecodeMaxRows = 16; // query rows per sequence the decode kernel 
 
 // Columns per decode unit: the (query row, query head) pairs of a KV head,
 // S rows x G heads of them, in mma N columns of 8.  A unit takes 16 columns
-// only for one query row with more than 8 heads per KV head; with several
-// query rows the per-column bounds of 16 columns cost registers the
-// consumers then spill, and two 8-column units, whose chunks sit next to each
-// other in the queue and share their K/V tiles through L2, ran faster (a
-// 4-row GQA-4 decode: 92.2 against 100.4 us per execute).
+// only for one query row with more than 8 heads per KV head; several query
+// rows go in 8-column units, two per KV head for 16 columns, whose chunks sit
+// next to each other in the queue and share their K/V tiles through L2 (a
+// 4-row GQA-4 decode: 92.2 against 100.4 us per execute while 16-column
+// units spilled registers; the same, 88.0 against 88.2 us, once the
+// consumers had 208 registers).
 inline int decode_group_heads(int rows, int cols) { return (rows == 1 && cols > 8) ? 16 : 8; }
 
 // Everything the decode schedule and the decode kernel read.
@@ -59,7 +60,8 @@ struct DecodeArgs {
   int64_t* sched;              // [8 + 3(B+1) + B]: C, c2, chunks, big chunks, split
                                // batches, mark, B, CTAs; the partial-slot prefix Q, the
                                // queue prefixes R1, R2; the split batches (then -1)
-  int4* queue;                 // [max_chunks] (b, chunk << 16 | unit of b, kv_len, qrow)
+  int4* queue;                 // [max_chunks] (b | q_len << 16, chunk << 16 | unit of b,
+                               // kv_len, first token row)
   int* claim;                  // [2]: next queue entry, CTAs done with the queue
   int64_t* prefill_mark;       // header word of a prefill plan: a decode plan clears it
   float* partials;             // [max_chunks][GH][D + 2]: acc, then m and l

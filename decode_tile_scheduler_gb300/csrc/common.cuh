@@ -139,43 +139,10 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// 1-D bulk copy shared -> global in the calling thread's bulk group; both
-// addresses 16-byte aligned, bytes % 16 == 0.  The shared-memory source must
-// have been made visible to the async proxy (fence_proxy_async_smem).
-__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-               "r"(smem_u32(src)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// wait until the committed bulk stores have read their shared-memory sources
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// wait until the committed bulk stores are complete
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// Ampere-style asynchronous copy of 8 bytes (for small gathers).
-__device__ __forceinline__ void cp_async_8(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
-}
-// Arrive on `bar` once this thread's earlier cp.async copies have landed; the
-// arrival counts against the barrier's expected count.
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Named barrier over `nthreads` threads (a multiple of 32).
 // Bounded barrier wait; after the first time-out in the CTA every later wait
 // returns at once, so a broken pipeline ends the kernel instead of hanging it.
 __device__ __forceinline__ void wait_or_abort(uint64_t* bar, uint32_t parity, int* err,
@@ -184,6 +151,7 @@ __device__ __forceinline__ void wait_or_abort(uint64_t* bar, uint32_t parity, in
   if (!mbar_wait(bar, parity, err)) *reinterpret_cast<volatile int*>(misc) = 1;
 }
 
+// Named barrier over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -11,9 +11,8 @@
 // form the N columns of every mma.sync, so each KV page is read once for all
 // of them (the GQA heads and, for multi-token decode, the query rows too; the
 // units of one KV head sit next to each other in the queue and share its
-// pages through L2).  Only the groups
-// holding columns of the sequence's own rows are scheduled ("active").  A
-// unit owns the KV tiles (128 positions) its rows see together; every column
+// pages through L2).  Only the groups holding columns of the sequence's own
+// rows are scheduled ("active").  A unit owns the KV tiles (128 positions) its rows see together; every column
 // is masked with its own row's bounds.
 //
 // Scheduler (decode_schedule_kernel): cost(u) = visible tiles (>= 1; 0 when
@@ -23,20 +22,20 @@
 // n1 = max(0, floor(c/C) - 1) big chunks of C tiles followed by the remaining
 // r = c - n1*C tiles (C <= r < 2C unless c < C) in small chunks of
 // c2 = ceil(C/k) tiles, k = 3 (6 with an FP8 cache, whose long units gain
-// from smaller last pieces).  The claim queue lists every big chunk (batch-major,
-// then chunk, then active unit of the batch) before every small chunk (same
-// order), so the work left at the end is always small pieces.  CTAs claim
+// from smaller last pieces).  The claim queue lists every big chunk
+// (batch-major, then chunk, then active unit of the batch) before every small
+// chunk (same order), so the work left at the end is always small pieces.  CTAs claim
 // chunks from the queue with one atomic each: an SM that streams faster
 // simply takes more chunks.  A unit cut into several chunks is split-KV: each
 // chunk writes its (m, l, acc) partial to the slot of its (unit, chunk
 // index), and a combine kernel chained behind the decode kernel folds them in
 // chunk order (deterministic, whichever CTAs ran them).
 //
-// Decode kernel: one producer warp streams K and V pages with TMA (page rows
-// from block_table) into a ring of shared-memory stages, with the rows of an
-// explicit mask when there is one; eight consumer warps (two warpgroups, with
-// the registers the producer's warpgroup gives up) each take 16 rows of
-// every tile.  The products are computed transposed ("swap AB"):
+// Decode kernel: producer warps (two, four with an FP8 cache) stream K and V
+// pages with TMA (page rows from block_table) into a ring of shared-memory
+// stages, with the rows of an explicit mask when there is one; eight consumer
+// warps (two warpgroups, with the registers the producers' warpgroup gives
+// up) each take 16 rows of every tile.  The products are computed transposed ("swap AB"):
 // S^T = K Q^T with the KV rows as the mma M dimension and the query columns
 // as N, then O^T += V^T P^T, where P^T comes out of the S^T accumulators with
 // movmatrix.  Softmax is online, in the exp2 domain, per column.  FP8 E4M3

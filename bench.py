@@ -91,6 +91,16 @@ class ClockSampler:
                 stdout=self.tmp, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # Wait (at most 5 s) for the first sample: nvidia-smi's start-up then
+        # lies before the timed region, which its samples cover from the
+        # first step on, and does not compete with the host's launches
+        # inside it.
+        t_end = time.time() + 5.0
+        while time.time() < t_end and self.proc.poll() is None:
+            if os.path.getsize(self.tmp.name) > 0:
+                break
+            time.sleep(0.01)
 
     def stop(self):
         if self.proc is None:

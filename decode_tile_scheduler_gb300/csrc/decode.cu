@@ -376,7 +376,9 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
     C = (T - 1 <= 0xffffffffLL && per <= 0xffffffffLL)
             ? (int64_t)((uint32_t)(T - 1) / (uint32_t)per) + 1
             : (T - 1) / per + 1;
-  const int64_t c2 = (C + a.small_div - 1) / a.small_div;
+  const int64_t c2 = C <= 0x7fffffffLL
+                         ? (int64_t)((uint32_t)(C + a.small_div - 1) / (uint32_t)a.small_div)
+                         : (C + a.small_div - 1) / a.small_div;
 
   // per batch: big and small chunks of its active units and whether it is
   // split -> three exclusive scans (all chunks before b = big + small before b)
@@ -610,6 +612,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rb = lane / Cfg::kNsub;   // page piece
     int it = 0, ucount = 0;             // tiles and chunks issued
     bool aborted = false;
+    // K/V pages are read once, unless two units of a KV head share them
+    // (several column groups, neighbours in the queue): those keep the
+    // default policy so that the second unit finds them in L2
+    const bool once = a.HG == 1;
+    const uint64_t pol = l2_evict_first_policy();
 
     // The chunk's page ids, one per lane, with one coalesced load when the
     // chunk spans at most 32 pages: each tile then finds its pages by a
@@ -704,7 +711,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (mine) {
         uint8_t* dst = st + isv * Cfg::kTileBytes + sub * (kKvTile * 128) + rb * a.box_rows * 128;
         const int col = (a.kv_layout == 1 ? 0 : r.hk * D) + (FP8 ? 0 : sub * 64);
-        tma_load_2d(dst, isv ? &tv : &tk, &full[s], col, (int)prow);
+        if (once)
+          tma_load_2d_hint(dst, isv ? &tv : &tk, &full[s], col, (int)prow, pol);
+        else
+          tma_load_2d(dst, isv ? &tv : &tk, &full[s], col, (int)prow);
         if constexpr (FP8) {
           float* sdst = reinterpret_cast<float*>(st + 2 * Cfg::kTileBytes) + isv * (kKvTile * NT) +
                         rb * a.box_rows * NT;
@@ -759,14 +769,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (the CTA's first queue entry is loaded beside the plan's header, not
     // after it: entry blockIdx.x lies inside the queue buffer, which holds
     // max_chunks >= gridDim.x entries, and is used only if the plan checks out)
+    // (all header words are loaded before any is tested: one round trip)
     const int4 ent0 = a.queue[blockIdx.x];
-    const bool plan_ok = a.sched[5] == kDecodePlanMark && a.sched[6] == a.B &&
-                         a.sched[7] == a.num_ctas && a.sched[0] >= 1 && a.sched[1] >= 1 &&
-                         a.sched[2] >= 0 && a.sched[2] <= a.max_chunks &&
-                         *a.prefill_mark != kPrefillPlanMark;
+    int64_t hd[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) hd[k] = a.sched[k];
+    const int64_t pmark = *a.prefill_mark;
+    const bool plan_ok = (hd[5] == kDecodePlanMark) & (hd[6] == a.B) & (hd[7] == a.num_ctas) &
+                         (hd[0] >= 1) & (hd[1] >= 1) & (hd[2] >= 0) & (hd[2] <= a.max_chunks) &
+                         (pmark != kPrefillPlanMark);
     if (!plan_ok && lane == 0 && blockIdx.x == 0) atomicExch(a.err, 2);
-    const int64_t C = plan_ok ? a.sched[0] : 1, c2 = plan_ok ? a.sched[1] : 1;
-    const int64_t N = plan_ok ? a.sched[2] : 0;
+    const int64_t C = plan_ok ? hd[0] : 1, c2 = plan_ok ? hd[1] : 1;
+    const int64_t N = plan_ok ? hd[2] : 0;
     const int UPB = a.KVN * a.HG;
     // CTA c starts with queue entry c (no claim on the way to the first
     // loads); the entries after the first gridDim.x are claimed with the
@@ -806,6 +820,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (without MR every column is row 0)
       const int i_first = MR ? r.c0 / a.G : 0;
       const int i_last = MR ? (r.c0 + max(r.ncols, 1) - 1) / a.G : 0;
+      // the chunk's page ids first: their load overlaps the message and the
+      // query copies below
+      const Pages pp = chunk_pages(r, t_begin, t_end);
       if (ent_ok && ci < gm.nch) {  // chunk description + the columns' query vectors
         const int qs = ucount & 1;
         wait_or_abort(&qempty[qs], ((ucount >> 1) & 1) ^ 1, a.err, misc);
@@ -834,7 +851,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++ucount;
       }
-      const Pages pp = chunk_pages(r, t_begin, t_end);
       for (int t = t_begin; r.ntiles > 0 && t < t_end; ++t) {
         if (!issue_tile(r, t, pp, i_first, i_last)) {
           aborted = true;
@@ -1512,16 +1528,24 @@ struct CombineItem {
   const float* base;   // the column's partial in the unit's first chunk
 };
 
+// Columns of a unit the combine visits: at most S_max * G of its GH are ever
+// used (one query row with fewer than 8 heads per KV head fills half of an
+// 8-column unit), so the items skip the rest and no combine block idles.
+__host__ __device__ __forceinline__ int combine_cols(const DecodeArgs& a) {
+  return a.GH < a.S_max * a.G ? a.GH : a.S_max * a.G;
+}
+
 // Item pr of the combine: (split batch m, active unit index act of it, column
-// col of the unit), pr = (m * UPB + act) * GH + col; false for indices past
-// the batch's active units or the unit's columns.
+// col of the unit), pr = (m * UPB + act) * GC + col with GC = combine_cols;
+// false for indices past the batch's active units or the unit's columns.
 __device__ __forceinline__ bool combine_item(const DecodeArgs& a, int64_t pr, int D,
                                              CombineItem* it) {
   const int64_t UPB = (int64_t)a.KVN * a.HG;
   const int64_t* Q = a.sched + kSchedHeader;
   const int64_t* SB = Q + 3 * ((int64_t)a.B + 1);
-  const int col = (int)(pr % a.GH);
-  const int64_t ma = pr / a.GH;
+  const int GC = combine_cols(a);
+  const int col = (int)(pr % GC);
+  const int64_t ma = pr / GC;
   const int act = (int)(ma % UPB);
   const int64_t b64 = SB[ma / UPB];
   // an entry outside the batches or the partial slots (a plan of other
@@ -1539,7 +1563,7 @@ __device__ __forceinline__ bool combine_item(const DecodeArgs& a, int64_t pr, in
   if (act >= A) return false;  // past the batch's active units
   const int hk = act / ha, hg = act % ha;
   const int c = hg * a.GH + col;
-  if (c >= qlen * a.G || col >= a.GH) return false;  // past the unit's columns
+  if (c >= qlen * a.G || col >= GC) return false;  // past the unit's columns
   if (Q[b] < 0 || Q[b + 1] < Q[b] + A || Q[b + 1] > a.max_chunks || (Q[b + 1] - Q[b]) % A) {
     atomicExch(a.err, 2);
     return false;
@@ -1564,7 +1588,7 @@ __global__ void __launch_bounds__(256, 4) decode_combine_flat(const DecodeArgs a
   // The schedule was complete before the decode kernel started its work, so
   // the first item is located while the decode kernel still runs; only the
   // partials need its completion.
-  const int64_t items = a.sched[4] * a.KVN * a.HG * a.GH;
+  const int64_t items = a.sched[4] * a.KVN * a.HG * combine_cols(a);
   const int d = 2 * (threadIdx.x % TPP);
   int64_t pr = (int64_t)blockIdx.x * PPB + threadIdx.x / TPP;
   CombineItem it;
@@ -1590,7 +1614,7 @@ __global__ void __launch_bounds__(256, 4) decode_combine_grouped(const DecodeArg
     return;  // no plan of these arguments: the decode kernel has reported it
   constexpr int TPP = D / 2, NGRP = 256 / TPP;
   __shared__ float4 st[NGRP][TPP];
-  const int64_t items = a.sched[4] * a.KVN * a.HG * a.GH;
+  const int64_t items = a.sched[4] * a.KVN * a.HG * combine_cols(a);
   const int grp = threadIdx.x / TPP, t = threadIdx.x % TPP, d = 2 * t;
   int64_t pr = blockIdx.x;
   CombineItem it;
@@ -1678,7 +1702,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUte
   // The plan bounds the chunks by n*W + 6*U, so a unit has about n*W/U + 6;
   // with more than 16 an item gets a whole CTA.  The choice depends on shapes
   // only, so results stay deterministic.
-  const int64_t items = a.num_units * a.GH;  // bound: every batch split
+  const int64_t items = a.num_units * combine_cols(a);  // bound: every batch split
   const int64_t est = (int64_t)a.num_ctas * a.chunks_per_cta / a.num_units + 2 * a.small_div;
   if (est > 16) {
     const int grid = (int)std::min<int64_t>(items, (int64_t)a.num_ctas * 8);

@@ -156,6 +156,30 @@ def test_schedule_many_batches_bit_exact_and_parity():
     check_close(out, lse, ro, rl, "2100 batches")
 
 
+@pytest.mark.parametrize("B", [33, 64, 65, 300])
+def test_schedule_batch_counts_bit_exact(B):
+    # batch counts across warp boundaries of the scheduler's block-wide scans
+    # and well inside its shared-memory path: the plan is the oracle's
+    g = np.random.default_rng(100 + B)
+    kv = [int(x) for x in g.integers(0, 3000, B)]
+    p = fi.make_fia(B=B, QN=16, KVN=2, D=128, q_lens=[1] * B, kv_lens=kv, block_size=64,
+                    seed=7 + B, device=dev)
+    c, out, lse = _run(p, 152)
+    lay = c.plan_layout()
+    ws = c.ws.cpu()
+    per_cta = (lay.max_chunks - 6 * lay.num_units) // 152
+    nsched = 8 + 3 * (B + 1) + B
+    sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
+    rs, rq = oracle.decode_schedule(p.to("cpu"), 152, per_cta)
+    assert np.array_equal(sched, rs)
+    N = int(sched[2])
+    queue = ws[lay.queue_off: lay.queue_off + 16 * N].view(torch.int32).numpy().reshape(N, 4)
+    assert np.array_equal(queue, rq)
+    if B == 65:
+        ro, rl = _ref(p)
+        check_close(out, lse, ro, rl, "65 batches")
+
+
 def test_execute_reuses_one_plan():
     # fia_plan once, fia_execute three times: the claim queue and the split
     # counters re-arm themselves, so every execute gives the same result

@@ -16,6 +16,7 @@
 
 #include "../../include/fia.h"
 #include "common.cuh"
+#include "internal.h"
 
 namespace fia {
 
@@ -104,6 +105,7 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 extern "C" size_t fia_sizeof_combine_params(void) { return sizeof(fia_combine_params); }
 
 extern "C" fia_status fia_lse_combine(const fia_combine_params* p, void* stream) {
+  fia::NvtxRange range("fia_lse_combine");
   using namespace fia;
   if (!p) return FIA_ERR_NULL_ARG;
   for (int i = 0; i < 8; ++i)

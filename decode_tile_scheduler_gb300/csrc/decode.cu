@@ -663,6 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         blk = 0;
       }
+      if (a.debug && mine && a.block_table && (blk < 0 || blk >= a.num_blocks))
+        atomicExch(a.err, 3);  // (read as zeros by the TMA box all the same)
       const int64_t prow = mine ? pool_row(a, r.b, r.hk, blk, jb, jp) : 0;
       constexpr int NT = D / 64;
       // FP8: the scales of one head inside a page are contiguous rows of NT

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -196,6 +197,15 @@ struct DecodePlan {
 // are long, so a smaller last piece shortens the wait for the slowest CTA at
 // the end of the queue (bf16 decode units are short, and more pieces there
 // cost more partial writes than they save).
+// FIA_DEBUG=1 (or any value not starting with 0) in the environment, read on
+// every call: the kernels also report a block_table entry that names a page
+// outside the pool for a position they read, with 3 in the error word (they
+// read such rows as zeros, or leave them out, either way).
+int debug_checks() {
+  const char* e = getenv("FIA_DEBUG");
+  return e && e[0] && e[0] != '0';
+}
+
 int decode_small_div(const fia_params* p) { return p->kv_dtype == FIA_KV_FP8_E4M3 ? 6 : 3; }
 
 // Decode workspace: [0, 256) error word (offset 0) and the claim counters
@@ -280,6 +290,7 @@ DecodeArgs decode_args(const fia_params* p, const DecodePlan& pl, void* ws) {
   a.prefill_mark = reinterpret_cast<int64_t*>(w + kWsPrefillMarkOff);
   a.partials = reinterpret_cast<float*>(w + pl.off_part);
   a.err = reinterpret_cast<int*>(w);
+  a.debug = debug_checks();
   return a;
 }
 
@@ -413,6 +424,8 @@ DequantArgs dequant_args(const fia_params* p, const PrefillPlan& pl, void* ws) {
   d.q = static_cast<const uint16_t*>(p->q);
   d.q_out = reinterpret_cast<uint16_t*>(w + pl.off_q);
   d.qfac = reinterpret_cast<float*>(w + pl.off_qfac);
+  d.err = reinterpret_cast<int*>(w);
+  d.debug = debug_checks();
   return d;
 }
 
@@ -449,6 +462,8 @@ PrefillArgs prefill_args(const fia_params* p, const PrefillPlan& pl, void* ws) {
   a.sinks = p->sinks;
   a.num_ctas = pl.n;
   a.max_cost = pl.max_cost;
+  a.num_blocks = p->block_table ? p->num_blocks : 0;
+  a.debug = debug_checks();
   char* w = static_cast<char*>(ws);
   a.err = reinterpret_cast<int*>(w);
   a.claim = reinterpret_cast<int*>(w + 16);
@@ -585,6 +600,7 @@ SparseArgs sparse_args(const sparse_attn_params* p, const SparsePlan& pl, void* 
   fast_divisor(a.cmp_block_size, &a.cmp_magic, &a.cmp_shift);
   a.num_ctas = pl.n;
   if (ws) a.err = reinterpret_cast<int*>(ws);
+  a.debug = debug_checks();
   return a;
 }
 
@@ -660,6 +676,7 @@ fia_status fia_get_workspace_size(const fia_params* p, size_t* bytes) {
 }
 
 fia_status fia_plan(const fia_params* p, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange range("fia_plan");
   fia_plan_layout l;
   fia_status st = fia_get_plan_layout(p, &l);
   if (st != FIA_OK) return st;
@@ -682,6 +699,7 @@ fia_status fia_plan(const fia_params* p, void* ws, size_t ws_bytes, void* stream
 }
 
 fia_status fia_execute(const fia_params* p, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange range("fia_execute");
   fia_plan_layout l;
   fia_status st = fia_get_plan_layout(p, &l);
   if (st != FIA_OK) return st;
@@ -724,6 +742,7 @@ fia_status fia_execute(const fia_params* p, void* ws, size_t ws_bytes, void* str
 }
 
 fia_status fia_run(const fia_params* p, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange range("fia_run");
   fia_status st = fia_plan(p, ws, ws_bytes, stream);
   if (st != FIA_OK) return st;
   return fia_execute(p, ws, ws_bytes, stream);
@@ -731,6 +750,7 @@ fia_status fia_run(const fia_params* p, void* ws, size_t ws_bytes, void* stream)
 
 fia_status sparse_attn_metadata(const sparse_attn_params* p, int32_t* metadata,
                                 size_t* workspace_bytes, void* stream) {
+  NvtxRange range("sparse_attn_metadata");
   if (!p || !metadata || !workspace_bytes) return FIA_ERR_NULL_ARG;
   if (!aligned16(metadata)) return FIA_ERR_BAD_SHAPE;  // the documented alignment
   SparsePlan pl;
@@ -746,6 +766,7 @@ fia_status sparse_attn_metadata(const sparse_attn_params* p, int32_t* metadata,
 
 fia_status sparse_attn_run(const sparse_attn_params* p, const int32_t* metadata, void* ws,
                            size_t ws_bytes, void* stream) {
+  NvtxRange range("sparse_attn_run");
   if (!p || !metadata) return FIA_ERR_NULL_ARG;
   if (!aligned16(metadata)) return FIA_ERR_BAD_SHAPE;
   SparsePlan pl;
@@ -755,7 +776,9 @@ fia_status sparse_attn_run(const sparse_attn_params* p, const int32_t* metadata,
   SparseArgs a = sparse_args(p, pl, ws);
   if (a.rows == 0) return FIA_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // (the kernel clears the status word itself once the metadata checks out)
+  // (the kernel clears the status word itself once the metadata checks out,
+  // except with FIA_DEBUG, where the host does it first)
+  if (a.debug && cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return FIA_ERR_CUDA;
   return launch_sparse(a, metadata, s) == cudaSuccess ? FIA_OK : FIA_ERR_CUDA;
 }
 

@@ -4,9 +4,21 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 namespace fia {
+
+// An NVTX range over one C-ABI call (plan, execute, run, the sparse calls,
+// the combine, the workspace-free decode): a profiler or tracer sees each
+// call with the kernels it launched.  nvtx3 is header-only and finds its
+// tool at run time; with none attached a range costs a few nanoseconds.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr int kKvTile = 128;   // KV positions per tile (one split granule)
 constexpr int kQTile = 128;    // query rows per prefill tile
@@ -66,6 +78,7 @@ struct DecodeArgs {
   int64_t* prefill_mark;       // header word of a prefill plan: a decode plan clears it
   float* partials;             // [max_chunks][GH][D + 2]: acc, then m and l
   int* err;
+  int debug;                   // FIA_DEBUG: report page ids outside the pool (error word 3)
 };
 
 // Target number of big chunks per persistent CTA in the decode schedule.
@@ -116,6 +129,8 @@ struct PrefillArgs {
   int* claim;             // [2]: next unit to claim, CTAs done claiming
   int* err;
   int64_t max_units;      // bound on the plan's unit count (the unit list's length)
+  int64_t num_blocks;     // pages in the pool (paged caches)
+  int debug;              // FIA_DEBUG: report page ids outside the pool (error word 3)
 };
 
 struct SparseArgs {
@@ -146,6 +161,7 @@ struct SparseArgs {
   int ori_shift, cmp_shift;
   int* err;
   int num_ctas;
+  int debug;             // FIA_DEBUG: report page ids outside the pool (error word 3)
 };
 
 // host launchers (return cudaSuccess or the launch error)
@@ -181,6 +197,8 @@ struct DequantArgs {
   const uint16_t* q;           // bf16
   uint16_t* q_out;             // fp16 [q_rows, QN, D]
   float* qfac;                 // [q_rows * QN]
+  int* err;                    // the workspace's error word
+  int debug;                   // FIA_DEBUG: report page ids outside the pool (error word 3)
 };
 cudaError_t launch_kv_dequant(const DequantArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -38,7 +38,10 @@ __device__ __forceinline__ bool locate(const DequantArgs& a, int b, int j, int h
                                        int64_t* code_off, int64_t* scale_row) {
   if (a.block_table) {
     const int64_t blk = a.block_table[(int64_t)b * a.max_blocks + j / a.block_size];
-    if (blk < 0 || blk >= a.num_blocks) return false;
+    if (blk < 0 || blk >= a.num_blocks) {
+      if (a.debug) atomicExch(a.err, 3);
+      return false;
+    }
     const int jp = j % a.block_size;
     *code_off = a.kv_layout == 1 ? ((blk * a.KVN + hk) * a.block_size + jp) * a.D + d0
                                  : ((blk * a.block_size + jp) * a.KVN + hk) * a.D + d0;

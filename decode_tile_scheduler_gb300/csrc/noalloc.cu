@@ -20,6 +20,7 @@
 // The array's first int32 is the run's error word; the caller gets a copy of
 // it through `status`, since it has no address of its own for the array.
 #include "../../include/fia.h"
+#include "internal.h"
 
 namespace {
 
@@ -40,6 +41,7 @@ fia_status scratch_address(void** out) {
 }  // namespace
 
 extern "C" fia_status fia_decode_run_noalloc(const fia_params* p, int32_t* status, void* stream) {
+  fia::NvtxRange range("fia_decode_run_noalloc");
   fia_plan_layout lay;
   fia_status st = fia_get_plan_layout(p, &lay);
   if (st != FIA_OK) return st;

@@ -151,6 +151,8 @@ __device__ __forceinline__ int tile_span(const PrefillArgs& a, int64_t q_len, in
 __device__ __forceinline__ int64_t kv_phys_row(const PrefillArgs& a, int b, int hk, int64_t j) {
   if (a.block_table) {
     const int64_t blk = a.block_table[(int64_t)b * a.max_blocks + j / a.block_size];
+    if (a.debug && (blk < 0 || blk >= a.num_blocks))
+      atomicExch(a.err, 3);  // (read as zeros by the TMA box all the same)
     if (a.kv_layout == 1) return (blk * a.KVN + hk) * a.block_size + j % a.block_size;
     return blk * a.block_size + j % a.block_size;
   }

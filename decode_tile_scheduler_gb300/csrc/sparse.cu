@@ -238,8 +238,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     return;
   }
   // the status word of this call: cleared here (a time-out, the only other
-  // error, is reported seconds later), set to 2 above on a metadata mismatch
-  if (c == 0 && tid == 0) *reinterpret_cast<volatile int*>(a.err) = 0;
+  // error, is reported seconds later), set to 2 above on a metadata mismatch;
+  // with FIA_DEBUG the host clears it before the launch instead, since a
+  // page reported by another CTA may come before this CTA's clear
+  if (c == 0 && tid == 0 && !a.debug) *reinterpret_cast<volatile int*>(a.err) = 0;
   const int64_t k_begin = md[kMdBase + c], k_end = md[kMdBase + c + 1];
   if (k_begin >= k_end) return;
   const int row_src_bytes = packed ? kPackedRow : D * 2;
@@ -293,6 +295,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
             ok[h2] = blk >= 0 && blk < a.cmp_num_blocks;
             off[h2] = (blk * a.cmp_block_size + (cr - pg * a.cmp_block_size)) * row_src_bytes;
           }
+          if (a.debug && !ok[h2] && pw == 0) atomicExch(a.err, 3);
         }
       }
       const uint64_t valid = (uint64_t)__ballot_sync(0xffffffffu, ok[0]) |

@@ -203,8 +203,12 @@ fia_status fia_plan(const fia_params *p, void *workspace, size_t workspace_bytes
  * is set; nothing ran), when a plan entry lies outside these arguments (that
  * entry ran as empty, its loads and stores kept inside their buffers), or
  * when a decode plan held more chunks than the workspace bound (not
- * reachable for validated inputs).  Reading it needs a device-to-host copy
- * after the stream has reached the call. */
+ * reachable for validated inputs); 3, only with FIA_DEBUG set in the
+ * environment (any value not starting with '0', read on every call), when a
+ * block_table entry for a key position the kernels read names a page outside
+ * [0, num_blocks) -- those rows are read as zeros either way; the word then
+ * stays 3 until the next plan.  Reading it needs a device-to-host copy after
+ * the stream has reached the call. */
 fia_status fia_execute(const fia_params *p, void *workspace, size_t workspace_bytes,
                        void *stream);
 
@@ -430,7 +434,10 @@ fia_status sparse_attn_metadata(const sparse_attn_params *p, int32_t *metadata,
  * kernel checks its header (magic, CTA count, rows, B, N1, topk, heads per
  * item, items, kv_dtype) on the device; on a mismatch it writes nothing to out/lse and sets the int32
  * status word at workspace offset 0 to FIA_ERR_BAD_SHAPE (0 otherwise; read
- * it with any device-to-host copy after the call). */
+ * it with any device-to-host copy after the call).  With FIA_DEBUG set in the
+ * environment the word is also 3 when a window or listed compressed row's
+ * page lies outside its block table or pool (such rows are left out either
+ * way). */
 fia_status sparse_attn_run(const sparse_attn_params *p, const int32_t *metadata,
                            void *workspace, size_t workspace_bytes, void *stream);
 

@@ -9,7 +9,7 @@
 // compressed rows (the listed top-k indices for CSA, scanned up to the first
 // -1 and kept when causally visible; every visible compressed row for HCA).
 // A work item is (query row, group of 8 query heads); the metadata kernel
-// hands each CTA a contiguous run of items of balanced weight.  In a CTA four
+// hands each CTA a contiguous run of items of balanced weight.  In a CTA eight
 // producer warps gather K~ in 64-row chunks (index -> block table -> pool
 // row, one bulk copy per row) into a ring of shared-memory stages, and eight
 // consumer warps run the whole item: S^T = K~ Q^T and O^T += V~^T P^T with
@@ -30,8 +30,14 @@ namespace {
 constexpr int kChunk = 64;                // K~ rows per stage
 constexpr int kHeads = 8;                 // query heads per work item (mma N)
 constexpr int kSCons = 8;                 // consumer warps
-constexpr int kSProd = 4;                 // producer warps (warp w gathers the rows r of a chunk with r mod kSProd = w)
+constexpr int kSProd = 8;                 // producer warps (warp w gathers the rows r of a chunk with r mod kSProd = w)
 constexpr int kSThreads = 32 * (kSProd + kSCons);
+// four warpgroups: the producers' two give registers to the consumers' two
+// (setmaxnreg), 256 * kSProdRegs + 256 * kSConsRegs = 512 * 128, the launch's
+constexpr int kSProdRegs = 72;
+constexpr int kSConsRegs = 184;
+static_assert(32 * kSProd * kSProdRegs + 32 * kSCons * kSConsRegs <= kSThreads * 128,
+              "register split");
 constexpr int kMdBase = 16;               // metadata: CTA begins from this entry
 constexpr int32_t kMdMagic = 0x46534D32;
 constexpr int kMaxK2 = 2048;              // longest index list (validated on the host)
@@ -247,6 +253,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int row_src_bytes = packed ? kPackedRow : D * 2;
 
   if (warp < kSProd) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSProdRegs) : "memory");
     // ======================= producers =======================
     // Every producer warp walks the same items and chunks; warp pw issues
     // the copies of the rows r = pw mod kSProd of each chunk (the copies of one
@@ -422,6 +429,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
 
   // ======================= consumers =======================
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSConsRegs) : "memory");
   // Warp cw: QK rows 16 rg .. 16 rg + 15 of each chunk over half hf of D
   // (the two halves' partial scores are summed through shared memory), and
   // P V for output columns cw * D/8 .. + D/8 over all 64 rows.

@@ -42,6 +42,7 @@ constexpr int kMdBase = 16;               // metadata: CTA begins from this entr
 constexpr int32_t kMdMagic = 0x46534D32;
 constexpr int kMaxK2 = 2048;              // longest index list (validated on the host)
 constexpr int kPackedRow = 640;           // bytes of a packed FP8 row (D = 512)
+constexpr float kSparseRescale = 8.0f;    // the reference moves past this (log2 units)
 
 struct SparseRow {
   int b;
@@ -468,7 +469,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
     float acc[MTW][4];
 #pragma unroll
     for (int i = 0; i < MTW; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m[2] = {-INFINITY, -INFINITY};  // running maxima of heads 2q, 2q+1 (exp2 domain)
+    // reference of heads 2q, 2q+1 (exp2 domain): no score seen lies more
+    // than 2^8 above it (-inf until a head's first visible row)
+    float m[2] = {-INFINITY, -INFINITY};
     float l[2] = {0.f, 0.f};              // this lane's share of the sums (row-group warps)
     bool stop = false;
     while (true) {
@@ -558,39 +561,66 @@ __global__ void __launch_bounds__(kSThreads, 1)
           x[e] = ((e < 2) ? v0 : v1) ? sfull * a.scale_log2 : -INFINITY;
         }
       }
-      // ---- chunk maxima per head: 16 rows here, then the 4 row groups ----
+      // ---- chunk maxima per head over this warp's 16 rows ----
+      float lm[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         float mx = fmaxf(x[e], x[2 + e]);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        lm[e] = mx;
         if (hf == 0 && g == 0) mxs[rg * kHeads + 2 * q4 + e] = mx;
       }
-      named_bar_sync(1, nthr);
-      float corr[2], mu[2];
+      // ---- P = exp2(x - m) against the shared reference m, which moves
+      // only when a chunk's maximum passes it by more than 2^8 (or with a
+      // head's first visible rows).  The row-group warps publish P^T against
+      // the current m, and the barrier that publishes it also ORs every
+      // warp's vote that m must move; only then (rarely, after an item's
+      // first chunk) do all warps take the chunk maxima, move m and write P^T
+      // again behind one more barrier. ----
+      bool must_move = false;
+      float pv[2][2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float mc = mxs[2 * q4 + e];
-#pragma unroll
-        for (int r2 = 1; r2 < 4; ++r2) mc = fmaxf(mc, mxs[r2 * kHeads + 2 * q4 + e]);
-        const float mn = fmaxf(m[e], mc);
-        mu[e] = mn == -INFINITY ? 0.f : mn;
-        corr[e] = mn == m[e] ? 1.f : (m[e] == -INFINITY ? 0.f : fast_exp2(m[e] - mu[e]));
-        m[e] = mn;
+        must_move |= lm[e] > m[e] + kSparseRescale || (m[e] == -INFINITY && lm[e] != -INFINITY);
+        const float mu = m[e] == -INFINITY ? 0.f : m[e];
+        pv[e][0] = fast_exp2(x[e] - mu);
+        pv[e][1] = fast_exp2(x[2 + e] - mu);
       }
-      // ---- P = exp2(x - m): the row-group warps keep the sums and publish P^T ----
-      if (hf == 0) {
+      auto put_p = [&]() {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float p0 = fast_exp2(x[e] - mu[e]), p1 = fast_exp2(x[2 + e] - mu[e]);
-          l[e] = l[e] * corr[e] + p0 + p1;
-          const __nv_bfloat16 b0 = __float2bfloat16_rn(p0), b1 = __float2bfloat16_rn(p1);
+          const __nv_bfloat16 b0 = __float2bfloat16_rn(pv[e][0]), b1 = __float2bfloat16_rn(pv[e][1]);
           pt[(2 * q4 + e) * Cfg::kPtStride + r0] = *reinterpret_cast<const uint16_t*>(&b0);
           pt[(2 * q4 + e) * Cfg::kPtStride + r1] = *reinterpret_cast<const uint16_t*>(&b1);
         }
+      };
+      if (hf == 0) put_p();
+      float corr[2] = {1.f, 1.f};
+      if (!named_bar_or(1, nthr, must_move)) {
+        if (hf == 0) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) l[e] += pv[e][0] + pv[e][1];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float mc = mxs[2 * q4 + e];
+#pragma unroll
+          for (int r2 = 1; r2 < 4; ++r2) mc = fmaxf(mc, mxs[r2 * kHeads + 2 * q4 + e]);
+          if (mc > m[e] + kSparseRescale || (m[e] == -INFINITY && mc != -INFINITY)) {
+            corr[e] = m[e] == -INFINITY ? 0.f : fast_exp2(m[e] - mc);
+            m[e] = mc;
+          }
+          const float mu = m[e] == -INFINITY ? 0.f : m[e];
+          pv[e][0] = fast_exp2(x[e] - mu);
+          pv[e][1] = fast_exp2(x[2 + e] - mu);
+          if (hf == 0) l[e] = l[e] * corr[e] + pv[e][0] + pv[e][1];
+        }
+        if (hf == 0) put_p();
+        named_bar_sync(1, nthr);
       }
-      named_bar_sync(1, nthr);
       // ---- O^T += V~^T P^T over this warp's columns ----
       if (__any_sync(0xffffffffu, corr[0] != 1.f || corr[1] != 1.f)) {
 #pragma unroll

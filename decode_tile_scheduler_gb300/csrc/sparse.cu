@@ -100,12 +100,30 @@ __device__ __forceinline__ float e8m0_value(uint32_t e) {
 // #{k : P_k < floor(c T / n)}.  Row u's items start at A = G * pre(u) and
 // item g of the row at A + g * cost(u), so a threshold t in (A, A + G cost]
 // gives the begin u * G + ceil((t - A) / cost).
+// Prefetches the 128-byte lines of [p, p + bytes) into L2, at most `cap`
+// per thread of the block (a hint: nothing is read).
+__device__ __forceinline__ void prefetch_lines(const void* p, int64_t bytes, int cap) {
+  if (p == nullptr || bytes <= 0) return;
+  const char* c = static_cast<const char*>(p);
+  const int64_t lines = (bytes + 127) >> 7;  // (lines - 1) * 128 < bytes
+  int64_t k = threadIdx.x;
+  for (int i = 0; i < cap && k < lines; ++i, k += blockDim.x)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(c + (k << 7)));
+}
+
 __global__ void __launch_bounds__(1024) sparse_metadata_kernel(const SparseArgs a, int32_t* md) {
   __shared__ int64_t warp_sums[32];
   __shared__ int64_t carry;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nthr = blockDim.x;
   const int64_t n = a.num_ctas, G = a.hgs;
   pdl_trigger();  // the attention kernel may set up while the metadata is built
+  // The attention kernel's first dependent loads after its wait are the
+  // block tables and the index lists: this block pulls them into L2 while it
+  // works (at most 512 KB of each).
+  prefetch_lines(a.ori_block_table, (int64_t)a.B * a.ori_max_blocks * 4, 4);
+  if (a.mode != 0)
+    prefetch_lines(a.cmp_block_table, (int64_t)a.B * a.cmp_max_blocks * 4, 4);
+  if (a.mode == 1) prefetch_lines(a.cmp_sparse_indices, a.rows * a.K2 * 4, 4);
   for (int k = tid; k < 1024; k += nthr) md[k] = 0;
   // pass 1: total weight
   if (tid == 0) carry = 0;

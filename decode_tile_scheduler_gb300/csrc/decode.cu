@@ -334,6 +334,15 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const DecodeArgs 
   __shared__ int sR[2][kSchedSmemBatches + 1];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   pdl_trigger();  // the decode kernel may set up while the plan is built
+  // The decode kernel's first dependent load after its wait is a chunk's
+  // page ids: this block pulls the block table into L2 while it works (four
+  // 128-byte lines per thread at most, 512 KB).
+  if (a.block_table) {
+    const char* bt = reinterpret_cast<const char*>(a.block_table);
+    const int64_t lines = ((int64_t)a.B * a.max_blocks * 4 + 127) >> 7;
+    for (int64_t k = tid, i = 0; i < 4 && k < lines; ++i, k += blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(bt + (k << 7)));
+  }
   const int B = a.B;
   const bool small = B <= kSchedSmemBatches;
   const int HG = a.HG;

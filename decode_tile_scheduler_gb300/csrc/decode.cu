@@ -21,8 +21,9 @@
 // per CTA, at least one tile), and a unit of cost c is cut into
 // n1 = max(0, floor(c/C) - 1) big chunks of C tiles followed by the remaining
 // r = c - n1*C tiles (C <= r < 2C unless c < C) in small chunks of
-// c2 = ceil(C/k) tiles, k = 3 (6 with an FP8 cache, whose long units gain
-// from smaller last pieces).  The claim queue lists every big chunk
+// c2 = ceil(C/k) tiles, k = 2 for a bf16 cache and one query row, else 1
+// (every chunk has a fixed cost, and the FP8 and multi-row units' tiles
+// cost the consumers more).  The claim queue lists every big chunk
 // (batch-major, then chunk, then active unit of the batch) before every small
 // chunk (same order), so the work left at the end is always small pieces.  CTAs claim
 // chunks from the queue with one atomic each: an SM that streams faster

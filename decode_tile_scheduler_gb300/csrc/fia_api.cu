@@ -193,10 +193,6 @@ struct DecodePlan {
   int64_t off_sched, off_queue, off_part, total;
 };
 
-// Small chunks are ceil(C/3) tiles, ceil(C/6) with an FP8 cache: its units
-// are long, so a smaller last piece shortens the wait for the slowest CTA at
-// the end of the queue (bf16 decode units are short, and more pieces there
-// cost more partial writes than they save).
 // FIA_DEBUG=1 (or any value not starting with 0) in the environment, read on
 // every call: the kernels also report a block_table entry that names a page
 // outside the pool for a position they read, with 3 in the error word (they
@@ -206,7 +202,17 @@ int debug_checks() {
   return e && e[0] && e[0] != '0';
 }
 
-int decode_small_div(const fia_params* p) { return p->kv_dtype == FIA_KV_FP8_E4M3 ? 6 : 3; }
+// The divisor k of the decode schedule's small chunks (c2 = ceil(C / k)): 2
+// for a bf16 cache with one query row per sequence, else 1 (the rest of a
+// unit then goes in at most two chunks of at most C tiles).  Every chunk
+// costs a fixed set-up and merge, and the FP8 and multi-row units do more
+// consumer work per tile, so for them fewer, longer chunks pay more than a
+// finer tail (fia_execute: long FP8 decode 139.4 -> 134.8 us, FP8 with 16
+// heads per KV head 120.3 -> 113.6 us, 4-row decode 88.2 -> 79.9 us against
+// k = 6, 6 and 3; one-row bf16 decode 58.9 -> 58.6 us against k = 3).
+int decode_small_div(const fia_params* p) {
+  return (p->kv_dtype == FIA_KV_FP8_E4M3 || p->max_seqlen_q > 1) ? 1 : 2;
+}
 
 // Decode workspace: [0, 256) error word (offset 0) and the claim counters
 // (offset 16); the schedule; the claim queue; the partial slots.  A unit of

@@ -66,7 +66,7 @@ struct DecodeArgs {
   // plan (workspace)
   int num_ctas;
   int chunks_per_cta;          // W: the chunk size aims at W chunks per CTA
-  int small_div;               // small chunks of ceil(C / small_div) tiles (3; 6 for FP8)
+  int small_div;               // small chunks of ceil(C / small_div) tiles (2; 1 for FP8 or rows > 1)
   int64_t num_units;           // B * KVN * HG
   int64_t max_chunks;          // partial slots: a bound on the number of chunks
   int64_t* sched;              // [8 + 3(B+1) + B]: C, c2, chunks, big chunks, split

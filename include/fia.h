@@ -306,9 +306,10 @@ fia_status fia_selftest_bounded_wait(int32_t *status, uint64_t limit_ns, void *s
  * index a).  Cost of an active unit = KV tiles (128 positions) its rows see
  * together, at least 1 (0 when the batch has no query row).  With T the total
  * cost, n CTAs and W = 5 chunks per CTA, C = max(1, ceil(T / (n W))) and
- * c2 = ceil(C / k), k = 3 (6 with an FP8 cache).  A unit of cost c gets
- * n1 = max(0, floor(c/C) - 1) chunks of C tiles, then chunks of c2 tiles
- * over the rest (at most 2k), so n W + 2k U bounds the chunks of U units.
+ * c2 = ceil(C / k), k = 2 for a bf16 cache and S = 1, else 1.  A unit of
+ * cost c gets n1 = max(0, floor(c/C) - 1) chunks of C tiles, then chunks of
+ * c2 tiles over the rest (at most 2k), so n W + 2k U bounds the chunks of U
+ * units.
  * sched holds int64 {C, c2, chunks N, big chunks F, split batches M, plan
  * mark 0x4649414445434F44, B, CTA count}, then Q[B+1] (partial slots before
  * batch b: chunk i of active unit a of batch b owns slot Q[b] + i*A(b) + a),

@@ -333,7 +333,7 @@ def decode_schedule(p, num_ctas: int, per_cta: int):
     G = p.QN // p.KVN
     HG = -(-(max(1, p.S_q) * G) // 8)  # units per KV head, at most (8-column groups)
     U = p.B * p.KVN * HG
-    k = 3 if p.kv_dtype == 0 else 6  # small chunks of ceil(C/k) tiles
+    k = 2 if (p.kv_dtype == 0 and max(p.S_q, 1) == 1) else 1  # small chunks: ceil(C/k) tiles
     cap = num_ctas * per_cta + 2 * k * U
     sched = np.zeros(8 + 3 * (p.B + 1) + p.B, dtype=np.int64)
     queue = np.zeros((max(cap, 1), 4), dtype=np.int32)

@@ -593,8 +593,8 @@ static int64_t or_tiles(int64_t lo, int64_t hi)
  * else the number of KV tiles its rows can see together (the interval from
  * the first row's lower bound to the last row's upper bound), at least 1.
  * With T the sum of all active units' costs, n CTAs and W chunks per CTA:
- *   C  = max(1, ceil(T / (n*W))),  c2 = ceil(C/k), k = 3 (6 with an FP8
- *   cache);
+ *   C  = max(1, ceil(T / (n*W))),  c2 = ceil(C/k), k = 2 for a bf16 cache
+ *   and one query row (S = 1), else 1;
  *   a unit of cost c has n1 = max(0, floor(c/C) - 1) big chunks of C tiles,
  *   then its remaining c - n1*C tiles in small chunks of c2 tiles (the last
  *   one shorter), n2 of them.
@@ -650,7 +650,7 @@ int64_t oracle_decode_schedule(const oracle_fia_args *a, int32_t num_ctas, int32
     C = or_ceil_div(T, (int64_t)num_ctas * per_cta);
     if (C < 1) C = 1;
     {
-        int64_t k = a->kv_dtype == OR_KV_BF16 ? 3 : 6;
+        int64_t k = (a->kv_dtype == OR_KV_BF16 && S == 1) ? 2 : 1;
         c2 = (C + k - 1) / k;
     }
     for (b = 0; b < B; ++b) {

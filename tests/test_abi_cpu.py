@@ -158,16 +158,16 @@ def test_workspace_too_small_is_reported_before_launch():
 def test_plan_layout_describes_decode_schedule():
     lay = fia.fia_get_plan_layout(_decode_params())
     assert lay.branch == 1 and lay.num_ctas == 152 and lay.num_units == 4 * 2 * 1
-    per_cta = (lay.max_chunks - 6 * lay.num_units) // lay.num_ctas
-    assert per_cta >= 1 and lay.max_chunks == 152 * per_cta + 6 * lay.num_units
+    # bf16 with one query row: small chunks of ceil(C/2) tiles, at most 4 per unit
+    per_cta = (lay.max_chunks - 4 * lay.num_units) // lay.num_ctas
+    assert per_cta >= 1 and lay.max_chunks == 152 * per_cta + 4 * lay.num_units
     assert lay.sched_off >= 256 and lay.queue_off >= lay.sched_off + 8 * (8 + 3 * 5 + 4)
     # partial slots: max_chunks x 8 heads x (D + 2) floats fit in the workspace
     assert lay.total_bytes >= lay.queue_off + 16 * lay.max_chunks + 4 * lay.max_chunks * 8 * 130
-    # an FP8 cache cuts its units' rest into chunks of ceil(C/6) tiles: at
-    # most 12 per unit
+    # an FP8 cache takes its units' rest in chunks of C tiles: at most 2 per unit
     lay8 = fia.fia_get_plan_layout(_decode_params(kv_dtype=fia.KV_FP8_E4M3, k_scale=FAKE,
                                                   v_scale=FAKE, quant_tile=64))
-    assert lay8.max_chunks == 152 * per_cta + 12 * lay8.num_units
+    assert lay8.max_chunks == 152 * per_cta + 2 * lay8.num_units
 
 
 # --------------------------------------------------------------------------

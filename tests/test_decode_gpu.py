@@ -102,7 +102,7 @@ def test_schedule_metadata_bit_exact():
         lay = c.plan_layout()
         ws = c.ws.cpu()
         U = lay.num_units
-        per_cta = (lay.max_chunks - 6 * U) // n
+        per_cta = (lay.max_chunks - 4 * U) // n  # bf16, one row: the bound n*W + 4*U
         nsched = 8 + 3 * (p.B + 1) + p.B
         sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
         rs, rq = oracle.decode_schedule(p.to("cpu"), n, per_cta)
@@ -113,7 +113,7 @@ def test_schedule_metadata_bit_exact():
 
 
 def test_schedule_fp8_bit_exact():
-    # an FP8 cache: small chunks of ceil(C/6) tiles, the bound n*W + 12*U
+    # an FP8 cache: the rest of a unit in chunks of C tiles, the bound n*W + 2*U
     import decode_tile_scheduler_gb300 as fia
     p = fi.make_fia(B=4, QN=32, KVN=4, D=128, q_lens=[1] * 4, kv_lens=[40000, 3, 9000, 129],
                     block_size=128, kv_dtype=fi.KV_FP8_E4M3, seed=31, device=dev)
@@ -121,7 +121,7 @@ def test_schedule_fp8_bit_exact():
         c, out, lse = _run(p, n)
         lay = c.plan_layout()
         ws = c.ws.cpu()
-        per_cta = (lay.max_chunks - 12 * lay.num_units) // n
+        per_cta = (lay.max_chunks - 2 * lay.num_units) // n
         nsched = 8 + 3 * (p.B + 1) + p.B
         sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
         rs, rq = oracle.decode_schedule(p.to("cpu"), n, per_cta)
@@ -144,7 +144,7 @@ def test_schedule_many_batches_bit_exact_and_parity():
     c, out, lse = _run(p, 152)
     lay = c.plan_layout()
     ws = c.ws.cpu()
-    per_cta = (lay.max_chunks - 6 * lay.num_units) // 152
+    per_cta = (lay.max_chunks - 4 * lay.num_units) // 152
     nsched = 8 + 3 * (B + 1) + B
     sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
     rs, rq = oracle.decode_schedule(p.to("cpu"), 152, per_cta)
@@ -167,7 +167,7 @@ def test_schedule_batch_counts_bit_exact(B):
     c, out, lse = _run(p, 152)
     lay = c.plan_layout()
     ws = c.ws.cpu()
-    per_cta = (lay.max_chunks - 6 * lay.num_units) // 152
+    per_cta = (lay.max_chunks - 4 * lay.num_units) // 152
     nsched = 8 + 3 * (B + 1) + B
     sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
     rs, rq = oracle.decode_schedule(p.to("cpu"), 152, per_cta)

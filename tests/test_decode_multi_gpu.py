@@ -145,7 +145,7 @@ def test_multi_row_schedule_bit_exact():
         lay = c.plan_layout()
         ws = c.ws.cpu()
         U = lay.num_units
-        per_cta = (lay.max_chunks - 6 * U) // n
+        per_cta = (lay.max_chunks - 2 * U) // n  # several rows: the bound n*W + 2*U
         nsched = 8 + 3 * (p.B + 1) + p.B
         sched = ws[lay.sched_off: lay.sched_off + 8 * nsched].view(torch.int64).numpy()
         rs, rq = oracle.decode_schedule(p.to("cpu"), n, per_cta)

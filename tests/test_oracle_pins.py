@@ -466,11 +466,11 @@ def test_decode_schedule_chunks_cover_each_unit_once(ctas, per_cta):
     costs = [max(1, -(-k // 128)) for k in kv]          # no mask: every tile, at least 1
     T = UPB * sum(costs)
     C = max(1, -(-T // (ctas * per_cta)))
-    c2 = -(-C // 3)
+    c2 = -(-C // 2)                                      # bf16, one query row: k = 2
     assert list(sched[:2]) == [C, c2] and list(sched[5:8]) == [0x4649414445434F44, p.B, ctas]
     N, F = int(sched[2]), int(sched[3])
     assert N == queue.shape[0] and 0 <= F <= N
-    assert N <= ctas * per_cta + 6 * B * UPB             # the workspace bound
+    assert N <= ctas * per_cta + 4 * B * UPB             # the workspace bound, 2k U
     Q = sched[8:8 + B + 1]
     # batches whose units need a split-KV combine, in order, then -1
     split = [b for b in range(B) if (Q[b + 1] - Q[b]) // UPB > 1]
@@ -501,9 +501,9 @@ def test_decode_schedule_chunks_cover_each_unit_once(ctas, per_cta):
         [(kv[x & 0xFFFF], x & 0xFFFF) for x, _, _, _ in queue.tolist()]
 
 
-def test_decode_schedule_fp8_small_chunks_are_a_sixth():
-    """With an FP8 cache the rest of a unit (between C and 2C tiles) goes in
-    chunks of ceil(C/6) tiles, at most 12 of them."""
+def test_decode_schedule_fp8_rest_in_at_most_two_chunks():
+    """With an FP8 cache (k = 1) the rest of a unit (between C and 2C tiles)
+    goes in chunks of C tiles, at most 2 of them."""
     kv = [30000, 70000, 128, 129 * 128]
     p = fi.make_fia(B=len(kv), QN=16, KVN=2, D=128, q_lens=[1] * len(kv), kv_lens=kv,
                     block_size=128, kv_dtype=fi.KV_FP8_E4M3, seed=4)
@@ -512,9 +512,9 @@ def test_decode_schedule_fp8_small_chunks_are_a_sixth():
         costs = [max(1, -(-k // 128)) for k in kv]
         T = 2 * sum(costs)
         C = max(1, -(-T // (ctas * per)))
-        c2 = -(-C // 6)
+        c2 = C
         assert list(sched[:2]) == [C, c2]
-        assert sched[2] <= ctas * per + 12 * 2 * len(kv)
+        assert sched[2] <= ctas * per + 2 * 2 * len(kv)
         chunks = _unit_chunks(sched, queue, p.B, 2)
         F = int(sched[3])
         for b, c in enumerate(costs):
@@ -523,7 +523,7 @@ def test_decode_schedule_fp8_small_chunks_are_a_sixth():
                 n1 = sum(pos < F for pos, _ in lst)
                 n2 = len(lst) - n1
                 rest = c - n1 * C
-                assert n2 <= 12 and (n2 - 1) * c2 < rest <= n2 * c2
+                assert n2 <= 2 and (n2 - 1) * c2 < rest <= n2 * c2
 
 
 def test_decode_schedule_band_counts_window_tiles_only():
@@ -585,7 +585,7 @@ def test_decode_schedule_multi_row_units(S, G, layout):
                     assert Q[b + 1] - Q[b] == len(idx) * A[b]
             assert Q[b + 1] - Q[b] == 0 or A[b] > 0
         assert len(chunks) == sum(A)
-        assert queue.shape[0] <= ctas * per + 6 * B * UPB
+        assert queue.shape[0] <= ctas * per + 2 * B * UPB  # several rows: k = 1
 
 
 def test_prefill_units_enumerate_every_tile_and_head_pair():

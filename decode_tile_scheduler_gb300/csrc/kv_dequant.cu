@@ -54,9 +54,12 @@ __device__ __forceinline__ bool locate(const DequantArgs& a, int b, int j, int h
 }
 
 // Largest K and V scale of every (batch, KV head) over its visible rows: a
-// warp per (batch, KV head, run of 1024 rows), a warp maximum, then one
-// atomic per warp (an atomic per row serialised on the few addresses).
-constexpr int kScaleRun = 1024;
+// warp per (batch, KV head, run of 128 rows), a warp maximum, then one
+// atomic per warp (an atomic per row serialised on the few addresses).  Each
+// row is a page lookup and then its scales, so a warp's runs are a chain of
+// dependent loads: short runs and many warps keep the chain short (runs of
+// 1024 rows took ~30 us on the varlen FP8 prefill).
+constexpr int kScaleRun = 128;
 __global__ void __launch_bounds__(256) scale_max_kernel(const DequantArgs a) {
   const int NT = a.D / 64;
   const int lane = threadIdx.x & 31;

@@ -202,7 +202,7 @@ cudaError_t launch_kv_dequant(const DequantArgs& a, int num_sms, cudaStream_t s)
     const int g1 = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)num_sms * 8);
     scale_max_kernel<<<g1, 256, 0, s>>>(a);
     const int64_t total = rows * (a.D / 16);
-    const int g2 = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms * 8);
+    const int g2 = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms * 32);
     kv_dequant_kernel<<<g2, 256, 0, s>>>(a);
   }
   const int64_t qr = a.q_rows * a.QN;

@@ -332,10 +332,10 @@ struct PrefillPlan {
   int n, per_pair, npairs, max_cost;
   int64_t U_max;
   int64_t off_seq, off_hist, off_list, total;
-  // FP8 caches: their fp16 copies [B, cap, KVN, D], the fp16 queries
-  // [rows, QN, D] with their factors [rows * QN], the largest scales and the
-  // K/V factors [B * KVN * 2] (all 0 for bf16 caches)
-  int64_t off_kbf, off_vbf, off_q, off_qfac, off_smax, off_kvfac;
+  // FP8 caches: their fp16 copies [B, cap, KVN, D], the largest scales and
+  // the K/V factors [B * KVN * 2] (all 0 for bf16 caches; the queries are
+  // converted to fp16 inside the prefill kernel)
+  int64_t off_kbf, off_vbf, off_smax, off_kvfac;
 };
 
 fia_status prefill_plan(const fia_params* p, PrefillPlan* pl) {
@@ -358,18 +358,13 @@ fia_status prefill_plan(const fia_params* p, PrefillPlan* pl) {
   off = align_up(off + 4 * ((int64_t)pl->max_cost + 2));
   pl->off_list = off;
   off = align_up(off + 8 * pl->U_max);
-  pl->off_kbf = pl->off_vbf = pl->off_q = pl->off_qfac = pl->off_smax = pl->off_kvfac = 0;
+  pl->off_kbf = pl->off_vbf = pl->off_smax = pl->off_kvfac = 0;
   if (p->kv_dtype == FIA_KV_FP8_E4M3) {
     const int64_t bytes = 2 * (int64_t)p->batch * kv_capacity_of(p) * p->num_kv_heads * p->head_dim;
-    const int64_t rows = q_rows_of(p);
     pl->off_kbf = off;
     off = align_up(off + bytes);
     pl->off_vbf = off;
     off = align_up(off + bytes);
-    pl->off_q = off;
-    off = align_up(off + 2 * rows * p->num_q_heads * p->head_dim);
-    pl->off_qfac = off;
-    off = align_up(off + 4 * rows * p->num_q_heads);
     pl->off_smax = off;
     off = align_up(off + 8 * (int64_t)p->batch * p->num_kv_heads);
     pl->off_kvfac = off;
@@ -380,16 +375,15 @@ fia_status prefill_plan(const fia_params* p, PrefillPlan* pl) {
 }
 
 // The parameters the tcgen05 prefill kernel runs on: for FP8 caches, their
-// fp16 copies in the workspace as contiguous caches [B, cap, KVN, D] and the
-// fp16 queries (16-bit elements move through the same tensor maps).
+// fp16 copies in the workspace as contiguous caches [B, cap, KVN, D] (16-bit
+// elements move through the same tensor maps; the bf16 queries are converted
+// to fp16 by the kernel itself).
 fia_params prefill_view(const fia_params* p, const PrefillPlan& pl, void* ws) {
   fia_params v = *p;
   if (p->kv_dtype != FIA_KV_FP8_E4M3) return v;
   char* w = static_cast<char*>(ws);
   v.k_cache = w + pl.off_kbf;
   v.v_cache = w + pl.off_vbf;
-  v.q = w + pl.off_q;
-  v.q_token_stride = (int64_t)p->num_q_heads * p->head_dim;
   v.max_seqlen_kv = (int32_t)kv_capacity_of(p);
   v.kv_dtype = FIA_KV_BF16;
   v.k_scale = v.v_scale = nullptr;
@@ -422,14 +416,6 @@ DequantArgs dequant_args(const fia_params* p, const PrefillPlan& pl, void* ws) {
   d.v_out = reinterpret_cast<uint16_t*>(w + pl.off_vbf);
   d.smax = reinterpret_cast<uint32_t*>(w + pl.off_smax);
   d.kvfac = reinterpret_cast<float*>(w + pl.off_kvfac);
-  d.QN = p->num_q_heads;
-  d.layout = p->layout;
-  d.S_q = p->max_seqlen_q;
-  d.q_rows = q_rows_of(p);
-  d.q_stride = p->q_token_stride ? p->q_token_stride : (int64_t)p->num_q_heads * p->head_dim;
-  d.q = static_cast<const uint16_t*>(p->q);
-  d.q_out = reinterpret_cast<uint16_t*>(w + pl.off_q);
-  d.qfac = reinterpret_cast<float*>(w + pl.off_qfac);
   d.err = reinterpret_cast<int*>(w);
   d.debug = debug_checks();
   return d;
@@ -720,9 +706,11 @@ fia_status fia_execute(const fia_params* p, void* ws, size_t ws_bytes, void* str
     PrefillArgs a = prefill_args(&v, pp, ws);
     if (p->kv_dtype == FIA_KV_FP8_E4M3) {
       char* w = static_cast<char*>(ws);
-      a.qfac = reinterpret_cast<const float*>(w + pp.off_qfac);
+      a.f16 = 1;
       a.kvfac = reinterpret_cast<const float*>(w + pp.off_kvfac);
     }
+    // (FP8 caches: the prefill kernel converts each bf16 query tile to fp16
+    // itself; the conversion pass covers K and V)
     CUtensorMap tq, tk, tv;
     st = q_map(&v, &tq);
     if (st != FIA_OK) return st;

@@ -104,9 +104,10 @@ struct PrefillArgs {
   int kv_layout;             // 0 [nb, bs, KVN, D], 1 [nb, KVN, bs, D]
   const uint8_t* mask;       // explicit mask (modes 0/1) or null
   int64_t mask_bstride, mask_rstride;
-  // fp16 operands (FP8 caches): the scores of row (token t, head h) are
-  // S' * qfac[t*QN + h] * kvfac[(b*KVN + hk)*2], the output O' * kvfac[.. + 1]
-  const float* qfac;
+  // fp16 operands (FP8 caches, f16 = 1): the kernel converts each bf16 query
+  // row to fp16 times 2^sh (sh per row), so the scores of row (token t, head
+  // h) are S' * 2^-sh * kvfac[(b*KVN + hk)*2], the output O' * kvfac[.. + 1]
+  int f16;
   const float* kvfac;
   int64_t out_stride;
   uint16_t* out;
@@ -175,8 +176,8 @@ cudaError_t launch_prefill_schedule(const PrefillArgs& a, cudaStream_t s);
 // FP8 K/V for the prefill kernel: every visible row of the paged (or
 // contiguous) E4M3 caches dequantised once into contiguous fp16 caches
 // [B, cap, KVN, D] in the workspace, each (batch, KV head) scaled by a power
-// of two that keeps it inside fp16, and the queries converted to fp16 with a
-// power-of-two shift per (token, head).
+// of two that keeps it inside fp16 (the prefill kernel converts the queries
+// itself, with a power-of-two shift per (token, head)).
 struct DequantArgs {
   int B, KVN, D, cap, kv_layout;
   const uint8_t* k;
@@ -191,12 +192,6 @@ struct DequantArgs {
   uint16_t* v_out;
   uint32_t* smax;              // [B * KVN * 2] largest K and V scale (bits), zeroed first
   float* kvfac;                // [B * KVN * 2] the power of two taken out of K and V
-  // queries
-  int QN, layout, S_q;
-  int64_t q_rows, q_stride;
-  const uint16_t* q;           // bf16
-  uint16_t* q_out;             // fp16 [q_rows, QN, D]
-  float* qfac;                 // [q_rows * QN]
   int* err;                    // the workspace's error word
   int debug;                   // FIA_DEBUG: report page ids outside the pool (error word 3)
 };

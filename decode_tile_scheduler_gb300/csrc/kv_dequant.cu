@@ -14,15 +14,17 @@
 //           largest K (V) scale, so |K'| < 2 * 448;
 //   Q':     every (token, head) times 2^sh, sh = 15 - (the exponent of its
 //           largest element), kept in [-100, 100] -- the same exact move the
-//           FP8 decode kernel makes.
+//           FP8 decode kernel makes; the prefill kernel's softmax warps do it
+//           to each query tile in shared memory as it lands (a pass here
+//           would read and write all of Q once more).
 // The scores of row (t, h) are then S' * 2^-sh * 2^EK, and the output O' * 2^EV.
 //
-// Three passes, all HBM-bound and short next to the prefill: the largest
-// scale of each (batch, KV head) (warp maxima, then atomic maxima over the
-// float bits, positive floats ordering like their bit patterns), the K/V
-// conversion (one thread per 16 elements of a (batch, row, head) vector), the
-// Q conversion (eight (token, head) rows per warp pass).  Rows at or past a batch's KV length are not
-// touched (the prefill kernel masks their scores and zeroes their V rows).
+// Two passes, short next to the prefill: the largest scale of each (batch,
+// KV head) (warp maxima, then atomic maxima over the float bits, positive
+// floats ordering like their bit patterns) and the K/V conversion (one thread
+// per 16 elements of a (batch, row, head) vector).  Rows at or past a batch's
+// KV length are not touched (the prefill kernel masks their scores and
+// zeroes their V rows).
 #include <algorithm>
 
 #include "common.cuh"
@@ -143,54 +145,6 @@ __global__ void __launch_bounds__(256) kv_dequant_kernel(const DequantArgs a) {
   }
 }
 
-// Q to fp16 (D = 128): a (token, head) row is 256 bytes, 16 lanes x 16
-// bytes, so a warp holds two rows per load and takes eight per pass with four
-// independent loads per lane in flight (one row per warp left each warp
-// waiting on a single load).  Row shift: sh = 15 - (the exponent of the row's
-// largest element), kept in [-100, 100], a maximum over the row's 16 lanes.
-constexpr int kQRowsPerPass = 8;
-__global__ void __launch_bounds__(256) q_convert_kernel(const DequantArgs a) {
-  const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
-  const int64_t total = a.q_rows * a.QN;
-  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kQRowsPerPass;
-       base < total; base += nw * kQRowsPerPass) {
-    uint4 v[kQRowsPerPass / 2];
-#pragma unroll
-    for (int u = 0; u < kQRowsPerPass / 2; ++u) {
-      const int64_t r = base + 2 * u + half;
-      v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (r < total) {
-        const int64_t tok = r / a.QN;
-        const int h = (int)(r - tok * a.QN);
-        v[u] = __ldg(reinterpret_cast<const uint4*>(a.q + tok * a.q_stride + (int64_t)h * a.D) + l16);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kQRowsPerPass / 2; ++u) {
-      const int64_t r = base + 2 * u + half;
-      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-      uint32_t e = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) e = max(e, max((w[k] >> 7) & 0xffu, (w[k] >> 23) & 0xffu));
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) e = max(e, __shfl_xor_sync(0xffffffffu, e, o));
-      const int sh = min(max(142 - (int)e, -100), 100);  // 15 - (e - 127)
-      const float up = __int_as_float((127 + sh) << 23);
-      uint32_t o[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
-        o[k] = pack_f16(f.x * up, f.y * up);
-      }
-      if (r < total) {
-        reinterpret_cast<uint4*>(a.q_out + r * a.D)[l16] = make_uint4(o[0], o[1], o[2], o[3]);
-        if (l16 == 0) a.qfac[r] = __int_as_float((127 - sh) << 23);
-      }
-    }
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_kv_dequant(const DequantArgs& a, int num_sms, cudaStream_t s) {
@@ -204,12 +158,6 @@ cudaError_t launch_kv_dequant(const DequantArgs& a, int num_sms, cudaStream_t s)
     const int64_t total = rows * (a.D / 16);
     const int g2 = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms * 32);
     kv_dequant_kernel<<<g2, 256, 0, s>>>(a);
-  }
-  const int64_t qr = a.q_rows * a.QN;
-  if (qr > 0) {
-    const int64_t warps = (qr + kQRowsPerPass - 1) / kQRowsPerPass;
-    const int g3 = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)num_sms * 8);
-    q_convert_kernel<<<g3, 256, 0, s>>>(a);
   }
   return cudaGetLastError();
 }

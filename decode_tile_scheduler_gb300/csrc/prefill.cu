@@ -53,7 +53,8 @@ struct PrefillCfg {
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   // barriers: mfull[2] mempty[2] qfull qempty kfull[KS] kempty[KS] vfull[VS]
   // vready[VS] vempty[VS] sfull[2] pfull[2] ofull[2] ofree[2] drain[2] tok[2]
-  static constexpr int kNumBars = 4 + 2 + 2 * kKStages + 3 * kVStages + 8 + 2 + 2;
+  // qconv[2]
+  static constexpr int kNumBars = 4 + 2 + 2 * kKStages + 3 * kVStages + 8 + 2 + 2 + 2;
   static constexpr int kOffMsg = kOffBar + 8 * kNumBars;
   static constexpr int kOffMisc = kOffMsg + 2 * 64;
   static constexpr int kSmem = kOffMisc + 64 + 1024;
@@ -307,6 +308,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* ofree = ofull + 2;
   uint64_t* drain = ofree + 2;  // [2], one per MMA thread
   uint64_t* tok = drain + 2;    // [2], MMA issue turn of each slot
+  uint64_t* qconv = tok + 2;    // [2] (F16) a slot's query tile converted to fp16
   PMsg* msg = reinterpret_cast<PMsg*>(smem + Cfg::kOffMsg);
   int* misc = reinterpret_cast<int*>(smem + Cfg::kOffMisc);  // [0] abort, [1] tmem base
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -335,6 +337,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     mbar_init(&drain[1], 1);
     mbar_init(&tok[0], 1);
     mbar_init(&tok[1], 1);
+    mbar_init(&qconv[0], 4);  // one arrival per softmax warp of the slot
+    mbar_init(&qconv[1], 4);
     misc[0] = 0;
     fence_barrier_init();
   }
@@ -483,7 +487,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const uint32_t sq = smem_u32(smem + Cfg::kOffQ);
       const uint32_t sk = smem_u32(smem + Cfg::kOffK);
       const uint32_t sv = smem_u32(smem + Cfg::kOffV);
-      int ucnt = 0, kv_it = 0, q_cnt = 0, p_it = 0, u_cnt = 0;
+      int ucnt = 0, kv_it = 0, q_cnt = 0, p_it = 0, u_cnt = 0, qc_cnt = 0;
       // Issue turns: in units with two slots the threads issue their MMA
       // batches strictly alternately (slot 0, slot 1, slot 0, ...), which
       // keeps the two softmax warpgroups half a period apart (ping-pong);
@@ -552,7 +556,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
           kv_it += n;
           continue;
         }
-        pwait(qfull, q_cnt & 1, a.err, misc);
+        // (F16: the slot's softmax warps convert the bf16 query tile to fp16
+        // in place once it lands and then release it to the tensor core)
+        if constexpr (F16) {
+          pwait(&qconv[s], qc_cnt & 1, a.err, misc);
+          ++qc_cnt;
+        } else {
+          pwait(qfull, q_cnt & 1, a.err, misc);
+        }
         ++q_cnt;
         const bool paired = m.nslots == 2;
         {
@@ -642,7 +653,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + lane_base + 256 * s;
     const uint32_t tO = tS + 128;
-    int ucnt = 0, s_it = 0, o_cnt = 0;
+    int ucnt = 0, s_it = 0, o_cnt = 0, qf_cnt = 0;
     while (true) {
       const int ms = ucnt & 1;
       pwait(&mfull[ms], (ucnt >> 1) & 1, a.err, misc);
@@ -651,6 +662,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       named_bar_sync(2 + s, 128);
       if (row == 0) mbar_arrive(&mempty[ms]);
       if (m.done || *reinterpret_cast<volatile int*>(misc)) break;
+      const int qf_par = qf_cnt & 1;  // (F16) the query tiles land once per unit with tiles
+      if (m.ntiles > 0) ++qf_cnt;
       if (s >= m.nslots) continue;
       const int h = s ? m.h1 : m.h0;
       const int64_t i = (int64_t)m.t * kQTile + row;
@@ -669,8 +682,48 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // powers of two here and in the output
       float sl = a.scale_log2, vfac = 1.f;
       if constexpr (F16) {
+        // This thread's row of the slot's bf16 query tile, to fp16 in place
+        // times 2^sh, sh = 15 - the exponent of the row's largest element
+        // (kept in [-100, 100]): fp16 then holds the row without overflow or
+        // lost bits, and 2^-sh goes into the row's score scale.  The row's
+        // 128-byte pieces are visited from a different chunk per row, so a
+        // warp's accesses spread over the banks; the chunks' order within a
+        // row does not matter here.  Then the slot's MMA thread may read it.
+        float qfac_row = 1.f;
+        if (m.ntiles > 0) {
+          pwait(qfull, qf_par, a.err, misc);
+          uint8_t* qr = smem + Cfg::kOffQ + s * Cfg::kTileBytes + row * 128;
+          uint4 qw[NSUB * 8];
+          uint32_t e = 0;
+#pragma unroll
+          for (int c = 0; c < NSUB * 8; ++c) {
+            const int cc = ((c & 7) + row) & 7;
+            qw[c] = *reinterpret_cast<const uint4*>(qr + (c >> 3) * 16384 + cc * 16);
+            const uint32_t wv[4] = {qw[c].x, qw[c].y, qw[c].z, qw[c].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) e = max(e, max((wv[k] >> 7) & 0xffu, (wv[k] >> 23) & 0xffu));
+          }
+          const int sh = min(max(142 - (int)e, -100), 100);  // 15 - (e - 127)
+          const float up = __int_as_float((127 + sh) << 23);
+#pragma unroll
+          for (int c = 0; c < NSUB * 8; ++c) {
+            const int cc = ((c & 7) + row) & 7;
+            const uint32_t wv[4] = {qw[c].x, qw[c].y, qw[c].z, qw[c].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[k]));
+              o[k] = pack_f16(f.x * up, f.y * up);
+            }
+            *reinterpret_cast<uint4*>(qr + (c >> 3) * 16384 + cc * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+          qfac_row = __int_as_float((127 - sh) << 23);
+          fence_proxy_async_smem();  // the fp16 tile, for the tensor core
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&qconv[s]);
+        }
         const int64_t hkv = ((int64_t)m.b * a.KVN + m.hk) * 2;
-        if (valid) sl *= __ldg(a.qfac + (m.q_row0 + row) * a.QN + h);
+        if (valid) sl *= qfac_row;
         sl *= __ldg(a.kvfac + hkv);
         vfac = __ldg(a.kvfac + hkv + 1);
       }
@@ -878,7 +931,7 @@ static cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& tq,
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t s) {
   const bool neg = a.scale_log2 < 0.f;
-  if (a.qfac)  // fp16 operands: FP8 caches, D = 128
+  if (a.f16)  // fp16 operands: FP8 caches, D = 128
     return neg ? launch_prefill_t<128, true, true>(a, tq, tk, tv, s)
                : launch_prefill_t<128, false, true>(a, tq, tk, tv, s);
   if (a.D == 64) return neg ? launch_prefill_t<64, true, false>(a, tq, tk, tv, s)

@@ -80,6 +80,24 @@ def test_sparse_trailing_invalid_indices_and_duplicates():
     check_close(out, lse, ro, rl, "trailing -1")
 
 
+def test_sparse_cta_count_invariance_and_one_cta_takes_every_item():
+    """A row's chunks all run in one CTA, in order, whatever the CTA count:
+    one CTA walking every item in turn (its stages and query buffer reused
+    item after item), a few CTAs, and the default give the same bits, and
+    match the oracle.  Rows of one, two and many chunks are mixed."""
+    sp = fi.make_sparse(B=5, N1=32, D=128, q_lens=[1, 2, 1, 3, 1],
+                        kv_lens=[4000, 30, 700, 129, 64], layout=fi.LAYOUT_TND, mode="csa",
+                        K2=300, win_left=63, seed=23, device=dev)
+    outs = []
+    for n in (1, 6, 0):
+        _, out, lse = _run(sp, n)
+        outs.append((out.clone(), lse.clone()))
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    ro, rl = oracle.sparse(sp.to("cpu"))
+    check_close(outs[0][0], outs[0][1], ro, rl, "one CTA")
+
+
 @pytest.mark.parametrize("num_sms", [1, 7, 152, 503, 1007])
 def test_sparse_metadata_bit_exact(num_sms):
     import decode_tile_scheduler_gb300 as fia

@@ -862,20 +862,35 @@ __global__ void __launch_bounds__(kPThreads, 1)
         pwait(&ofull[s], o_cnt & 1, a.err, misc);
         ++o_cnt;
         tc_fence_after();
+        // the whole O row into registers, then the slot's O is released (the
+        // next unit's first P V may overwrite it) before the global stores
+        uint32_t v[D];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tO + 32 * c, v);
-          tmem_wait_ld();
-          if (valid) {
-            uint32_t w[16];
+        for (int c = 0; c < D / 32; ++c)
+          tmem_ld32(tO + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ofree[s]);
+        if (valid) {
+          // 32-byte stores where the row allows (a row is D bf16 = 2D bytes)
+          const bool wide = (reinterpret_cast<uintptr_t>(orow) & 31) == 0;
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16(__uint_as_float(v[2 * e]) * scl, __uint_as_float(v[2 * e + 1]) * scl);
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t w[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              *reinterpret_cast<uint4*>(orow + 32 * c + 8 * e) =
-                  make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            for (int e = 0; e < 8; ++e)
+              w[e] = pack_bf16(__uint_as_float(v[16 * c + 2 * e]) * scl,
+                               __uint_as_float(v[16 * c + 2 * e + 1]) * scl);
+            if (wide) {
+              asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(orow + 16 * c),
+                           "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                           "r"(w[6]), "r"(w[7])
+                           : "memory");
+            } else {
+              *reinterpret_cast<uint4*>(orow + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4*>(orow + 16 * c + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+            }
           }
         }
       } else if (valid) {
@@ -887,11 +902,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int64_t li = a.layout == 1 ? (m.q_row0 + row) * a.QN + h
                                          : ((int64_t)m.b * a.QN + h) * a.S_q + i;
         a.lse[li] = lse;
-      }
-      if (m.ntiles > 0) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ofree[s]);
       }
     }
   }

@@ -180,7 +180,7 @@ class L2Flush:
         torch.sum(self.r, dim=0, out=self.sink[0])
         # Hold the stream for ~100 us (200k cycles at 2.07 GHz) after the
         # flush so that the host has queued the whole step (two or three C-ABI
-        # calls, 3-12 us each on the GPU machine's host, the Python wrapper
+        # calls, 3-12 us each on a 16-core Arm host, the Python wrapper
         # included) before its first event runs: the events then time device
         # work only, never the host's launch latency (which the e2e figure
         # includes).

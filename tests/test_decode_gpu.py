@@ -317,6 +317,26 @@ def test_fp8_long_decode_workload_every_row():
     check_close(out, lse, ro, rl, "long FP8 decode, every row")
 
 
+# The other decode workloads the bench times, at their bench sizes, every
+# (query row, head) against the oracle: the same sequences with 4 query rows
+# each (multi-token decode), with head-major pages, and the long FP8 decode
+# with 16 query heads per KV head.
+BENCH_FORMS = {
+    "mtp_decode_s4": lambda: fi.workload_paged_decode(device=dev, S_q=4),
+    "paged_decode_bnnbsd": lambda: fi.workload_paged_decode(device=dev,
+                                                            kv_layout=fi.KV_LAYOUT_BNNBSD),
+    "fp8_gqa16_decode": lambda: fi.workload_fp8_long_decode(device=dev, KVN=4),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BENCH_FORMS))
+def test_bench_decode_forms_every_row(name):
+    p = BENCH_FORMS[name]()
+    _, out, lse = _run(p)
+    ro, rl = _ref(p)
+    check_close(out, lse, ro, rl, name)
+
+
 # Query magnitudes across the whole bf16 range.  The FP8 products run in fp16,
 # so the kernel moves each head's query by a power of two before narrowing it;
 # the bf16 products see the query unchanged.  Powers of two keep the inputs
